@@ -1,0 +1,410 @@
+"""Benchmark of the CSA2 decode step on GB300.
+
+Workload (default): one decoder CSA2 group of 4 layers (1 Full + 3 Reuse), batch 64, context
+131072 per sequence, compression ratio 1, FP4 main KV (E2M1 + E4M3 per 16 channels), 128-token
+bf16 window per layer, indexer Q 4x128 bf16 + fp32 weights, main Q 16x512 bf16, Top-512.
+A step = append of the new token (FP4 quantise + indexer-K row) -> indexer scores over all
+131072 keys -> exact Top-512 -> four layers of split-KV sparse attention (+ combine), issued as
+one `csa2_group_step` C-ABI call.  Inputs are synthetic N(0, 1) (torch's CUDA generator, seed 0)
+and resident in HBM; the 2.1 GB indexer-K scan per step is larger than L2, so no flush is needed.
+
+Prints one JSON line.  `value` = decode tokens/s over all ranks (64 sequences per GPU per step),
+`e2e` = the same through host buffers (per-step H2D of the step's inputs from pinned memory,
+D2H of the four layers' outputs), `roofline` = the indexer-score kernel against the measured HBM
+copy bandwidth, `cpu_baseline` = the oracle on the host cores on a bounded sample.
+`--impl reference` times the oracle (the CPU reference of this method) instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+B_PER_GPU, T_CTX, N_LAYERS, K_SEL, W_WIN = 64, 131072, 4, 512, 128
+WORKLOAD = "csa2_decode_group_1full_3reuse_b64_t131072"
+METRIC = "CSA2 decode tokens/s and KV HBM GB/s at 128K ctx; % of GB300 HBM roofline"
+# algorithmic bytes per sequence per step: indexer-K scan + 4 layers x (512 FP4 rows of 288 B +
+# 128 bf16 window rows of 1 KiB + Q and O of 16 KiB each) + the append (bf16 row in, FP4 out, KI row)
+BYTES_KI_PER_SEQ = T_CTX * 128 * 2
+BYTES_ATTN_PER_SEQ_LAYER = K_SEL * 288 + W_WIN * 1024 + 2 * 16 * 512 * 2
+BYTES_APPEND_PER_SEQ = 512 * 2 + 288 + 2 * 128 * 2
+BYTES_PER_SEQ = BYTES_KI_PER_SEQ + N_LAYERS * BYTES_ATTN_PER_SEQ_LAYER + BYTES_APPEND_PER_SEQ
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "index_score_decode_b64_t131072.md")
+SCORE_SRC = os.path.join(ROOT, "compressed_sparse_attention_step_gb300", "csrc", "index_score.cu")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the score kernel from the committed ncu summary, if the kernel
+    source is unchanged since the capture (its sha256 is recorded in the summary)."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+        src = hashlib.sha256(open(SCORE_SRC, "rb").read()).hexdigest()[:16]
+        vals = {}
+        for line in txt.splitlines():
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip().strip("`- ")] = v.strip().strip("`")
+        if vals.get("kernel_source_sha256") != src:
+            return None
+        return int(float(vals["traffic_bytes_per_launch"]))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling in the background; samples are time-stamped on arrival."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1]
+        near = inside or [s for (t, s) in self.samples if t0 - 0.5 <= t <= t1 + 0.5]
+        if not near:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in near if num(s[0]) is not None]
+        mx = [num(s[1]) for s in near if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in near for i in range(4) if len(s) > 4 + i and s[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "samples_near": len(near),
+                "power_w_max": max((num(s[2]) or 0.0) for s in near)}
+
+
+# ----------------------------------------------------------------------------------------------
+# oracle (CPU baseline / reference arm)
+# ----------------------------------------------------------------------------------------------
+def oracle_inputs(n_seq, seed=0):
+    """A bounded sample of the workload for the oracle: n_seq sequences at the full context.
+    Indexer keys, queries, weights and windows are the seeded N(0, 1) draws; the FP4 cache rows
+    are random code bytes with scales in the range N(0, 1) rows quantise to (only the 512
+    selected rows per layer are read, so their values do not change the work)."""
+    import csa2_synth as syn
+    g = np.random.default_rng(seed)
+    codes = g.integers(0, 256, (n_seq, T_CTX, 256), dtype=np.uint8)
+    scales = g.integers(0x2C, 0x3C, (n_seq, T_CTX, 32), dtype=np.uint8)
+    KI = np.stack([syn.normal_bf16(seed, syn.T_KI, b, (T_CTX, 128)) for b in range(n_seq)])
+    L = N_LAYERS
+    q = np.stack([np.stack([syn.normal_bf16(seed, syn.T_Q + l, b, (1, 16, 512)) for b in range(n_seq)]) for l in range(L)])
+    qI = np.stack([np.stack([syn.normal_bf16(seed, syn.T_QI + l, b, (1, 4, 128)) for b in range(n_seq)]) for l in range(L)])
+    w = np.stack([np.stack([syn.normal_f32(seed, syn.T_W + l, b, (1, 4)) for b in range(n_seq)]) for l in range(L)])
+    swa = np.stack([np.stack([syn.normal_bf16(seed, syn.T_SWA + l, b, (W_WIN, 512)) for b in range(n_seq)]) for l in range(L)])
+    return codes, scales, KI, q, qI, w, swa
+
+
+def oracle_step(orc, inp, threads):
+    codes, scales, KI, q, qI, w, swa = inp
+    n = codes.shape[0]
+    orc.group_step([0, 2, 2, 2], [T_CTX] * n, codes, scales, KI, q, qI, w, swa, np.full(n, W_WIN, np.int32),
+                   threads=threads)
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, same workload and metric (bounded sample)."""
+    if rank != 0:
+        return
+    import oracle as orc
+    orc.build()
+    threads = cpu_threads()
+    n_seq = min(64, 2 * threads)         # two sequences per host thread per step
+    inp = oracle_inputs(n_seq)
+    for _ in range(min(args.warmup, 1)):
+        oracle_step(orc, inp, threads)
+    budget = 150.0
+    times = []
+    t_start = time.time()
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(orc, inp, threads)
+        times.append(time.perf_counter() - t0)
+        if time.time() - t_start + times[-1] > budget:
+            break
+    ms = 1e3 * statistics.mean(times)
+    val = n_seq / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": len(times), "steps_requested": args.steps, "warmup": min(args.warmup, 1),
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32/f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": n_seq, "seq_len": T_CTX, "parallelism": "host threads",
+                       "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n_seq} sequences x {T_CTX} context, 4 layers (1 Full + 3 Reuse) per step"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------------
+def build_workload(torch, c, syn, dev):
+    B, T, L = B_PER_GPU, T_CTX, N_LAYERS
+    seed = syn.SEEDS["decode_group_1f3r_b64_t131072"]
+    codes = torch.empty((B, T, 256), dtype=torch.uint8, device=dev)
+    scales = torch.empty((B, T, 32), dtype=torch.uint8, device=dev)
+    for b in range(B):   # the library's own quantiser fills the FP4 cache, one sequence at a time
+        kv = syn.device_normal_bf16((1, T, 512), seed, syn.T_KV * 1000 + b, device=dev)
+        c.csa2_fp4_quantize_append(kv, codes[b:b + 1], scales[b:b + 1])
+        del kv
+    KI = syn.device_normal_bf16((B, T, 128), seed, syn.T_KI * 1000, device=dev)
+    q = [syn.device_normal_bf16((B, 1, 16, 512), seed, syn.T_Q + l, device=dev) for l in range(L)]
+    qI = [syn.device_normal_bf16((B, 1, 4, 128), seed, syn.T_QI + l, device=dev) for l in range(L)]
+    w = [syn.device_normal_bf16((B, 1, 4), seed, syn.T_W + l, device=dev).float() for l in range(L)]
+    swa = [syn.device_normal_bf16((B, W_WIN, 512), seed, syn.T_SWA + l, device=dev) for l in range(L)]
+    kv_new = syn.device_normal_bf16((B, 1, 512), seed, syn.T_KV_NEW, device=dev)
+    ki_new = syn.device_normal_bf16((B, 1, 128), seed, syn.T_KI_NEW, device=dev)
+    lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+    swa_len = torch.full((B,), W_WIN, dtype=torch.int32, device=dev)
+    out = [torch.empty((B, 1, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    idx = [torch.empty((B, K_SEL), dtype=torch.int32, device=dev), None, None, None]
+    ws = torch.empty(c.group_workspace_size(B, 1, T, K_SEL, W_WIN), dtype=torch.uint8, device=dev)
+    return dict(codes=codes, scales=scales, KI=KI, q=q, qI=qI, w=w, swa=swa, kv_new=kv_new, ki_new=ki_new,
+                lens=lens, swa_len=swa_len, out=out, idx=idx, ws=ws)
+
+
+def make_desc(c, wl, events=None, q=None, qI=None, w=None, kv_new=None, ki_new=None, out=None):
+    return c.make_group_desc(
+        [c.MODE_FULL, c.MODE_REUSE, c.MODE_REUSE, c.MODE_REUSE], B=B_PER_GPU, Nq=1, cap=T_CTX, lens=wl["lens"],
+        codes=wl["codes"], scales=wl["scales"], KI=wl["KI"], q=q or wl["q"], qI=qI or wl["qI"], w=w or wl["w"],
+        swa=wl["swa"], swa_len=wl["swa_len"], out=out or wl["out"], idx=wl["idx"], K=K_SEL, W=W_WIN,
+        kv_new=kv_new if kv_new is not None else wl["kv_new"], ki_new=ki_new if ki_new is not None else wl["ki_new"],
+        events=events)
+
+
+def launches_per_step(c):
+    ns = int(c.lib().csa2_attn_auto_split(B_PER_GPU, K_SEL, W_WIN))
+    # quantise-append + indexer-K append + score + select + per layer (attention [+ combine])
+    return 4 + N_LAYERS * (2 if ns > 1 else 1)
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import csa2_synth as syn
+    import compressed_sparse_attention_step_gb300 as c
+    from compressed_sparse_attention_step_gb300 import _build
+
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError("libcsa2.so is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    c.lib()
+    wl = build_workload(torch, c, syn, dev)
+    stream = torch.cuda.current_stream()
+    K, Wm = args.steps, args.warmup
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- device-resident step --------------------------------------------------------------------
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev_pairs:   # materialise the event handles
+        a.record()
+        b.record()
+    descs = [make_desc(c, wl, events=p) for p in ev_pairs]
+    plain = make_desc(c, wl)
+    for _ in range(Wm):
+        c.csa2_group_step(plain, wl["ws"])
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    time.sleep(0.1)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        c.csa2_group_step(descs[i], wl["ws"])
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    score_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if world > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+
+    # ---- end to end through host buffers ---------------------------------------------------------
+    L = N_LAYERS
+    h_q = [x.cpu().pin_memory() for x in wl["q"]]
+    h_qI = wl["qI"][0].cpu().pin_memory()
+    h_w = wl["w"][0].cpu().pin_memory()
+    h_kv = wl["kv_new"].cpu().pin_memory()
+    h_ki = wl["ki_new"].cpu().pin_memory()
+    h_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in wl["out"]]
+    d_q = [torch.empty_like(x) for x in wl["q"]]
+    d_qI, d_w = torch.empty_like(wl["qI"][0]), torch.empty_like(wl["w"][0])
+    d_kv, d_ki = torch.empty_like(wl["kv_new"]), torch.empty_like(wl["ki_new"])
+    e2e_desc = make_desc(c, wl, q=d_q, qI=[d_qI, None, None, None], w=[d_w, None, None, None], kv_new=d_kv,
+                         ki_new=d_ki)
+    h2d = sum(x.numel() * x.element_size() for x in h_q + [h_qI, h_w, h_kv, h_ki])
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+    def e2e_step():
+        for l in range(L):
+            d_q[l].copy_(h_q[l], non_blocking=True)
+        d_qI.copy_(h_qI, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        d_kv.copy_(h_kv, non_blocking=True)
+        d_ki.copy_(h_ki, non_blocking=True)
+        c.csa2_group_step(e2e_desc, wl["ws"])
+        for l in range(L):
+            h_out[l].copy_(wl["out"][l], non_blocking=True)
+
+    for _ in range(Wm):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record()
+    for _ in range(K):
+        e2e_step()
+    f1.record()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = f0.elapsed_time(f1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if sampler:
+        sampler.stop()
+    if rank != 0:
+        return
+
+    ms_step = ms_total / K
+    tokens = B_PER_GPU * world
+    value = tokens / (ms_step / 1e3)
+    kv_gbs = BYTES_PER_SEQ * B_PER_GPU * world / (ms_step / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    score_avg = statistics.mean(score_ms)
+    score_bytes = B_PER_GPU * BYTES_KI_PER_SEQ
+    achieved = score_bytes / (score_avg / 1e3) / 1e9
+    traffic = profiled_traffic()
+
+    # ---- CPU baseline: the oracle on a bounded sample --------------------------------------------
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle as orc
+        orc.build()
+        threads = cpu_threads()
+        n_seq = min(64, 2 * threads)
+        inp = oracle_inputs(n_seq)
+        t0 = time.perf_counter()
+        oracle_step(orc, inp, threads)
+        dt = time.perf_counter() - t0
+        cpu = {"value": n_seq / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"one step over {n_seq} of the 64 sequences at full context ({T_CTX}), 1 Full + 3 Reuse, "
+                         f"{dt:.1f} s wall on {threads} threads"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16/fp4 in, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": tokens, "seq_len": T_CTX, "parallelism": f"replicas x{world}",
+                   "layers": "1 Full + 3 Reuse", "top_k": K_SEL, "window": W_WIN,
+                   "l2": "inputs larger than L2 (2.1 GB indexer-K scan per step)"},
+        "kv_gbs": kv_gbs, "hbm_frac_step": kv_gbs / peak, "bytes_per_step": BYTES_PER_SEQ * B_PER_GPU * world,
+        "roofline": {"kernel": "index_score_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} (hbm copy)",
+                     "traffic": traffic, "algorithmic_bytes": score_bytes, "avg_launch_ms": score_avg},
+        "e2e": {"value": tokens / (e2e_ms / K / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d * world,
+                "d2h_bytes_per_step": d2h * world, "ms_per_step": e2e_ms / K},
+        "gpu_launches": launches_per_step(c) * K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,470 @@
+// Sparse attention of each query's 16 heads over its selected FP4 main-KV rows plus its
+// sliding-window rows ("Every layer retains its own main Q and sliding-window key-value cache",
+// ai-maestro.online "DeepSeek AI released DeepSeek-V4.1-Flash with 1M context, FP4", section
+// "Compressed Sparse Attention 2"; the 128-token window: section "Causal Encoder-Decoder
+// architecture"; E2M1 codes with an E4M3 scale per 16 channels: section "FP4 KV, Bounded Replay,
+// and other extensions").  K = V = the dequantised row.
+//
+// Split-KV flash decoding.  A query's rows form a list of 32-row chunks (selected FP4 rows,
+// then window rows); each CTA (4 warps) takes a contiguous run of chunks, balanced by bytes, and
+// keeps an online softmax (m, l, O) over them; a combine kernel merges the splits in a fixed
+// order.  Inside a CTA, warp w owns latent channels [128w, 128w+128) for everything:
+//  - it gathers only its slice of each row (cp.async, 16 B pieces, XOR-swizzled in shared
+//    memory), dequantises its FP4 slice to bf16 (E2M1 pair table times the E4M3 scale; the
+//    product is exact in bf16), and keeps its slice of Q in registers;
+//  - S_w = Q[:, slice] K[:, slice]^T and O[:, slice] += P V[:, slice] run on tensor cores with
+//    the 16 heads as the M = 16 dimension of mma.m16n8k16 (bf16 in, fp32 accumulate);
+//  - the four partial S are summed in a fixed order, so the only block-wide barriers are the
+//    two around the softmax of each chunk.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kCH = 32;          // rows per chunk
+constexpr int kPitchP = 40;      // bf16 per row of the P tile (80 B: conflict-free ldmatrix)
+constexpr int kPitchS = 36;      // floats per row of the partial-S tiles
+constexpr int kCostFp4 = 9;      // relative bytes of a 32-row FP4 chunk (288 B per row)
+constexpr int kCostSwa = 32;     // relative bytes of a 32-row bf16 window chunk (1 KiB per row)
+constexpr int kMaxSplit = 32;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct AttnSmem {
+  uint16_t q[CSA2_H * CSA2_D];
+  uint16_t kv[2][kCH * CSA2_D];
+  uint8_t raw_codes[2][kCH * CSA2_CODE_BYTES];
+  uint8_t raw_scales[2][kCH * CSA2_SCALE_BYTES];
+  uint16_t p[CSA2_H * kPitchP];
+  float s[4][CSA2_H * kPitchS];
+  float corr[CSA2_H];
+  float m_fin[CSA2_H];
+  float l_fin[CSA2_H];
+  uint32_t lut_e2m1x2[256];
+  uint16_t lut_e4m3[256];
+};
+
+// bf16 bits of the E2M1 value of a 4-bit code (sign included).
+__device__ __forceinline__ uint32_t e2m1_bf16(uint32_t nib) {
+  const uint32_t c = nib & 7u;
+  const uint32_t mag = (c < 2u) ? (c ? 0x3F00u : 0u) : ((((126u + (c >> 1)) << 7)) | ((c & 1u) << 6));
+  return mag | ((nib & 8u) << 12);
+}
+// bf16 bits of an E4M3 (FN) value (exact: 4 significant bits, range 2^-9 .. 448).
+__device__ __forceinline__ uint32_t e4m3_bf16(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : float(m) * 0.001953125f;
+  return (__float_as_uint(v) >> 16) | ((b & 0x80u) << 8);
+}
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                             *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__host__ __device__ __forceinline__ int chunk_cost_start(int c, int nfp4) {
+  return kCostFp4 * min(c, nfp4) + kCostSwa * max(c - nfp4, 0);
+}
+
+__global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
+    const uint16_t* __restrict__ q, int Nq, const uint8_t* __restrict__ codes,
+    const uint8_t* __restrict__ scales, int64_t cap, const int32_t* __restrict__ idx,
+    const int32_t* __restrict__ n_valid, int k, const uint16_t* __restrict__ swa,
+    const int32_t* __restrict__ swa_len, int W, float scale_log2, uint16_t* __restrict__ out,
+    float* __restrict__ lse, int n_split, float* __restrict__ ws, unsigned int* flags) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
+  const int inst = blockIdx.y;
+  const int split = blockIdx.x;
+  const int b = inst / Nq, qi = inst - b * Nq;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  const int mat = lane >> 3, mrow = lane & 7;
+
+  for (int i = t; i < 256; i += kThreads) {
+    sm.lut_e2m1x2[i] = e2m1_bf16(i & 15) | (e2m1_bf16(i >> 4) << 16);
+    sm.lut_e4m3[i] = uint16_t(e4m3_bf16(uint32_t(i)));
+  }
+
+  // ---- this split's chunks ------------------------------------------------------------------
+  const int nfp4 = (k + kCH - 1) / kCH;
+  const int nswa = swa ? (W + kCH - 1) / kCH : 0;
+  const int nch = nfp4 + nswa;
+  const int total_cost = max(chunk_cost_start(nch, nfp4), 1);
+  int c_begin = nch, c_end = nch;
+  for (int c = 0; c < nch; ++c) {
+    const int sc = chunk_cost_start(c, nfp4) * n_split / total_cost;
+    if (sc >= split && c_begin == nch) c_begin = c;
+    if (sc >= split + 1) { c_end = c; break; }
+  }
+
+  const int n_fp4_valid = min(k, n_valid ? max(n_valid[inst], 0) : k);
+  const int32_t* irow = idx + int64_t(inst) * k;
+  const int SW = W - 1 + Nq;
+  const int swa_lo = swa ? SW - min(max(swa_len[b], 0), SW) : SW;
+  const uint8_t* cbase = codes + int64_t(b) * cap * CSA2_CODE_BYTES;
+  const uint8_t* sbase = scales + int64_t(b) * cap * CSA2_SCALE_BYTES;
+  const uint16_t* swbase = swa ? swa + int64_t(b) * SW * CSA2_D : nullptr;
+
+  auto fp4_pos = [&](int slot) -> int64_t {
+    if (slot >= n_fp4_valid) return -1;
+    const int32_t p = __ldg(irow + slot);
+    if (p < 0) return -1;
+    if (int64_t(p) >= cap) { atomicOr(flags, CSA2_FLAG_INDEX_OOB); return -1; }
+    return p;
+  };
+  auto swa_row = [&](int wr) -> int {
+    if (wr >= W) return -1;
+    const int br = qi + wr;
+    return br >= swa_lo ? br : -1;
+  };
+  auto row_valid = [&](int c, int r) -> bool {
+    return (c < nfp4) ? fp4_pos(c * kCH + r) >= 0 : swa_row((c - nfp4) * kCH + r) >= 0;
+  };
+
+  // gather of chunk c into buffer buf: this warp's channel slice only
+  auto issue = [&](int c, int buf) {
+    if (c < nfp4) {
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int task = it * 32 + lane, r = task >> 2, piece = task & 3;
+        const int64_t pos = fp4_pos(c * kCH + r);
+        if (pos >= 0)
+          cp_async16(smem_u32(sm.raw_codes[buf] + r * CSA2_CODE_BYTES + (((4 * warp + piece) ^ (r & 7)) << 4)),
+                     cbase + pos * CSA2_CODE_BYTES + 64 * warp + 16 * piece, 16);
+      }
+      const int64_t pos = fp4_pos(c * kCH + lane);
+      if (pos >= 0)
+        cp_async8(smem_u32(sm.raw_scales[buf] + lane * CSA2_SCALE_BYTES + 8 * warp),
+                  sbase + pos * CSA2_SCALE_BYTES + 8 * warp, 8);
+    } else {
+      const int cw = c - nfp4;
+#pragma unroll 4
+      for (int it = 0; it < 16; ++it) {
+        const int task = it * 32 + lane, r = task >> 4, piece = task & 15;
+        const int br = swa_row(cw * kCH + r);
+        const uint16_t* src = br >= 0 ? swbase + int64_t(br) * CSA2_D + 128 * warp + 8 * piece : swa;
+        cp_async16(smem_u32(sm.kv[buf] + r * CSA2_D + (((16 * warp + piece) ^ (r & 7)) << 3)), src,
+                   br >= 0 ? 16 : 0);
+      }
+    }
+  };
+
+  // FP4 slice of chunk c (raw buffer) -> bf16 rows of the KV tile; empty rows become zeros
+  auto dequant = [&](int c, int buf) {
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int task = it * 32 + lane, r = task >> 2, piece = task & 3;
+      uint4 o[4];
+      if (fp4_pos(c * kCH + r) >= 0) {
+        const uint4 cb = *reinterpret_cast<const uint4*>(
+            sm.raw_codes[buf] + r * CSA2_CODE_BYTES + (((4 * warp + piece) ^ (r & 7)) << 4));
+        const uint32_t sraw = *reinterpret_cast<const uint16_t*>(sm.raw_scales[buf] + r * CSA2_SCALE_BYTES +
+                                                                 8 * warp + 2 * piece);
+        const uint32_t sa = sm.lut_e4m3[sraw & 0xFFu], sb = sm.lut_e4m3[sraw >> 8];
+        const uint32_t sA = sa | (sa << 16), sB = sb | (sb << 16);
+        const uint32_t words[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          const uint32_t sc = wi < 2 ? sA : sB;
+          const uint32_t wv = words[wi];
+          o[wi].x = bmul2(sm.lut_e2m1x2[wv & 0xFFu], sc);
+          o[wi].y = bmul2(sm.lut_e2m1x2[(wv >> 8) & 0xFFu], sc);
+          o[wi].z = bmul2(sm.lut_e2m1x2[(wv >> 16) & 0xFFu], sc);
+          o[wi].w = bmul2(sm.lut_e2m1x2[wv >> 24], sc);
+        }
+      } else {
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) o[wi] = make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi)
+        *reinterpret_cast<uint4*>(sm.kv[buf] + r * CSA2_D + (((16 * warp + 4 * piece + wi) ^ (r & 7)) << 3)) = o[wi];
+    }
+  };
+
+  float oacc[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f;  // softmax state of head (t >> 3), same in its 8 threads
+  const int sh = t >> 3, sc4 = (t & 7) * 4;
+
+  if (c_begin < c_end) {
+    // Q slice of this warp: 16 rows x 256 B
+    const uint16_t* qrow = q + int64_t(inst) * CSA2_H * CSA2_D;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int task = it * 32 + lane, r = task >> 4, piece = task & 15;
+      cp_async16(smem_u32(sm.q + r * CSA2_D + (((16 * warp + piece) ^ (r & 7)) << 3)),
+                 qrow + r * CSA2_D + 128 * warp + 8 * piece, 16);
+    }
+    issue(c_begin, 0);
+    cp_async_commit();
+    __syncthreads();  // LUTs visible
+
+    uint32_t qa[8][4];
+    for (int c = c_begin; c < c_end; ++c) {
+      const int buf = (c - c_begin) & 1;
+      if (c + 1 < c_end) {
+        issue(c + 1, buf ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncwarp();
+      if (c == c_begin) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int r = mrow + ((mat & 1) << 3);
+          const int ch = 16 * warp + 2 * kk + (mat >> 1);
+          ldmatrix_x4(qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
+                      smem_u32(sm.q + r * CSA2_D + ((ch ^ (r & 7)) << 3)));
+        }
+      }
+      if (c < nfp4) {
+        dequant(c, buf);
+        __syncwarp();
+      }
+      // ---- S_w = Q[:, slice] K[:, slice]^T for the 32 rows --------------------------------
+      float sacc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          const int kr = 16 * np + mrow + ((mat >> 1) << 3);
+          const int ch = 16 * warp + 2 * kk + (mat & 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(b0, b1, b2, b3, smem_u32(sm.kv[buf] + kr * CSA2_D + ((ch ^ (kr & 7)) << 3)));
+          mma_bf16_16816(sacc[2 * np], qa[kk], b0, b1);
+          mma_bf16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
+        }
+      }
+      float* sw = sm.s[warp];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        *reinterpret_cast<float2*>(sw + g * kPitchS + 8 * nt + 2 * tq) = make_float2(sacc[nt][0], sacc[nt][1]);
+        *reinterpret_cast<float2*>(sw + (g + 8) * kPitchS + 8 * nt + 2 * tq) =
+            make_float2(sacc[nt][2], sacc[nt][3]);
+      }
+      __syncthreads();
+      // ---- online softmax: thread t owns head sh, columns sc4 .. sc4+3 -----------------------
+      {
+        float v[4];
+        float vmax = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int col = sc4 + e;
+          const int o = sh * kPitchS + col;
+          const float x = (sm.s[0][o] + sm.s[1][o]) + (sm.s[2][o] + sm.s[3][o]);
+          v[e] = row_valid(c, col) ? x * scale_log2 : -INFINITY;
+          vmax = fmaxf(vmax, v[e]);
+        }
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
+        const float m_new = fmaxf(m_run, vmax);
+        float corr = 1.0f, p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (m_new != -INFINITY) {
+          corr = exp2f(m_run - m_new);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) p[e] = exp2f(v[e] - m_new);
+        }
+        float rs = (p[0] + p[1]) + (p[2] + p[3]);
+        rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+        rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+        rs += __shfl_xor_sync(0xffffffffu, rs, 4);
+        l_run = l_run * corr + rs;
+        m_run = m_new;
+        *reinterpret_cast<uint2*>(sm.p + sh * kPitchP + sc4) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
+        if ((t & 7) == 0) sm.corr[sh] = corr;
+      }
+      __syncthreads();
+      // ---- O[:, slice] = corr * O + P V[:, slice] -----------------------------------------------
+      {
+        const float cr0 = sm.corr[g], cr1 = sm.corr[g + 8];
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          oacc[nt][0] *= cr0;
+          oacc[nt][1] *= cr0;
+          oacc[nt][2] *= cr1;
+          oacc[nt][3] *= cr1;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          uint32_t pa[4];
+          {
+            const int r = mrow + ((mat & 1) << 3);
+            ldmatrix_x4(pa[0], pa[1], pa[2], pa[3], smem_u32(sm.p + r * kPitchP + 16 * kk + ((mat >> 1) << 3)));
+          }
+#pragma unroll
+          for (int np = 0; np < 8; ++np) {
+            const int kr = 16 * kk + mrow + ((mat & 1) << 3);
+            const int ch = 16 * warp + 2 * np + (mat >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(b0, b1, b2, b3, smem_u32(sm.kv[buf] + kr * CSA2_D + ((ch ^ (kr & 7)) << 3)));
+            mma_bf16_16816(oacc[2 * np], pa, b0, b1);
+            mma_bf16_16816(oacc[2 * np + 1], pa, b2, b3);
+          }
+        }
+      }
+    }
+  }
+
+  if ((t & 7) == 0) {
+    sm.m_fin[sh] = m_run;
+    sm.l_fin[sh] = l_run;
+  }
+  __syncthreads();
+
+  if (n_split == 1) {
+    const float l0 = sm.l_fin[g], l1 = sm.l_fin[g + 8];
+    const float i0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, i1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
+    uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      const int ch = 128 * warp + 8 * nt + 2 * tq;
+      *reinterpret_cast<uint32_t*>(orow + g * CSA2_D + ch) = pack_bf16x2(oacc[nt][0] * i0, oacc[nt][1] * i0);
+      *reinterpret_cast<uint32_t*>(orow + (g + 8) * CSA2_D + ch) = pack_bf16x2(oacc[nt][2] * i1, oacc[nt][3] * i1);
+    }
+    if (lse && t < CSA2_H) {
+      const float l = sm.l_fin[t];
+      lse[int64_t(inst) * CSA2_H + t] = l > 0.0f ? (sm.m_fin[t] + log2f(l)) * kLn2 : -INFINITY;
+    }
+  } else {
+    float* po = ws + (int64_t(inst) * n_split + split) * (CSA2_H * CSA2_D);
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      const int ch = 128 * warp + 8 * nt + 2 * tq;
+      *reinterpret_cast<float2*>(po + g * CSA2_D + ch) = make_float2(oacc[nt][0], oacc[nt][1]);
+      *reinterpret_cast<float2*>(po + (g + 8) * CSA2_D + ch) = make_float2(oacc[nt][2], oacc[nt][3]);
+    }
+    if (t < CSA2_H) {
+      float* ml = ws + int64_t(gridDim.y) * n_split * (CSA2_H * CSA2_D) +
+                  (int64_t(inst) * n_split + split) * (2 * CSA2_H);
+      ml[2 * t] = sm.m_fin[t];
+      ml[2 * t + 1] = sm.l_fin[t];
+    }
+  }
+}
+
+// Merge the splits of one query in split order: o = sum_j 2^(m_j-M) O_j / sum_j 2^(m_j-M) l_j.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ ws, int n_split,
+                                                           int64_t instances, uint16_t* __restrict__ out,
+                                                           float* __restrict__ lse) {
+  const int64_t inst = blockIdx.x;
+  const int t = threadIdx.x;
+  const int h = t >> 4, c0 = (t & 15) * 32;
+  const float* ml = ws + instances * n_split * (CSA2_H * CSA2_D) + inst * n_split * (2 * CSA2_H);
+  float M = -INFINITY;
+  for (int j = 0; j < n_split; ++j) M = fmaxf(M, ml[j * 2 * CSA2_H + 2 * h]);
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  float L = 0.0f;
+  if (M != -INFINITY) {
+    for (int j = 0; j < n_split; ++j) {
+      const float mj = ml[j * 2 * CSA2_H + 2 * h];
+      const float a = exp2f(mj - M);
+      L += a * ml[j * 2 * CSA2_H + 2 * h + 1];
+      const float4* po = reinterpret_cast<const float4*>(ws + (inst * n_split + j) * (CSA2_H * CSA2_D) +
+                                                         h * CSA2_D + c0);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 x = po[v];
+        acc[4 * v] += a * x.x;
+        acc[4 * v + 1] += a * x.y;
+        acc[4 * v + 2] += a * x.z;
+        acc[4 * v + 3] += a * x.w;
+      }
+    }
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  uint32_t o[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+  uint4* dst = reinterpret_cast<uint4*>(out + (inst * CSA2_H + h) * CSA2_D + c0);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+  if (lse && (t & 15) == 0) lse[inst * CSA2_H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+}  // namespace
+
+size_t attn_ws_bytes(int64_t instances, int n_split) {
+  if (n_split <= 1) return 0;
+  return size_t(instances) * size_t(n_split) * (CSA2_H * CSA2_D + 2 * CSA2_H) * sizeof(float);
+}
+
+int attn_auto_split(int64_t instances, int k, int W) {
+  const int nch = (k + kCH - 1) / kCH + (W + kCH - 1) / kCH;
+  if (instances <= 0 || nch <= 0) return 1;
+  const int64_t target = 2 * 152;  // two resident CTAs per SM
+  int64_t s = (target + instances - 1) / instances;
+  s = std::min<int64_t>(s, std::min(nch, kMaxSplit));
+  return int(std::max<int64_t>(s, 1));
+}
+
+cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
+                               const uint8_t* scales, int64_t cap, const int32_t* idx,
+                               const int32_t* n_valid, int k, const uint16_t* swa,
+                               const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
+                               float* lse, int n_split, float* ws, cudaStream_t st) {
+  const int64_t instances = int64_t(B) * Nq;
+  if (instances == 0) return cudaSuccess;
+  unsigned int* flags = device_flags_ptr();
+  if (!flags) return cudaErrorUnknown;
+  const size_t smem = sizeof(AttnSmem);
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  const dim3 grid{unsigned(n_split), unsigned(instances), 1u};
+  sparse_attn_kernel<<<grid, kThreads, smem, st>>>(q, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len,
+                                                   W, scale_log2, out, lse, n_split, ws, flags);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || n_split == 1) return e;
+  attn_combine_kernel<<<unsigned(instances), 256, 0, st>>>(ws, n_split, instances, out, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2
+
+extern "C" csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq, const uint8_t* codes,
+                                               const uint8_t* scales, int64_t cap, const int32_t* idx,
+                                               const int32_t* n_valid, int k, const uint16_t* swa,
+                                               const int32_t* swa_len, int W, float softmax_scale,
+                                               uint16_t* out, float* lse, int n_split, void* ws,
+                                               size_t ws_bytes, csa2_stream_t stream) {
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (B < 0 || Nq < 0 || cap < 0 || k < 0 || k > CSA2_MAX_ATTN_K || n_split < 0 || n_split > csa2::kMaxSplit)
+    return CSA2_ERR_INVALID_ARG;
+  if (swa && (W < 1 || W > CSA2_MAX_W || !swa_len)) return CSA2_ERR_INVALID_ARG;
+  if (!swa) W = 0;
+  const int64_t instances = int64_t(B) * Nq;
+  if (instances == 0) return CSA2_OK;
+  if (instances > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (!q || !out || !al16(q) || !al16(out)) return CSA2_ERR_INVALID_ARG;
+  if (k > 0 && (!codes || !scales || !idx || !al16(codes) || !al16(scales))) return CSA2_ERR_INVALID_ARG;
+  if (swa && !al16(swa)) return CSA2_ERR_INVALID_ARG;
+  if (k == 0 && !swa) { /* no rows: still defined (zeros, lse = -inf) */ }
+  const int ns = n_split ? n_split : csa2::attn_auto_split(instances, k, W);
+  const size_t need = csa2::attn_ws_bytes(instances, ns);
+  if (need && (!ws || ws_bytes < need || !al16(ws))) return CSA2_ERR_WORKSPACE;
+  return csa2::launch_sparse_attn(q, B, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len, W,
+                                  softmax_scale, out, lse, ns, static_cast<float*>(ws),
+                                  reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CSA2_OK
+             : CSA2_ERR_CUDA;
+}

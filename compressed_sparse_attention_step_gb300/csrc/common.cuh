@@ -1,0 +1,148 @@
+// Shared device helpers of the CSA2 library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+
+namespace csa2 {
+
+// Address of the current device's flag word (CSA2_FLAG_*), defined in group.cu; kernels that
+// report data-dependent problems receive it as an argument.  NULL if the lookup failed.
+unsigned int* device_flags_ptr();
+
+// ---------------------------------------------------------------------------------------------
+// bf16 bit helpers (values are carried as raw 16-bit patterns)
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs).
+__device__ __forceinline__ uint32_t f2bf_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return f2bf_bits(lo) | (f2bf_bits(hi) << 16);
+}
+
+// Ordered 32-bit key of a score: larger key <=> larger score; -0 and +0 share one key.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Memory helpers
+// ---------------------------------------------------------------------------------------------
+// Streaming 16-byte load: evict-first in L1 and L2 (data read once).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// cp.async of 16 bytes (or zero-fill when src_bytes == 0), cached in L2 only.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// Warp-level tensor-core helpers (bf16 inputs, fp32 accumulate)
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                            uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A(16x16, row) * B(16x8, col) + D
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Block-wide exclusive scan of one uint32 per thread (blockDim.x multiple of 32, <= 1024).
+// `tmp` is >= 32 words of shared memory.  Returns the exclusive prefix; *total gets the sum.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* tmp, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t s = (lane < nw) ? tmp[lane] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    tmp[lane] = s;  // inclusive warp-sum prefix
+  }
+  __syncthreads();
+  const uint32_t warp_base = (wid == 0) ? 0u : tmp[wid - 1];
+  const uint32_t tot = tmp[nw - 1];
+  __syncthreads();
+  if (total) *total = tot;
+  return warp_base + x - v;
+}
+
+}  // namespace csa2
+
+// Internal launchers shared across translation units (all return cudaGetLastError()).
+namespace csa2 {
+cudaError_t launch_fp4_quantize(const uint16_t* x, int B, int n_new, uint8_t* codes, uint8_t* scales,
+                                int64_t cap, const int32_t* offsets, int offset_bias,
+                                cudaStream_t st);
+cudaError_t launch_copy_rows_append(const uint16_t* src, int B, int n_new, int row_elems,
+                                    uint16_t* dst, int64_t cap, const int32_t* lens, cudaStream_t st);
+cudaError_t launch_block_keys(const uint16_t* KI, int B, int64_t cap, const int32_t* lens,
+                              uint16_t* block_keys, int only_new, int n_new, cudaStream_t st);
+cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
+                               int64_t key_stride_rows, const int32_t* lens, int64_t cap_entries,
+                               int block_div, const int32_t* cand, const int32_t* cand_len,
+                               int64_t n_cand, int ratio, const int32_t* q_pos, float* scores,
+                               int64_t ld, int32_t* n_valid, cudaStream_t st);
+cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
+                        int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,
+                        int expand8, int32_t* pool_len, cudaStream_t st);
+cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
+                               const uint8_t* scales, int64_t cap, const int32_t* idx,
+                               const int32_t* n_valid, int k, const uint16_t* swa,
+                               const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
+                               float* lse, int n_split, float* ws, cudaStream_t st);
+size_t attn_ws_bytes(int64_t instances, int n_split);
+int attn_auto_split(int64_t instances, int k, int W);
+}  // namespace csa2

@@ -1,0 +1,263 @@
+// FP4 main-KV codec: E2M1 codes with one E4M3 scale per 16 channels, NVFP4 without the global
+// scale (ai-maestro.online "DeepSeek AI released DeepSeek-V4.1-Flash with 1M context, FP4",
+// section "FP4 KV, Bounded Replay, and other extensions").  Also the plain row-append copy and
+// the block-key builder of the hierarchical indexer.
+//
+// All kernels here stream: one thread per 16-channel group (32 B of bf16 in, 8 B of codes and
+// 1 B of scale out), so a warp covers one 512-channel row with fully coalesced accesses.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace csa2 {
+namespace {
+
+// E4M3 (FN) byte -> fp32 value (exact).  Scale bytes are never NaN (encoded with satfinite).
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : float(m) * 0.001953125f;
+  return (b & 0x80u) ? -v : v;
+}
+
+// E2M1 magnitude code (0..7) -> fp32 bits of {0, .5, 1, 1.5, 2, 3, 4, 6}.
+__device__ __forceinline__ uint32_t e2m1_mag_bits(uint32_t c) {
+  return (c < 2u) ? (c ? 0x3F000000u : 0u) : (((126u + (c >> 1)) << 23) | ((c & 1u) << 22));
+}
+
+// Quantise one 16-channel group held as 8 packed bf16 pairs.
+//
+// The E2M1 code of q = fp32(x / s) under round-to-nearest-even is the number of midpoints
+// {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5} that |q| passes, where a midpoint between codes c and
+// c+1 counts on equality only when c+1 is even (ties to the even mantissa); magnitudes above 6
+// saturate to code 7.  The comparison is done as |x| against midpoint * s instead of dividing:
+// each product has at most 3 + 4 significant bits, so it is exact in fp32, and x (8 significant
+// bits) either equals a product or differs from it by at least 2^-9 of its size, far more than
+// the 2^-24 rounding of the quotient.  Hence |x| > m*s <=> fp32(|x|/s) > m and equality holds
+// exactly when the quotient is the tie, which makes the codes bit-identical to dividing.
+__device__ __forceinline__ void quantize_group(const uint32_t (&wv)[8], uint32_t& lo, uint32_t& hi,
+                                               uint32_t& sb) {
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = max(amax, max(wv[i] & 0x7FFFu, (wv[i] >> 16) & 0x7FFFu));
+  const float s32 = __fdiv_rn(__uint_as_float(amax << 16), 6.0f);
+  sb = __nv_cvt_float_to_fp8(s32, __NV_SATFINITE, __NV_E4M3);
+  const float s = e4m3_value(sb);
+  lo = 0u;
+  hi = 0u;
+  if (s > 0.0f) {
+    const float t0 = 0.25f * s, t1 = 0.75f * s, t2 = 1.25f * s, t3 = 1.75f * s;
+    const float t4 = 2.5f * s, t5 = 3.5f * s, t6 = 5.0f * s;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t h = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
+      const float a = __uint_as_float((h & 0x7FFFu) << 16);
+      uint32_t c = uint32_t(a > t0) + uint32_t(a >= t1) + uint32_t(a > t2) + uint32_t(a >= t3) +
+                   uint32_t(a > t4) + uint32_t(a >= t5) + uint32_t(a > t6);
+      c |= (h >> 12) & 8u;  // sign of x
+      if (i < 8) lo |= c << (4 * i);
+      else hi |= c << (4 * (i - 8));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) fp4_quantize_kernel(
+    const uint16_t* __restrict__ x, int64_t n_groups, int n_new, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, int64_t cap, const int32_t* __restrict__ offsets, int offset_bias,
+    unsigned int* flags) {
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= n_groups) return;
+  const int64_t row = gid >> 5;
+  const int g = int(gid & 31);
+  const int64_t b = row / n_new, r = row - b * n_new;
+  const int64_t pos = (offsets ? int64_t(offsets[b]) + offset_bias : 0) + r;
+  if (pos < 0 || pos >= cap) {
+    if (g == 0) atomicOr(flags, CSA2_FLAG_APPEND_OOB);
+    return;
+  }
+  const uint16_t* src = x + row * CSA2_D + g * CSA2_GROUP;
+  const uint4 v0 = ld_stream16(src), v1 = ld_stream16(src + 8);
+  const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  uint32_t lo, hi, sb;
+  quantize_group(wv, lo, hi, sb);
+  const int64_t crow = b * cap + pos;
+  *reinterpret_cast<uint2*>(codes + crow * CSA2_CODE_BYTES + g * 8) = make_uint2(lo, hi);
+  scales[crow * CSA2_SCALE_BYTES + g] = uint8_t(sb);
+}
+
+__global__ void __launch_bounds__(256) fp4_dequantize_kernel(const uint8_t* __restrict__ codes,
+                                                             const uint8_t* __restrict__ scales,
+                                                             int64_t n_groups,
+                                                             uint16_t* __restrict__ out) {
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= n_groups) return;
+  const int64_t row = gid >> 5;
+  const int g = int(gid & 31);
+  const uint2 c = __ldcs(reinterpret_cast<const uint2*>(codes + row * CSA2_CODE_BYTES + g * 8));
+  const float s = e4m3_value(scales[row * CSA2_SCALE_BYTES + g]);
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const uint32_t word = (i < 8) ? c.x : c.y;
+    const uint32_t byte = (word >> (4 * (i & 7))) & 0xFFu;
+    uint32_t pair = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t nib = (byte >> (4 * h)) & 15u;
+      // the product of a 2-bit and a 4-bit significand is exact in fp32 and in bf16
+      const float v = __uint_as_float(e2m1_mag_bits(nib & 7u)) * s;
+      const uint32_t bits = (__float_as_uint(v) >> 16) | ((nib & 8u) << 12);
+      pair |= bits << (16 * h);
+    }
+    o[i >> 1] = pair;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out + row * CSA2_D + g * CSA2_GROUP);
+  __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
+  __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
+}
+
+// dst row (lens[b] - n_new + r) of sequence b <- src row r of sequence b; 16 B per thread.
+__global__ void __launch_bounds__(256) copy_rows_append_kernel(const uint16_t* __restrict__ src,
+                                                               int B, int n_new, int row_vecs,
+                                                               uint16_t* __restrict__ dst,
+                                                               int64_t cap,
+                                                               const int32_t* __restrict__ lens,
+                                                               unsigned int* flags) {
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = int64_t(B) * n_new * row_vecs;
+  if (gid >= total) return;
+  const int64_t row = gid / row_vecs;
+  const int v = int(gid - row * row_vecs);
+  const int64_t b = row / n_new, r = row - b * n_new;
+  const int64_t pos = int64_t(lens[b]) - n_new + r;
+  if (pos < 0 || pos >= cap) {
+    if (v == 0) atomicOr(flags, CSA2_FLAG_APPEND_OOB);
+    return;
+  }
+  const uint4 val = reinterpret_cast<const uint4*>(src)[row * row_vecs + v];
+  reinterpret_cast<uint4*>(dst)[(b * cap + pos) * row_vecs + v] = val;
+}
+
+// Block keys: key of block j = bf16_RNE(0.125 * sum_{i<8} KI[8j+i]) with the sum in token order
+// in fp32 (ai-maestro "Compressed Sparse Attention 2": blocks of eight tokens).  One thread per
+// (sequence, block, 8-channel slice).  With only_new, just the blocks completed by the last
+// n_new appended rows: j in [floor((lens-n_new)/8), floor(lens/8)).
+__global__ void __launch_bounds__(256) block_keys_kernel(const uint16_t* __restrict__ KI, int B,
+                                                         int64_t cap, const int32_t* __restrict__ lens,
+                                                         uint16_t* __restrict__ bkeys,
+                                                         int64_t blocks_per_seq, int only_new,
+                                                         int n_new) {
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = int64_t(B) * blocks_per_seq * 16;
+  if (gid >= total) return;
+  const int sl = int(gid & 15);
+  const int64_t t = gid >> 4;
+  const int64_t b = t / blocks_per_seq;
+  int64_t j = t - b * blocks_per_seq;
+  const int64_t T = min(int64_t(lens[b]), cap);
+  const int64_t nb = T / CSA2_BLOCK;
+  if (only_new) j += max(int64_t(0), (T - n_new) / CSA2_BLOCK);
+  if (j >= nb) return;
+  float acc[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < CSA2_BLOCK; ++i) {
+    const uint4 v = *reinterpret_cast<const uint4*>(KI + ((b * cap + j * CSA2_BLOCK + i) * CSA2_DI + sl * 8));
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      acc[2 * c] = __fadd_rn(acc[2 * c], bf16lo(wv[c]));
+      acc[2 * c + 1] = __fadd_rn(acc[2 * c + 1], bf16hi(wv[c]));
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    o[c] = pack_bf16x2(__fmul_rn(acc[2 * c], 0.125f), __fmul_rn(acc[2 * c + 1], 0.125f));
+  *reinterpret_cast<uint4*>(bkeys + ((b * (cap / CSA2_BLOCK) + j) * CSA2_DI + sl * 8)) =
+      make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+inline unsigned grid_for(int64_t threads, int block) { return unsigned((threads + block - 1) / block); }
+
+}  // namespace
+
+cudaError_t launch_fp4_quantize(const uint16_t* x, int B, int n_new, uint8_t* codes, uint8_t* scales,
+                                int64_t cap, const int32_t* offsets, int offset_bias,
+                                cudaStream_t st) {
+  const int64_t n_groups = int64_t(B) * n_new * (CSA2_D / CSA2_GROUP);
+  if (n_groups == 0) return cudaSuccess;
+  unsigned int* flags = device_flags_ptr();
+  if (!flags) return cudaErrorUnknown;
+  fp4_quantize_kernel<<<grid_for(n_groups, 256), 256, 0, st>>>(x, n_groups, n_new, codes, scales, cap,
+                                                               offsets, offset_bias, flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_rows_append(const uint16_t* src, int B, int n_new, int row_elems,
+                                    uint16_t* dst, int64_t cap, const int32_t* lens, cudaStream_t st) {
+  const int row_vecs = row_elems / 8;
+  const int64_t total = int64_t(B) * n_new * row_vecs;
+  if (total == 0) return cudaSuccess;
+  unsigned int* flags = device_flags_ptr();
+  if (!flags) return cudaErrorUnknown;
+  copy_rows_append_kernel<<<grid_for(total, 256), 256, 0, st>>>(src, B, n_new, row_vecs, dst, cap,
+                                                                lens, flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_keys(const uint16_t* KI, int B, int64_t cap, const int32_t* lens,
+                              uint16_t* block_keys, int only_new, int n_new, cudaStream_t st) {
+  const int64_t bps = only_new ? int64_t(n_new / CSA2_BLOCK + 1) : cap / CSA2_BLOCK;
+  const int64_t total = int64_t(B) * bps * 16;
+  if (total == 0) return cudaSuccess;
+  block_keys_kernel<<<grid_for(total, 256), 256, 0, st>>>(KI, B, cap, lens, block_keys, bps, only_new,
+                                                          n_new);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2
+
+// ------------------------------------------------------------------------------------------------
+// C ABI
+// ------------------------------------------------------------------------------------------------
+namespace {
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+extern "C" csa2_status csa2_fp4_quantize_append(const uint16_t* x, int B, int n_new, int d,
+                                                uint8_t* codes, uint8_t* scales, int64_t cap,
+                                                const int32_t* offsets, csa2_stream_t stream) {
+  if (d != CSA2_D) return CSA2_ERR_UNSUPPORTED;
+  if (B < 0 || n_new < 0 || cap < 0 || (!offsets && n_new > cap)) return CSA2_ERR_INVALID_ARG;
+  if (int64_t(B) * n_new == 0) return CSA2_OK;
+  if (!x || !codes || !scales || !al16(x) || !al16(codes) || !al16(scales)) return CSA2_ERR_INVALID_ARG;
+  if (offsets && (reinterpret_cast<uintptr_t>(offsets) & 3u)) return CSA2_ERR_INVALID_ARG;
+  return csa2::launch_fp4_quantize(x, B, n_new, codes, scales, cap, offsets, 0,
+                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CSA2_OK
+             : CSA2_ERR_CUDA;
+}
+
+extern "C" csa2_status csa2_fp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows,
+                                           int d, uint16_t* out, csa2_stream_t stream) {
+  if (d != CSA2_D) return CSA2_ERR_UNSUPPORTED;
+  if (rows < 0) return CSA2_ERR_INVALID_ARG;
+  if (rows == 0) return CSA2_OK;
+  if (!codes || !scales || !out || !al16(codes) || !al16(scales) || !al16(out)) return CSA2_ERR_INVALID_ARG;
+  const int64_t n_groups = rows * (CSA2_D / CSA2_GROUP);
+  csa2::fp4_dequantize_kernel<<<csa2::grid_for(n_groups, 256), 256, 0,
+                                reinterpret_cast<cudaStream_t>(stream)>>>(codes, scales, n_groups, out);
+  return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+}
+
+extern "C" csa2_status csa2_block_keys_build(const uint16_t* KI, int B, int64_t cap, const int32_t* lens,
+                                             uint16_t* block_keys, csa2_stream_t stream) {
+  if (B < 0 || cap < 0) return CSA2_ERR_INVALID_ARG;
+  if (B == 0 || cap < CSA2_BLOCK) return CSA2_OK;
+  if (!KI || !lens || !block_keys || !al16(KI) || !al16(block_keys)) return CSA2_ERR_INVALID_ARG;
+  return csa2::launch_block_keys(KI, B, cap, lens, block_keys, 0, 0,
+                                 reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CSA2_OK
+             : CSA2_ERR_CUDA;
+}

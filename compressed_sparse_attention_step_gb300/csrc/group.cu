@@ -1,0 +1,272 @@
+// CSA2 layer-group driver, hierarchical pool entry point, workspace sizing and status helpers.
+//
+// A group runs its layers in order on one stream (ai-maestro.online "DeepSeek AI released
+// DeepSeek-V4.1-Flash with 1M context, FP4", section "Compressed Sparse Attention 2"):
+//   Full     [append new rows] -> [block scores -> Top-keep blocks -> pool] -> scores -> Top-K
+//   Reindex  scores (pool or all visible entries) with its own indexer Q -> Top-K
+//   Reuse    nothing: the latest indices are used as they are
+// and every layer then runs split-KV sparse attention with its own Q and window.  Scores live in
+// the caller's workspace; the selection kernels read them while they are still in L2.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace csa2 {
+
+__device__ unsigned int g_device_flags = 0;
+
+unsigned int* device_flags_ptr() {
+  static unsigned int* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  if (dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_flags) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
+
+namespace {
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct GroupWs {
+  size_t scores_off, nv_off, attn_off, total;
+  int64_t score_ld;
+};
+
+GroupWs group_ws_layout(int B, int Nq, int64_t cap, int K, int W, int hierarchical, int keep, int n_split) {
+  GroupWs L{};
+  const int64_t rows = int64_t(B) * Nq;
+  int64_t ld = cap;
+  if (hierarchical) ld = std::max<int64_t>(cap / CSA2_BLOCK, int64_t(keep) * CSA2_BLOCK);
+  L.score_ld = ld;
+  L.scores_off = 0;
+  L.nv_off = align256(size_t(rows) * size_t(ld) * sizeof(float));
+  L.attn_off = L.nv_off + align256(size_t(rows) * sizeof(int32_t));
+  const int ns = n_split ? n_split : attn_auto_split(rows, K, W);
+  L.total = L.attn_off + align256(attn_ws_bytes(rows, ns));
+  return L;
+}
+
+}  // namespace
+}  // namespace csa2
+
+using csa2::al16;
+
+extern "C" size_t csa2_workspace_size(int op, const csa2_dims* d) {
+  if (!d) return 0;
+  const int64_t rows = int64_t(d->B) * d->Nq;
+  switch (op) {
+    case CSA2_OP_TOPK:
+      return 0;
+    case CSA2_OP_BLOCK_POOL:
+      return csa2::align256(size_t(rows) * size_t(std::max<int64_t>(d->cap / CSA2_BLOCK, 1)) * sizeof(float));
+    case CSA2_OP_SPARSE_ATTN: {
+      const int W = d->W;
+      const int ns = d->n_split ? d->n_split : csa2::attn_auto_split(rows, d->k, W);
+      return csa2::attn_ws_bytes(rows, ns);
+    }
+    case CSA2_OP_GROUP_STEP:
+      return csa2::group_ws_layout(d->B, d->Nq, d->cap, d->k, d->W, d->hierarchical, d->n_blocks_keep,
+                                   d->n_split)
+          .total;
+    default:
+      return 0;
+  }
+}
+
+extern "C" int csa2_attn_auto_split(int64_t instances, int k, int W) {
+  return csa2::attn_auto_split(instances, k, W);
+}
+
+extern "C" const char* csa2_status_string(csa2_status s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_INVALID_ARG: return "invalid argument";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported dimension";
+    case CSA2_ERR_CUDA: return "CUDA error";
+    case CSA2_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+extern "C" csa2_status csa2_device_flags(uint32_t* flags, int clear, csa2_stream_t stream) {
+  if (!flags) return CSA2_ERR_INVALID_ARG;
+  unsigned int* dptr = csa2::device_flags_ptr();
+  if (!dptr) return CSA2_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return CSA2_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, dptr, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA2_ERR_CUDA;
+  *flags = v;
+  if (clear && cudaMemset(dptr, 0, sizeof(unsigned int)) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (clear && cudaDeviceSynchronize() != cudaSuccess) return CSA2_ERR_CUDA;
+  return CSA2_OK;
+}
+
+extern "C" csa2_status csa2_block_pool(const uint16_t* qI, const float* w, int B, int Nq,
+                                       const uint16_t* block_keys, int64_t cap, const int32_t* lens,
+                                       int ratio, const int32_t* q_pos, int keep, int32_t* pool,
+                                       int32_t* pool_len, void* ws, size_t ws_bytes,
+                                       csa2_stream_t stream) {
+  if (B < 0 || Nq < 0 || cap < 0 || ratio < 1 || keep < 1 || keep > CSA2_MAX_K) return CSA2_ERR_INVALID_ARG;
+  const int64_t rows = int64_t(B) * Nq;
+  if (rows == 0) return CSA2_OK;
+  if (rows > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (!qI || !w || !block_keys || !lens || !pool || !pool_len || !al16(qI) || !al16(block_keys))
+    return CSA2_ERR_INVALID_ARG;
+  const int64_t nb = cap / CSA2_BLOCK;
+  csa2_dims d{};
+  d.B = B;
+  d.Nq = Nq;
+  d.cap = cap;
+  const size_t need = csa2_workspace_size(CSA2_OP_BLOCK_POOL, &d);
+  if (!ws || ws_bytes < need || !al16(ws)) return CSA2_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float* sc = static_cast<float*>(ws);
+  if (nb == 0) {
+    // no complete block can exist: empty pools
+    if (cudaMemsetAsync(pool_len, 0, size_t(rows) * sizeof(int32_t), st) != cudaSuccess) return CSA2_ERR_CUDA;
+    if (cudaMemsetAsync(pool, 0xFF, size_t(rows) * keep * CSA2_BLOCK * sizeof(int32_t), st) != cudaSuccess)
+      return CSA2_ERR_CUDA;
+    return CSA2_OK;
+  }
+  // the visible block count of each row is returned through pool_len, then consumed
+  if (csa2::launch_index_score(qI, w, B, Nq, block_keys, nb, lens, cap, CSA2_BLOCK, nullptr, nullptr, 0,
+                               ratio, q_pos, sc, nb, pool_len, st) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  if (csa2::launch_topk(sc, int(rows), nb, nb, pool_len, keep, nullptr, 0, pool, nullptr, 1, pool_len, st) !=
+      cudaSuccess)
+    return CSA2_ERR_CUDA;
+  return CSA2_OK;
+}
+
+extern "C" size_t csa2_group_desc_size(void) { return sizeof(csa2_group_desc); }
+
+extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_t ws_bytes,
+                                       csa2_stream_t stream) {
+  if (!g) return CSA2_ERR_INVALID_ARG;
+  const int L = g->n_layers;
+  if (L < 1 || L > CSA2_MAX_LAYERS) return CSA2_ERR_INVALID_ARG;
+  if (g->B < 0 || g->Nq < 0 || g->cap < 0 || g->ratio < 1) return CSA2_ERR_INVALID_ARG;
+  if (g->K < 1 || g->K > CSA2_MAX_ATTN_K || g->W < 0 || g->W > CSA2_MAX_W) return CSA2_ERR_INVALID_ARG;
+  if (g->n_split < 0 || g->n_split > 32 || g->n_new < 0) return CSA2_ERR_INVALID_ARG;
+  if (g->hierarchical && (g->n_blocks_keep < 1 || g->n_blocks_keep > CSA2_MAX_K)) return CSA2_ERR_INVALID_ARG;
+  const int64_t rows = int64_t(g->B) * g->Nq;
+  if (rows == 0) return CSA2_OK;
+  if (rows > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (g->modes[0] != CSA2_MODE_FULL && g->modes[0] != CSA2_MODE_REINDEX) return CSA2_ERR_INVALID_ARG;
+  if (!g->lens || !g->codes || !g->scales || !g->KI || !al16(g->codes) || !al16(g->scales) || !al16(g->KI))
+    return CSA2_ERR_INVALID_ARG;
+  if (g->hierarchical && (!g->block_keys || !g->pool || !g->pool_len || !al16(g->block_keys)))
+    return CSA2_ERR_INVALID_ARG;
+  if (g->W > 0 && !g->swa_len) return CSA2_ERR_INVALID_ARG;
+  bool any_full = false;
+  for (int l = 0; l < L; ++l) {
+    const int m = g->modes[l];
+    if (m != CSA2_MODE_FULL && m != CSA2_MODE_REINDEX && m != CSA2_MODE_REUSE) return CSA2_ERR_INVALID_ARG;
+    if (!g->q[l] || !g->out[l] || !al16(g->q[l]) || !al16(g->out[l])) return CSA2_ERR_INVALID_ARG;
+    if (g->W > 0 && (!g->swa[l] || !al16(g->swa[l]))) return CSA2_ERR_INVALID_ARG;
+    if (m != CSA2_MODE_REUSE) {
+      if (!g->qI[l] || !g->w[l] || !g->idx[l] || !al16(g->qI[l])) return CSA2_ERR_INVALID_ARG;
+      any_full |= (m == CSA2_MODE_FULL);
+    }
+  }
+  if (g->n_new > 0 && (g->kv_new || g->ki_new)) {
+    if (g->modes[0] != CSA2_MODE_FULL) return CSA2_ERR_INVALID_ARG;
+    if ((g->kv_new && !al16(g->kv_new)) || (g->ki_new && !al16(g->ki_new))) return CSA2_ERR_INVALID_ARG;
+  }
+  (void)any_full;
+  const csa2::GroupWs lay = csa2::group_ws_layout(g->B, g->Nq, g->cap, g->K, g->W, g->hierarchical,
+                                                  g->n_blocks_keep, g->n_split);
+  if (!ws || ws_bytes < lay.total || !al16(ws)) return CSA2_ERR_WORKSPACE;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* wsb = static_cast<char*>(ws);
+  float* scores = reinterpret_cast<float*>(wsb + lay.scores_off);
+  int32_t* nv = reinterpret_cast<int32_t*>(wsb + lay.nv_off);
+  float* attn_ws = reinterpret_cast<float*>(wsb + lay.attn_off);
+  const int ns = g->n_split ? g->n_split : csa2::attn_auto_split(rows, g->K, g->W);
+  const int64_t nb = g->cap / CSA2_BLOCK;
+  const int64_t pool_w = int64_t(g->n_blocks_keep) * CSA2_BLOCK;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+
+  // ---- append (Full layer of a decode step) ----------------------------------------------------
+  if (g->n_new > 0) {
+    if (g->kv_new &&
+        !ok(csa2::launch_fp4_quantize(g->kv_new, g->B, g->n_new, g->codes, g->scales, g->cap, g->lens,
+                                      -g->n_new, st)))
+      return CSA2_ERR_CUDA;
+    if (g->ki_new) {
+      if (!ok(csa2::launch_copy_rows_append(g->ki_new, g->B, g->n_new, CSA2_DI, g->KI, g->cap, g->lens, st)))
+        return CSA2_ERR_CUDA;
+      if (g->hierarchical &&
+          !ok(csa2::launch_block_keys(g->KI, g->B, g->cap, g->lens, g->block_keys, 1, g->n_new, st)))
+        return CSA2_ERR_CUDA;
+    }
+  }
+
+  const int32_t* latest = nullptr;
+  bool first_score = true;
+  for (int l = 0; l < L; ++l) {
+    const int mode = g->modes[l];
+    if (mode != CSA2_MODE_REUSE) {
+      const bool timed = first_score && g->ev_score_begin && g->ev_score_end;
+      if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_begin), st) != cudaSuccess)
+        return CSA2_ERR_CUDA;
+      if (g->hierarchical) {
+        if (mode == CSA2_MODE_FULL) {
+          if (nb > 0) {
+            if (!ok(csa2::launch_index_score(g->qI[l], g->w[l], g->B, g->Nq, g->block_keys, nb, g->lens, g->cap,
+                                             CSA2_BLOCK, nullptr, nullptr, 0, g->ratio, g->q_pos, scores, nb,
+                                             g->pool_len, st)))
+              return CSA2_ERR_CUDA;
+            if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
+              return CSA2_ERR_CUDA;
+            if (!ok(csa2::launch_topk(scores, int(rows), nb, nb, g->pool_len, g->n_blocks_keep, nullptr, 0, g->pool,
+                                      nullptr, 1, g->pool_len, st)))
+              return CSA2_ERR_CUDA;
+          } else {
+            if (!ok(cudaMemsetAsync(g->pool_len, 0, size_t(rows) * sizeof(int32_t), st))) return CSA2_ERR_CUDA;
+            if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
+              return CSA2_ERR_CUDA;
+          }
+        }
+        if (!ok(csa2::launch_index_score(g->qI[l], g->w[l], g->B, g->Nq, g->KI, g->cap, g->lens, g->cap, 1,
+                                         g->pool, g->pool_len, pool_w, g->ratio, g->q_pos, scores, pool_w, nv,
+                                         st)))
+          return CSA2_ERR_CUDA;
+        if (timed && mode != CSA2_MODE_FULL &&
+            cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
+          return CSA2_ERR_CUDA;
+        if (!ok(csa2::launch_topk(scores, int(rows), pool_w, pool_w, nv, g->K, g->pool, pool_w, g->idx[l], nullptr,
+                                  0, nullptr, st)))
+          return CSA2_ERR_CUDA;
+      } else {
+        if (!ok(csa2::launch_index_score(g->qI[l], g->w[l], g->B, g->Nq, g->KI, g->cap, g->lens, g->cap, 1,
+                                         nullptr, nullptr, 0, g->ratio, g->q_pos, scores, g->cap, nv, st)))
+          return CSA2_ERR_CUDA;
+        if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
+          return CSA2_ERR_CUDA;
+        if (!ok(csa2::launch_topk(scores, int(rows), g->cap, g->cap, nv, g->K, nullptr, 0, g->idx[l], nullptr, 0,
+                                  nullptr, st)))
+          return CSA2_ERR_CUDA;
+      }
+      first_score = false;
+      latest = g->idx[l];
+    } else if (g->idx[l] && g->idx[l] != latest) {
+      if (!ok(cudaMemcpyAsync(g->idx[l], latest, size_t(rows) * g->K * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                              st)))
+        return CSA2_ERR_CUDA;
+    }
+    if (!ok(csa2::launch_sparse_attn(g->q[l], g->B, g->Nq, g->codes, g->scales, g->cap, latest, nullptr, g->K,
+                                     g->W > 0 ? g->swa[l] : nullptr, g->swa_len, g->W, g->softmax_scale,
+                                     g->out[l], g->lse[l], ns, attn_ws, st)))
+      return CSA2_ERR_CUDA;
+  }
+  return CSA2_OK;
+}

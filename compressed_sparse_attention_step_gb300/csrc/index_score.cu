@@ -1,0 +1,187 @@
+// Lightning-indexer scoring: s_t = sum_h w_h * relu(qI_h . KI_t) for every visible cached
+// indexer key (or every position of a candidate pool).  Full layers select with it, Reindex
+// layers rescore with their own indexer Q (ai-maestro.online "DeepSeek AI released
+// DeepSeek-V4.1-Flash with 1M context, FP4", section "Compressed Sparse Attention 2").
+//
+// HBM-bound streaming kernel (256 B of indexer K per position, ~2 FMA per byte): eight lanes
+// share one position, each lane owning 16 consecutive channels (two 16-byte loads), so a warp
+// reads four whole 256-byte rows per step and four steps are kept in flight per lane.  The
+// indexer query slice (4 heads x 16 channels) stays in registers for the whole CTA.
+//
+// The fp32 result is bit-identical to the canonical order: per head, lane j computes the
+// fused-multiply-add chain p_j over channels 16j..16j+15 from +0; the 8-lane reduction is a
+// reduce-scatter whose additions are exactly ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)) (IEEE addition
+// is commutative, so either operand order gives the same bits); then relu, w_h * r_h, and
+// (m0 + m1) + (m2 + m3).  Only _rn intrinsics are used, so nothing is contracted or reordered.
+#include "common.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kU = 4;                                // 4-position groups in flight per lane
+constexpr int kPosPerWarpIt = 4 * kU;                // 16
+constexpr int kPosPerCtaIt = kWarps * kPosPerWarpIt; // 128
+
+template <bool kCand>
+__global__ void __launch_bounds__(kThreads, 2) index_score_kernel(
+    const uint16_t* __restrict__ qI, const float* __restrict__ w, int Nq,
+    const uint16_t* __restrict__ KI, int64_t key_stride_rows, const int32_t* __restrict__ lens,
+    int64_t cap_entries, int block_div, const int32_t* __restrict__ cand,
+    const int32_t* __restrict__ cand_len, int64_t n_cand, int ratio,
+    const int32_t* __restrict__ q_pos, float* __restrict__ scores, int64_t ld,
+    int32_t* __restrict__ n_valid_out, int64_t chunk, unsigned int* flags) {
+  const int row = blockIdx.y;
+  const int b = row / Nq, qi = row - b * Nq;
+  const int64_t T = min(max(int64_t(lens[b]), int64_t(0)), cap_entries);
+  const int64_t p = q_pos ? int64_t(q_pos[row]) : int64_t(ratio) * T - Nq + qi;
+  const int64_t nvis = (p + 1 < 0) ? 0 : min((p + 1) / ratio, T);   // visible cache entries
+
+  int64_t nv;  // scored prefix of this row
+  const int32_t* crow = nullptr;
+  if (kCand) {
+    crow = cand + int64_t(row) * n_cand;
+    const int64_t cl = min(max(int64_t(cand_len[row]), int64_t(0)), n_cand);
+    int64_t lo = 0, hi = cl;  // first pool entry not visible (the pool is ascending)
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (int64_t(crow[mid]) < nvis) lo = mid + 1;
+      else hi = mid;
+    }
+    nv = lo;
+  } else {
+    nv = nvis / block_div;
+  }
+  if (n_valid_out && blockIdx.x == 0 && threadIdx.x == 0) n_valid_out[row] = int32_t(nv);
+
+  const int64_t c0 = int64_t(blockIdx.x) * chunk;
+  const int64_t c1 = min(c0 + chunk, ld);
+  if (c0 >= c1) return;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane >> 3;  // position within the warp's group of four
+  const int j = lane & 7;     // channel chunk 16j .. 16j+15
+
+  float qf[4][16];
+  const uint16_t* qrow = qI + int64_t(row) * (CSA2_HI * CSA2_DI);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint4 a = *reinterpret_cast<const uint4*>(qrow + h * CSA2_DI + 16 * j);
+    const uint4 c = *reinterpret_cast<const uint4*>(qrow + h * CSA2_DI + 16 * j + 8);
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      qf[h][2 * e] = bf16lo(v[e]);
+      qf[h][2 * e + 1] = bf16hi(v[e]);
+    }
+  }
+  // head held by this lane after the reduce-scatter
+  const int my_head = 2 * (j & 1) + ((j >> 1) & 1);
+  const float wh = w[int64_t(row) * CSA2_HI + my_head];
+  const bool odd = (j & 1) != 0, second = (j & 2) != 0;
+
+  const uint16_t* kbase = KI + int64_t(b) * key_stride_rows * CSA2_DI + 16 * j;
+  float* srow = scores + int64_t(row) * ld;
+
+  for (int64_t base = c0 + warp * kPosPerWarpIt; base < c1; base += kPosPerCtaIt) {
+    uint4 kv[kU][2];
+    bool ok[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t t = base + u * 4 + sub;
+      const int64_t pos = (t < nv && t < c1) ? (kCand ? int64_t(crow[t]) : t) : -1;
+      ok[u] = pos >= 0 && pos < key_stride_rows;
+      if (kCand && t < nv && t < c1 && !ok[u] && j == 0) atomicOr(flags, CSA2_FLAG_INDEX_OOB);
+      if (ok[u]) {
+        const uint16_t* kp = kbase + pos * CSA2_DI;
+        kv[u][0] = ld_stream16(kp);
+        kv[u][1] = ld_stream16(kp + 8);
+      } else {
+        kv[u][0] = make_uint4(0, 0, 0, 0);
+        kv[u][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t kw[8] = {kv[u][0].x, kv[u][0].y, kv[u][0].z, kv[u][0].w,
+                              kv[u][1].x, kv[u][1].y, kv[u][1].z, kv[u][1].w};
+      float P[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc = __fmaf_rn(qf[h][2 * e], bf16lo(kw[e]), acc);
+          acc = __fmaf_rn(qf[h][2 * e + 1], bf16hi(kw[e]), acc);
+        }
+        P[h] = acc;
+      }
+      // step 1 (lanes j, j^1): even lanes keep heads 0,1, odd lanes keep heads 2,3
+      const float s0 = odd ? P[0] : P[2], s1 = odd ? P[1] : P[3];
+      const float k0 = odd ? P[2] : P[0], k1 = odd ? P[3] : P[1];
+      const float A0 = __fadd_rn(k0, __shfl_xor_sync(0xffffffffu, s0, 1));
+      const float A1 = __fadd_rn(k1, __shfl_xor_sync(0xffffffffu, s1, 1));
+      // step 2 (lanes j, j^2): keep one head of the pair
+      const float sendB = second ? A0 : A1, keepB = second ? A1 : A0;
+      const float Bv = __fadd_rn(keepB, __shfl_xor_sync(0xffffffffu, sendB, 2));
+      // step 3 (lanes j, j^4): the two halves of the channels
+      const float dot = __fadd_rn(Bv, __shfl_xor_sync(0xffffffffu, Bv, 4));
+      const float r = dot > 0.0f ? dot : 0.0f;
+      const float m = __fmul_rn(wh, r);
+      const float m2 = __fadd_rn(m, __shfl_xor_sync(0xffffffffu, m, 2));  // heads (0,1) / (2,3)
+      const float s = __fadd_rn(m2, __shfl_xor_sync(0xffffffffu, m2, 1));
+      const int64_t t = base + u * 4 + sub;
+      if (j == 0 && t < c1) srow[t] = ok[u] ? s : -INFINITY;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
+                               int64_t key_stride_rows, const int32_t* lens, int64_t cap_entries,
+                               int block_div, const int32_t* cand, const int32_t* cand_len,
+                               int64_t n_cand, int ratio, const int32_t* q_pos, float* scores,
+                               int64_t ld, int32_t* n_valid, cudaStream_t st) {
+  const int64_t rows = int64_t(B) * Nq;
+  if (rows == 0 || ld == 0) return cudaSuccess;
+  // chunk: a multiple of the CTA step, sized for at least ~8 CTAs per SM over the grid
+  int64_t chunk = (rows * ld + 152 * 8 - 1) / (152 * 8);
+  chunk = ((chunk + kPosPerCtaIt - 1) / kPosPerCtaIt) * kPosPerCtaIt;
+  chunk = max(int64_t(kPosPerCtaIt), min(chunk, int64_t(2048)));
+  const dim3 grid(unsigned((ld + chunk - 1) / chunk), unsigned(rows));
+  unsigned int* flags = device_flags_ptr();
+  if (!flags) return cudaErrorUnknown;
+  if (cand)
+    index_score_kernel<true><<<grid, kThreads, 0, st>>>(qI, w, Nq, KI, key_stride_rows, lens,
+                                                        cap_entries, block_div, cand, cand_len, n_cand,
+                                                        ratio, q_pos, scores, ld, n_valid, chunk, flags);
+  else
+    index_score_kernel<false><<<grid, kThreads, 0, st>>>(qI, w, Nq, KI, key_stride_rows, lens,
+                                                         cap_entries, block_div, nullptr, nullptr, 0,
+                                                         ratio, q_pos, scores, ld, n_valid, chunk,
+                                                         flags);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2
+
+extern "C" csa2_status csa2_index_score(const uint16_t* qI, const float* w, int B, int Nq,
+                                        const uint16_t* KI, int64_t cap, const int32_t* lens,
+                                        const int32_t* cand, const int32_t* cand_len, int64_t n_cand,
+                                        int ratio, const int32_t* q_pos, float* scores,
+                                        int32_t* n_valid, csa2_stream_t stream) {
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (B < 0 || Nq < 0 || cap < 0 || ratio < 1) return CSA2_ERR_INVALID_ARG;
+  if (int64_t(B) * Nq > 65535) return CSA2_ERR_UNSUPPORTED;  // grid.y limit
+  if (int64_t(B) * Nq == 0) return CSA2_OK;
+  if (!qI || !w || !KI || !lens || !scores || !al16(qI) || !al16(KI)) return CSA2_ERR_INVALID_ARG;
+  if (cand && (!cand_len || n_cand < 0)) return CSA2_ERR_INVALID_ARG;
+  const int64_t ld = cand ? n_cand : cap;
+  return csa2::launch_index_score(qI, w, B, Nq, KI, cap, lens, cap, 1, cand, cand_len, n_cand, ratio,
+                                  q_pos, scores, ld, n_valid,
+                                  reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CSA2_OK
+             : CSA2_ERR_CUDA;
+}

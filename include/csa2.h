@@ -1,0 +1,279 @@
+/*
+ * csa2.h - C ABI of the CSA2 step library (libcsa2.so): Compressed Sparse Attention 2 over an
+ * FP4 main-KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The method (DeepSeek-V4.1-Flash, as described on the web pages cited below):
+ *  - every attention layer is statically Full, Reindex or Reuse; Full selects fresh Top-512
+ *    indices with its indexer Q against cached indexer K, Reindex rescores the same cache with
+ *    its own indexer Q, Reuse takes the latest indices and skips the indexer
+ *    (ai-maestro.online "DeepSeek AI released DeepSeek-V4.1-Flash with 1M context, FP4",
+ *    section "Compressed Sparse Attention 2"; wpnews.pro "DeepSeek V4.1 Flash Specs: KV Cache
+ *    Compression Explained", section "What is Compressed Sparse Attention 2 CSA2?");
+ *  - a Hierarchical Sparse Indexer lets the Full layer keep 2,048 blocks of eight tokens, a
+ *    pool of up to 16,384 positions that later Reindex layers score instead of the whole
+ *    context (same ai-maestro section; kongchang.com "DeepSeek V4.1 Flash Deep Dive",
+ *    section "Compressed Absorption Attention (2nd Gen)");
+ *  - main KV is stored as E2M1 codes with one E4M3 scale per 16 channels, NVFP4 without its
+ *    global scale (ai-maestro section "FP4 KV, Bounded Replay, and other extensions");
+ *  - every layer keeps its own main Q and a 128-token sliding-window KV (ai-maestro sections
+ *    "Causal Encoder-Decoder architecture" and "Compressed Sparse Attention 2").
+ * The pages give no dimensions, score formula or rounding rules.  This library fixes them:
+ *   d = 512 latent channels shared as K and V, 16 main heads, indexer Q of 4 heads x 128 bf16
+ *   with fp32 head weights, score s_t = sum_h w_h * relu(qI_h . KI_t) in a fixed fp32 order,
+ *   Top-K ties broken by the lower position, scale byte = E4M3_RNE_satfinite(amax / 6).
+ *
+ * Conventions (all entry points):
+ *  - Pointers are DEVICE pointers owned by the caller, unless stated otherwise.  The library
+ *    never allocates device memory and never synchronises, except csa2_device_flags().
+ *  - bf16 tensors are passed as uint16_t bit patterns; all arrays are contiguous, row-major,
+ *    and 16-byte aligned (checked: misalignment returns CSA2_ERR_INVALID_ARG).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream).  Argument errors are reported synchronously by the return value and launch
+ *    nothing.  Launch failures return CSA2_ERR_CUDA (from cudaGetLastError).
+ *  - Data-dependent problems found on the device (a cache row outside [0, cap), a selected
+ *    index outside the cache) are skipped, never dereferenced, and recorded as bits in a
+ *    per-device flag word read by csa2_device_flags().
+ *  - Scratch memory, where an entry point needs it, is the caller's `ws` buffer of at least
+ *    csa2_workspace_size() bytes.
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* csa2_stream_t; /* cudaStream_t */
+typedef struct CUevent_st* csa2_event_t;   /* cudaEvent_t  */
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1, /* null/misaligned pointer, size out of range              */
+  CSA2_ERR_UNSUPPORTED = 2, /* a dimension other than the fixed ones below              */
+  CSA2_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed              */
+  CSA2_ERR_WORKSPACE = 4,   /* ws is NULL or smaller than csa2_workspace_size()         */
+} csa2_status;
+
+/* Fixed dimensions. */
+#define CSA2_D 512          /* main latent channels (K = V)                      */
+#define CSA2_GROUP 16       /* channels per E4M3 scale                           */
+#define CSA2_CODE_BYTES 256 /* packed E2M1 bytes per cache row                   */
+#define CSA2_SCALE_BYTES 32 /* E4M3 scale bytes per cache row                    */
+#define CSA2_H 16           /* main heads                                        */
+#define CSA2_HI 4           /* indexer heads                                     */
+#define CSA2_DI 128         /* indexer width                                     */
+#define CSA2_BLOCK 8        /* tokens per block of the hierarchical indexer      */
+#define CSA2_MAX_K 2048     /* largest Top-K (blocks kept by the pool)           */
+#define CSA2_MAX_ATTN_K 512 /* largest number of selected rows attended          */
+#define CSA2_MAX_W 128      /* largest sliding window                            */
+#define CSA2_MAX_LAYERS 16  /* layers per group descriptor                       */
+
+/* Layer modes (ai-maestro "Compressed Sparse Attention 2"). */
+#define CSA2_MODE_FULL 0
+#define CSA2_MODE_REINDEX 1
+#define CSA2_MODE_REUSE 2
+
+/* Device flag bits (csa2_device_flags). */
+#define CSA2_FLAG_APPEND_OOB 1u /* an appended row fell outside [0, cap): row skipped   */
+#define CSA2_FLAG_INDEX_OOB 2u  /* a selected index was >= cap: row treated as empty    */
+
+/*
+ * FP4 quantise-and-append.  "Main key-value cache quantises to E2M1 with one E4M3 scale per
+ * 16 channels ... NVFP4 without its global scale" (ai-maestro "FP4 KV, Bounded Replay, and
+ * other extensions"); quantised as it is written, without a separate pass (wpnews.pro TL;DR).
+ *   x       bf16 [B][n_new][d], d must be 512.
+ *   codes   uint8 [B][cap][256]: byte i of a row holds channel 2i in its low nibble and
+ *           channel 2i+1 in its high nibble, E2M1 (sign, 2-bit exponent bias 1, 1 mantissa).
+ *   scales  uint8 [B][cap][32]: E4M3 (FN) scale of channels 16g..16g+15.
+ *   offsets int32 [B] or NULL: row r of sequence b is written to cache row offsets[b] + r
+ *           (NULL: row r).  Rows outside [0, cap) are skipped (CSA2_FLAG_APPEND_OOB).
+ * Per group: s8 = E4M3_RNE_satfinite(fp32(amax / 6)); code_i = E2M1_RNE_satfinite(fp32(x_i / s))
+ * with s the decoded scale; s == 0 gives all-zero codes; the code's sign bit is x_i's sign.
+ */
+csa2_status csa2_fp4_quantize_append(const uint16_t* x, int B, int n_new, int d, uint8_t* codes,
+                                     uint8_t* scales, int64_t cap, const int32_t* offsets,
+                                     csa2_stream_t stream);
+
+/*
+ * FP4 dequantisation of `rows` cache rows: out[r][c] = E2M1(code) * E4M3(scale), exact in bf16.
+ *   codes [rows][256], scales [rows][32] -> out bf16 [rows][512].  d must be 512.
+ */
+csa2_status csa2_fp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows, int d,
+                                uint16_t* out, csa2_stream_t stream);
+
+/*
+ * Lightning-indexer scores of indexer Q against cached indexer K ("Full: ... projects the
+ * indexer K ... selects fresh Top-512", "Reindex: ... rescores them with its own indexer Q",
+ * ai-maestro "Compressed Sparse Attention 2").  s_t = sum_h w_h * relu(qI_h . KI_t), in the
+ * fixed fp32 order: per head eight fused-multiply-add chains over channels 16j..16j+15 from
+ * +0, combined as ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)); relu; (w0 r0 + w1 r1) + (w2 r2 + w3 r3).
+ *   qI      bf16 [B][Nq][4][128];  w fp32 [B][Nq][4];  KI bf16 [B][cap][128]
+ *   lens    int32 [B]: entries T_b present in sequence b's cache (clamped to cap).
+ *   ratio   tokens per cache entry (>= 1); query i of sequence b sits at token position
+ *           q_pos[b*Nq+i] (q_pos may be NULL: position ratio*T_b - Nq + i) and sees entry j
+ *           iff ratio*j + ratio - 1 <= its position (causal mask over compressed entries).
+ *   cand    NULL: row r of `scores` is [cap] and entry t holds the score of cache entry t.
+ *           else int32 [B*Nq][n_cand] ascending cache positions (a pool) with cand_len[B*Nq]
+ *           valid entries; entry i of the row holds the score of position cand[r][i].
+ *   scores  fp32 [B*Nq][cap or n_cand]: the visible entries form a prefix of length
+ *           n_valid[r] (nullable output); the rest of the row is set to -inf.
+ */
+csa2_status csa2_index_score(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
+                             int64_t cap, const int32_t* lens, const int32_t* cand,
+                             const int32_t* cand_len, int64_t n_cand, int ratio,
+                             const int32_t* q_pos, float* scores, int32_t* n_valid,
+                             csa2_stream_t stream);
+
+/*
+ * Exact Top-K per row ("selects fresh Top-512 indices", ai-maestro "Compressed Sparse
+ * Attention 2"; Top-2,048 blocks for the pool).  Larger score first, equal scores (with -0 ==
+ * +0) by lower column; the selected columns are returned in ascending order, padded with -1.
+ *   scores  fp32 [rows][ld]; row r uses columns [0, n_valid[r]) (n_valid NULL: [0, n)), n <= ld.
+ *           Scores must not be NaN.
+ *   k       1..2048.
+ *   map     NULL, or int32 [rows][map_ld]: output map[r][col] instead of col (an ascending map
+ *           such as a pool keeps the output ascending).
+ *   idx     int32 [rows][k];  n_sel int32 [rows] (nullable): min(k, valid columns).
+ *   ws      workspace of csa2_workspace_size(CSA2_OP_TOPK, ...) bytes (currently 0: may be NULL).
+ */
+csa2_status csa2_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
+                      int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,
+                      void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/*
+ * Block keys of the hierarchical indexer: key of block j = bf16_RNE(0.125 * sum of indexer keys
+ * 8j .. 8j+7, summed in token order in fp32), for the complete blocks j < lens[b] / 8 of each
+ * sequence (ai-maestro "Compressed Sparse Attention 2": "2,048 blocks of eight tokens").
+ *   KI bf16 [B][cap][128] -> block_keys bf16 [B][cap/8][128].  Other rows are not written.
+ */
+csa2_status csa2_block_keys_build(const uint16_t* KI, int B, int64_t cap, const int32_t* lens,
+                                  uint16_t* block_keys, csa2_stream_t stream);
+
+/*
+ * Hierarchical pool of the Full layer: score the visible complete blocks of each query with
+ * its indexer Q (same score as csa2_index_score), keep the top min(keep, blocks) blocks (ties
+ * to the lower block) and expand them into ascending token positions.
+ *   block_keys bf16 [B][cap/8][128]; lens, ratio, q_pos as csa2_index_score.
+ *   pool int32 [B*Nq][keep*8] (-1 padded), pool_len int32 [B*Nq].  keep in 1..2048.
+ *   ws   csa2_workspace_size(CSA2_OP_BLOCK_POOL, ...) bytes.
+ */
+csa2_status csa2_block_pool(const uint16_t* qI, const float* w, int B, int Nq,
+                            const uint16_t* block_keys, int64_t cap, const int32_t* lens, int ratio,
+                            const int32_t* q_pos, int keep, int32_t* pool, int32_t* pool_len,
+                            void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/*
+ * Sparse attention of each query's 16 heads over its selected FP4 rows plus its sliding-window
+ * rows ("Every layer retains its own main Q and sliding-window key-value cache", ai-maestro
+ * "Compressed Sparse Attention 2"; 128-token window, "Causal Encoder-Decoder architecture").
+ * K = V = the dequantised row; softmax over the union of the rows (a token in both sets
+ * counts twice); split-KV over the rows with an online-softmax combine.
+ *   q      bf16 [B][Nq][16][512]
+ *   idx    int32 [B*Nq][k] cache positions (k <= 512); entries < 0, or at or past n_valid[r]
+ *          (n_valid nullable), are empty.  Positions >= cap are treated as empty and flagged.
+ *   swa    bf16 [B][W-1+Nq][512] or NULL (no window); query i attends rows i .. i+W-1, of which
+ *          rows >= (W-1+Nq) - swa_len[b] hold tokens (swa_len int32 [B]).  W <= 128.
+ *   out    bf16 [B][Nq][16][512];  lse fp32 [B][Nq][16] (nullable), natural log; a query with
+ *          no rows gets out = 0 and lse = -inf.
+ *   n_split  split-KV factor, 0 = chosen from the problem size.
+ *   ws     csa2_workspace_size(CSA2_OP_SPARSE_ATTN, ...) bytes for the chosen split.
+ */
+csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq, const uint8_t* codes,
+                                    const uint8_t* scales, int64_t cap, const int32_t* idx,
+                                    const int32_t* n_valid, int k, const uint16_t* swa,
+                                    const int32_t* swa_len, int W, float softmax_scale,
+                                    uint16_t* out, float* lse, int n_split, void* ws,
+                                    size_t ws_bytes, csa2_stream_t stream);
+
+/*
+ * One CSA2 layer group (ai-maestro "Compressed Sparse Attention 2": Full / Reindex / Reuse,
+ * groups such as 1 Full + 3 Reuse, 1 Full + 5 Reuse, Reindex + 3 Reuse).  Layers run in order:
+ *   FULL     optionally appends the step's new rows first (kv_new -> FP4 cache rows and ki_new
+ *            -> indexer-K rows at lens[b] - n_new .. lens[b] - 1, refreshing completed block
+ *            keys when hierarchical), then scores (pool: blocks first) and selects Top-K.
+ *   REINDEX  rescores with its own qI / w: the pool of the latest Full layer when hierarchical
+ *            (pool / pool_len hold it, possibly from an earlier group), else all visible
+ *            entries; selects Top-K.
+ *   REUSE    attends with the latest layer's indices; no scoring.
+ * Every layer attends with its own q and window.  The first layer must be FULL or REINDEX.
+ */
+typedef struct csa2_group_desc {
+  int n_layers;                       /* 1 .. CSA2_MAX_LAYERS                            */
+  int modes[CSA2_MAX_LAYERS];         /* CSA2_MODE_* per layer                           */
+  int B, Nq;                          /* sequences, queries per sequence                 */
+  int K;                              /* selected rows per query, 1..512                 */
+  int W;                              /* window, 0..128                                  */
+  int ratio;                          /* tokens per cache entry, >= 1                    */
+  int hierarchical;                   /* 0: flat indexer, 1: block pool                  */
+  int n_blocks_keep;                  /* blocks kept by the pool, 1..2048                */
+  int n_split;                        /* attention split, 0 = automatic                  */
+  int n_new;                          /* rows appended by the Full layer (0: none)       */
+  int64_t cap;                        /* cache capacity (entries) per sequence           */
+  const int32_t* lens;                /* [B] entries present (after the append)          */
+  const int32_t* q_pos;               /* [B*Nq] query token positions, or NULL           */
+  uint8_t* codes;                     /* [B][cap][256] FP4 main KV                       */
+  uint8_t* scales;                    /* [B][cap][32]                                    */
+  uint16_t* KI;                       /* [B][cap][128] indexer keys                      */
+  uint16_t* block_keys;               /* [B][cap/8][128] (hierarchical)                  */
+  const uint16_t* kv_new;             /* [B][n_new][512] bf16, or NULL                   */
+  const uint16_t* ki_new;             /* [B][n_new][128] bf16, or NULL                   */
+  const uint16_t* q[CSA2_MAX_LAYERS];  /* [B][Nq][16][512]                               */
+  const uint16_t* qI[CSA2_MAX_LAYERS]; /* [B][Nq][4][128]  (FULL / REINDEX)              */
+  const float* w[CSA2_MAX_LAYERS];     /* [B][Nq][4]       (FULL / REINDEX)              */
+  const uint16_t* swa[CSA2_MAX_LAYERS];/* [B][W-1+Nq][512] or NULL                       */
+  const int32_t* swa_len;             /* [B] valid window rows                           */
+  uint16_t* out[CSA2_MAX_LAYERS];     /* [B][Nq][16][512]                                */
+  float* lse[CSA2_MAX_LAYERS];        /* [B][Nq][16] or NULL                             */
+  int32_t* idx[CSA2_MAX_LAYERS];      /* [B*Nq][K]: written by FULL / REINDEX (required),
+                                         for REUSE a copy of the reused indices if non-NULL */
+  int32_t* pool;                      /* [B*Nq][keep*8] (hierarchical)                   */
+  int32_t* pool_len;                  /* [B*Nq]         (hierarchical)                   */
+  float softmax_scale;                /* e.g. 1/sqrt(512)                                */
+  csa2_event_t ev_score_begin;        /* optional: recorded before / after the first     */
+  csa2_event_t ev_score_end;          /*   scoring kernel of the group (profiling)       */
+} csa2_group_desc;
+
+csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_t ws_bytes,
+                            csa2_stream_t stream);
+
+/* Workspace sizing. */
+#define CSA2_OP_TOPK 1
+#define CSA2_OP_BLOCK_POOL 2
+#define CSA2_OP_SPARSE_ATTN 3
+#define CSA2_OP_GROUP_STEP 4
+
+typedef struct csa2_dims {
+  int B, Nq;
+  int64_t cap;          /* cache capacity per sequence                        */
+  int64_t n;            /* CSA2_OP_TOPK: columns per row                      */
+  int k;                /* Top-K / selected rows                              */
+  int W;                /* window                                             */
+  int n_split;          /* CSA2_OP_SPARSE_ATTN / GROUP_STEP: 0 = automatic    */
+  int hierarchical;     /* CSA2_OP_GROUP_STEP                                 */
+  int n_blocks_keep;    /* CSA2_OP_BLOCK_POOL / GROUP_STEP                    */
+} csa2_dims;
+
+/* Bytes of workspace `op` needs for `dims` (0 if none); 0 with dims == NULL. */
+size_t csa2_workspace_size(int op, const csa2_dims* dims);
+
+/* Split-KV factor the library picks for `instances` (= B*Nq) attention queries of k rows. */
+int csa2_attn_auto_split(int64_t instances, int k, int W);
+
+/* sizeof(csa2_group_desc) as compiled into the library (lets bindings check their layout). */
+size_t csa2_group_desc_size(void);
+
+/* Static text for a status code. */
+const char* csa2_status_string(csa2_status s);
+
+/* Synchronises `stream`, returns the current device's flag word (CSA2_FLAG_*) in *flags (a
+ * HOST pointer) and clears it when `clear` is nonzero. */
+csa2_status csa2_device_flags(uint32_t* flags, int clear, csa2_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H_ */

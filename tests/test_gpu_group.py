@@ -1,0 +1,96 @@
+"""GPU parity of the whole CSA2 layer-group step against the oracle: bit-exact indices (and pools)
+for every layer, attention outputs within tolerance.  Covers the single Full-layer decode at
+T = 4096, decode groups with Reuse and Reindex layers and ragged contexts (the step appends the
+new token itself), hierarchical pools with Reindex layers, a ratio-2 prefill chunk, and the two
+full-size decode workloads (batch 64 at 128K; batch 8 at 1M with the pool) on sampled sequences
+in the same launch configuration the benchmark times."""
+import numpy as np
+import pytest
+
+import csa2_synth as syn
+from tests._cases import GroupCase
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+F, RX, R = 0, 1, 2
+
+
+def test_full_layer_decode_b1_t4096(orc):
+    gc = GroupCase(syn.SEEDS["full_layer_decode_b1_t4096"], [4096], [F])
+    gc.run()
+    gc.check(orc)
+
+
+def test_decode_group_ragged_with_reuse(orc):
+    gc = GroupCase(51, [5000, 4096, 700, 300, 9], [F, R, R, R])
+    gc.run()
+    ref = gc.check(orc)
+    for l in (1, 2, 3):
+        assert np.array_equal(ref["idx"][l], ref["idx"][0])
+
+
+def test_decode_group_with_reindex_and_split_counts(orc):
+    gc = GroupCase(52, [3000, 2049], [F, R, RX, R])
+    for ns in (1, 7):
+        gc.run(n_split=ns)
+        gc.check(orc)
+
+
+def test_hierarchical_group_pool_and_reindex(orc):
+    # block count above and below the 2048 kept; T % 8 == 0 (the append completes a block) and not
+    gc = GroupCase(53, [8 * 3000, 8 * 2300 + 5, 8 * 900], [F, RX, R, R, R], hierarchical=True)
+    gc.run()
+    gc.check(orc)
+
+
+def test_group_starting_with_reindex_reuses_pool(orc):
+    gc = GroupCase(54, [8 * 2600], [F, R], hierarchical=True)
+    gc.run()
+    pool = gc.pool.clone()
+    gc2 = GroupCase(54, [8 * 2600], [RX, R, R], hierarchical=True, append=False)
+    gc2.pool.copy_(pool)
+    gc2.pool_len.copy_(gc.pool_len)
+    gc2.run()
+    torch.cuda.synchronize()
+    assert torch.equal(gc2.pool, pool)
+    # Reindex over the kept pool equals the oracle's Reindex of the group [F, RX]
+    gc3 = GroupCase(54, [8 * 2600], [F, RX], hierarchical=True, append=False)
+    ref = gc3.oracle(orc)
+    # layer 0 of gc2 used its own qI (tensor id T_QI + 0) like layer 1 of gc3 uses T_QI + 1: compare
+    # by running the oracle's Reindex with gc2's layer-0 inputs instead
+    qI0 = gc2.h_qI(0, 0)
+    w0 = gc2.h_w(0, 0)
+    KI = gc2.h_ki(0)[: 8 * 2600]
+    p = ref["pool"][0, 0][: ref["pool_len"][0, 0]]
+    s = orc.index_score(qI0[0], w0[0], KI, pos=p)
+    exp, _ = orc.topk(s, 512, p)
+    assert np.array_equal(gc2.idx[0].cpu().numpy()[0], exp)
+
+
+def test_prefill_chunk_ratio2_causal(orc):
+    Nq, T = 24, 300
+    q_pos = np.arange(2 * T - Nq, 2 * T, dtype=np.int32)[None]      # the last 24 of 600 tokens
+    gc = GroupCase(55, [T], [F, R, R], Nq=Nq, ratio=2, K=128, W=32, append=False, q_pos=q_pos)
+    gc.run()
+    gc.check(orc)
+
+
+def test_decode_group_full_size_b64_t131072(orc):
+    """Batched decode workload: batch 64, 128K context, 1 Full + 3 Reuse, sampled sequences."""
+    gc = GroupCase(syn.SEEDS["decode_group_1f3r_b64_t131072"], [131072] * 64, [F, R, R, R],
+                   host_seqs=[0, 63])
+    gc.run()
+    gc.check(orc, seqs=[0, 63], threads=2)
+
+
+def test_hier_decode_full_size_b8_t1m(orc):
+    """Hierarchical decode workload: batch 8, 1M context, Full + Reindex + 3 Reuse, one sampled
+    sequence (the pool, both layers' indices and all outputs)."""
+    gc = GroupCase(syn.SEEDS["hier_decode_b8_t1m"], [1 << 20] * 8, [F, RX, R, R, R], hierarchical=True,
+                   host_seqs=[5])
+    gc.run()
+    gc.check(orc, seqs=[5])
