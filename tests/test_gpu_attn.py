@@ -86,7 +86,7 @@ def test_decode_attention_ragged(orc, n_split):
 
 
 def test_multi_query_windows_and_no_window(orc):
-    B, Nq, cap, k, W = 2, 5, 400, 512 - 64, 16
+    B, Nq, cap, k, W = 2, 5, 600, 512 - 64, 16
     kv, q, swa, idx = _case(42, B, Nq, cap, k, W)
     swa_len = np.array([W - 1 + Nq, 9], np.int32)
     got, glse = _run(kv, q, swa, idx, None, swa_len, W, 0)

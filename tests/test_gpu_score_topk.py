@@ -65,6 +65,7 @@ def test_scores_causal_ratio2_and_pool(orc):
     for r in range(B * Nq):
         cand[r, :clen[r]] = np.sort(g.choice(lens[r // Nq], clen[r], replace=False))
     sc = torch.zeros((B * Nq, n_cand), device="cuda")
+    nv = torch.zeros(B * Nq, dtype=torch.int32, device="cuda")
     c.csa2_index_score(bf16_dev(qI), to_dev(w), bf16_dev(KI), to_dev(np.array(lens, np.int32)), sc,
                        cand=to_dev(cand), cand_len=to_dev(clen), ratio=2, q_pos=to_dev(q_pos.reshape(-1)),
                        n_valid=nv)
