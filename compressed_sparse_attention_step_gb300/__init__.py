@@ -182,16 +182,20 @@ def csa2_index_score(qI, w, KI, lens, scores, *, cand=None, cand_len=None, ratio
         _ptr(n_valid, "n_valid", (torch.int32,)), _stream(stream)))
 
 
-def csa2_topk(scores, k, idx, *, n_valid=None, n=None, map_=None, n_sel=None, stream=None):
+def csa2_topk(scores, k, idx, *, n_valid=None, n=None, map_=None, n_sel=None, ws=None, stream=None):
     """scores fp32 [rows, ld] -> idx int32 [rows, k] (ascending, -1 padded)."""
     torch = _torch()
     rows, ld = scores.shape
     n = ld if n is None else n
     map_ld = map_.shape[-1] if map_ is not None else 0
+    need = workspace_size(OP_TOPK, B=rows, Nq=1, n=n, k=k)
+    if ws is None and need:
+        ws = _ws(need, scores.device)
     _check("csa2_topk", lib().csa2_topk(
         _ptr(scores, "scores", (torch.float32,)), rows, n, ld, _ptr(n_valid, "n_valid", (torch.int32,), rows),
         k, _ptr(map_, "map", (torch.int32,)), map_ld, _ptr(idx, "idx", (torch.int32,), rows * k),
-        _ptr(n_sel, "n_sel", (torch.int32,), rows), None, 0, _stream(stream)))
+        _ptr(n_sel, "n_sel", (torch.int32,), rows), _ptr(ws, "ws"), 0 if ws is None else ws.numel(),
+        _stream(stream)))
 
 
 def csa2_block_keys_build(KI, lens, block_keys, stream=None):

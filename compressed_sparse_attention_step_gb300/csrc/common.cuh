@@ -135,9 +135,12 @@ cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq
                                int block_div, const int32_t* cand, const int32_t* cand_len,
                                int64_t n_cand, int ratio, const int32_t* q_pos, float* scores,
                                int64_t ld, int32_t* n_valid, cudaStream_t st);
+// Exact Top-K of `rows` score rows.  Rows longer than one slice are spread over several CTAs and
+// need workspace (topk_ws_bytes); ws may be NULL when topk_ws_bytes(...) == 0.
+size_t topk_ws_bytes(int rows, int64_t n);
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
                         int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,
-                        int expand8, int32_t* pool_len, cudaStream_t st);
+                        int expand8, int32_t* pool_len, void* ws, cudaStream_t st);
 cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
                                const uint8_t* scales, int64_t cap, const int32_t* idx,
                                const int32_t* n_valid, int k, const uint16_t* swa,

@@ -34,7 +34,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct GroupWs {
-  size_t scores_off, nv_off, attn_off, total;
+  size_t scores_off, nv_off, topk_off, attn_off, total;
   int64_t score_ld;
 };
 
@@ -46,7 +46,8 @@ GroupWs group_ws_layout(int B, int Nq, int64_t cap, int K, int W, int hierarchic
   L.score_ld = ld;
   L.scores_off = 0;
   L.nv_off = align256(size_t(rows) * size_t(ld) * sizeof(float));
-  L.attn_off = L.nv_off + align256(size_t(rows) * sizeof(int32_t));
+  L.topk_off = L.nv_off + align256(size_t(rows) * sizeof(int32_t));
+  L.attn_off = L.topk_off + align256(topk_ws_bytes(int(rows), ld));
   const int ns = n_split ? n_split : attn_auto_split(rows, K, W);
   L.total = L.attn_off + align256(attn_ws_bytes(rows, ns));
   return L;
@@ -62,9 +63,11 @@ extern "C" size_t csa2_workspace_size(int op, const csa2_dims* d) {
   const int64_t rows = int64_t(d->B) * d->Nq;
   switch (op) {
     case CSA2_OP_TOPK:
-      return 0;
-    case CSA2_OP_BLOCK_POOL:
-      return csa2::align256(size_t(rows) * size_t(std::max<int64_t>(d->cap / CSA2_BLOCK, 1)) * sizeof(float));
+      return csa2::topk_ws_bytes(int(rows), d->n);
+    case CSA2_OP_BLOCK_POOL: {
+      const int64_t nb = std::max<int64_t>(d->cap / CSA2_BLOCK, 1);
+      return csa2::align256(size_t(rows) * size_t(nb) * sizeof(float)) + csa2::topk_ws_bytes(int(rows), nb);
+    }
     case CSA2_OP_SPARSE_ATTN: {
       const int W = d->W;
       const int ns = d->n_split ? d->n_split : csa2::attn_auto_split(rows, d->k, W);
@@ -139,7 +142,8 @@ extern "C" csa2_status csa2_block_pool(const uint16_t* qI, const float* w, int B
   if (csa2::launch_index_score(qI, w, B, Nq, block_keys, nb, lens, cap, CSA2_BLOCK, nullptr, nullptr, 0,
                                ratio, q_pos, sc, nb, pool_len, st) != cudaSuccess)
     return CSA2_ERR_CUDA;
-  if (csa2::launch_topk(sc, int(rows), nb, nb, pool_len, keep, nullptr, 0, pool, nullptr, 1, pool_len, st) !=
+  void* tws = static_cast<char*>(ws) + csa2::align256(size_t(rows) * size_t(nb) * sizeof(float));
+  if (csa2::launch_topk(sc, int(rows), nb, nb, pool_len, keep, nullptr, 0, pool, nullptr, 1, pool_len, tws, st) !=
       cudaSuccess)
     return CSA2_ERR_CUDA;
   return CSA2_OK;
@@ -189,6 +193,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   char* wsb = static_cast<char*>(ws);
   float* scores = reinterpret_cast<float*>(wsb + lay.scores_off);
   int32_t* nv = reinterpret_cast<int32_t*>(wsb + lay.nv_off);
+  void* tws = wsb + lay.topk_off;
   float* attn_ws = reinterpret_cast<float*>(wsb + lay.attn_off);
   const int ns = g->n_split ? g->n_split : csa2::attn_auto_split(rows, g->K, g->W);
   const int64_t nb = g->cap / CSA2_BLOCK;
@@ -228,7 +233,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
             if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
               return CSA2_ERR_CUDA;
             if (!ok(csa2::launch_topk(scores, int(rows), nb, nb, g->pool_len, g->n_blocks_keep, nullptr, 0, g->pool,
-                                      nullptr, 1, g->pool_len, st)))
+                                      nullptr, 1, g->pool_len, tws, st)))
               return CSA2_ERR_CUDA;
           } else {
             if (!ok(cudaMemsetAsync(g->pool_len, 0, size_t(rows) * sizeof(int32_t), st))) return CSA2_ERR_CUDA;
@@ -244,7 +249,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
             cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
           return CSA2_ERR_CUDA;
         if (!ok(csa2::launch_topk(scores, int(rows), pool_w, pool_w, nv, g->K, g->pool, pool_w, g->idx[l], nullptr,
-                                  0, nullptr, st)))
+                                  0, nullptr, tws, st)))
           return CSA2_ERR_CUDA;
       } else {
         if (!ok(csa2::launch_index_score(g->qI[l], g->w[l], g->B, g->Nq, g->KI, g->cap, g->lens, g->cap, 1,
@@ -253,7 +258,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
         if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
           return CSA2_ERR_CUDA;
         if (!ok(csa2::launch_topk(scores, int(rows), g->cap, g->cap, nv, g->K, nullptr, 0, g->idx[l], nullptr, 0,
-                                  nullptr, st)))
+                                  nullptr, tws, st)))
           return CSA2_ERR_CUDA;
       }
       first_score = false;

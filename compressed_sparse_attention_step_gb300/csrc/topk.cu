@@ -1,32 +1,37 @@
 // Exact Top-K selection ("selects fresh Top-512 indices", ai-maestro.online "DeepSeek AI released
 // DeepSeek-V4.1-Flash with 1M context, FP4", section "Compressed Sparse Attention 2"; Top-2,048
-// blocks for the hierarchical pool).  Order: larger score first, equal scores by lower column.
+// blocks for the hierarchical pool).  Order: larger score first, equal scores by lower column;
+// the k selected columns are returned in ascending order.
 //
-// One CTA of 1024 threads per row, radix select on ordered 32-bit score keys:
-//  1. histogram of the top 12 key bits over the row (shared-memory atomics);
-//  2. the bin b1 holding the k-th largest key is found with a block scan; every key above b1 is
-//     selected outright (fewer than k of them);
-//  3. fast path (bin b1 holds <= 8192 keys, the common case): one more pass over the row
-//     collects the selected columns and the (key, column) candidates of bin b1 in shared
-//     memory; radix rounds on the low 20 key bits then on the column bits (ascending, so equal
-//     keys go to the lower column) find the exact threshold; the k columns are sorted with a
-//     bitonic network and written ascending;
-//  4. fallback (bin b1 larger, e.g. massive ties): the same radix rounds run over the row in
-//     global memory, and a final ordered pass with a block scan writes the selected columns in
-//     ascending order directly.
-// All counts are integers and the output is a pure function of the scores: deterministic.
+// Radix select on ordered 32-bit score keys (-0 and +0 share a key), in three launches so that a
+// long row is read by many SMs at once:
+//  1. slice histograms: each CTA takes an 8192-key slice of a row and adds a histogram of the top
+//     12 key bits (shared-memory atomics) into the row's global histogram;
+//  2. slice collection: each CTA finds, from the row histogram, the bin b1 that holds the k-th
+//     largest key and appends every key of its slice in a bin >= b1 (at most k - 1 + |b1| keys
+//     per row) to the row's candidate list (warp-aggregated atomic appends);
+//  3. per row: the candidates are loaded into shared memory and radix rounds on the key bits,
+//     then on the column bits (ascending, so equal keys go to the lower column), find the exact
+//     k-th (key, column); the k winners are sorted with a bitonic network and written.
+// A row whose candidates overflow the list (massive ties) is finished by one CTA with the same
+// rounds over the row in global memory and an ordered, scan-based output.  Short rows use that
+// single-CTA path directly.  Counts are integers and every decision is a pure function of the
+// scores, so the result is deterministic.
 #include "common.cuh"
 
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kCap = 8192;  // candidates kept in shared memory
+constexpr int kSelThreads = 1024;    // per-row selection CTA
+constexpr int kSliceThreads = 256;   // slice histogram / collection CTAs
+constexpr int64_t kSlice = 8192;     // keys per slice CTA
+constexpr int kCandCap = 10240;      // candidates per row (>= k - 1 + typical |b1|)
+constexpr int kBins = 4096;          // first-level bins (top 12 key bits)
 
 struct SelSmem {
-  uint32_t hist[4096];
-  uint32_t cand_key[kCap];
-  int32_t cand_col[kCap];
+  uint32_t hist[kBins];
+  uint32_t cand_key[kCandCap];
+  int32_t cand_col[kCandCap];
   int32_t sel[CSA2_MAX_K];
   uint32_t scan_tmp[32];
   uint32_t nsel, ncand;
@@ -34,30 +39,62 @@ struct SelSmem {
   uint32_t run_g, run_e;
 };
 
-__device__ __forceinline__ uint32_t load_key(const float* s, int64_t i) { return score_key(__ldg(s + i)); }
+struct SliceSmem {
+  uint32_t hist[kBins];
+  uint32_t scan_tmp[32];
+  uint32_t res_bin, res_before;
+};
 
-// Find the bin where the cumulative count, walking from the highest bin down (from_top) or from
-// the lowest bin up, first reaches `need` (1 <= need <= total).  Writes sm.res_bin and
-// sm.res_before (count strictly before that bin in walking order).  All threads call it.
-__device__ void find_bin(SelSmem& sm, int nbins, uint32_t need, bool from_top) {
-  const int t = threadIdx.x;
-  const int per = (nbins + kThreads - 1) / kThreads;  // 1..4
-  // thread t owns walk positions [t*per, t*per + per)
+// Visit keys [lo, hi) of a row in tiles of 4 * U * blockDim.x (each thread takes U groups of 4
+// consecutive keys, with 16-byte loads when aligned).  Every thread makes the same number of
+// calls (valid = false past hi), so warp collectives inside f are safe.
+template <int U, class F>
+__device__ __forceinline__ void for_each_key(const float* s, int64_t lo, int64_t hi, F&& f) {
+  const int nt = blockDim.x;
+  for (int64_t base = lo; base < hi; base += int64_t(4) * nt * U) {
+    float v[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i0 = base + (int64_t(u) * nt + threadIdx.x) * 4;
+      if (i0 + 3 < hi && ((reinterpret_cast<uintptr_t>(s + i0) & 15u) == 0)) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(s + i0));
+        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[u][e] = (i0 + e < hi) ? __ldg(s + i0 + e) : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i0 = base + (int64_t(u) * nt + threadIdx.x) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f(i0 + e, score_key(v[u][e]), i0 + e < hi);
+    }
+  }
+}
+
+// Bin where the cumulative count, walking from the highest bin down (from_top) or from the lowest
+// bin up, first reaches need (1 <= need <= total).  Result in *res_bin / *res_before (count
+// strictly before that bin in walking order).  All threads of the block call it.
+__device__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, bool from_top, uint32_t* scan_tmp,
+                         uint32_t* res_bin, uint32_t* res_before) {
+  const int t = threadIdx.x, nt = blockDim.x;
+  const int per = (nbins + nt - 1) / nt;
   uint32_t local = 0;
   for (int e = 0; e < per; ++e) {
     const int wpos = t * per + e;
-    if (wpos < nbins) local += sm.hist[from_top ? nbins - 1 - wpos : wpos];
+    if (wpos < nbins) local += hist[from_top ? nbins - 1 - wpos : wpos];
   }
-  const uint32_t excl = block_exclusive_scan(local, sm.scan_tmp, nullptr);
+  const uint32_t excl = block_exclusive_scan(local, scan_tmp, nullptr);
   if (excl < need && excl + local >= need) {
     uint32_t cum = excl;
     for (int e = 0; e < per; ++e) {
       const int wpos = t * per + e;
       const int bin = from_top ? nbins - 1 - wpos : wpos;
-      const uint32_t h = sm.hist[bin];
+      const uint32_t h = hist[bin];
       if (cum + h >= need) {
-        sm.res_bin = uint32_t(bin);
-        sm.res_before = cum;
+        *res_bin = uint32_t(bin);
+        *res_before = cum;
         break;
       }
       cum += h;
@@ -66,181 +103,174 @@ __device__ void find_bin(SelSmem& sm, int nbins, uint32_t need, bool from_top) {
   __syncthreads();
 }
 
-__device__ __forceinline__ void zero_hist(SelSmem& sm, int nbins) {
-  for (int i = threadIdx.x; i < nbins; i += kThreads) sm.hist[i] = 0;
+__device__ __forceinline__ void zero(uint32_t* h, int n) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) h[i] = 0;
   __syncthreads();
 }
 
-__device__ __forceinline__ int32_t out_value(const int32_t* mrow, int32_t col) {
-  return mrow ? __ldg(mrow + col) : col;
+// Histogram of the top 12 key bits of keys [lo, hi) into h (shared memory).
+__device__ __forceinline__ void hist12(const float* s, int64_t lo, int64_t hi, uint32_t* h) {
+  for_each_key<2>(s, lo, hi, [&](int64_t, uint32_t key, bool valid) {
+    if (valid) atomicAdd(&h[key >> 20], 1u);
+  });
 }
 
-__global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(
-    const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid,
-    int k, const int32_t* __restrict__ map, int64_t map_ld, int32_t* __restrict__ idx,
-    int32_t* __restrict__ n_sel, int expand8, int32_t* __restrict__ pool_len) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
-  const int row = blockIdx.x;
-  const int t = threadIdx.x;
-  const float* s = scores + int64_t(row) * ld;
-  const int32_t* mrow = map ? map + int64_t(row) * map_ld : nullptr;
-  const int64_t nv = n_valid ? min(max(int64_t(n_valid[row]), int64_t(0)), n) : n;
-  __syncthreads();  // every thread has read n_valid before pool_len (possibly the same array) is written
-  const int out_w = expand8 ? k * CSA2_BLOCK : k;
-  int32_t* out = idx + int64_t(row) * out_w;
-
-  auto emit = [&](int slot, int32_t col) {
-    const int32_t v = out_value(mrow, col);
+// Output of one row (optionally through a column -> position map, optionally expanded to the
+// eight positions of each selected block).
+struct RowOut {
+  const int32_t* mrow;
+  int32_t* out;
+  int out_w, expand8;
+  __device__ __forceinline__ void emit(int slot, int32_t col) const {
+    const int32_t v = mrow ? __ldg(mrow + col) : col;
     if (expand8) {
 #pragma unroll
       for (int r = 0; r < CSA2_BLOCK; ++r) out[slot * CSA2_BLOCK + r] = v * CSA2_BLOCK + r;
     } else {
       out[slot] = v;
     }
-  };
-  auto finish = [&](int64_t cnt) {
-    if (t == 0) {
-      if (n_sel) n_sel[row] = int32_t(cnt);
-      if (pool_len) pool_len[row] = int32_t(cnt * (expand8 ? CSA2_BLOCK : 1));
-    }
-    for (int i = int(cnt) * (expand8 ? CSA2_BLOCK : 1) + t; i < out_w; i += kThreads) out[i] = -1;
-  };
-
-  if (nv <= k) {  // everything valid is selected, already ascending
-    for (int i = t; i < nv; i += kThreads) emit(i, i);
-    finish(nv);
-    return;
   }
+};
 
-  // ---- pass 0: histogram of the top 12 key bits --------------------------------------------
-  zero_hist(sm, 4096);
-  for (int64_t i = t; i < nv; i += kThreads) atomicAdd(&sm.hist[load_key(s, i) >> 20], 1u);
-  __syncthreads();
-  find_bin(sm, 4096, uint32_t(k), true);
-  const uint32_t b1 = sm.res_bin;
-  uint32_t need = uint32_t(k) - sm.res_before;  // still to take from bin b1 (>= 1)
-  const uint32_t cnt1 = sm.hist[b1];
-  __syncthreads();
+__device__ void finish_row(const RowOut& o, int64_t cnt, int row, int32_t* n_sel, int32_t* pool_len) {
+  if (threadIdx.x == 0) {
+    if (n_sel) n_sel[row] = int32_t(cnt);
+    if (pool_len) pool_len[row] = int32_t(cnt * (o.expand8 ? CSA2_BLOCK : 1));
+  }
+  for (int i = int(cnt) * (o.expand8 ? CSA2_BLOCK : 1) + threadIdx.x; i < o.out_w; i += blockDim.x) o.out[i] = -1;
+}
 
-  if (cnt1 <= uint32_t(kCap)) {
-    // ---- fast path ---------------------------------------------------------------------------
-    if (t == 0) { sm.nsel = 0; sm.ncand = 0; }
+// The k largest of the nc candidates in shared memory (nc >= k) by (key desc, column asc), sorted
+// by column and emitted.
+__device__ void select_candidates(SelSmem& sm, int nc, int k, const RowOut& o) {
+  const int t = threadIdx.x;
+  uint32_t need = uint32_t(k), prefix = 0, mask = 0;
+  const int kshift[3] = {21, 10, 0}, kwidth[3] = {11, 11, 10};
+  for (int r = 0; r < 3; ++r) {
+    const int nb = 1 << kwidth[r];
+    zero(sm.hist, nb);
+    for (int c = t; c < nc; c += blockDim.x) {
+      const uint32_t key = sm.cand_key[c];
+      if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> kshift[r]) & uint32_t(nb - 1)], 1u);
+    }
     __syncthreads();
-    for (int64_t i = t; i < nv; i += kThreads) {
-      const uint32_t key = load_key(s, i);
-      const uint32_t bin = key >> 20;
-      if (bin > b1) {
-        sm.sel[atomicAdd(&sm.nsel, 1u)] = int32_t(i);
-      } else if (bin == b1) {
-        const uint32_t c = atomicAdd(&sm.ncand, 1u);
+    find_bin(sm.hist, nb, need, true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+    prefix |= sm.res_bin << kshift[r];
+    mask |= uint32_t(nb - 1) << kshift[r];
+    need -= sm.res_before;
+    __syncthreads();
+  }
+  const uint32_t tau = prefix;                       // the k-th largest key
+  const uint32_t nties = sm.hist[sm.res_bin];         // candidates equal to tau
+  __syncthreads();
+  int32_t col_cut = 0x7FFFFFFF;                       // take ties at tau with column <= col_cut
+  if (need < nties) {
+    uint32_t cpre = 0;
+    const int cshift[3] = {20, 10, 0}, cwidth[3] = {11, 10, 10};
+    for (int r = 0; r < 3; ++r) {
+      const int nb = 1 << cwidth[r];
+      zero(sm.hist, nb);
+      const uint32_t hi_mask = (r == 0) ? 0u : (0xFFFFFFFFu << (cshift[r] + cwidth[r]));
+      for (int c = t; c < nc; c += blockDim.x) {
+        const uint32_t col = uint32_t(sm.cand_col[c]);
+        if (sm.cand_key[c] == tau && (col & hi_mask) == cpre)
+          atomicAdd(&sm.hist[(col >> cshift[r]) & uint32_t(nb - 1)], 1u);
+      }
+      __syncthreads();
+      find_bin(sm.hist, nb, need, false, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+      cpre |= sm.res_bin << cshift[r];
+      need -= sm.res_before;
+      __syncthreads();
+    }
+    col_cut = int32_t(cpre);
+  }
+  if (t == 0) sm.nsel = 0;
+  __syncthreads();
+  for (int c = t; c < nc; c += blockDim.x) {
+    const uint32_t key = sm.cand_key[c];
+    if (key > tau || (key == tau && sm.cand_col[c] <= col_cut)) sm.sel[atomicAdd(&sm.nsel, 1u)] = sm.cand_col[c];
+  }
+  __syncthreads();
+  int P = 1;
+  while (P < k) P <<= 1;
+  for (int i = k + t; i < P; i += blockDim.x) sm.sel[i] = 0x7FFFFFFF;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = t; i < P / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = ((lo & size) == 0);
+        const int32_t a = sm.sel[lo], b = sm.sel[hi];
+        if ((a > b) == up) { sm.sel[lo] = b; sm.sel[hi] = a; }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = t; i < k; i += blockDim.x) o.emit(i, sm.sel[i]);
+}
+
+// Whole-row selection by one CTA (short rows, and rows whose candidates overflow).
+__device__ void select_row(SelSmem& sm, const float* s, int64_t nv, int k, const RowOut& o) {
+  const int t = threadIdx.x, lane = t & 31;
+  const unsigned lanes_below = (1u << lane) - 1u;
+  zero(sm.hist, kBins);
+  hist12(s, 0, nv, sm.hist);
+  __syncthreads();
+  find_bin(sm.hist, kBins, uint32_t(k), true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+  const uint32_t b1 = sm.res_bin;
+  const uint32_t ncand = sm.res_before + sm.hist[b1];   // keys in bins >= b1
+  uint32_t need = uint32_t(k) - sm.res_before;
+  __syncthreads();
+  if (ncand <= uint32_t(kCandCap)) {
+    if (t == 0) sm.ncand = 0;
+    __syncthreads();
+    for_each_key<2>(s, 0, nv, [&](int64_t i, uint32_t key, bool valid) {
+      const bool take = valid && (key >> 20) >= b1;
+      const unsigned m = __ballot_sync(0xffffffffu, take);
+      if (!m) return;
+      uint32_t base = 0;
+      if (lane == 0) base = atomicAdd(&sm.ncand, uint32_t(__popc(m)));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (take) {
+        const uint32_t c = base + __popc(m & lanes_below);
         sm.cand_key[c] = key;
         sm.cand_col[c] = int32_t(i);
       }
-    }
+    });
     __syncthreads();
-    const int nc = int(sm.ncand);
-    // rounds on key bits [19:10] and [9:0] (largest first)
-    zero_hist(sm, 1024);
-    for (int c = t; c < nc; c += kThreads) atomicAdd(&sm.hist[(sm.cand_key[c] >> 10) & 1023u], 1u);
-    __syncthreads();
-    find_bin(sm, 1024, need, true);
-    const uint32_t d1 = sm.res_bin;
-    need -= sm.res_before;
-    __syncthreads();
-    zero_hist(sm, 1024);
-    for (int c = t; c < nc; c += kThreads) {
-      const uint32_t key = sm.cand_key[c];
-      if (((key >> 10) & 1023u) == d1) atomicAdd(&sm.hist[key & 1023u], 1u);
-    }
-    __syncthreads();
-    find_bin(sm, 1024, need, true);
-    const uint32_t tau = (b1 << 20) | (d1 << 10) | sm.res_bin;
-    need -= sm.res_before;            // ties at tau to take, lowest columns first
-    const uint32_t nties = sm.hist[sm.res_bin];
-    __syncthreads();
-    int32_t col_cut = 0x7FFFFFFF;     // take ties with column <= col_cut
-    if (need < nties) {
-      // rounds on column bits [30:20], [19:10], [9:0] (smallest first)
-      uint32_t prefix = 0;
-      const int shifts[3] = {20, 10, 0};
-      const int widths[3] = {11, 10, 10};
-      for (int r = 0; r < 3; ++r) {
-        const int nb = 1 << widths[r];
-        zero_hist(sm, nb);
-        const uint32_t hi_mask = (r == 0) ? 0u : (0xFFFFFFFFu << (shifts[r] + widths[r]));
-        for (int c = t; c < nc; c += kThreads) {
-          const uint32_t col = uint32_t(sm.cand_col[c]);
-          if (sm.cand_key[c] == tau && (col & hi_mask) == prefix)
-            atomicAdd(&sm.hist[(col >> shifts[r]) & uint32_t(nb - 1)], 1u);
-        }
-        __syncthreads();
-        find_bin(sm, nb, need, false);
-        prefix |= sm.res_bin << shifts[r];
-        need -= sm.res_before;
-        __syncthreads();
-      }
-      col_cut = int32_t(prefix);
-    }
-    for (int c = t; c < nc; c += kThreads) {
-      const uint32_t key = sm.cand_key[c];
-      if (key > tau || (key == tau && sm.cand_col[c] <= col_cut)) sm.sel[atomicAdd(&sm.nsel, 1u)] = sm.cand_col[c];
-    }
-    __syncthreads();
-    // bitonic sort of the k selected columns (padded to a power of two)
-    int P = 1;
-    while (P < k) P <<= 1;
-    for (int i = k + t; i < P; i += kThreads) sm.sel[i] = 0x7FFFFFFF;
-    __syncthreads();
-    for (int size = 2; size <= P; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = t; i < P / 2; i += kThreads) {
-          const int lo = 2 * i - (i & (stride - 1));
-          const int hi = lo + stride;
-          const bool up = ((lo & size) == 0);
-          const int32_t a = sm.sel[lo], b = sm.sel[hi];
-          if ((a > b) == up) { sm.sel[lo] = b; sm.sel[hi] = a; }
-        }
-        __syncthreads();
-      }
-    }
-    for (int i = t; i < k; i += kThreads) emit(i, sm.sel[i]);
-    finish(k);
+    select_candidates(sm, int(sm.ncand), k, o);
     return;
   }
-
-  // ---- fallback: radix rounds over the row in global memory ------------------------------------
-  zero_hist(sm, 1024);
-  for (int64_t i = t; i < nv; i += kThreads) {
-    const uint32_t key = load_key(s, i);
-    if ((key >> 20) == b1) atomicAdd(&sm.hist[(key >> 10) & 1023u], 1u);
-  }
+  // rounds on key bits [19:10] and [9:0] over the row, then an ordered pass
+  zero(sm.hist, 1024);
+  for_each_key<2>(s, 0, nv, [&](int64_t, uint32_t key, bool valid) {
+    if (valid && (key >> 20) == b1) atomicAdd(&sm.hist[(key >> 10) & 1023u], 1u);
+  });
   __syncthreads();
-  find_bin(sm, 1024, need, true);
-  const uint32_t d1 = sm.res_bin;
+  find_bin(sm.hist, 1024, need, true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+  const uint32_t pre22 = (b1 << 10) | sm.res_bin;
   need -= sm.res_before;
   __syncthreads();
-  zero_hist(sm, 1024);
-  const uint32_t pre22 = (b1 << 10) | d1;
-  for (int64_t i = t; i < nv; i += kThreads) {
-    const uint32_t key = load_key(s, i);
-    if ((key >> 10) == pre22) atomicAdd(&sm.hist[key & 1023u], 1u);
-  }
+  zero(sm.hist, 1024);
+  for_each_key<2>(s, 0, nv, [&](int64_t, uint32_t key, bool valid) {
+    if (valid && (key >> 10) == pre22) atomicAdd(&sm.hist[key & 1023u], 1u);
+  });
   __syncthreads();
-  find_bin(sm, 1024, need, true);
+  find_bin(sm.hist, 1024, need, true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
   const uint32_t tau = (pre22 << 10) | sm.res_bin;
   need -= sm.res_before;  // ties at tau to take, in column order
   if (t == 0) { sm.run_g = 0; sm.run_e = 0; }
   __syncthreads();
-  // ordered output: slot(i) = #(key > tau before i) + min(#(key == tau before i), need)
+  // slot(i) = #(key > tau before i) + min(#(key == tau before i), need)
   constexpr int kItems = 4;
-  for (int64_t base = 0; base < nv; base += int64_t(kThreads) * kItems) {
+  for (int64_t base = 0; base < nv; base += int64_t(blockDim.x) * kItems) {
     uint32_t keys[kItems];
     uint32_t g = 0, e = 0;
 #pragma unroll
     for (int it = 0; it < kItems; ++it) {
       const int64_t i = base + int64_t(t) * kItems + it;
-      keys[it] = (i < nv) ? load_key(s, i) : 0u;
+      keys[it] = (i < nv) ? score_key(__ldg(s + i)) : 0u;
       if (i < nv) { g += keys[it] > tau; e += keys[it] == tau; }
     }
     uint32_t tot;
@@ -251,10 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(
       const int64_t i = base + int64_t(t) * kItems + it;
       if (i >= nv) break;
       if (keys[it] > tau) {
-        emit(int(G + min(E, need)), int32_t(i));
+        o.emit(int(G + min(E, need)), int32_t(i));
         ++G;
       } else if (keys[it] == tau) {
-        if (E < need) emit(int(G + E), int32_t(i));
+        if (E < need) o.emit(int(G + E), int32_t(i));
         ++E;
       }
     }
@@ -262,27 +292,139 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(
     if (t == 0) { sm.run_g += tot >> 16; sm.run_e += tot & 0xFFFFu; }
     __syncthreads();
   }
-  finish(k);
+}
+
+__device__ __forceinline__ int64_t row_valid(const int32_t* n_valid, int row, int64_t n) {
+  return n_valid ? min(max(int64_t(n_valid[row]), int64_t(0)), n) : n;
+}
+
+// ---- launch 1: slice histograms -------------------------------------------------------------------
+__global__ void __launch_bounds__(kSliceThreads) topk_slice_hist_kernel(const float* __restrict__ scores, int64_t n,
+                                                                        int64_t ld, const int32_t* __restrict__ n_valid,
+                                                                        int k, uint32_t* __restrict__ ghist) {
+  __shared__ SliceSmem sm;
+  const int row = blockIdx.y;
+  const int64_t nv = row_valid(n_valid, row, n);
+  const int64_t lo = int64_t(blockIdx.x) * kSlice, hi = min(lo + kSlice, nv);
+  if (nv <= k || lo >= hi) return;
+  zero(sm.hist, kBins);
+  hist12(scores + int64_t(row) * ld, lo, hi, sm.hist);
+  __syncthreads();
+  uint32_t* g = ghist + int64_t(row) * kBins;
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x)
+    if (sm.hist[i]) atomicAdd(g + i, sm.hist[i]);
+}
+
+// ---- launch 2: slice collection of the keys in bins >= b1 -----------------------------------------
+__global__ void __launch_bounds__(kSliceThreads) topk_slice_collect_kernel(
+    const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid, int k,
+    const uint32_t* __restrict__ ghist, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_col,
+    uint32_t* __restrict__ cand_cnt) {
+  __shared__ SliceSmem sm;
+  const int row = blockIdx.y;
+  const int64_t nv = row_valid(n_valid, row, n);
+  const int64_t lo = int64_t(blockIdx.x) * kSlice, hi = min(lo + kSlice, nv);
+  if (nv <= k || lo >= hi) return;
+  const uint32_t* g = ghist + int64_t(row) * kBins;
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) sm.hist[i] = g[i];
+  __syncthreads();
+  find_bin(sm.hist, kBins, uint32_t(k), true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+  const uint32_t b1 = sm.res_bin;
+  const int lane = threadIdx.x & 31;
+  const unsigned lanes_below = (1u << lane) - 1u;
+  uint32_t* ck = cand_key + int64_t(row) * kCandCap;
+  int32_t* cc = cand_col + int64_t(row) * kCandCap;
+  for_each_key<2>(scores + int64_t(row) * ld, lo, hi, [&](int64_t i, uint32_t key, bool valid) {
+    const bool take = valid && (key >> 20) >= b1;
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    if (!m) return;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(cand_cnt + row, uint32_t(__popc(m)));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (take) {
+      const uint32_t c = base + __popc(m & lanes_below);
+      if (c < uint32_t(kCandCap)) {
+        ck[c] = key;
+        cc[c] = int32_t(i);
+      }
+    }
+  });
+}
+
+// ---- launch 3 (or the only launch for short rows): per-row selection ------------------------------
+__global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
+    const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid, int k,
+    const int32_t* __restrict__ map, int64_t map_ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
+    int expand8, int32_t* __restrict__ pool_len, const uint32_t* __restrict__ cand_key,
+    const int32_t* __restrict__ cand_col, const uint32_t* __restrict__ cand_cnt) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
+  const int row = blockIdx.x;
+  const float* s = scores + int64_t(row) * ld;
+  const int64_t nv = row_valid(n_valid, row, n);
+  __syncthreads();  // every thread has read n_valid before pool_len (possibly the same array) is written
+  RowOut o{map ? map + int64_t(row) * map_ld : nullptr, idx + int64_t(row) * (expand8 ? k * CSA2_BLOCK : k),
+           expand8 ? k * CSA2_BLOCK : k, expand8};
+  if (nv <= k) {  // everything valid is selected, already ascending
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) o.emit(i, i);
+    finish_row(o, nv, row, n_sel, pool_len);
+    return;
+  }
+  const uint32_t cnt = cand_cnt ? cand_cnt[row] : 0xFFFFFFFFu;
+  if (cnt <= uint32_t(kCandCap)) {
+    const uint32_t* ck = cand_key + int64_t(row) * kCandCap;
+    const int32_t* cc = cand_col + int64_t(row) * kCandCap;
+    for (int i = threadIdx.x; i < int(cnt); i += blockDim.x) {
+      sm.cand_key[i] = ck[i];
+      sm.cand_col[i] = cc[i];
+    }
+    __syncthreads();
+    select_candidates(sm, int(cnt), k, o);
+  } else {
+    select_row(sm, s, nv, k, o);
+  }
+  finish_row(o, k, row, n_sel, pool_len);
 }
 
 }  // namespace
 
+// workspace: row histograms, candidate keys and columns, candidate counts
+size_t topk_ws_bytes(int rows, int64_t n) {
+  if (n <= kSlice) return 0;
+  return size_t(rows) * (kBins * sizeof(uint32_t) + kCandCap * (sizeof(uint32_t) + sizeof(int32_t)) + 16);
+}
+
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
                         int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,
-                        int expand8, int32_t* pool_len, cudaStream_t st) {
+                        int expand8, int32_t* pool_len, void* ws, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const size_t smem = sizeof(SelSmem);
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(smem));
+    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  topk_select_kernel<<<rows, kThreads, smem, st>>>(scores, n, ld, n_valid, k, map, map_ld, idx, n_sel,
-                                                   expand8, pool_len);
+  uint32_t *ghist = nullptr, *ckey = nullptr, *ccnt = nullptr;
+  int32_t* ccol = nullptr;
+  if (topk_ws_bytes(rows, n) > 0) {
+    if (!ws) return cudaErrorInvalidValue;
+    char* p = static_cast<char*>(ws);
+    ghist = reinterpret_cast<uint32_t*>(p);
+    ckey = ghist + size_t(rows) * kBins;
+    ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);
+    ccnt = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
+    cudaError_t e = cudaMemsetAsync(ghist, 0, size_t(rows) * kBins * sizeof(uint32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ccnt, 0, size_t(rows) * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    const dim3 grid{unsigned((n + kSlice - 1) / kSlice), unsigned(rows), 1u};
+    topk_slice_hist_kernel<<<grid, kSliceThreads, 0, st>>>(scores, n, ld, n_valid, k, ghist);
+    topk_slice_collect_kernel<<<grid, kSliceThreads, 0, st>>>(scores, n, ld, n_valid, k, ghist, ckey, ccol, ccnt);
+  }
+  topk_select_kernel<<<rows, kSelThreads, smem, st>>>(scores, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8,
+                                                      pool_len, ckey, ccol, ccnt);
   return cudaGetLastError();
 }
 
@@ -292,13 +434,14 @@ extern "C" csa2_status csa2_topk(const float* scores, int rows, int64_t n, int64
                                  const int32_t* n_valid, int k, const int32_t* map, int64_t map_ld,
                                  int32_t* idx, int32_t* n_sel, void* ws, size_t ws_bytes,
                                  csa2_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (rows < 0 || n < 0 || ld < n || k < 1 || k > CSA2_MAX_K || n >= (int64_t(1) << 31))
     return CSA2_ERR_INVALID_ARG;
   if (rows == 0) return CSA2_OK;
+  if (rows > 65535) return CSA2_ERR_UNSUPPORTED;
   if (!scores || !idx || (map && map_ld < n)) return CSA2_ERR_INVALID_ARG;
-  return csa2::launch_topk(scores, rows, n, ld, n_valid, k, map, map_ld, idx, n_sel, 0, nullptr,
+  const size_t need = csa2::topk_ws_bytes(rows, n);
+  if (need && (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u))) return CSA2_ERR_WORKSPACE;
+  return csa2::launch_topk(scores, rows, n, ld, n_valid, k, map, map_ld, idx, n_sel, 0, nullptr, ws,
                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? CSA2_OK
              : CSA2_ERR_CUDA;

@@ -39,7 +39,8 @@ def test_struct_layout_and_status_strings(L):
 
 
 def test_workspace_sizes(L):
-    assert csa2.workspace_size(csa2.OP_TOPK, B=4, Nq=1, n=1000, k=512) == 0
+    assert csa2.workspace_size(csa2.OP_TOPK, B=4, Nq=1, n=8192, k=512) == 0      # one CTA per row
+    assert csa2.workspace_size(csa2.OP_TOPK, B=4, Nq=1, n=131072, k=512) > 4 * 4096 * 4
     a = csa2.workspace_size(csa2.OP_SPARSE_ATTN, B=64, Nq=1, k=512, W=128)
     ns = L.csa2_attn_auto_split(64, 512, 128)
     assert ns == 5 and a == 64 * ns * (16 * 512 + 32) * 4
@@ -75,6 +76,7 @@ def test_argument_validation_without_gpu(L):
     # empty problems are no-ops
     assert L.csa2_fp4_quantize_append(None, 0, 0, 512, None, None, 0, None, None) == 0
     assert L.csa2_topk(None, 0, 0, 0, None, 1, None, 0, None, None, None, 0, None) == 0
+    assert L.csa2_topk(fake, 2, 1 << 17, 1 << 17, None, 512, None, 0, fake, None, None, 0, None) == 4  # needs ws
     # group descriptor checks
     g = csa2.GroupDesc()
     g.n_layers = 0
