@@ -6,9 +6,13 @@
 // and other extensions").  K = V = the dequantised row.
 //
 // Split-KV flash decoding.  A query's rows form a list of 32-row chunks (selected FP4 rows,
-// then window rows); each CTA (4 warps) takes a contiguous run of chunks, balanced by bytes, and
-// keeps an online softmax (m, l, O) over them; a combine kernel merges the splits in a fixed
-// order.  Inside a CTA, warp w owns latent channels [128w, 128w+128) for everything:
+// then window rows); each CTA (4 warps) takes an equal share of consecutive chunks and keeps an
+// online softmax (m, l, O) over them.  The selected positions of the CTA's share are staged in
+// shared memory once, and every row of the share is prefetched into L2 up front so that the
+// double-buffered per-chunk copies wait on L2 rather than on HBM.  The last CTA of a query to
+// finish (an atomic ticket) merges the splits in split order, so the result does not depend on
+// which CTA finishes last.
+// Inside a CTA, warp w owns latent channels [128w, 128w+128) for everything:
 //  - it gathers only its slice of each row (cp.async, 16 B pieces, XOR-swizzled in shared
 //    memory), dequantises its FP4 slice to bf16 (E2M1 pair table times the E4M3 scale; the
 //    product is exact in bf16), and keeps its slice of Q in registers;
@@ -29,8 +33,6 @@ constexpr int kThreads = 128;
 constexpr int kCH = 32;          // rows per chunk
 constexpr int kPitchP = 40;      // bf16 per row of the P tile (80 B: conflict-free ldmatrix)
 constexpr int kPitchS = 36;      // floats per row of the partial-S tiles
-constexpr int kCostFp4 = 9;      // relative bytes of a 32-row FP4 chunk (288 B per row)
-constexpr int kCostSwa = 32;     // relative bytes of a 32-row bf16 window chunk (1 KiB per row)
 constexpr int kMaxSplit = 32;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -46,6 +48,8 @@ struct AttnSmem {
   float l_fin[CSA2_H];
   uint32_t lut_e2m1x2[256];
   uint16_t lut_e4m3[256];
+  int32_t pos[CSA2_MAX_ATTN_K];  // cache row of each selected slot of this split, -1 if empty
+  int is_last;
 };
 
 // bf16 bits of the E2M1 value of a 4-bit code (sign included).
@@ -66,16 +70,13 @@ __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-__host__ __device__ __forceinline__ int chunk_cost_start(int c, int nfp4) {
-  return kCostFp4 * min(c, nfp4) + kCostSwa * max(c - nfp4, 0);
-}
-
 __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     const uint16_t* __restrict__ q, int Nq, const uint8_t* __restrict__ codes,
     const uint8_t* __restrict__ scales, int64_t cap, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ n_valid, int k, const uint16_t* __restrict__ swa,
     const int32_t* __restrict__ swa_len, int W, float scale_log2, uint16_t* __restrict__ out,
-    float* __restrict__ lse, int n_split, float* __restrict__ ws, unsigned int* flags) {
+    float* __restrict__ lse, int n_split, float* __restrict__ ws, unsigned int* __restrict__ tickets,
+    unsigned int* flags) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
   const int inst = blockIdx.y;
@@ -94,13 +95,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   const int nfp4 = (k + kCH - 1) / kCH;
   const int nswa = swa ? (W + kCH - 1) / kCH : 0;
   const int nch = nfp4 + nswa;
-  const int total_cost = max(chunk_cost_start(nch, nfp4), 1);
-  int c_begin = nch, c_end = nch;
-  for (int c = 0; c < nch; ++c) {
-    const int sc = chunk_cost_start(c, nfp4) * n_split / total_cost;
-    if (sc >= split && c_begin == nch) c_begin = c;
-    if (sc >= split + 1) { c_end = c; break; }
-  }
+  const int c_begin = split * nch / n_split, c_end = (split + 1) * nch / n_split;
 
   const int n_fp4_valid = min(k, n_valid ? max(n_valid[inst], 0) : k);
   const int32_t* irow = idx + int64_t(inst) * k;
@@ -110,13 +105,31 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   const uint8_t* sbase = scales + int64_t(b) * cap * CSA2_SCALE_BYTES;
   const uint16_t* swbase = swa ? swa + int64_t(b) * SW * CSA2_D : nullptr;
 
-  auto fp4_pos = [&](int slot) -> int64_t {
-    if (slot >= n_fp4_valid) return -1;
-    const int32_t p = __ldg(irow + slot);
-    if (p < 0) return -1;
-    if (int64_t(p) >= cap) { atomicOr(flags, CSA2_FLAG_INDEX_OOB); return -1; }
-    return p;
-  };
+  // stage the cache rows of this split's selected slots and start pulling every row of the split
+  // into L2 at once
+  for (int slot = c_begin * kCH + t; slot < min(c_end, nfp4) * kCH; slot += kThreads) {
+    int32_t p = slot < n_fp4_valid ? __ldg(irow + slot) : -1;
+    if (int64_t(p) >= cap) {
+      atomicOr(flags, CSA2_FLAG_INDEX_OOB);
+      p = -1;
+    }
+    sm.pos[slot] = p < 0 ? -1 : p;
+    if (p >= 0) {
+      const uint8_t* cr = cbase + int64_t(p) * CSA2_CODE_BYTES;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(cr));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(cr + 128));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(sbase + int64_t(p) * CSA2_SCALE_BYTES));
+    }
+  }
+  if (swa) {
+    const int w0 = max(c_begin, nfp4) * kCH - nfp4 * kCH, w1 = min(c_end * kCH - nfp4 * kCH, W);
+    for (int e = t; e < max(w1 - w0, 0) * 8; e += kThreads) {   // 8 lines of 128 B per row
+      const int br = qi + w0 + (e >> 3);
+      if (br >= swa_lo) asm volatile("prefetch.global.L2 [%0];" ::"l"(swbase + int64_t(br) * CSA2_D + (e & 7) * 64));
+    }
+  }
+  __syncthreads();
+  auto fp4_pos = [&](int slot) -> int64_t { return sm.pos[slot]; };
   auto swa_row = [&](int wr) -> int {
     if (wr >= W) return -1;
     const int br = qi + wr;
@@ -337,69 +350,75 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
       const float l = sm.l_fin[t];
       lse[int64_t(inst) * CSA2_H + t] = l > 0.0f ? (sm.m_fin[t] + log2f(l)) * kLn2 : -INFINITY;
     }
-  } else {
-    float* po = ws + (int64_t(inst) * n_split + split) * (CSA2_H * CSA2_D);
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int ch = 128 * warp + 8 * nt + 2 * tq;
-      *reinterpret_cast<float2*>(po + g * CSA2_D + ch) = make_float2(oacc[nt][0], oacc[nt][1]);
-      *reinterpret_cast<float2*>(po + (g + 8) * CSA2_D + ch) = make_float2(oacc[nt][2], oacc[nt][3]);
-    }
-    if (t < CSA2_H) {
-      float* ml = ws + int64_t(gridDim.y) * n_split * (CSA2_H * CSA2_D) +
-                  (int64_t(inst) * n_split + split) * (2 * CSA2_H);
-      ml[2 * t] = sm.m_fin[t];
-      ml[2 * t + 1] = sm.l_fin[t];
-    }
+    return;
   }
-}
-
-// Merge the splits of one query in split order: o = sum_j 2^(m_j-M) O_j / sum_j 2^(m_j-M) l_j.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ ws, int n_split,
-                                                           int64_t instances, uint16_t* __restrict__ out,
-                                                           float* __restrict__ lse) {
-  const int64_t inst = blockIdx.x;
-  const int t = threadIdx.x;
-  const int h = t >> 4, c0 = (t & 15) * 32;
-  const float* ml = ws + instances * n_split * (CSA2_H * CSA2_D) + inst * n_split * (2 * CSA2_H);
-  float M = -INFINITY;
-  for (int j = 0; j < n_split; ++j) M = fmaxf(M, ml[j * 2 * CSA2_H + 2 * h]);
-  float acc[32];
+  // ---- split partials, then the last CTA of this query merges them ------------------------------
+  const int64_t instances = gridDim.y;
+  float* po = ws + (int64_t(inst) * n_split + split) * (CSA2_H * CSA2_D);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-  float L = 0.0f;
-  if (M != -INFINITY) {
-    for (int j = 0; j < n_split; ++j) {
-      const float mj = ml[j * 2 * CSA2_H + 2 * h];
-      const float a = exp2f(mj - M);
-      L += a * ml[j * 2 * CSA2_H + 2 * h + 1];
-      const float4* po = reinterpret_cast<const float4*>(ws + (inst * n_split + j) * (CSA2_H * CSA2_D) +
-                                                         h * CSA2_D + c0);
+  for (int nt = 0; nt < 16; ++nt) {
+    const int ch = 128 * warp + 8 * nt + 2 * tq;
+    *reinterpret_cast<float2*>(po + g * CSA2_D + ch) = make_float2(oacc[nt][0], oacc[nt][1]);
+    *reinterpret_cast<float2*>(po + (g + 8) * CSA2_D + ch) = make_float2(oacc[nt][2], oacc[nt][3]);
+  }
+  float* mlb = ws + instances * n_split * (CSA2_H * CSA2_D);
+  if (t < CSA2_H) {
+    float* ml = mlb + (int64_t(inst) * n_split + split) * (2 * CSA2_H);
+    ml[2 * t] = sm.m_fin[t];
+    ml[2 * t + 1] = sm.l_fin[t];
+  }
+  __threadfence();
+  __syncthreads();
+  if (t == 0) sm.is_last = (atomicAdd(tickets + inst, 1u) == unsigned(n_split - 1));
+  __syncthreads();
+  if (!sm.is_last) return;
+  __threadfence();
+  // o = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j, splits in order; thread: head t>>3, 64 channels
+  {
+    const int h = t >> 3, c0 = (t & 7) * 64;
+    const float* ml = mlb + int64_t(inst) * n_split * (2 * CSA2_H);
+    float M = -INFINITY;
+    for (int j = 0; j < n_split; ++j) M = fmaxf(M, __ldcg(ml + j * 2 * CSA2_H + 2 * h));
+    float L = 0.0f;
+    float acc[64];
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const float4 x = po[v];
-        acc[4 * v] += a * x.x;
-        acc[4 * v + 1] += a * x.y;
-        acc[4 * v + 2] += a * x.z;
-        acc[4 * v + 3] += a * x.w;
+    for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+    if (M != -INFINITY) {
+      for (int j = 0; j < n_split; ++j) {
+        const float a = exp2f(__ldcg(ml + j * 2 * CSA2_H + 2 * h) - M);
+        L += a * __ldcg(ml + j * 2 * CSA2_H + 2 * h + 1);
+        const float4* pj = reinterpret_cast<const float4*>(ws + (int64_t(inst) * n_split + j) * (CSA2_H * CSA2_D) +
+                                                           h * CSA2_D + c0);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          const float4 x = __ldcg(pj + v);
+          acc[4 * v] += a * x.x;
+          acc[4 * v + 1] += a * x.y;
+          acc[4 * v + 2] += a * x.z;
+          acc[4 * v + 3] += a * x.w;
+        }
       }
     }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    uint4* dst = reinterpret_cast<uint4*>(out + (int64_t(inst) * CSA2_H + h) * CSA2_D + c0);
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      dst[v] = make_uint4(pack_bf16x2(acc[8 * v] * inv, acc[8 * v + 1] * inv),
+                          pack_bf16x2(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
+                          pack_bf16x2(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
+                          pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
+    if (lse && (t & 7) == 0) lse[int64_t(inst) * CSA2_H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
-  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  uint32_t o[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-  uint4* dst = reinterpret_cast<uint4*>(out + (inst * CSA2_H + h) * CSA2_D + c0);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-  if (lse && (t & 15) == 0) lse[inst * CSA2_H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  if (t == 0) tickets[inst] = 0u;  // ready for the next launch
 }
 
 }  // namespace
 
+// partial O and (m, l) of every split, then one ticket per query (zeroed before each launch)
 size_t attn_ws_bytes(int64_t instances, int n_split) {
   if (n_split <= 1) return 0;
-  return size_t(instances) * size_t(n_split) * (CSA2_H * CSA2_D + 2 * CSA2_H) * sizeof(float);
+  return size_t(instances) * size_t(n_split) * (CSA2_H * CSA2_D + 2 * CSA2_H) * sizeof(float) +
+         size_t(instances) * sizeof(unsigned int);
 }
 
 int attn_auto_split(int64_t instances, int k, int W) {
@@ -430,12 +449,15 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
     attr_set[dev] = true;
   }
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  unsigned int* tickets = nullptr;
+  if (n_split > 1) {
+    tickets = reinterpret_cast<unsigned int*>(ws + instances * n_split * (CSA2_H * CSA2_D + 2 * CSA2_H));
+    cudaError_t e = cudaMemsetAsync(tickets, 0, size_t(instances) * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return e;
+  }
   const dim3 grid{unsigned(n_split), unsigned(instances), 1u};
   sparse_attn_kernel<<<grid, kThreads, smem, st>>>(q, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len,
-                                                   W, scale_log2, out, lse, n_split, ws, flags);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || n_split == 1) return e;
-  attn_combine_kernel<<<unsigned(instances), 256, 0, st>>>(ws, n_split, instances, out, lse);
+                                                   W, scale_log2, out, lse, n_split, ws, tickets, flags);
   return cudaGetLastError();
 }
 
