@@ -43,7 +43,7 @@ class GroupDesc(ctypes.Structure):
     _fields_ = [
         ("n_layers", I32), ("modes", I32 * MAX_LAYERS),
         ("B", I32), ("Nq", I32), ("K", I32), ("W", I32), ("ratio", I32),
-        ("hierarchical", I32), ("n_blocks_keep", I32), ("n_split", I32), ("n_new", I32),
+        ("hierarchical", I32), ("n_blocks_keep", I32), ("n_split", I32), ("n_new", I32), ("seq_chunks", I32),
         ("cap", I64), ("lens", P), ("q_pos", P),
         ("codes", P), ("scales", P), ("KI", P), ("block_keys", P),
         ("kv_new", P), ("ki_new", P),
@@ -262,7 +262,7 @@ def group_workspace_size(B, Nq, cap, K=512, W=128, hierarchical=False, keep=2048
 def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa, swa_len, out, idx,
                     K=512, W=128, ratio=1, hierarchical=False, keep=2048, n_split=0, q_pos=None,
                     block_keys=None, pool=None, pool_len=None, kv_new=None, ki_new=None, lse=None,
-                    softmax_scale=None, events=None):
+                    softmax_scale=None, events=None, seq_chunks=0):
     """Build a csa2_group_desc from torch tensors (per-layer arguments are lists; entries of
     qI/w/idx may be None for Reuse layers).  Keeps references to the tensors on the result."""
     torch = _torch()
@@ -281,6 +281,7 @@ def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa
     elif ki_new is not None:
         n_new = ki_new.shape[1]
     g.n_new = n_new
+    g.seq_chunks = int(seq_chunks)
     g.cap = cap
     bf = _bf16_types()
     g.lens = _ptr(lens, "lens", (torch.int32,), B)

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/csa2.h"
 
 namespace csa2 {
@@ -148,4 +150,16 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
                                float* lse, int n_split, float* ws, cudaStream_t st);
 size_t attn_ws_bytes(int64_t instances, int n_split);
 int attn_auto_split(int64_t instances, int k, int W);
+
+// Library-owned side stream (highest priority) and events of the current device, created on first
+// use; the group step overlaps sequence chunks with them.  `mu` serialises the enqueue of a step.
+constexpr int kMaxSeqChunks = 16;
+struct DeviceStreams {
+  bool ready = false;
+  cudaStream_t aux = nullptr;
+  cudaEvent_t fork[kMaxSeqChunks] = {};
+  cudaEvent_t join = nullptr;
+  std::mutex mu;
+};
+DeviceStreams* device_streams();
 }  // namespace csa2

@@ -1,6 +1,6 @@
 // CSA2 layer-group driver, hierarchical pool entry point, workspace sizing and status helpers.
 //
-// A group runs its layers in order on one stream (ai-maestro.online "DeepSeek AI released
+// A group runs its layers in order (ai-maestro.online "DeepSeek AI released
 // DeepSeek-V4.1-Flash with 1M context, FP4", section "Compressed Sparse Attention 2"):
 //   Full     [append new rows] -> [block scores -> Top-keep blocks -> pool] -> scores -> Top-K
 //   Reindex  scores (pool or all visible entries) with its own indexer Q -> Top-K
@@ -8,6 +8,7 @@
 // and every layer then runs split-KV sparse attention with its own Q and window.  Scores live in
 // the caller's workspace; the selection kernels read them while they are still in L2.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -26,6 +27,25 @@ unsigned int* device_flags_ptr() {
     ptrs[dev] = static_cast<unsigned int*>(p);
   }
   return ptrs[dev];
+}
+
+DeviceStreams* device_streams() {
+  static DeviceStreams res[64];
+  static std::mutex init_mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return nullptr;
+  DeviceStreams& r = res[dev];
+  std::lock_guard<std::mutex> guard(init_mu);
+  if (!r.ready) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithPriority(&r.aux, cudaStreamNonBlocking, greatest) != cudaSuccess) return nullptr;
+    for (auto& e : r.fork)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&r.join, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    r.ready = true;
+  }
+  return &r;
 }
 
 namespace {
@@ -195,12 +215,30 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   int32_t* nv = reinterpret_cast<int32_t*>(wsb + lay.nv_off);
   void* tws = wsb + lay.topk_off;
   float* attn_ws = reinterpret_cast<float*>(wsb + lay.attn_off);
-  const int ns = g->n_split ? g->n_split : csa2::attn_auto_split(rows, g->K, g->W);
+  const int ns_all = g->n_split ? g->n_split : csa2::attn_auto_split(rows, g->K, g->W);
   const int64_t nb = g->cap / CSA2_BLOCK;
   const int64_t pool_w = int64_t(g->n_blocks_keep) * CSA2_BLOCK;
+  const int64_t sld = lay.score_ld;
+  const int Nq = g->Nq, K = g->K, SW = g->W - 1 + g->Nq;
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  auto rec = [&](csa2_event_t e, cudaStream_t s2) {
+    return !e || cudaEventRecord(reinterpret_cast<cudaEvent_t>(e), s2) == cudaSuccess;
+  };
 
-  // ---- append (Full layer of a decode step) ----------------------------------------------------
+  // Sequence chunks: the first indexer scan of chunk c runs on `stream` while the rest of chunk c-1
+  // (selection, pool work, attention of every layer) runs on the side stream.
+  int n_chunks = g->seq_chunks > 0 ? g->seq_chunks : (g->B >= 32 ? 4 : 1);
+  n_chunks = std::max(1, std::min({n_chunks, g->B, csa2::kMaxSeqChunks}));
+  csa2::DeviceStreams* ds = nullptr;
+  if (n_chunks > 1) {
+    ds = csa2::device_streams();
+    if (!ds) return CSA2_ERR_CUDA;
+  }
+  std::unique_lock<std::mutex> lock;
+  if (ds) lock = std::unique_lock<std::mutex>(ds->mu);
+  cudaStream_t aux = ds ? ds->aux : st;
+
+  // ---- append (Full layer of a decode step), before any scoring --------------------------------
   if (g->n_new > 0) {
     if (g->kv_new &&
         !ok(csa2::launch_fp4_quantize(g->kv_new, g->B, g->n_new, g->codes, g->scales, g->cap, g->lens,
@@ -214,64 +252,93 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
         return CSA2_ERR_CUDA;
     }
   }
+  if (!rec(g->ev_score_begin, st)) return CSA2_ERR_CUDA;
 
-  const int32_t* latest = nullptr;
-  bool first_score = true;
-  for (int l = 0; l < L; ++l) {
-    const int mode = g->modes[l];
-    if (mode != CSA2_MODE_REUSE) {
-      const bool timed = first_score && g->ev_score_begin && g->ev_score_end;
-      if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_begin), st) != cudaSuccess)
+  for (int c = 0; c < n_chunks; ++c) {
+    const int b0 = int(int64_t(g->B) * c / n_chunks), b1 = int(int64_t(g->B) * (c + 1) / n_chunks);
+    const int Bc = b1 - b0;
+    const int64_t r0 = int64_t(b0) * Nq, rc = int64_t(Bc) * Nq;
+    // chunk views
+    const int32_t* lens = g->lens + b0;
+    const int32_t* qpos = g->q_pos ? g->q_pos + r0 : nullptr;
+    uint8_t* codes = g->codes + int64_t(b0) * g->cap * CSA2_CODE_BYTES;
+    uint8_t* scl = g->scales + int64_t(b0) * g->cap * CSA2_SCALE_BYTES;
+    const uint16_t* KI = g->KI + int64_t(b0) * g->cap * CSA2_DI;
+    const uint16_t* bkeys = g->block_keys ? g->block_keys + int64_t(b0) * nb * CSA2_DI : nullptr;
+    int32_t* pool = g->pool ? g->pool + r0 * pool_w : nullptr;
+    int32_t* pool_len = g->pool_len ? g->pool_len + r0 : nullptr;
+    float* sc = scores + r0 * sld;
+    int32_t* nvc = nv + r0;
+    const int32_t* swl = g->swa_len ? g->swa_len + b0 : nullptr;
+    auto qI_of = [&](int l) { return g->qI[l] + r0 * (CSA2_HI * CSA2_DI); };
+    auto w_of = [&](int l) { return g->w[l] + r0 * CSA2_HI; };
+    auto idx_of = [&](int l) { return g->idx[l] + r0 * K; };
+    // attention split of a chunk: at most 4 when chunks overlap, and within the sized workspace
+    int ns = g->n_split ? g->n_split : std::min(csa2::attn_auto_split(rc, K, g->W), n_chunks > 1 ? 4 : 32);
+    while (ns > 1 && csa2::attn_ws_bytes(rc, ns) > csa2::attn_ws_bytes(rows, ns_all)) --ns;
+
+    // stage 1 (stream): the first scan over this chunk's keys (layer 0 is Full or Reindex)
+    if (g->hierarchical && g->modes[0] == CSA2_MODE_FULL) {
+      if (nb > 0 &&
+          !ok(csa2::launch_index_score(qI_of(0), w_of(0), Bc, Nq, bkeys, nb, lens, g->cap, CSA2_BLOCK, nullptr,
+                                       nullptr, 0, g->ratio, qpos, sc, nb, pool_len, st)))
         return CSA2_ERR_CUDA;
-      if (g->hierarchical) {
-        if (mode == CSA2_MODE_FULL) {
-          if (nb > 0) {
-            if (!ok(csa2::launch_index_score(g->qI[l], g->w[l], g->B, g->Nq, g->block_keys, nb, g->lens, g->cap,
-                                             CSA2_BLOCK, nullptr, nullptr, 0, g->ratio, g->q_pos, scores, nb,
-                                             g->pool_len, st)))
-              return CSA2_ERR_CUDA;
-            if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
-              return CSA2_ERR_CUDA;
-            if (!ok(csa2::launch_topk(scores, int(rows), nb, nb, g->pool_len, g->n_blocks_keep, nullptr, 0, g->pool,
-                                      nullptr, 1, g->pool_len, tws, st)))
-              return CSA2_ERR_CUDA;
-          } else {
-            if (!ok(cudaMemsetAsync(g->pool_len, 0, size_t(rows) * sizeof(int32_t), st))) return CSA2_ERR_CUDA;
-            if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
-              return CSA2_ERR_CUDA;
-          }
-        }
-        if (!ok(csa2::launch_index_score(g->qI[l], g->w[l], g->B, g->Nq, g->KI, g->cap, g->lens, g->cap, 1,
-                                         g->pool, g->pool_len, pool_w, g->ratio, g->q_pos, scores, pool_w, nv,
-                                         st)))
-          return CSA2_ERR_CUDA;
-        if (timed && mode != CSA2_MODE_FULL &&
-            cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
-          return CSA2_ERR_CUDA;
-        if (!ok(csa2::launch_topk(scores, int(rows), pool_w, pool_w, nv, g->K, g->pool, pool_w, g->idx[l], nullptr,
-                                  0, nullptr, tws, st)))
-          return CSA2_ERR_CUDA;
-      } else {
-        if (!ok(csa2::launch_index_score(g->qI[l], g->w[l], g->B, g->Nq, g->KI, g->cap, g->lens, g->cap, 1,
-                                         nullptr, nullptr, 0, g->ratio, g->q_pos, scores, g->cap, nv, st)))
-          return CSA2_ERR_CUDA;
-        if (timed && cudaEventRecord(reinterpret_cast<cudaEvent_t>(g->ev_score_end), st) != cudaSuccess)
-          return CSA2_ERR_CUDA;
-        if (!ok(csa2::launch_topk(scores, int(rows), g->cap, g->cap, nv, g->K, nullptr, 0, g->idx[l], nullptr, 0,
-                                  nullptr, tws, st)))
-          return CSA2_ERR_CUDA;
-      }
-      first_score = false;
-      latest = g->idx[l];
-    } else if (g->idx[l] && g->idx[l] != latest) {
-      if (!ok(cudaMemcpyAsync(g->idx[l], latest, size_t(rows) * g->K * sizeof(int32_t), cudaMemcpyDeviceToDevice,
-                              st)))
+    } else if (!g->hierarchical) {
+      if (!ok(csa2::launch_index_score(qI_of(0), w_of(0), Bc, Nq, KI, g->cap, lens, g->cap, 1, nullptr, nullptr, 0,
+                                       g->ratio, qpos, sc, g->cap, nvc, st)))
         return CSA2_ERR_CUDA;
     }
-    if (!ok(csa2::launch_sparse_attn(g->q[l], g->B, g->Nq, g->codes, g->scales, g->cap, latest, nullptr, g->K,
-                                     g->W > 0 ? g->swa[l] : nullptr, g->swa_len, g->W, g->softmax_scale,
-                                     g->out[l], g->lse[l], ns, attn_ws, st)))
+    if (c == n_chunks - 1 && !rec(g->ev_score_end, st)) return CSA2_ERR_CUDA;
+    if (ds && (!ok(cudaEventRecord(ds->fork[c], st)) || !ok(cudaStreamWaitEvent(aux, ds->fork[c], 0))))
       return CSA2_ERR_CUDA;
+
+    // stage 2 (side stream): everything else of this chunk, layer by layer
+    const int32_t* latest = nullptr;
+    for (int l = 0; l < L; ++l) {
+      const int mode = g->modes[l];
+      if (mode != CSA2_MODE_REUSE) {
+        if (g->hierarchical) {
+          if (mode == CSA2_MODE_FULL) {
+            if (nb > 0 && l != 0 &&
+                !ok(csa2::launch_index_score(qI_of(l), w_of(l), Bc, Nq, bkeys, nb, lens, g->cap, CSA2_BLOCK, nullptr,
+                                             nullptr, 0, g->ratio, qpos, sc, nb, pool_len, aux)))
+              return CSA2_ERR_CUDA;
+            if (nb > 0) {
+              if (!ok(csa2::launch_topk(sc, int(rc), nb, nb, pool_len, g->n_blocks_keep, nullptr, 0, pool, nullptr, 1,
+                                        pool_len, tws, aux)))
+                return CSA2_ERR_CUDA;
+            } else if (!ok(cudaMemsetAsync(pool_len, 0, size_t(rc) * sizeof(int32_t), aux))) {
+              return CSA2_ERR_CUDA;
+            }
+          }
+          if (!ok(csa2::launch_index_score(qI_of(l), w_of(l), Bc, Nq, KI, g->cap, lens, g->cap, 1, pool, pool_len,
+                                           pool_w, g->ratio, qpos, sc, pool_w, nvc, aux)))
+            return CSA2_ERR_CUDA;
+          if (!ok(csa2::launch_topk(sc, int(rc), pool_w, pool_w, nvc, K, pool, pool_w, idx_of(l), nullptr, 0, nullptr,
+                                    tws, aux)))
+            return CSA2_ERR_CUDA;
+        } else {
+          if (l != 0 &&
+              !ok(csa2::launch_index_score(qI_of(l), w_of(l), Bc, Nq, KI, g->cap, lens, g->cap, 1, nullptr, nullptr, 0,
+                                           g->ratio, qpos, sc, g->cap, nvc, aux)))
+            return CSA2_ERR_CUDA;
+          if (!ok(csa2::launch_topk(sc, int(rc), g->cap, g->cap, nvc, K, nullptr, 0, idx_of(l), nullptr, 0, nullptr,
+                                    tws, aux)))
+            return CSA2_ERR_CUDA;
+        }
+        latest = idx_of(l);
+      } else if (g->idx[l] && idx_of(l) != latest) {
+        if (!ok(cudaMemcpyAsync(idx_of(l), latest, size_t(rc) * K * sizeof(int32_t), cudaMemcpyDeviceToDevice, aux)))
+          return CSA2_ERR_CUDA;
+      }
+      const uint16_t* swa = g->W > 0 ? g->swa[l] + int64_t(b0) * SW * CSA2_D : nullptr;
+      if (!ok(csa2::launch_sparse_attn(g->q[l] + r0 * (CSA2_H * CSA2_D), Bc, Nq, codes, scl, g->cap, latest, nullptr,
+                                       K, swa, swl, g->W, g->softmax_scale, g->out[l] + r0 * (CSA2_H * CSA2_D),
+                                       g->lse[l] ? g->lse[l] + r0 * CSA2_H : nullptr, ns, attn_ws, aux)))
+        return CSA2_ERR_CUDA;
+    }
   }
+  if (ds && (!ok(cudaEventRecord(ds->join, aux)) || !ok(cudaStreamWaitEvent(st, ds->join, 0))))
+    return CSA2_ERR_CUDA;
   return CSA2_OK;
 }

@@ -199,6 +199,13 @@ csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq, const uint
  *            entries; selects Top-K.
  *   REUSE    attends with the latest layer's indices; no scoring.
  * Every layer attends with its own q and window.  The first layer must be FULL or REINDEX.
+ * Execution: the batch is cut into `seq_chunks` groups of whole sequences (auto: 4 from 32
+ * sequences up, else 1).  The first indexer scan of group c runs on `stream` while the remaining
+ * work of group c-1 runs on a library-owned, highest-priority stream of the current device
+ * (created with its events on first use), which waits on an event recorded on `stream` and is
+ * joined back into `stream` before the call returns.  All of the step's work is therefore ordered
+ * after earlier work on `stream` and before later work on it; calls from several host threads
+ * are serialised while they enqueue.
  */
 typedef struct csa2_group_desc {
   int n_layers;                       /* 1 .. CSA2_MAX_LAYERS                            */
@@ -211,6 +218,7 @@ typedef struct csa2_group_desc {
   int n_blocks_keep;                  /* blocks kept by the pool, 1..2048                */
   int n_split;                        /* attention split, 0 = automatic                  */
   int n_new;                          /* rows appended by the Full layer (0: none)       */
+  int seq_chunks;                     /* sequence chunks pipelined over two streams, 0 = auto */
   int64_t cap;                        /* cache capacity (entries) per sequence           */
   const int32_t* lens;                /* [B] entries present (after the append)          */
   const int32_t* q_pos;               /* [B*Nq] query token positions, or NULL           */
@@ -232,8 +240,8 @@ typedef struct csa2_group_desc {
   int32_t* pool;                      /* [B*Nq][keep*8] (hierarchical)                   */
   int32_t* pool_len;                  /* [B*Nq]         (hierarchical)                   */
   float softmax_scale;                /* e.g. 1/sqrt(512)                                */
-  csa2_event_t ev_score_begin;        /* optional: recorded before / after the first     */
-  csa2_event_t ev_score_end;          /*   scoring kernel of the group (profiling)       */
+  csa2_event_t ev_score_begin;        /* optional: recorded on `stream` before the first  */
+  csa2_event_t ev_score_end;          /*   indexer scan of the step and after the last   */
 } csa2_group_desc;
 
 csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_t ws_bytes,

@@ -151,7 +151,7 @@ class GroupCase:
     def h_w(self, l, b): return syn.normal_f32(self.seed, syn.T_W + l, b, (self.Nq, HI))
     def h_swa(self, l, b): return syn.normal_bf16(self.seed, syn.T_SWA + l, b, (self.W - 1 + self.Nq, D))
 
-    def desc(self, events=None, n_split=0):
+    def desc(self, events=None, n_split=0, seq_chunks=0):
         c = self.c
         return c.make_group_desc(
             self.modes, B=self.B, Nq=self.Nq, cap=self.cap, lens=self.lens, codes=self.codes, scales=self.scales,
@@ -159,11 +159,11 @@ class GroupCase:
             idx=self.idx, K=self.K, W=self.W, ratio=self.ratio, hierarchical=self.hierarchical, keep=self.keep,
             n_split=n_split, q_pos=self.qp_dev, block_keys=self.block_keys, pool=self.pool,
             pool_len=self.pool_len, kv_new=self.kv_new if self.append else None,
-            ki_new=self.ki_new if self.append else None, lse=self.lse, events=events)
+            ki_new=self.ki_new if self.append else None, lse=self.lse, events=events, seq_chunks=seq_chunks)
 
-    def run(self, n_split=0):
+    def run(self, n_split=0, seq_chunks=0):
         import torch
-        d = self.desc(n_split=n_split)
+        d = self.desc(n_split=n_split, seq_chunks=seq_chunks)
         self.c.csa2_group_step(d, self.ws)
         torch.cuda.synchronize()
 

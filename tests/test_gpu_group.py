@@ -40,6 +40,21 @@ def test_decode_group_with_reindex_and_split_counts(orc):
         gc.check(orc)
 
 
+def test_decode_group_pipelined_sequence_chunks(orc):
+    """The step cut into sequence chunks overlapped over two streams (ragged chunks) gives the
+    same indices and outputs as the oracle, with and without a Reindex layer."""
+    gc = GroupCase(56, [5000, 4096, 700, 2300, 9, 1500, 3333], [F, R, RX, R])
+    for chunks in (3, 7):
+        gc.run(seq_chunks=chunks)
+        gc.check(orc)
+
+
+def test_hierarchical_group_pipelined_sequence_chunks(orc):
+    gc = GroupCase(57, [8 * 3000, 8 * 2300 + 5, 8 * 900 + 1], [F, RX, R], hierarchical=True)
+    gc.run(seq_chunks=2)
+    gc.check(orc)
+
+
 def test_hierarchical_group_pool_and_reindex(orc):
     # block count above and below the 2048 kept; T % 8 == 0 (the append completes a block) and not
     gc = GroupCase(53, [8 * 3000, 8 * 2300 + 5, 8 * 900], [F, RX, R, R, R], hierarchical=True)
