@@ -227,7 +227,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
 
   // Sequence chunks: the first indexer scan of chunk c runs on `stream` while the rest of chunk c-1
   // (selection, pool work, attention of every layer) runs on the side stream.
-  int n_chunks = g->seq_chunks > 0 ? g->seq_chunks : (g->B >= 32 ? 4 : 1);
+  int n_chunks = g->seq_chunks > 0 ? g->seq_chunks : 1;
   n_chunks = std::max(1, std::min({n_chunks, g->B, csa2::kMaxSeqChunks}));
   csa2::DeviceStreams* ds = nullptr;
   if (n_chunks > 1) {

@@ -199,8 +199,8 @@ csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq, const uint
  *            entries; selects Top-K.
  *   REUSE    attends with the latest layer's indices; no scoring.
  * Every layer attends with its own q and window.  The first layer must be FULL or REINDEX.
- * Execution: the batch is cut into `seq_chunks` groups of whole sequences (auto: 4 from 32
- * sequences up, else 1).  The first indexer scan of group c runs on `stream` while the remaining
+ * Execution: the batch is cut into `seq_chunks` groups of whole sequences (0: one group).  With
+ * more than one group, the first indexer scan of group c runs on `stream` while the remaining
  * work of group c-1 runs on a library-owned, highest-priority stream of the current device
  * (created with its events on first use), which waits on an event recorded on `stream` and is
  * joined back into `stream` before the call returns.  All of the step's work is therefore ordered
@@ -218,7 +218,7 @@ typedef struct csa2_group_desc {
   int n_blocks_keep;                  /* blocks kept by the pool, 1..2048                */
   int n_split;                        /* attention split, 0 = automatic                  */
   int n_new;                          /* rows appended by the Full layer (0: none)       */
-  int seq_chunks;                     /* sequence chunks pipelined over two streams, 0 = auto */
+  int seq_chunks;                     /* sequence chunks pipelined over two streams, 0 = 1 */
   int64_t cap;                        /* cache capacity (entries) per sequence           */
   const int32_t* lens;                /* [B] entries present (after the append)          */
   const int32_t* q_pos;               /* [B*Nq] query token positions, or NULL           */
