@@ -5,22 +5,26 @@
 // architecture"; E2M1 codes with an E4M3 scale per 16 channels: section "FP4 KV, Bounded Replay,
 // and other extensions").  K = V = the dequantised row.
 //
-// Split-KV flash decoding.  A query's rows form a list of 32-row chunks (selected FP4 rows,
-// then window rows); each CTA (4 warps) takes an equal share of consecutive chunks and keeps an
-// online softmax (m, l, O) over them.  The selected positions of the CTA's share are staged in
-// shared memory once, and every row of the share is prefetched into L2 up front so that the
-// double-buffered per-chunk copies wait on L2 rather than on HBM.  The last CTA of a query to
-// finish (an atomic ticket) merges the splits in split order, so the result does not depend on
-// which CTA finishes last.
-// Inside a CTA, warp w owns latent channels [128w, 128w+128) for everything:
-//  - it gathers only its slice of each row (cp.async, 16 B pieces, XOR-swizzled in shared
-//    memory), dequantises its FP4 slice to bf16 (E2M1 pair table times the E4M3 scale; the
-//    product is exact in bf16), and keeps its slice of Q in registers;
-//  - S_w = Q[:, slice] K[:, slice]^T and O[:, slice] += P V[:, slice] run on tensor cores with
-//    the 16 heads as the M = 16 dimension of mma.m16n8k16 (bf16 in, fp32 accumulate);
-//  - the four partial S are summed in a fixed order, so the only block-wide barriers are the
-//    two around the softmax of each chunk.
-#include <cuda_bf16.h>
+// Split-KV flash decoding.  A query's rows form a list of 32-row chunks (selected FP4 rows, then
+// window rows); each CTA takes an equal share of consecutive chunks and keeps an online softmax
+// (m, l, O) over them.  The selected positions of the share are staged in shared memory once and
+// every row of the share is prefetched into L2 up front, so the double-buffered per-chunk copies
+// wait on L2 rather than on HBM.  The last CTA of a query to finish (an atomic ticket) merges the
+// splits in split order, so the result does not depend on which CTA finishes last.
+//
+// Inside a CTA, warp w (of 8) owns latent channels [64w, 64w+64) for everything: it gathers only
+// its slice of each row (cp.async, 16-byte pieces, XOR-swizzled in shared memory), converts it to
+// f16 in shared memory, keeps its Q slice in registers, and computes S_w = Q[:, slice] K[:, slice]^T
+// and O[:, slice] += P V[:, slice]
+// on tensor cores with the 16 heads as the M = 16 dimension of mma.m16n8k16 (f16 inputs, fp32
+// accumulate).  The eight partial S are summed in a fixed order, so the only block-wide barriers
+// are the two around each chunk's softmax.
+//
+// Tensor-core inputs are f16: an FP4 row is dequantised with the hardware E2M1 -> f16x2
+// conversion and one f16 multiply by its E4M3 scale, which is exact (at most 6 significant bits,
+// magnitudes in [2^-10, 2688]); window rows and Q are converted from bf16, which is exact for
+// magnitudes in [2^-14, 65504] (and rounds below); P is rounded to f16.
+#include <cuda_fp16.h>
 
 #include <algorithm>
 
@@ -29,46 +33,58 @@
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
 constexpr int kCH = 32;          // rows per chunk
-constexpr int kPitchP = 40;      // bf16 per row of the P tile (80 B: conflict-free ldmatrix)
+constexpr int kPitchP = 40;      // f16 per row of the P tile (80 B: conflict-free ldmatrix)
 constexpr int kPitchS = 36;      // floats per row of the partial-S tiles
 constexpr int kMaxSplit = 32;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct AttnSmem {
-  uint16_t q[CSA2_H * CSA2_D];
-  uint16_t kv[2][kCH * CSA2_D];
-  uint8_t raw_codes[2][kCH * CSA2_CODE_BYTES];
+  uint16_t kv[2][kCH * CSA2_D];                    // f16, swizzled 16-byte chunks (kv[1] first stages Q)
+  uint8_t raw_codes[2][kCH * CSA2_CODE_BYTES];     // swizzled 16-byte pieces
   uint8_t raw_scales[2][kCH * CSA2_SCALE_BYTES];
   uint16_t p[CSA2_H * kPitchP];
-  float s[4][CSA2_H * kPitchS];
+  float s[kWarps][CSA2_H * kPitchS];
   float corr[CSA2_H];
   float m_fin[CSA2_H];
   float l_fin[CSA2_H];
-  uint32_t lut_e2m1x2[256];
-  uint16_t lut_e4m3[256];
   int32_t pos[CSA2_MAX_ATTN_K];  // cache row of each selected slot of this split, -1 if empty
   int is_last;
 };
 
-// bf16 bits of the E2M1 value of a 4-bit code (sign included).
-__device__ __forceinline__ uint32_t e2m1_bf16(uint32_t nib) {
-  const uint32_t c = nib & 7u;
-  const uint32_t mag = (c < 2u) ? (c ? 0x3F00u : 0u) : ((((126u + (c >> 1)) << 7)) | ((c & 1u) << 6));
-  return mag | ((nib & 8u) << 12);
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Two E2M1 codes (one byte: the even channel in the low nibble) -> f16x2 (even channel low).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
+  return r;
 }
-// bf16 bits of an E4M3 (FN) value (exact: 4 significant bits, range 2^-9 .. 448).
-__device__ __forceinline__ uint32_t e4m3_bf16(uint32_t b) {
+// E4M3 (FN) byte -> f16 bits (exact: 4 significant bits, magnitudes 2^-9 .. 448).
+__device__ __forceinline__ uint32_t e4m3_f16(uint32_t b) {
   const uint32_t e = (b >> 3) & 15u, m = b & 7u;
   const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : float(m) * 0.001953125f;
-  return (__float_as_uint(v) >> 16) | ((b & 0x80u) << 8);
+  return __half_as_ushort(__float2half_rn((b & 0x80u) ? -v : v));
 }
-__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
-  __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a),
-                             *reinterpret_cast<const __nv_bfloat162*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
+// bf16x2 -> f16x2 (round to nearest)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
+  return h2_bits(__floats2half2_rn(bf16lo(u), bf16hi(u)));
 }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) { return h2_bits(__floats2half2_rn(lo, hi)); }
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// byte offset of logical 16-byte chunk cc (0..63) of row r in a 1 KiB-per-row swizzled tile
+__device__ __forceinline__ int swz(int r, int cc) { return r * (CSA2_D * 2) + ((cc ^ (r & 7)) << 4); }
 
 __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     const uint16_t* __restrict__ q, int Nq, const uint8_t* __restrict__ codes,
@@ -85,11 +101,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int g = lane >> 2, tq = lane & 3;
   const int mat = lane >> 3, mrow = lane & 7;
-
-  for (int i = t; i < 256; i += kThreads) {
-    sm.lut_e2m1x2[i] = e2m1_bf16(i & 15) | (e2m1_bf16(i >> 4) << 16);
-    sm.lut_e4m3[i] = uint16_t(e4m3_bf16(uint32_t(i)));
-  }
+  const uint32_t kv_base[2] = {smem_u32(sm.kv[0]), smem_u32(sm.kv[1])};
 
   // ---- this split's chunks ------------------------------------------------------------------
   const int nfp4 = (k + kCH - 1) / kCH;
@@ -105,8 +117,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   const uint8_t* sbase = scales + int64_t(b) * cap * CSA2_SCALE_BYTES;
   const uint16_t* swbase = swa ? swa + int64_t(b) * SW * CSA2_D : nullptr;
 
-  // stage the cache rows of this split's selected slots and start pulling every row of the split
-  // into L2 at once
+  // stage the cache rows of this split's selected slots and pull every row of the share into L2
   for (int slot = c_begin * kCH + t; slot < min(c_end, nfp4) * kCH; slot += kThreads) {
     int32_t p = slot < n_fp4_valid ? __ldg(irow + slot) : -1;
     if (int64_t(p) >= cap) {
@@ -129,97 +140,132 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     }
   }
   __syncthreads();
-  auto fp4_pos = [&](int slot) -> int64_t { return sm.pos[slot]; };
+
   auto swa_row = [&](int wr) -> int {
     if (wr >= W) return -1;
     const int br = qi + wr;
     return br >= swa_lo ? br : -1;
   };
   auto row_valid = [&](int c, int r) -> bool {
-    return (c < nfp4) ? fp4_pos(c * kCH + r) >= 0 : swa_row((c - nfp4) * kCH + r) >= 0;
+    return (c < nfp4) ? sm.pos[c * kCH + r] >= 0 : swa_row((c - nfp4) * kCH + r) >= 0;
   };
 
   // gather of chunk c into buffer buf: this warp's channel slice only
   auto issue = [&](int c, int buf) {
     if (c < nfp4) {
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int task = it * 32 + lane, r = task >> 2, piece = task & 3;
-        const int64_t pos = fp4_pos(c * kCH + r);
+      for (int it = 0; it < 2; ++it) {  // 32 rows x 2 pieces of 16 code bytes
+        const int task = it * 32 + lane, r = task >> 1, piece = 2 * warp + (task & 1);
+        const int32_t pos = sm.pos[c * kCH + r];
         if (pos >= 0)
-          cp_async16(smem_u32(sm.raw_codes[buf] + r * CSA2_CODE_BYTES + (((4 * warp + piece) ^ (r & 7)) << 4)),
-                     cbase + pos * CSA2_CODE_BYTES + 64 * warp + 16 * piece, 16);
+          cp_async16(smem_u32(sm.raw_codes[buf] + r * CSA2_CODE_BYTES + ((piece ^ (r & 7)) << 4)),
+                     cbase + int64_t(pos) * CSA2_CODE_BYTES + 16 * piece, 16);
       }
-      const int64_t pos = fp4_pos(c * kCH + lane);
+      const int32_t pos = sm.pos[c * kCH + lane];  // 4 scale bytes of row `lane`
       if (pos >= 0)
-        cp_async8(smem_u32(sm.raw_scales[buf] + lane * CSA2_SCALE_BYTES + 8 * warp),
-                  sbase + pos * CSA2_SCALE_BYTES + 8 * warp, 8);
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(
+                         smem_u32(sm.raw_scales[buf] + lane * CSA2_SCALE_BYTES + 4 * warp)),
+                     "l"(sbase + int64_t(pos) * CSA2_SCALE_BYTES + 4 * warp)
+                     : "memory");
     } else {
       const int cw = c - nfp4;
-#pragma unroll 4
-      for (int it = 0; it < 16; ++it) {
-        const int task = it * 32 + lane, r = task >> 4, piece = task & 15;
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {  // 32 rows x 8 pieces of 16 B (64 bf16)
+        const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
         const int br = swa_row(cw * kCH + r);
-        const uint16_t* src = br >= 0 ? swbase + int64_t(br) * CSA2_D + 128 * warp + 8 * piece : swa;
-        cp_async16(smem_u32(sm.kv[buf] + r * CSA2_D + (((16 * warp + piece) ^ (r & 7)) << 3)), src,
-                   br >= 0 ? 16 : 0);
+        const uint16_t* src = br >= 0 ? swbase + int64_t(br) * CSA2_D + 8 * cc : swa;
+        cp_async16(kv_base[buf] + swz(r, cc), src, br >= 0 ? 16 : 0);
       }
     }
   };
 
-  // FP4 slice of chunk c (raw buffer) -> bf16 rows of the KV tile; empty rows become zeros
-  auto dequant = [&](int c, int buf) {
+  // this warp's slice of chunk c -> f16 rows of the KV tile; empty FP4 rows become zeros
+  auto convert = [&](int c, int buf) {
+    uint8_t* kvb = reinterpret_cast<uint8_t*>(sm.kv[buf]);
+    if (c < nfp4) {
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int task = it * 32 + lane, r = task >> 2, piece = task & 3;
-      uint4 o[4];
-      if (fp4_pos(c * kCH + r) >= 0) {
-        const uint4 cb = *reinterpret_cast<const uint4*>(
-            sm.raw_codes[buf] + r * CSA2_CODE_BYTES + (((4 * warp + piece) ^ (r & 7)) << 4));
-        const uint32_t sraw = *reinterpret_cast<const uint16_t*>(sm.raw_scales[buf] + r * CSA2_SCALE_BYTES +
-                                                                 8 * warp + 2 * piece);
-        const uint32_t sa = sm.lut_e4m3[sraw & 0xFFu], sb = sm.lut_e4m3[sraw >> 8];
-        const uint32_t sA = sa | (sa << 16), sB = sb | (sb << 16);
-        const uint32_t words[4] = {cb.x, cb.y, cb.z, cb.w};
+      for (int it = 0; it < 2; ++it) {
+        const int task = it * 32 + lane, r = task >> 1, piece = 2 * warp + (task & 1);
+        uint4 o[4];
+        if (sm.pos[c * kCH + r] >= 0) {
+          const uint4 cb = *reinterpret_cast<const uint4*>(sm.raw_codes[buf] + r * CSA2_CODE_BYTES +
+                                                           ((piece ^ (r & 7)) << 4));
+          const uint8_t* sr = sm.raw_scales[buf] + r * CSA2_SCALE_BYTES + 2 * piece;
+          const uint32_t sa = e4m3_f16(sr[0]), sb = e4m3_f16(sr[1]);
+          const __half2 sA = bits_h2(sa | (sa << 16)), sB = bits_h2(sb | (sb << 16));
+          const uint32_t words[4] = {cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          const uint32_t sc = wi < 2 ? sA : sB;
-          const uint32_t wv = words[wi];
-          o[wi].x = bmul2(sm.lut_e2m1x2[wv & 0xFFu], sc);
-          o[wi].y = bmul2(sm.lut_e2m1x2[(wv >> 8) & 0xFFu], sc);
-          o[wi].z = bmul2(sm.lut_e2m1x2[(wv >> 16) & 0xFFu], sc);
-          o[wi].w = bmul2(sm.lut_e2m1x2[wv >> 24], sc);
+          for (int wi = 0; wi < 4; ++wi) {
+            const __half2 sc = wi < 2 ? sA : sB;
+            const uint32_t wv = words[wi];
+            o[wi].x = h2_bits(__hmul2(bits_h2(e2m1x2_to_f16x2(wv)), sc));
+            o[wi].y = h2_bits(__hmul2(bits_h2(e2m1x2_to_f16x2(wv >> 8)), sc));
+            o[wi].z = h2_bits(__hmul2(bits_h2(e2m1x2_to_f16x2(wv >> 16)), sc));
+            o[wi].w = h2_bits(__hmul2(bits_h2(e2m1x2_to_f16x2(wv >> 24)), sc));
+          }
+        } else {
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi) o[wi] = make_uint4(0, 0, 0, 0);
         }
-      } else {
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) o[wi] = make_uint4(0, 0, 0, 0);
+        for (int wi = 0; wi < 4; ++wi) *reinterpret_cast<uint4*>(kvb + swz(r, 4 * piece + wi)) = o[wi];
       }
+    } else {
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi)
-        *reinterpret_cast<uint4*>(sm.kv[buf] + r * CSA2_D + (((16 * warp + 4 * piece + wi) ^ (r & 7)) << 3)) = o[wi];
+      for (int it = 0; it < 8; ++it) {
+        const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
+        uint4* p = reinterpret_cast<uint4*>(kvb + swz(r, cc));
+        uint4 v = *p;
+        v.x = bf16x2_to_f16x2(v.x);
+        v.y = bf16x2_to_f16x2(v.y);
+        v.z = bf16x2_to_f16x2(v.z);
+        v.w = bf16x2_to_f16x2(v.w);
+        *p = v;
+      }
     }
   };
 
-  float oacc[16][4];
+  float oacc[8][4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f;  // softmax state of head (t >> 3), same in its 8 threads
-  const int sh = t >> 3, sc4 = (t & 7) * 4;
+  for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f;  // softmax state of head (t >> 4), same in its 16 threads
+  const int sh = t >> 4, sc2 = (t & 15) * 2;
 
+  uint32_t qa[4][4];  // this warp's Q slice (16 heads x 64 channels) as four f16 A fragments
   if (c_begin < c_end) {
-    // Q slice of this warp: 16 rows x 256 B
+    // Q slice of this warp: 16 rows x 128 B of bf16, staged in kv[1] (free until chunk c_begin+1
+    // is issued, and each warp touches only its own channel slice), converted to f16, then loaded
+    // into registers
     const uint16_t* qrow = q + int64_t(inst) * CSA2_H * CSA2_D;
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int task = it * 32 + lane, r = task >> 4, piece = task & 15;
-      cp_async16(smem_u32(sm.q + r * CSA2_D + (((16 * warp + piece) ^ (r & 7)) << 3)),
-                 qrow + r * CSA2_D + 128 * warp + 8 * piece, 16);
+    for (int it = 0; it < 4; ++it) {
+      const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
+      cp_async16(kv_base[1] + swz(r, cc), qrow + r * CSA2_D + 8 * cc, 16);
     }
+    cp_async_commit();
     issue(c_begin, 0);
     cp_async_commit();
-    __syncthreads();  // LUTs visible
+    cp_async_wait<1>();
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
+      uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sm.kv[1]) + swz(r, cc));
+      uint4 v = *p;
+      v.x = bf16x2_to_f16x2(v.x);
+      v.y = bf16x2_to_f16x2(v.y);
+      v.z = bf16x2_to_f16x2(v.z);
+      v.w = bf16x2_to_f16x2(v.w);
+      *p = v;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int r = mrow + ((mat & 1) << 3);
+      ldmatrix_x4(qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kv_base[1] + swz(r, 8 * warp + 2 * kk + (mat >> 1)));
+    }
+    __syncwarp();
 
-    uint32_t qa[8][4];
     for (int c = c_begin; c < c_end; ++c) {
       const int buf = (c - c_begin) & 1;
       if (c + 1 < c_end) {
@@ -230,80 +276,66 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         cp_async_wait<0>();
       }
       __syncwarp();
-      if (c == c_begin) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int r = mrow + ((mat & 1) << 3);
-          const int ch = 16 * warp + 2 * kk + (mat >> 1);
-          ldmatrix_x4(qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
-                      smem_u32(sm.q + r * CSA2_D + ((ch ^ (r & 7)) << 3)));
-        }
-      }
-      if (c < nfp4) {
-        dequant(c, buf);
-        __syncwarp();
-      }
-      // ---- S_w = Q[:, slice] K[:, slice]^T for the 32 rows --------------------------------
+      convert(c, buf);
+      __syncwarp();
+      // ---- S_w = Q[:, slice] K[:, slice]^T for the 32 rows ------------------------------------
       float sacc[4][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
         for (int np = 0; np < 2; ++np) {
           const int kr = 16 * np + mrow + ((mat >> 1) << 3);
-          const int ch = 16 * warp + 2 * kk + (mat & 1);
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(b0, b1, b2, b3, smem_u32(sm.kv[buf] + kr * CSA2_D + ((ch ^ (kr & 7)) << 3)));
-          mma_bf16_16816(sacc[2 * np], qa[kk], b0, b1);
-          mma_bf16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
+          ldmatrix_x4(b0, b1, b2, b3, kv_base[buf] + swz(kr, 8 * warp + 2 * kk + (mat & 1)));
+          mma_f16_16816(sacc[2 * np], qa[kk], b0, b1);
+          mma_f16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
         }
       }
       float* sw = sm.s[warp];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         *reinterpret_cast<float2*>(sw + g * kPitchS + 8 * nt + 2 * tq) = make_float2(sacc[nt][0], sacc[nt][1]);
-        *reinterpret_cast<float2*>(sw + (g + 8) * kPitchS + 8 * nt + 2 * tq) =
-            make_float2(sacc[nt][2], sacc[nt][3]);
+        *reinterpret_cast<float2*>(sw + (g + 8) * kPitchS + 8 * nt + 2 * tq) = make_float2(sacc[nt][2], sacc[nt][3]);
       }
       __syncthreads();
-      // ---- online softmax: thread t owns head sh, columns sc4 .. sc4+3 -----------------------
+      // ---- online softmax: thread t owns head sh, columns sc2, sc2+1 ---------------------------
       {
-        float v[4];
+        float v[2];
         float vmax = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = sc4 + e;
-          const int o = sh * kPitchS + col;
-          const float x = (sm.s[0][o] + sm.s[1][o]) + (sm.s[2][o] + sm.s[3][o]);
-          v[e] = row_valid(c, col) ? x * scale_log2 : -INFINITY;
+        for (int e = 0; e < 2; ++e) {
+          const int o = sh * kPitchS + sc2 + e;
+          float x = sm.s[0][o];
+#pragma unroll
+          for (int w2 = 1; w2 < kWarps; ++w2) x += sm.s[w2][o];
+          v[e] = row_valid(c, sc2 + e) ? x * scale_log2 : -INFINITY;
           vmax = fmaxf(vmax, v[e]);
         }
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
         const float m_new = fmaxf(m_run, vmax);
-        float corr = 1.0f, p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float corr = 1.0f, p0 = 0.0f, p1 = 0.0f;
         if (m_new != -INFINITY) {
           corr = exp2f(m_run - m_new);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) p[e] = exp2f(v[e] - m_new);
+          p0 = exp2f(v[0] - m_new);
+          p1 = exp2f(v[1] - m_new);
         }
-        float rs = (p[0] + p[1]) + (p[2] + p[3]);
-        rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-        rs += __shfl_xor_sync(0xffffffffu, rs, 2);
-        rs += __shfl_xor_sync(0xffffffffu, rs, 4);
+        float rs = p0 + p1;
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) rs += __shfl_xor_sync(0xffffffffu, rs, off);
         l_run = l_run * corr + rs;
         m_run = m_new;
-        *reinterpret_cast<uint2*>(sm.p + sh * kPitchP + sc4) = make_uint2(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]));
-        if ((t & 7) == 0) sm.corr[sh] = corr;
+        *reinterpret_cast<uint32_t*>(sm.p + sh * kPitchP + sc2) = pack_f16x2(p0, p1);
+        if ((t & 15) == 0) sm.corr[sh] = corr;
       }
       __syncthreads();
-      // ---- O[:, slice] = corr * O + P V[:, slice] -----------------------------------------------
+      // ---- O[:, slice] = corr * O + P V[:, slice] ---------------------------------------------
       {
         const float cr0 = sm.corr[g], cr1 = sm.corr[g + 8];
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
+        for (int nt = 0; nt < 8; ++nt) {
           oacc[nt][0] *= cr0;
           oacc[nt][1] *= cr0;
           oacc[nt][2] *= cr1;
@@ -317,20 +349,19 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
             ldmatrix_x4(pa[0], pa[1], pa[2], pa[3], smem_u32(sm.p + r * kPitchP + 16 * kk + ((mat >> 1) << 3)));
           }
 #pragma unroll
-          for (int np = 0; np < 8; ++np) {
+          for (int np = 0; np < 4; ++np) {
             const int kr = 16 * kk + mrow + ((mat & 1) << 3);
-            const int ch = 16 * warp + 2 * np + (mat >> 1);
             uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(b0, b1, b2, b3, smem_u32(sm.kv[buf] + kr * CSA2_D + ((ch ^ (kr & 7)) << 3)));
-            mma_bf16_16816(oacc[2 * np], pa, b0, b1);
-            mma_bf16_16816(oacc[2 * np + 1], pa, b2, b3);
+            ldmatrix_x4_trans(b0, b1, b2, b3, kv_base[buf] + swz(kr, 8 * warp + 2 * np + (mat >> 1)));
+            mma_f16_16816(oacc[2 * np], pa, b0, b1);
+            mma_f16_16816(oacc[2 * np + 1], pa, b2, b3);
           }
         }
       }
     }
   }
 
-  if ((t & 7) == 0) {
+  if ((t & 15) == 0) {
     sm.m_fin[sh] = m_run;
     sm.l_fin[sh] = l_run;
   }
@@ -341,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     const float i0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, i1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
     uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D;
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int ch = 128 * warp + 8 * nt + 2 * tq;
+    for (int nt = 0; nt < 8; ++nt) {
+      const int ch = 64 * warp + 8 * nt + 2 * tq;
       *reinterpret_cast<uint32_t*>(orow + g * CSA2_D + ch) = pack_bf16x2(oacc[nt][0] * i0, oacc[nt][1] * i0);
       *reinterpret_cast<uint32_t*>(orow + (g + 8) * CSA2_D + ch) = pack_bf16x2(oacc[nt][2] * i1, oacc[nt][3] * i1);
     }
@@ -356,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   const int64_t instances = gridDim.y;
   float* po = ws + (int64_t(inst) * n_split + split) * (CSA2_H * CSA2_D);
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const int ch = 128 * warp + 8 * nt + 2 * tq;
+  for (int nt = 0; nt < 8; ++nt) {
+    const int ch = 64 * warp + 8 * nt + 2 * tq;
     *reinterpret_cast<float2*>(po + g * CSA2_D + ch) = make_float2(oacc[nt][0], oacc[nt][1]);
     *reinterpret_cast<float2*>(po + (g + 8) * CSA2_D + ch) = make_float2(oacc[nt][2], oacc[nt][3]);
   }
@@ -373,16 +404,16 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   __syncthreads();
   if (!sm.is_last) return;
   __threadfence();
-  // o = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j, splits in order; thread: head t>>3, 64 channels
+  // o = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j, splits in order; thread: head t>>4, 32 channels
   {
-    const int h = t >> 3, c0 = (t & 7) * 64;
+    const int h = t >> 4, c0 = (t & 15) * 32;
     const float* ml = mlb + int64_t(inst) * n_split * (2 * CSA2_H);
     float M = -INFINITY;
     for (int j = 0; j < n_split; ++j) M = fmaxf(M, __ldcg(ml + j * 2 * CSA2_H + 2 * h));
     float L = 0.0f;
-    float acc[64];
+    float acc[32];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
     if (M != -INFINITY) {
       for (int j = 0; j < n_split; ++j) {
         const float a = exp2f(__ldcg(ml + j * 2 * CSA2_H + 2 * h) - M);
@@ -390,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         const float4* pj = reinterpret_cast<const float4*>(ws + (int64_t(inst) * n_split + j) * (CSA2_H * CSA2_D) +
                                                            h * CSA2_D + c0);
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
+        for (int v = 0; v < 8; ++v) {
           const float4 x = __ldcg(pj + v);
           acc[4 * v] += a * x.x;
           acc[4 * v + 1] += a * x.y;
@@ -402,12 +433,12 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     uint4* dst = reinterpret_cast<uint4*>(out + (int64_t(inst) * CSA2_H + h) * CSA2_D + c0);
 #pragma unroll
-    for (int v = 0; v < 8; ++v)
+    for (int v = 0; v < 4; ++v)
       dst[v] = make_uint4(pack_bf16x2(acc[8 * v] * inv, acc[8 * v + 1] * inv),
                           pack_bf16x2(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
                           pack_bf16x2(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
                           pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
-    if (lse && (t & 7) == 0) lse[int64_t(inst) * CSA2_H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    if (lse && (t & 15) == 0) lse[int64_t(inst) * CSA2_H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
   if (t == 0) tickets[inst] = 0u;  // ready for the next launch
 }
@@ -480,7 +511,6 @@ extern "C" csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq,
   if (!q || !out || !al16(q) || !al16(out)) return CSA2_ERR_INVALID_ARG;
   if (k > 0 && (!codes || !scales || !idx || !al16(codes) || !al16(scales))) return CSA2_ERR_INVALID_ARG;
   if (swa && !al16(swa)) return CSA2_ERR_INVALID_ARG;
-  if (k == 0 && !swa) { /* no rows: still defined (zeros, lse = -inf) */ }
   const int ns = n_split ? n_split : csa2::attn_auto_split(instances, k, W);
   const size_t need = csa2::attn_ws_bytes(instances, ns);
   if (need && (!ws || ws_bytes < need || !al16(ws))) return CSA2_ERR_WORKSPACE;

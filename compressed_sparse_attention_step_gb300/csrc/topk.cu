@@ -8,11 +8,13 @@
 //  1. slice histograms: each CTA takes an 8192-key slice of a row and adds a histogram of the top
 //     12 key bits (shared-memory atomics) into the row's global histogram;
 //  2. slice collection: each CTA finds, from the row histogram, the bin b1 that holds the k-th
-//     largest key and appends every key of its slice in a bin >= b1 (at most k - 1 + |b1| keys
-//     per row) to the row's candidate list (warp-aggregated atomic appends);
+//     largest key, gathers every key of its slice in a bin >= b1 in shared memory, then publishes
+//     them to the row's candidate list (at most k - 1 + |b1| keys per row) with one atomic
+//     reservation;
 //  3. per row: the candidates are loaded into shared memory and radix rounds on the key bits,
 //     then on the column bits (ascending, so equal keys go to the lower column), find the exact
-//     k-th (key, column); the k winners are sorted with a bitonic network and written.
+//     k-th (key, column); the winners are written in column order, placed by a prefix count over
+//     a bitmap of the selected columns (or by a bitonic sort for very long rows).
 // A row whose candidates overflow the list (massive ties) is finished by one CTA with the same
 // rounds over the row in global memory and an ordered, scan-based output.  Short rows use that
 // single-CTA path directly.  Counts are integers and every decision is a pure function of the
@@ -22,27 +24,37 @@
 namespace csa2 {
 namespace {
 
-constexpr int kSelThreads = 1024;    // per-row selection CTA
+constexpr int kSelThreads = 512;     // per-row selection CTA
 constexpr int kSliceThreads = 256;   // slice histogram / collection CTAs
 constexpr int64_t kSlice = 8192;     // keys per slice CTA
 constexpr int kCandCap = 10240;      // candidates per row (>= k - 1 + typical |b1|)
 constexpr int kBins = 4096;          // first-level bins (top 12 key bits)
 
+constexpr int64_t kBitmapCols = 262144;   // rows up to this long are ordered through a bitmap
+
 struct SelSmem {
   uint32_t hist[kBins];
   uint32_t cand_key[kCandCap];
   int32_t cand_col[kCandCap];
-  int32_t sel[CSA2_MAX_K];
+  union {
+    int32_t sel[CSA2_MAX_K];
+    uint32_t bits[kBitmapCols / 32];
+  };
   uint32_t scan_tmp[32];
   uint32_t nsel, ncand;
   uint32_t res_bin, res_before;
   uint32_t run_g, run_e;
 };
 
+constexpr int kSliceCand = 2048;     // candidates one slice CTA buffers before publishing them
+
 struct SliceSmem {
   uint32_t hist[kBins];
+  uint32_t cand_key[kSliceCand];
+  int32_t cand_col[kSliceCand];
   uint32_t scan_tmp[32];
   uint32_t res_bin, res_before;
+  uint32_t n, base;
 };
 
 // Visit keys [lo, hi) of a row in tiles of 4 * U * blockDim.x (each thread takes U groups of 4
@@ -140,9 +152,9 @@ __device__ void finish_row(const RowOut& o, int64_t cnt, int row, int32_t* n_sel
   for (int i = int(cnt) * (o.expand8 ? CSA2_BLOCK : 1) + threadIdx.x; i < o.out_w; i += blockDim.x) o.out[i] = -1;
 }
 
-// The k largest of the nc candidates in shared memory (nc >= k) by (key desc, column asc), sorted
-// by column and emitted.
-__device__ void select_candidates(SelSmem& sm, int nc, int k, const RowOut& o) {
+// The k largest of the nc candidates in shared memory (nc >= k) by (key desc, column asc), emitted
+// in column order; columns are < ncols.
+__device__ void select_candidates(SelSmem& sm, int nc, int k, int64_t ncols, const RowOut& o) {
   const int t = threadIdx.x;
   uint32_t need = uint32_t(k), prefix = 0, mask = 0;
   const int kshift[3] = {21, 10, 0}, kwidth[3] = {11, 11, 10};
@@ -183,6 +195,36 @@ __device__ void select_candidates(SelSmem& sm, int nc, int k, const RowOut& o) {
       __syncthreads();
     }
     col_cut = int32_t(cpre);
+  }
+  if (ncols <= kBitmapCols) {
+    // slot of a winner = number of winners in lower columns: bitmap + prefix popcounts
+    const int nwords = int((ncols + 31) / 32);
+    for (int i = t; i < nwords; i += blockDim.x) sm.bits[i] = 0u;
+    __syncthreads();
+    for (int c = t; c < nc; c += blockDim.x) {
+      const uint32_t key = sm.cand_key[c];
+      const int32_t col = sm.cand_col[c];
+      if (key > tau || (key == tau && col <= col_cut)) atomicOr(&sm.bits[col >> 5], 1u << (col & 31));
+    }
+    __syncthreads();
+    const int per = (nwords + int(blockDim.x) - 1) / int(blockDim.x);
+    uint32_t local = 0;
+    for (int e = 0; e < per; ++e) {
+      const int wi = t * per + e;
+      if (wi < nwords) local += __popc(sm.bits[wi]);
+    }
+    uint32_t slot = block_exclusive_scan(local, sm.scan_tmp, nullptr);
+    for (int e = 0; e < per; ++e) {
+      const int wi = t * per + e;
+      if (wi >= nwords) break;
+      uint32_t wv = sm.bits[wi];
+      while (wv) {
+        const int b = __ffs(wv) - 1;
+        o.emit(int(slot++), int32_t(wi * 32 + b));
+        wv &= wv - 1u;
+      }
+    }
+    return;
   }
   if (t == 0) sm.nsel = 0;
   __syncthreads();
@@ -239,7 +281,7 @@ __device__ void select_row(SelSmem& sm, const float* s, int64_t nv, int k, const
       }
     });
     __syncthreads();
-    select_candidates(sm, int(sm.ncand), k, o);
+    select_candidates(sm, int(sm.ncand), k, nv, o);
     return;
   }
   // rounds on key bits [19:10] and [9:0] over the row, then an ordered pass
@@ -302,7 +344,7 @@ __device__ __forceinline__ int64_t row_valid(const int32_t* n_valid, int row, in
 __global__ void __launch_bounds__(kSliceThreads) topk_slice_hist_kernel(const float* __restrict__ scores, int64_t n,
                                                                         int64_t ld, const int32_t* __restrict__ n_valid,
                                                                         int k, uint32_t* __restrict__ ghist) {
-  __shared__ SliceSmem sm;
+  __shared__ struct { uint32_t hist[kBins]; } sm;
   const int row = blockIdx.y;
   const int64_t nv = row_valid(n_valid, row, n);
   const int64_t lo = int64_t(blockIdx.x) * kSlice, hi = min(lo + kSlice, nv);
@@ -332,23 +374,41 @@ __global__ void __launch_bounds__(kSliceThreads) topk_slice_collect_kernel(
   const uint32_t b1 = sm.res_bin;
   const int lane = threadIdx.x & 31;
   const unsigned lanes_below = (1u << lane) - 1u;
-  uint32_t* ck = cand_key + int64_t(row) * kCandCap;
-  int32_t* cc = cand_col + int64_t(row) * kCandCap;
+  if (threadIdx.x == 0) sm.n = 0;
+  __syncthreads();
+  // candidates of the slice gather in shared memory first (shared-memory atomics only) ...
   for_each_key<2>(scores + int64_t(row) * ld, lo, hi, [&](int64_t i, uint32_t key, bool valid) {
     const bool take = valid && (key >> 20) >= b1;
     const unsigned m = __ballot_sync(0xffffffffu, take);
     if (!m) return;
     uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(cand_cnt + row, uint32_t(__popc(m)));
+    if (lane == 0) base = atomicAdd(&sm.n, uint32_t(__popc(m)));
     base = __shfl_sync(0xffffffffu, base, 0);
     if (take) {
       const uint32_t c = base + __popc(m & lanes_below);
-      if (c < uint32_t(kCandCap)) {
-        ck[c] = key;
-        cc[c] = int32_t(i);
+      if (c < uint32_t(kSliceCand)) {
+        sm.cand_key[c] = key;
+        sm.cand_col[c] = int32_t(i);
       }
     }
   });
+  __syncthreads();
+  // ... then one global reservation per CTA publishes them (a count beyond either buffer makes the
+  // row's total exceed kCandCap, which sends the row to the whole-row path)
+  const uint32_t nloc = sm.n;
+  if (threadIdx.x == 0)
+    sm.base = atomicAdd(cand_cnt + row, nloc <= uint32_t(kSliceCand) ? nloc : uint32_t(kCandCap) + 1u);
+  __syncthreads();
+  if (nloc > uint32_t(kSliceCand)) return;
+  uint32_t* ck = cand_key + int64_t(row) * kCandCap;
+  int32_t* cc = cand_col + int64_t(row) * kCandCap;
+  for (uint32_t c = threadIdx.x; c < nloc; c += blockDim.x) {
+    const uint32_t dst = sm.base + c;
+    if (dst < uint32_t(kCandCap)) {
+      ck[dst] = sm.cand_key[c];
+      cc[dst] = sm.cand_col[c];
+    }
+  }
 }
 
 // ---- launch 3 (or the only launch for short rows): per-row selection ------------------------------
@@ -379,7 +439,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
       sm.cand_col[i] = cc[i];
     }
     __syncthreads();
-    select_candidates(sm, int(cnt), k, o);
+    select_candidates(sm, int(cnt), k, nv, o);
   } else {
     select_row(sm, s, nv, k, o);
   }
