@@ -20,8 +20,8 @@
 // accumulate).  The eight partial S are summed in a fixed order, so the only block-wide barriers
 // are the two around each chunk's softmax.
 //
-// Tensor-core inputs are f16: an FP4 row is dequantised with the hardware E2M1 -> f16x2
-// conversion and one f16 multiply by its E4M3 scale, which is exact (at most 6 significant bits,
+// Tensor-core inputs are f16: an FP4 row is dequantised with the hardware E2M1 -> f16x2 and
+// E4M3 -> f16x2 conversions and one f16 multiply by the scale, which is exact (at most 6 significant bits,
 // magnitudes in [2^-10, 2688]); window rows and Q are converted from bf16, which is exact for
 // magnitudes in [2^-14, 65504] (and rounds below); P is rounded to f16.
 #include <cuda_fp16.h>
@@ -57,17 +57,24 @@ struct AttnSmem {
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// Two E2M1 codes (one byte: the even channel in the low nibble) -> f16x2 (even channel low).
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
-  return r;
+// Four code bytes (eight E2M1 codes, the even channel in the low nibble of each byte) -> four f16x2
+// (even channel in the low half), with the hardware conversion.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2,
+                                                  uint32_t& o3) {
+  asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(w));
 }
-// E4M3 (FN) byte -> f16 bits (exact: 4 significant bits, magnitudes 2^-9 .. 448).
-__device__ __forceinline__ uint32_t e4m3_f16(uint32_t b) {
-  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
-  const float v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : float(m) * 0.001953125f;
-  return __half_as_ushort(__float2half_rn((b & 0x80u) ? -v : v));
+// Two E4M3 (FN) scale bytes (first in the low byte) -> f16x2 (first in the low half); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
 }
 // bf16x2 -> f16x2 (round to nearest)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
@@ -101,7 +108,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int g = lane >> 2, tq = lane & 3;
   const int mat = lane >> 3, mrow = lane & 7;
-  const uint32_t kv_base[2] = {smem_u32(sm.kv[0]), smem_u32(sm.kv[1])};
+  const uint32_t kv0 = smem_u32(sm.kv[0]);
+  auto kv_addr = [&](int buf) -> uint32_t { return kv0 + uint32_t(buf) * uint32_t(kCH * CSA2_D * 2); };
 
   // ---- this split's chunks ------------------------------------------------------------------
   const int nfp4 = (k + kCH - 1) / kCH;
@@ -174,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
         const int br = swa_row(cw * kCH + r);
         const uint16_t* src = br >= 0 ? swbase + int64_t(br) * CSA2_D + 8 * cc : swa;
-        cp_async16(kv_base[buf] + swz(r, cc), src, br >= 0 ? 16 : 0);
+        cp_async16(kv_addr(buf) + swz(r, cc), src, br >= 0 ? 16 : 0);
       }
     }
   };
@@ -190,18 +198,19 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         if (sm.pos[c * kCH + r] >= 0) {
           const uint4 cb = *reinterpret_cast<const uint4*>(sm.raw_codes[buf] + r * CSA2_CODE_BYTES +
                                                            ((piece ^ (r & 7)) << 4));
-          const uint8_t* sr = sm.raw_scales[buf] + r * CSA2_SCALE_BYTES + 2 * piece;
-          const uint32_t sa = e4m3_f16(sr[0]), sb = e4m3_f16(sr[1]);
-          const __half2 sA = bits_h2(sa | (sa << 16)), sB = bits_h2(sb | (sb << 16));
+          const uint16_t s2 = *reinterpret_cast<const uint16_t*>(sm.raw_scales[buf] + r * CSA2_SCALE_BYTES + 2 * piece);
+          const __half2 sab = bits_h2(e4m3x2_to_f16x2(s2));
+          const __half2 sA = __low2half2(sab), sB = __high2half2(sab);
           const uint32_t words[4] = {cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
           for (int wi = 0; wi < 4; ++wi) {
             const __half2 sc = wi < 2 ? sA : sB;
-            const uint32_t wv = words[wi];
-            o[wi].x = h2_bits(__hmul2(bits_h2(e2m1x2_to_f16x2(wv)), sc));
-            o[wi].y = h2_bits(__hmul2(bits_h2(e2m1x2_to_f16x2(wv >> 8)), sc));
-            o[wi].z = h2_bits(__hmul2(bits_h2(e2m1x2_to_f16x2(wv >> 16)), sc));
-            o[wi].w = h2_bits(__hmul2(bits_h2(e2m1x2_to_f16x2(wv >> 24)), sc));
+            uint32_t f0, f1, f2, f3;
+            e2m1x8_to_f16x2x4(words[wi], f0, f1, f2, f3);
+            o[wi].x = h2_bits(__hmul2(bits_h2(f0), sc));
+            o[wi].y = h2_bits(__hmul2(bits_h2(f1), sc));
+            o[wi].z = h2_bits(__hmul2(bits_h2(f2), sc));
+            o[wi].w = h2_bits(__hmul2(bits_h2(f3), sc));
           }
         } else {
 #pragma unroll
@@ -240,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
       const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
-      cp_async16(kv_base[1] + swz(r, cc), qrow + r * CSA2_D + 8 * cc, 16);
+      cp_async16(kv_addr(1) + swz(r, cc), qrow + r * CSA2_D + 8 * cc, 16);
     }
     cp_async_commit();
     issue(c_begin, 0);
@@ -262,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const int r = mrow + ((mat & 1) << 3);
-      ldmatrix_x4(qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kv_base[1] + swz(r, 8 * warp + 2 * kk + (mat >> 1)));
+      ldmatrix_x4(qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kv_addr(1) + swz(r, 8 * warp + 2 * kk + (mat >> 1)));
     }
     __syncwarp();
 
@@ -288,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         for (int np = 0; np < 2; ++np) {
           const int kr = 16 * np + mrow + ((mat >> 1) << 3);
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(b0, b1, b2, b3, kv_base[buf] + swz(kr, 8 * warp + 2 * kk + (mat & 1)));
+          ldmatrix_x4(b0, b1, b2, b3, kv_addr(buf) + swz(kr, 8 * warp + 2 * kk + (mat & 1)));
           mma_f16_16816(sacc[2 * np], qa[kk], b0, b1);
           mma_f16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
         }
@@ -352,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
           for (int np = 0; np < 4; ++np) {
             const int kr = 16 * kk + mrow + ((mat & 1) << 3);
             uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(b0, b1, b2, b3, kv_base[buf] + swz(kr, 8 * warp + 2 * np + (mat >> 1)));
+            ldmatrix_x4_trans(b0, b1, b2, b3, kv_addr(buf) + swz(kr, 8 * warp + 2 * np + (mat >> 1)));
             mma_f16_16816(oacc[2 * np], pa, b0, b1);
             mma_f16_16816(oacc[2 * np + 1], pa, b2, b3);
           }

@@ -3,33 +3,32 @@
 // blocks for the hierarchical pool).  Order: larger score first, equal scores by lower column;
 // the k selected columns are returned in ascending order.
 //
-// Radix select on ordered 32-bit score keys (-0 and +0 share a key), in three launches so that a
-// long row is read by many SMs at once:
-//  1. slice histograms: each CTA takes an 8192-key slice of a row and adds a histogram of the top
-//     12 key bits (shared-memory atomics) into the row's global histogram;
-//  2. slice collection: each CTA finds, from the row histogram, the bin b1 that holds the k-th
-//     largest key, gathers every key of its slice in a bin >= b1 in shared memory, then publishes
-//     them to the row's candidate list (at most k - 1 + |b1| keys per row) with one atomic
-//     reservation;
-//  3. per row: the candidates are loaded into shared memory and radix rounds on the key bits,
-//     then on the column bits (ascending, so equal keys go to the lower column), find the exact
-//     k-th (key, column); the winners are written in column order, placed by a prefix count over
-//     a bitmap of the selected columns (or by a bitonic sort for very long rows).
-// A row whose candidates overflow the list (massive ties) is finished by one CTA with the same
-// rounds over the row in global memory and an ordered, scan-based output.  Short rows use that
-// single-CTA path directly.  Counts are integers and every decision is a pure function of the
+// Radix select on ordered 32-bit score keys (-0 and +0 share a key), in one launch of
+// (slices x rows) CTAs so that a long row is read by several SMs at once:
+//  1. each CTA takes a slice of up to 32768 keys of its row, builds a histogram of their top 12 key
+//     bits in shared memory, finds the bin holding the slice's own k-th largest key, and appends
+//     every key of the slice in that bin or above (a superset of the slice's share of the row's
+//     Top-K) to the row's candidate list with one atomic reservation;
+//  2. the last CTA of the row to finish (an atomic ticket) loads the candidates into shared memory;
+//     radix rounds on the key bits, then on the column bits (ascending, so equal keys go to the
+//     lower column), find the exact k-th (key, column); the winners are written in column order,
+//     placed by prefix popcounts over a bitmap of the selected columns (a bitonic sort for very
+//     long rows); it then clears the row's counters for the next launch.
+// A row whose candidates overflow the list (massive ties) is finished by that CTA with the same
+// rounds over the row in global memory and an ordered, scan-based output; rows of one slice use
+// that single-CTA path directly.  Counts are integers and every decision is a pure function of the
 // scores, so the result is deterministic.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace csa2 {
 namespace {
 
-constexpr int kSelThreads = 512;     // per-row selection CTA
-constexpr int kSliceThreads = 256;   // slice histogram / collection CTAs
-constexpr int64_t kSlice = 8192;     // keys per slice CTA
-constexpr int kCandCap = 10240;      // candidates per row (>= k - 1 + typical |b1|)
-constexpr int kBins = 4096;          // first-level bins (top 12 key bits)
-
+constexpr int kThreads = 512;          // CTA size
+constexpr int64_t kSlice = 32768;      // keys per slice CTA
+constexpr int kCandCap = 10240;        // candidates per row
+constexpr int kBins = 4096;            // first-level bins (top 12 key bits)
 constexpr int64_t kBitmapCols = 262144;   // rows up to this long are ordered through a bitmap
 
 struct SelSmem {
@@ -41,20 +40,10 @@ struct SelSmem {
     uint32_t bits[kBitmapCols / 32];
   };
   uint32_t scan_tmp[32];
-  uint32_t nsel, ncand;
+  uint32_t nsel, ncand, base;
   uint32_t res_bin, res_before;
   uint32_t run_g, run_e;
-};
-
-constexpr int kSliceCand = 2048;     // candidates one slice CTA buffers before publishing them
-
-struct SliceSmem {
-  uint32_t hist[kBins];
-  uint32_t cand_key[kSliceCand];
-  int32_t cand_col[kSliceCand];
-  uint32_t scan_tmp[32];
-  uint32_t res_bin, res_before;
-  uint32_t n, base;
+  int is_last;
 };
 
 // Visit keys [lo, hi) of a row in tiles of 4 * U * blockDim.x (each thread takes U groups of 4
@@ -85,34 +74,55 @@ __device__ __forceinline__ void for_each_key(const float* s, int64_t lo, int64_t
   }
 }
 
-// Bin where the cumulative count, walking from the highest bin down (from_top) or from the lowest
-// bin up, first reaches need (1 <= need <= total).  Result in *res_bin / *res_before (count
-// strictly before that bin in walking order).  All threads of the block call it.
-__device__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, bool from_top, uint32_t* scan_tmp,
-                         uint32_t* res_bin, uint32_t* res_before) {
-  const int t = threadIdx.x, nt = blockDim.x;
-  const int per = (nbins + nt - 1) / nt;
-  uint32_t local = 0;
-  for (int e = 0; e < per; ++e) {
-    const int wpos = t * per + e;
-    if (wpos < nbins) local += hist[from_top ? nbins - 1 - wpos : wpos];
+template <int NB>
+__device__ void find_bin_n(const uint32_t* hist, uint32_t need, bool from_top, uint32_t* scan_tmp,
+                           uint32_t* res_bin, uint32_t* res_before) {
+  constexpr int per = NB / kThreads;   // 8, 4 or 2 bins per thread
+  static_assert(per * kThreads == NB && (per == 8 || per == 4 || per == 2), "bin count");
+  const int t = threadIdx.x;
+  // the run of walk positions [t*per, t*per + per) covers bins [lo_bin, lo_bin + per)
+  const int lo_bin = from_top ? NB - (t + 1) * per : t * per;
+  uint32_t h[per];
+  if constexpr (per >= 4) {
+#pragma unroll
+    for (int v = 0; v < per / 4; ++v) {
+      const uint4 a = reinterpret_cast<const uint4*>(hist + lo_bin)[v];
+      h[4 * v] = a.x; h[4 * v + 1] = a.y; h[4 * v + 2] = a.z; h[4 * v + 3] = a.w;
+    }
+  } else {
+    const uint2 a = *reinterpret_cast<const uint2*>(hist + lo_bin);
+    h[0] = a.x; h[1] = a.y;
   }
+  uint32_t local = 0;
+#pragma unroll
+  for (int e = 0; e < per; ++e) local += h[e];
   const uint32_t excl = block_exclusive_scan(local, scan_tmp, nullptr);
   if (excl < need && excl + local >= need) {
     uint32_t cum = excl;
+    bool done = false;
+#pragma unroll
     for (int e = 0; e < per; ++e) {
-      const int wpos = t * per + e;
-      const int bin = from_top ? nbins - 1 - wpos : wpos;
-      const uint32_t h = hist[bin];
-      if (cum + h >= need) {
-        *res_bin = uint32_t(bin);
+      const int i = from_top ? per - 1 - e : e;   // walk order within the run
+      if (!done && cum + h[i] >= need) {
+        *res_bin = uint32_t(lo_bin + i);
         *res_before = cum;
-        break;
+        done = true;
       }
-      cum += h;
+      cum += h[i];
     }
   }
   __syncthreads();
+}
+
+// Bin where the cumulative count, walking from the highest bin down (from_top) or from the lowest
+// bin up, first reaches need (1 <= need <= total).  Result in *res_bin / *res_before (count
+// strictly before that bin in walking order).  All threads of the block call it.  Each thread
+// reads its run of bins with vector loads (a strided scalar walk would hit one bank per warp).
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, bool from_top,
+                                         uint32_t* scan_tmp, uint32_t* res_bin, uint32_t* res_before) {
+  if (nbins == 4096) find_bin_n<4096>(hist, need, from_top, scan_tmp, res_bin, res_before);
+  else if (nbins == 2048) find_bin_n<2048>(hist, need, from_top, scan_tmp, res_bin, res_before);
+  else find_bin_n<1024>(hist, need, from_top, scan_tmp, res_bin, res_before);
 }
 
 __device__ __forceinline__ void zero(uint32_t* h, int n) {
@@ -340,103 +350,91 @@ __device__ __forceinline__ int64_t row_valid(const int32_t* n_valid, int row, in
   return n_valid ? min(max(int64_t(n_valid[row]), int64_t(0)), n) : n;
 }
 
-// ---- launch 1: slice histograms -------------------------------------------------------------------
-__global__ void __launch_bounds__(kSliceThreads) topk_slice_hist_kernel(const float* __restrict__ scores, int64_t n,
-                                                                        int64_t ld, const int32_t* __restrict__ n_valid,
-                                                                        int k, uint32_t* __restrict__ ghist) {
-  __shared__ struct { uint32_t hist[kBins]; } sm;
-  const int row = blockIdx.y;
-  const int64_t nv = row_valid(n_valid, row, n);
-  const int64_t lo = int64_t(blockIdx.x) * kSlice, hi = min(lo + kSlice, nv);
-  if (nv <= k || lo >= hi) return;
-  zero(sm.hist, kBins);
-  hist12(scores + int64_t(row) * ld, lo, hi, sm.hist);
-  __syncthreads();
-  uint32_t* g = ghist + int64_t(row) * kBins;
-  for (int i = threadIdx.x; i < kBins; i += blockDim.x)
-    if (sm.hist[i]) atomicAdd(g + i, sm.hist[i]);
-}
-
-// ---- launch 2: slice collection of the keys in bins >= b1 -----------------------------------------
-__global__ void __launch_bounds__(kSliceThreads) topk_slice_collect_kernel(
-    const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid, int k,
-    const uint32_t* __restrict__ ghist, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_col,
-    uint32_t* __restrict__ cand_cnt) {
-  __shared__ SliceSmem sm;
-  const int row = blockIdx.y;
-  const int64_t nv = row_valid(n_valid, row, n);
-  const int64_t lo = int64_t(blockIdx.x) * kSlice, hi = min(lo + kSlice, nv);
-  if (nv <= k || lo >= hi) return;
-  const uint32_t* g = ghist + int64_t(row) * kBins;
-  for (int i = threadIdx.x; i < kBins; i += blockDim.x) sm.hist[i] = g[i];
-  __syncthreads();
-  find_bin(sm.hist, kBins, uint32_t(k), true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
-  const uint32_t b1 = sm.res_bin;
-  const int lane = threadIdx.x & 31;
-  const unsigned lanes_below = (1u << lane) - 1u;
-  if (threadIdx.x == 0) sm.n = 0;
-  __syncthreads();
-  // candidates of the slice gather in shared memory first (shared-memory atomics only) ...
-  for_each_key<2>(scores + int64_t(row) * ld, lo, hi, [&](int64_t i, uint32_t key, bool valid) {
-    const bool take = valid && (key >> 20) >= b1;
-    const unsigned m = __ballot_sync(0xffffffffu, take);
-    if (!m) return;
-    uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&sm.n, uint32_t(__popc(m)));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (take) {
-      const uint32_t c = base + __popc(m & lanes_below);
-      if (c < uint32_t(kSliceCand)) {
-        sm.cand_key[c] = key;
-        sm.cand_col[c] = int32_t(i);
-      }
-    }
-  });
-  __syncthreads();
-  // ... then one global reservation per CTA publishes them (a count beyond either buffer makes the
-  // row's total exceed kCandCap, which sends the row to the whole-row path)
-  const uint32_t nloc = sm.n;
-  if (threadIdx.x == 0)
-    sm.base = atomicAdd(cand_cnt + row, nloc <= uint32_t(kSliceCand) ? nloc : uint32_t(kCandCap) + 1u);
-  __syncthreads();
-  if (nloc > uint32_t(kSliceCand)) return;
-  uint32_t* ck = cand_key + int64_t(row) * kCandCap;
-  int32_t* cc = cand_col + int64_t(row) * kCandCap;
-  for (uint32_t c = threadIdx.x; c < nloc; c += blockDim.x) {
-    const uint32_t dst = sm.base + c;
-    if (dst < uint32_t(kCandCap)) {
-      ck[dst] = sm.cand_key[c];
-      cc[dst] = sm.cand_col[c];
-    }
-  }
-}
-
-// ---- launch 3 (or the only launch for short rows): per-row selection ------------------------------
-__global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
+__global__ void __launch_bounds__(kThreads, 1) topk_kernel(
     const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid, int k,
     const int32_t* __restrict__ map, int64_t map_ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
-    int expand8, int32_t* __restrict__ pool_len, const uint32_t* __restrict__ cand_key,
-    const int32_t* __restrict__ cand_col, const uint32_t* __restrict__ cand_cnt) {
+    int expand8, int32_t* __restrict__ pool_len, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_col,
+    uint32_t* __restrict__ row_ctl /* [rows][2]: candidate count, ticket */) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
-  const int row = blockIdx.x;
+  const int row = blockIdx.y, nslices = gridDim.x;
+  const int t = threadIdx.x, lane = t & 31;
+  const unsigned lanes_below = (1u << lane) - 1u;
   const float* s = scores + int64_t(row) * ld;
   const int64_t nv = row_valid(n_valid, row, n);
   __syncthreads();  // every thread has read n_valid before pool_len (possibly the same array) is written
   RowOut o{map ? map + int64_t(row) * map_ld : nullptr, idx + int64_t(row) * (expand8 ? k * CSA2_BLOCK : k),
            expand8 ? k * CSA2_BLOCK : k, expand8};
   if (nv <= k) {  // everything valid is selected, already ascending
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) o.emit(i, i);
-    finish_row(o, nv, row, n_sel, pool_len);
+    if (blockIdx.x == 0) {
+      for (int i = t; i < nv; i += kThreads) o.emit(i, i);
+      finish_row(o, nv, row, n_sel, pool_len);
+    }
     return;
   }
-  const uint32_t cnt = cand_cnt ? cand_cnt[row] : 0xFFFFFFFFu;
+  if (nslices == 1) {
+    select_row(sm, s, nv, k, o);
+    finish_row(o, k, row, n_sel, pool_len);
+    return;
+  }
+  uint32_t* ctl = row_ctl + 2 * int64_t(row);
+  // ---- phase 1: this slice's local superset of the Top-K --------------------------------------
+  const int64_t lo = int64_t(blockIdx.x) * kSlice, hi = min(lo + kSlice, nv);
+  if (lo < hi) {
+    zero(sm.hist, kBins);
+    hist12(s, lo, hi, sm.hist);
+    __syncthreads();
+    const uint32_t kk = uint32_t(hi - lo < int64_t(k) ? hi - lo : int64_t(k));
+    find_bin(sm.hist, kBins, kk, true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+    const uint32_t lb1 = sm.res_bin;
+    const uint32_t nloc = sm.res_before + sm.hist[lb1];   // keys of the slice in bins >= lb1
+    if (t == 0) sm.ncand = 0;
+    __syncthreads();
+    if (nloc <= uint32_t(kCandCap)) {
+      for_each_key<2>(s, lo, hi, [&](int64_t i, uint32_t key, bool valid) {
+        const bool take = valid && (key >> 20) >= lb1;
+        const unsigned m = __ballot_sync(0xffffffffu, take);
+        if (!m) return;
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&sm.ncand, uint32_t(__popc(m)));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (take) {
+          const uint32_t c = base + __popc(m & lanes_below);
+          sm.cand_key[c] = key;
+          sm.cand_col[c] = int32_t(i);
+        }
+      });
+      __syncthreads();
+    }
+    if (t == 0)   // an oversized slice pushes the row's count past the list: whole-row path
+      sm.base = atomicAdd(ctl, nloc <= uint32_t(kCandCap) ? nloc : uint32_t(kCandCap) + 1u);
+    __syncthreads();
+    if (nloc <= uint32_t(kCandCap)) {
+      uint32_t* ck = cand_key + int64_t(row) * kCandCap;
+      int32_t* cc = cand_col + int64_t(row) * kCandCap;
+      for (uint32_t c = t; c < nloc; c += kThreads) {
+        const uint32_t dst = sm.base + c;
+        if (dst < uint32_t(kCandCap)) {
+          ck[dst] = sm.cand_key[c];
+          cc[dst] = sm.cand_col[c];
+        }
+      }
+    }
+  }
+  // ---- phase 2: the last slice CTA of the row selects ------------------------------------------
+  __threadfence();
+  __syncthreads();
+  if (t == 0) sm.is_last = (atomicAdd(ctl + 1, 1u) == unsigned(nslices - 1));
+  __syncthreads();
+  if (!sm.is_last) return;
+  __threadfence();
+  const uint32_t cnt = __ldcg(ctl);
   if (cnt <= uint32_t(kCandCap)) {
     const uint32_t* ck = cand_key + int64_t(row) * kCandCap;
     const int32_t* cc = cand_col + int64_t(row) * kCandCap;
-    for (int i = threadIdx.x; i < int(cnt); i += blockDim.x) {
-      sm.cand_key[i] = ck[i];
-      sm.cand_col[i] = cc[i];
+    for (int i = t; i < int(cnt); i += kThreads) {
+      sm.cand_key[i] = __ldcg(ck + i);
+      sm.cand_col[i] = __ldcg(cc + i);
     }
     __syncthreads();
     select_candidates(sm, int(cnt), k, nv, o);
@@ -444,14 +442,24 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_select_kernel(
     select_row(sm, s, nv, k, o);
   }
   finish_row(o, k, row, n_sel, pool_len);
+  if (t == 0) {
+    ctl[0] = 0u;
+    ctl[1] = 0u;
+  }
 }
 
 }  // namespace
 
-// workspace: row histograms, candidate keys and columns, candidate counts
+int topk_slices(int64_t n, int k) {
+  const int64_t by_len = (n + kSlice - 1) / kSlice;
+  const int64_t by_cap = std::max<int64_t>(1, kCandCap / (int64_t(k) + 1024));  // k - 1 + |bin| per slice
+  return int(std::max<int64_t>(1, std::min(by_len, by_cap)));
+}
+
+// workspace: candidate keys and columns per row, then (count, ticket) per row
 size_t topk_ws_bytes(int rows, int64_t n) {
   if (n <= kSlice) return 0;
-  return size_t(rows) * (kBins * sizeof(uint32_t) + kCandCap * (sizeof(uint32_t) + sizeof(int32_t)) + 16);
+  return size_t(rows) * (kCandCap * (sizeof(uint32_t) + sizeof(int32_t)) + 2 * sizeof(uint32_t));
 }
 
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
@@ -463,28 +471,25 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  uint32_t *ghist = nullptr, *ckey = nullptr, *ccnt = nullptr;
+  int nslices = 1;
+  uint32_t *ckey = nullptr, *ctl = nullptr;
   int32_t* ccol = nullptr;
   if (topk_ws_bytes(rows, n) > 0) {
     if (!ws) return cudaErrorInvalidValue;
-    char* p = static_cast<char*>(ws);
-    ghist = reinterpret_cast<uint32_t*>(p);
-    ckey = ghist + size_t(rows) * kBins;
+    nslices = topk_slices(n, k);
+    ckey = static_cast<uint32_t*>(ws);
     ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);
-    ccnt = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
-    cudaError_t e = cudaMemsetAsync(ghist, 0, size_t(rows) * kBins * sizeof(uint32_t), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ccnt, 0, size_t(rows) * sizeof(uint32_t), st);
+    ctl = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
+    cudaError_t e = cudaMemsetAsync(ctl, 0, size_t(rows) * 2 * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
-    const dim3 grid{unsigned((n + kSlice - 1) / kSlice), unsigned(rows), 1u};
-    topk_slice_hist_kernel<<<grid, kSliceThreads, 0, st>>>(scores, n, ld, n_valid, k, ghist);
-    topk_slice_collect_kernel<<<grid, kSliceThreads, 0, st>>>(scores, n, ld, n_valid, k, ghist, ckey, ccol, ccnt);
   }
-  topk_select_kernel<<<rows, kSelThreads, smem, st>>>(scores, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8,
-                                                      pool_len, ckey, ccol, ccnt);
+  const dim3 grid{unsigned(nslices), unsigned(rows), 1u};
+  topk_kernel<<<grid, kThreads, smem, st>>>(scores, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len,
+                                            ckey, ccol, ctl);
   return cudaGetLastError();
 }
 
