@@ -5,7 +5,7 @@
 //
 // Radix select on ordered 32-bit score keys (-0 and +0 share a key), in one launch of
 // (slices x rows) CTAs so that a long row is read by several SMs at once:
-//  1. each CTA takes a slice of up to 32768 keys of its row, builds a histogram of their top 12 key
+//  1. each CTA takes one slice of its row (about 32768 keys; fewer, longer slices when k is large), builds a histogram of their top 12 key
 //     bits in shared memory, finds the bin holding the slice's own k-th largest key, and appends
 //     every key of the slice in that bin or above (a superset of the slice's share of the row's
 //     Top-K) to the row's candidate list with one atomic reservation;
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
     const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid, int k,
     const int32_t* __restrict__ map, int64_t map_ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
     int expand8, int32_t* __restrict__ pool_len, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_col,
-    uint32_t* __restrict__ row_ctl /* [rows][2]: candidate count, ticket */) {
+    uint32_t* __restrict__ row_ctl /* [rows][2]: candidate count, ticket */, int64_t slice_len) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   const int row = blockIdx.y, nslices = gridDim.x;
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
   }
   uint32_t* ctl = row_ctl + 2 * int64_t(row);
   // ---- phase 1: this slice's local superset of the Top-K --------------------------------------
-  const int64_t lo = int64_t(blockIdx.x) * kSlice, hi = min(lo + kSlice, nv);
+  const int64_t lo = int64_t(blockIdx.x) * slice_len, hi = min(lo + slice_len, nv);
   if (lo < hi) {
     zero(sm.hist, kBins);
     hist12(s, lo, hi, sm.hist);
@@ -476,11 +476,13 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
     attr_set[dev] = true;
   }
   int nslices = 1;
+  int64_t slice_len = n;
   uint32_t *ckey = nullptr, *ctl = nullptr;
   int32_t* ccol = nullptr;
   if (topk_ws_bytes(rows, n) > 0) {
     if (!ws) return cudaErrorInvalidValue;
     nslices = topk_slices(n, k);
+    slice_len = ((n + nslices - 1) / nslices + 3) / 4 * 4;   // the slices cover the row; 16-byte starts
     ckey = static_cast<uint32_t*>(ws);
     ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);
     ctl = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
@@ -489,7 +491,7 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
   }
   const dim3 grid{unsigned(nslices), unsigned(rows), 1u};
   topk_kernel<<<grid, kThreads, smem, st>>>(scores, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len,
-                                            ckey, ccol, ctl);
+                                            ckey, ccol, ctl, slice_len);
   return cudaGetLastError();
 }
 
