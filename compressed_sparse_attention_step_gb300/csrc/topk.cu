@@ -132,7 +132,7 @@ __device__ __forceinline__ void zero(uint32_t* h, int n) {
 
 // Histogram of the top 12 key bits of keys [lo, hi) into h (shared memory).
 __device__ __forceinline__ void hist12(const float* s, int64_t lo, int64_t hi, uint32_t* h) {
-  for_each_key<2>(s, lo, hi, [&](int64_t, uint32_t key, bool valid) {
+  for_each_key<8>(s, lo, hi, [&](int64_t, uint32_t key, bool valid) {
     if (valid) atomicAdd(&h[key >> 20], 1u);
   });
 }
@@ -277,7 +277,7 @@ __device__ void select_row(SelSmem& sm, const float* s, int64_t nv, int k, const
   if (ncand <= uint32_t(kCandCap)) {
     if (t == 0) sm.ncand = 0;
     __syncthreads();
-    for_each_key<2>(s, 0, nv, [&](int64_t i, uint32_t key, bool valid) {
+    for_each_key<8>(s, 0, nv, [&](int64_t i, uint32_t key, bool valid) {
       const bool take = valid && (key >> 20) >= b1;
       const unsigned m = __ballot_sync(0xffffffffu, take);
       if (!m) return;
@@ -296,7 +296,7 @@ __device__ void select_row(SelSmem& sm, const float* s, int64_t nv, int k, const
   }
   // rounds on key bits [19:10] and [9:0] over the row, then an ordered pass
   zero(sm.hist, 1024);
-  for_each_key<2>(s, 0, nv, [&](int64_t, uint32_t key, bool valid) {
+  for_each_key<8>(s, 0, nv, [&](int64_t, uint32_t key, bool valid) {
     if (valid && (key >> 20) == b1) atomicAdd(&sm.hist[(key >> 10) & 1023u], 1u);
   });
   __syncthreads();
@@ -305,7 +305,7 @@ __device__ void select_row(SelSmem& sm, const float* s, int64_t nv, int k, const
   need -= sm.res_before;
   __syncthreads();
   zero(sm.hist, 1024);
-  for_each_key<2>(s, 0, nv, [&](int64_t, uint32_t key, bool valid) {
+  for_each_key<8>(s, 0, nv, [&](int64_t, uint32_t key, bool valid) {
     if (valid && (key >> 10) == pre22) atomicAdd(&sm.hist[key & 1023u], 1u);
   });
   __syncthreads();
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
     if (t == 0) sm.ncand = 0;
     __syncthreads();
     if (nloc <= uint32_t(kCandCap)) {
-      for_each_key<2>(s, lo, hi, [&](int64_t i, uint32_t key, bool valid) {
+      for_each_key<8>(s, lo, hi, [&](int64_t i, uint32_t key, bool valid) {
         const bool take = valid && (key >> 20) >= lb1;
         const unsigned m = __ballot_sync(0xffffffffu, take);
         if (!m) return;
