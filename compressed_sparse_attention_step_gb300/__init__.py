@@ -86,6 +86,8 @@ def lib():
             "csa2_status_string": [I32],
             "csa2_device_flags": [ctypes.POINTER(ctypes.c_uint32), I32, P],
             "csa2_group_desc_size": [],
+            "csa2_sparse_attn_decode_static": [P, I32, I32, P, P, I64, P, P, I32, P, P, I32, F32, P, P, I32, P],
+            "csa2_sparse_attn_static_scratch_bytes": [],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -94,6 +96,7 @@ def lib():
         L.csa2_workspace_size.restype = SZ
         L.csa2_status_string.restype = ctypes.c_char_p
         L.csa2_group_desc_size.restype = SZ
+        L.csa2_sparse_attn_static_scratch_bytes.restype = SZ
         if L.csa2_group_desc_size() != ctypes.sizeof(GroupDesc):
             raise RuntimeError("csa2_group_desc layout mismatch between binding and library")
         _lib = L

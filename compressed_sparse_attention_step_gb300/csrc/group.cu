@@ -113,6 +113,7 @@ extern "C" const char* csa2_status_string(csa2_status s) {
     case CSA2_ERR_UNSUPPORTED: return "unsupported dimension";
     case CSA2_ERR_CUDA: return "CUDA error";
     case CSA2_ERR_WORKSPACE: return "workspace missing or too small";
+    case CSA2_ERR_TOO_LARGE: return "problem exceeds the library's built-in scratch";
   }
   return "unknown status";
 }

@@ -55,6 +55,7 @@ typedef enum {
   CSA2_ERR_UNSUPPORTED = 2, /* a dimension other than the fixed ones below              */
   CSA2_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed              */
   CSA2_ERR_WORKSPACE = 4,   /* ws is NULL or smaller than csa2_workspace_size()         */
+  CSA2_ERR_TOO_LARGE = 5,   /* the problem needs more than the library's built-in scratch */
 } csa2_status;
 
 /* Fixed dimensions. */
@@ -187,6 +188,31 @@ csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq, const uint
                                     const int32_t* swa_len, int W, float softmax_scale,
                                     uint16_t* out, float* lse, int n_split, void* ws,
                                     size_t ws_bytes, csa2_stream_t stream);
+
+/*
+ * csa2_sparse_attn_decode without a workspace argument.  The pages have no counterpart: this is an
+ * interface convenience.  Some callers cannot allocate device memory when they call: code running
+ * inside a memory allocator's callbacks (allocating would re-enter the allocator), a service whose
+ * device memory budget is reserved up front (nothing is left to allocate from), a plugin handed only
+ * its input and output buffers (it owns no allocator).  This entry point takes the same arguments as
+ * csa2_sparse_attn_decode minus ws / ws_bytes and allocates nothing.  Its scratch (the split
+ * partials and one ticket per query) is a fixed array of csa2_sparse_attn_static_scratch_bytes()
+ * (16 MiB) inside the library, which every GPU that loads the library reserves until the process
+ * exits; a call whose split needs more returns CSA2_ERR_TOO_LARGE (for example a decode batch of 64
+ * queries at the automatic split of 5 needs about 10.5 MB).  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress), so make that first call before any stream capture
+ * on the device.  Every call uses the same array and leaves its contents behind (the tickets are
+ * cleared at the start of each call): calls that may overlap on the GPU, from any stream or host
+ * thread, race and must be ordered by the caller.
+ */
+csa2_status csa2_sparse_attn_decode_static(const uint16_t* q, int B, int Nq, const uint8_t* codes,
+                                           const uint8_t* scales, int64_t cap, const int32_t* idx,
+                                           const int32_t* n_valid, int k, const uint16_t* swa,
+                                           const int32_t* swa_len, int W, float softmax_scale,
+                                           uint16_t* out, float* lse, int n_split, csa2_stream_t stream);
+
+/* Bytes of the built-in scratch used by csa2_sparse_attn_decode_static. */
+size_t csa2_sparse_attn_static_scratch_bytes(void);
 
 /*
  * One CSA2 layer group (ai-maestro "Compressed Sparse Attention 2": Full / Reindex / Reuse,

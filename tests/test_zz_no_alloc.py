@@ -1,0 +1,76 @@
+"""The allocation-free attention entry point.
+
+csa2_sparse_attn_decode_static serves callers that cannot allocate device memory when they call
+(for instance code running inside a memory allocator's callbacks, or a plugin that is handed only
+its input and output buffers): it keeps its split-KV scratch in a fixed array inside the library.
+These tests call it through the C ABI and check that it reproduces csa2_sparse_attn_decode (which
+takes a caller workspace) within the attention tolerance, on two calls in a row (the array keeps the
+previous call's contents), and that an oversized problem is refused.  The file is collected last so
+that a run stopping at the first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import csa2_synth as syn
+from tests._cases import SCALE, assert_attn_close, bf16_dev, bf16_host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+import compressed_sparse_attention_step_gb300 as c  # noqa: E402
+
+
+def _inputs(seed, B, cap, k, W):
+    kv = np.stack([syn.normal_bf16(seed, syn.T_KV, b, (cap, 512)) for b in range(B)])
+    q = np.stack([syn.normal_bf16(seed, syn.T_Q, b, (1, 16, 512)) for b in range(B)])
+    swa = np.stack([syn.normal_bf16(seed, syn.T_SWA, b, (W, 512)) for b in range(B)])
+    g = np.random.default_rng(seed)
+    idx = np.stack([np.sort(g.choice(cap, k, replace=False)) for _ in range(B)]).astype(np.int32)
+    codes = torch.empty((B, cap, 256), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((B, cap, 32), dtype=torch.uint8, device="cuda")
+    c.csa2_fp4_quantize_append(bf16_dev(kv), codes, scales)
+    swa_len = np.minimum(np.full(B, W), np.arange(B) * 37 + 5).astype(np.int32)
+    return bf16_dev(q), codes, scales, to_dev(idx), bf16_dev(swa), to_dev(swa_len)
+
+
+def _call_static(q, codes, scales, idx, swa, swa_len, out, lse, n_split=0):
+    B, cap, k = q.shape[0], codes.shape[1], idx.shape[1]
+    st = c.lib().csa2_sparse_attn_decode_static(
+        q.data_ptr(), B, 1, codes.data_ptr(), scales.data_ptr(), cap, idx.data_ptr(), None, k,
+        swa.data_ptr(), swa_len.data_ptr(), 128, SCALE, out.data_ptr(), lse.data_ptr(), n_split,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    return st
+
+
+@pytest.mark.parametrize("seed,B", [(71, 7), (72, 64)])
+def test_static_scratch_matches_workspace_entry_point(seed, B):
+    q, codes, scales, idx, swa, swa_len = _inputs(seed, B, 2000, 512, 128)
+    ref = torch.empty((B, 1, 16, 512), dtype=torch.bfloat16, device="cuda")
+    ref_lse = torch.empty((B, 1, 16), dtype=torch.float32, device="cuda")
+    c.csa2_sparse_attn_decode(q, codes, scales, idx, ref, swa=swa, swa_len=swa_len, W=128,
+                              softmax_scale=SCALE, lse=ref_lse)
+    torch.cuda.synchronize()
+    want = syn.bf16_bits_to_f32(bf16_host(ref)).astype(np.float64)
+    for _ in range(2):   # the second call starts from the first call's leftovers
+        out = torch.full((B, 1, 16, 512), 9.0, dtype=torch.bfloat16, device="cuda")
+        lse = torch.zeros((B, 1, 16), dtype=torch.float32, device="cuda")
+        assert _call_static(q, codes, scales, idx, swa, swa_len, out, lse) == 0
+        torch.cuda.synchronize()
+        assert_attn_close(bf16_host(out), want, "static-scratch attention")
+        assert np.allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), atol=1e-2)
+
+
+def test_static_scratch_refuses_oversized_split():
+    cap_bytes = int(c.lib().csa2_sparse_attn_static_scratch_bytes())
+    B = 64
+    q, codes, scales, idx, swa, swa_len = _inputs(73, B, 600, 512, 128)
+    out = torch.zeros((B, 1, 16, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((B, 1, 16), dtype=torch.float32, device="cuda")
+    n_split = 20                              # 64 x 20 splits of 32 KiB exceed 16 MiB
+    assert 64 * n_split * (16 * 512 + 32) * 4 > cap_bytes
+    assert _call_static(q, codes, scales, idx, swa, swa_len, out, lse, n_split=n_split) == 5
+    assert c.lib().csa2_status_string(5) == b"problem exceeds the library's built-in scratch"
