@@ -197,7 +197,7 @@ def csa2_topk(scores, k, idx, *, n_valid=None, n=None, map_=None, n_sel=None, ws
     _check("csa2_topk", lib().csa2_topk(
         _ptr(scores, "scores", (torch.float32,)), rows, n, ld, _ptr(n_valid, "n_valid", (torch.int32,), rows),
         k, _ptr(map_, "map", (torch.int32,)), map_ld, _ptr(idx, "idx", (torch.int32,), rows * k),
-        _ptr(n_sel, "n_sel", (torch.int32,), rows), _ptr(ws, "ws"), 0 if ws is None else ws.numel(),
+        _ptr(n_sel, "n_sel", (torch.int32,), rows), _ptr(ws, "ws"), _nbytes(ws),
         _stream(stream)))
 
 
@@ -212,6 +212,10 @@ def csa2_block_keys_build(KI, lens, block_keys, stream=None):
 def workspace_size(op, *, B=0, Nq=1, cap=0, n=0, k=0, W=0, n_split=0, hierarchical=0, n_blocks_keep=0):
     d = Dims(B, Nq, cap, n, k, W, n_split, hierarchical, n_blocks_keep)
     return int(lib().csa2_workspace_size(op, ctypes.byref(d)))
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
 
 
 def _ws(nbytes, device):
@@ -230,7 +234,7 @@ def csa2_block_pool(qI, w, block_keys, cap, lens, keep, pool, pool_len, *, ratio
         _ptr(block_keys, "block_keys", _bf16_types()), cap, _ptr(lens, "lens", (torch.int32,), B), ratio,
         _ptr(q_pos, "q_pos", (torch.int32,), B * Nq), keep,
         _ptr(pool, "pool", (torch.int32,), B * Nq * keep * BLOCK), _ptr(pool_len, "pool_len", (torch.int32,), B * Nq),
-        _ptr(ws, "ws"), ws.numel(), _stream(stream)))
+        _ptr(ws, "ws"), _nbytes(ws), _stream(stream)))
 
 
 def csa2_sparse_attn_decode(q, codes, scales, idx, out, *, n_valid=None, swa=None, swa_len=None, W=0,
@@ -254,7 +258,7 @@ def csa2_sparse_attn_decode(q, codes, scales, idx, out, *, n_valid=None, swa=Non
         _ptr(n_valid, "n_valid", (torch.int32,), B * Nq), k, _ptr(swa, "swa", _bf16_types()),
         _ptr(swa_len, "swa_len", (torch.int32,), B), W, float(softmax_scale),
         _ptr(out, "out", _bf16_types(), B * Nq * H * D), _ptr(lse, "lse", (torch.float32,), B * Nq * H), ns,
-        _ptr(ws, "ws"), 0 if ws is None else ws.numel(), _stream(stream)))
+        _ptr(ws, "ws"), _nbytes(ws), _stream(stream)))
 
 
 def group_workspace_size(B, Nq, cap, K=512, W=128, hierarchical=False, keep=2048, n_split=0):
@@ -314,7 +318,7 @@ def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa
 
 
 def csa2_group_step(desc, ws, stream=None):
-    _check("csa2_group_step", lib().csa2_group_step(ctypes.byref(desc), _ptr(ws, "ws"), ws.numel(),
+    _check("csa2_group_step", lib().csa2_group_step(ctypes.byref(desc), _ptr(ws, "ws"), _nbytes(ws),
                                                     _stream(stream)))
 
 

@@ -5,25 +5,35 @@
 // architecture"; E2M1 codes with an E4M3 scale per 16 channels: section "FP4 KV, Bounded Replay,
 // and other extensions").  K = V = the dequantised row.
 //
-// Split-KV flash decoding.  A query's rows form a list of 32-row chunks (selected FP4 rows, then
-// window rows); each CTA takes an equal share of consecutive chunks and keeps an online softmax
-// (m, l, O) over them.  The selected positions of the share are staged in shared memory once and
-// every row of the share is prefetched into L2 up front, so the double-buffered per-chunk copies
-// wait on L2 rather than on HBM.  The last CTA of a query to finish (an atomic ticket) merges the
-// splits in split order, so the result does not depend on which CTA finishes last.
+// A query's rows form 64-row tiles: the window rows (ceil(W/64) tiles), then the selected FP4 rows
+// (ceil(k/64) tiles).  A CTA takes a contiguous range of one query's tiles (the split); two CTAs
+// fit on an SM so that one's loads and conversions overlap the other's tensor-core work.  Per CTA:
+//   - the first window tile is copied straight into the operand buffer while the source rows of
+//     the other tiles are resolved and pulled into L2;
+//   - the next FP4 tile's bytes are copied (cp.async) into a staging buffer while the current tile
+//     is processed; window rows are loaded into registers before the operand buffer frees up;
+//   - per tile, the rows are written to shared memory as a 64 x 512 operand in the 128-byte-swizzled
+//     layout the tensor core reads (FP4 rows dequantised to f16 with the E2M1 -> f16x2 and
+//     E4M3 -> f16x2 hardware conversions and one exact f16 multiply; window rows as bf16);
+//   - four warps each issue a quarter of S^T = K Q^T on the 5th-generation tensor core
+//     (tcgen05.mma, M = 64 rows, N = 16 heads, 128 of the 512 channels each) into their own
+//     tensor-memory accumulator; a chain of N = 16 MMAs is bound by per-instruction latency, so
+//     independent chains from several warps run side by side;
+//   - the warps read the four partial S^T back (one row per lane), add them, run the online
+//     softmax and write P^T;
+//   - four warps each issue one 128-channel block of O^T += V^T P^T (M = 128 channels, N = 16
+//     heads, K = 64 rows), V^T being the same shared-memory tile read channel-major; O^T stays in
+//     tensor memory across the CTA's tiles and is rescaled there when the running maximum moves.
+// Splits of a query are merged by the last CTA to finish (an atomic ticket), in split order, so
+// the result does not depend on which CTA finishes last.
 //
-// Inside a CTA, warp w (of 8) owns latent channels [64w, 64w+64) for everything: it gathers only
-// its slice of each row (cp.async, 16-byte pieces, XOR-swizzled in shared memory), converts it to
-// f16 in shared memory, keeps its Q slice in registers, and computes S_w = Q[:, slice] K[:, slice]^T
-// and O[:, slice] += P V[:, slice]
-// on tensor cores with the 16 heads as the M = 16 dimension of mma.m16n8k16 (f16 inputs, fp32
-// accumulate).  The eight partial S are summed in a fixed order, so the only block-wide barriers
-// are the two around each chunk's softmax.
+// Operand types: a tile's MMA operands share one type.  FP4 tiles run in f16: the dequantised row
+// is exact in f16 (at most 6 significant bits, magnitudes in [2^-10, 2688]), Q is converted from
+// bf16 (exact for magnitudes in [2^-14, 65504]) and P is rounded to f16.  Window tiles run in bf16
+// with Q and the rows as given and P rounded to bf16.  Accumulation is fp32.
 //
-// Tensor-core inputs are f16: an FP4 row is dequantised with the hardware E2M1 -> f16x2 and
-// E4M3 -> f16x2 conversions and one f16 multiply by the scale, which is exact (at most 6 significant bits,
-// magnitudes in [2^-10, 2688]); window rows and Q are converted from bf16, which is exact for
-// magnitudes in [2^-14, 65504] (and rounds below); P is rounded to f16.
+// Tensor-memory layouts used: for M = 128 accumulator row r is lane r; for M = 64 row r is lane
+// 32 (r / 16) + r % 16; column n is column n in both.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -33,26 +43,46 @@
 namespace csa2 {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kCH = 32;          // rows per chunk
-constexpr int kPitchP = 40;      // f16 per row of the P tile (80 B: conflict-free ldmatrix)
-constexpr int kPitchS = 36;      // floats per row of the partial-S tiles
+constexpr int kThreads = 256;
+constexpr int kRows = 64;            // rows per tile = MMA M of S^T
 constexpr int kMaxSplit = 32;
+constexpr int kMaxTiles = (CSA2_MAX_ATTN_K + kRows - 1) / kRows + (CSA2_MAX_W + kRows - 1) / kRows;
+constexpr int kIssuers = 4;          // warps whose lane 0 issues tensor-core work (independent chains)
+constexpr uint32_t kOCol = 16 * kIssuers;  // S^T partial i in columns [16 i, 16 i + 16); O^T block i at kOCol + 16 i
+constexpr uint32_t kTmemCols = 128;
 constexpr float kLn2 = 0.6931471805599453f;
 
-struct AttnSmem {
-  uint16_t kv[2][kCH * CSA2_D];                    // f16, swizzled 16-byte chunks (kv[1] first stages Q)
-  uint8_t raw_codes[2][kCH * CSA2_CODE_BYTES];     // swizzled 16-byte pieces
-  uint8_t raw_scales[2][kCH * CSA2_SCALE_BYTES];
-  uint16_t p[CSA2_H * kPitchP];
-  float s[kWarps][CSA2_H * kPitchS];
-  float corr[CSA2_H];
-  float m_fin[CSA2_H];
-  float l_fin[CSA2_H];
-  int32_t pos[CSA2_MAX_ATTN_K];  // cache row of each selected slot of this split, -1 if empty
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr uint32_t kTileGroup = kRows * 128;                 // 8 KiB per 64-channel group
+constexpr uint32_t kTileOff = 0;                             // 8 groups x 64 rows x 128 B
+constexpr uint32_t kQGroup = CSA2_H * 128;                   // 2 KiB
+constexpr uint32_t kQOff = kTileOff + 8 * kTileGroup;        // Q: 8 groups x 16 heads x 128 B
+constexpr uint32_t kPOff = kQOff + 8 * kQGroup;              // P^T: 16 heads x 64 rows (128 B)
+constexpr uint32_t kRawOff = kPOff + kQGroup;                // staged FP4 codes: 64 rows x 256 B
+constexpr uint32_t kRawScOff = kRawOff + kRows * CSA2_CODE_BYTES;  // staged scales: 64 rows x 32 B
+constexpr uint32_t kMiscOff = kRawScOff + kRows * CSA2_SCALE_BYTES;
+
+struct Misc {
+  unsigned long long mbar;
+  uint32_t tmem_base;
   int is_last;
+  int32_t pos[kMaxTiles][kRows];  // source row of each row of the CTA's tiles, -1 if empty
+  float red[4][CSA2_H];           // per-quarter partial max / sum
+  float m_run[CSA2_H];            // running maximum (log2 units), per head
+  float l_run[CSA2_H];            // running sum, per head
+  float corr[CSA2_H];             // rescale factor of the current tile, per head
 };
+constexpr size_t kSmemBytes = 1024 + kMiscOff + sizeof(Misc);
+
+// byte offset of 16-byte chunk cc (0..63) of row r in a 128-byte-swizzled K-major operand whose
+// 64-channel groups are `group` bytes apart
+__device__ __forceinline__ uint32_t sw128(uint32_t group, int r, int cc) {
+  return uint32_t(cc >> 3) * group + uint32_t(r) * 128u + uint32_t(((cc & 7) ^ (r & 7)) << 4);
+}
+// byte offset of 16-byte piece p (0..15) of staged FP4 row r (XOR-swizzled against bank conflicts)
+__device__ __forceinline__ uint32_t raw_off(int r, int p) {
+  return uint32_t(r) * CSA2_CODE_BYTES + uint32_t((p ^ (r & 7)) << 4);
+}
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
@@ -76,22 +106,133 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
 }
-// bf16x2 -> f16x2 (round to nearest)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
   return h2_bits(__floats2half2_rn(bf16lo(u), bf16hi(u)));
 }
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) { return h2_bits(__floats2half2_rn(lo, hi)); }
 
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+// ---- tcgen05 / mbarrier wrappers -----------------------------------------------------------------
+// Shared-memory matrix descriptor: start address, leading / stride byte offsets, descriptor
+// version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((addr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, A/B f16 or bf16, A K-major or MN-major,
+// B K-major, N = 16.
+__device__ __forceinline__ uint32_t instr_desc(int m, bool bf16, bool a_mn_major) {
+  return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | (a_mn_major ? (1u << 15) : 0u) |
+         ((uint32_t(CSA2_H) >> 3) << 17) | ((uint32_t(m) >> 4) << 24);
+}
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      "{ .reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for phase `parity` of the mbarrier, for at most about one second.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p; }\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 63u) == 0u) {
+      const uint64_t now = global_ns();
+      if (it == 0u) t0 = now;
+      else if (now - t0 > 1000000000ull) return false;
+    }
+  }
 }
 
-// byte offset of logical 16-byte chunk cc (0..63) of row r in a 1 KiB-per-row swizzled tile
-__device__ __forceinline__ int swz(int r, int cc) { return r * (CSA2_D * 2) + ((cc ^ (r & 7)) << 4); }
+// Columns c, c + 16, c + 32, c + 48 (8 each) of this warp's 32 lanes, one wait for all four.
+__device__ __forceinline__ void tmem_ld8x4(uint32_t taddr, float (&v)[4][8]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%33];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%34];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24, %25, %26, %27, %28, %29, %30, %31}, [%35];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "r"(taddr + 16), "r"(taddr + 32), "r"(taddr + 48)
+      : "memory");
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[g][i] = __uint_as_float(r[8 * g + i]);
+}
+// Columns c .. c + 31 of this warp's 32 lanes as two groups of 16, one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, float (&v)[2][16]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "r"(taddr + 16)
+      : "memory");
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[g][i] = __uint_as_float(r[16 * g + i]);
+}
+__device__ __forceinline__ void tmem_st16x2(uint32_t taddr, const float (&v)[2][16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%1], {%18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33};\n\t"
+      "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr), "r"(taddr + 16),
+      "r"(__float_as_uint(v[0][0])), "r"(__float_as_uint(v[0][1])), "r"(__float_as_uint(v[0][2])), "r"(__float_as_uint(v[0][3])), "r"(__float_as_uint(v[0][4])), "r"(__float_as_uint(v[0][5])), "r"(__float_as_uint(v[0][6])), "r"(__float_as_uint(v[0][7])), "r"(__float_as_uint(v[0][8])), "r"(__float_as_uint(v[0][9])), "r"(__float_as_uint(v[0][10])), "r"(__float_as_uint(v[0][11])), "r"(__float_as_uint(v[0][12])), "r"(__float_as_uint(v[0][13])), "r"(__float_as_uint(v[0][14])), "r"(__float_as_uint(v[0][15])), "r"(__float_as_uint(v[1][0])), "r"(__float_as_uint(v[1][1])), "r"(__float_as_uint(v[1][2])), "r"(__float_as_uint(v[1][3])), "r"(__float_as_uint(v[1][4])), "r"(__float_as_uint(v[1][5])), "r"(__float_as_uint(v[1][6])), "r"(__float_as_uint(v[1][7])), "r"(__float_as_uint(v[1][8])), "r"(__float_as_uint(v[1][9])), "r"(__float_as_uint(v[1][10])), "r"(__float_as_uint(v[1][11])), "r"(__float_as_uint(v[1][12])), "r"(__float_as_uint(v[1][13])), "r"(__float_as_uint(v[1][14])), "r"(__float_as_uint(v[1][15]))
+      : "memory");
+}
+
+// Eight values per lane (heads 0..7 of a row) -> lane l returns the combination over the warp's
+// 32 lanes for head (l >> 2), in a fixed tree order.
+template <bool kMax>
+__device__ __forceinline__ float reduce_scatter8(const float (&v)[8], int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4;
+  float a[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = u16 ? v[i] : v[i + 4], keep = u16 ? v[i + 4] : v[i];
+    a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+  float b[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = u8 ? a[i] : a[i + 2], keep = u8 ? a[i + 2] : a[i];
+    b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+  float c;
+  {
+    const float send = u4 ? b[0] : b[1], keep = u4 ? b[1] : b[0];
+    c = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  c = op(c, __shfl_xor_sync(0xffffffffu, c, 2));
+  c = op(c, __shfl_xor_sync(0xffffffffu, c, 1));
+  return c;
+}
 
 __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     const uint16_t* __restrict__ q, int Nq, const uint8_t* __restrict__ codes,
@@ -100,359 +241,471 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     const int32_t* __restrict__ swa_len, int W, float scale_log2, uint16_t* __restrict__ out,
     float* __restrict__ lse, int n_split, float* __restrict__ ws, unsigned int* __restrict__ tickets,
     unsigned int* flags) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
-  const int inst = blockIdx.y;
-  const int split = blockIdx.x;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+  unsigned char* base = smem_raw + (base_s - raw_s);
+  Misc& ms = *reinterpret_cast<Misc*>(base + kMiscOff);
+  const uint32_t tile_s = base_s + kTileOff, q_s = base_s + kQOff, p_s = base_s + kPOff;
+  const uint32_t mbar = smem_u32(&ms.mbar);
+
+  const int inst = blockIdx.y, split = blockIdx.x;
   const int b = inst / Nq, qi = inst - b * Nq;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int g = lane >> 2, tq = lane & 3;
-  const int mat = lane >> 3, mrow = lane & 7;
-  const uint32_t kv0 = smem_u32(sm.kv[0]);
-  auto kv_addr = [&](int buf) -> uint32_t { return kv0 + uint32_t(buf) * uint32_t(kCH * CSA2_D * 2); };
+  const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter; heads / channel blocks half
 
-  // ---- this split's chunks ------------------------------------------------------------------
-  const int nfp4 = (k + kCH - 1) / kCH;
-  const int nswa = swa ? (W + kCH - 1) / kCH : 0;
-  const int nch = nfp4 + nswa;
-  const int c_begin = split * nch / n_split, c_end = (split + 1) * nch / n_split;
-
+  // ---- this split's tiles: window tiles first, then FP4 tiles ---------------------------------------
+  const int nwin = swa ? (W + kRows - 1) / kRows : 0;
+  const int ntiles = nwin + (k + kRows - 1) / kRows;
+  const int t_begin = split * ntiles / n_split, t_end = (split + 1) * ntiles / n_split;
   const int n_fp4_valid = min(k, n_valid ? max(n_valid[inst], 0) : k);
-  const int32_t* irow = idx + int64_t(inst) * k;
   const int SW = W - 1 + Nq;
   const int swa_lo = swa ? SW - min(max(swa_len[b], 0), SW) : SW;
+  // a tile can hold a row: window tiles reaching a stored row, FP4 tiles below n_fp4_valid
+  auto live = [&](int tile) {
+    if (tile < nwin) return qi + min((tile + 1) * kRows, W) - 1 >= swa_lo;
+    return (tile - nwin) * kRows < n_fp4_valid;
+  };
+  int first_live = -1, last_live = -1;
+  for (int tile = t_begin; tile < t_end; ++tile)
+    if (live(tile)) {
+      if (first_live < 0) first_live = tile;
+      last_live = tile;
+    }
+
+  const int32_t* irow = idx + int64_t(inst) * k;
   const uint8_t* cbase = codes + int64_t(b) * cap * CSA2_CODE_BYTES;
   const uint8_t* sbase = scales + int64_t(b) * cap * CSA2_SCALE_BYTES;
   const uint16_t* swbase = swa ? swa + int64_t(b) * SW * CSA2_D : nullptr;
+  const uint16_t* qrow = q + int64_t(inst) * CSA2_H * CSA2_D;
 
-  // stage the cache rows of this split's selected slots and pull every row of the share into L2
-  for (int slot = c_begin * kCH + t; slot < min(c_end, nfp4) * kCH; slot += kThreads) {
-    int32_t p = slot < n_fp4_valid ? __ldg(irow + slot) : -1;
-    if (int64_t(p) >= cap) {
-      atomicOr(flags, CSA2_FLAG_INDEX_OOB);
-      p = -1;
+  // window row of tile row r of window tile `tile`, or -1
+  auto win_row = [&](int tile, int r) {
+    const int wr = tile * kRows + r;
+    return (wr < W && qi + wr >= swa_lo) ? qi + wr : -1;
+  };
+  // window tile -> operand tile (cp.async; empty rows are zero-filled)
+  // thread t: rows (t & 7) + 8 (j & 7), 16-byte chunks (t >> 3) + 32 (j >> 3), j = 0..15
+  auto copy_window = [&](int tile) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int r = (t & 7) + 8 * (j & 7), cc = (t >> 3) + 32 * (j >> 3);
+      const int br = win_row(tile, r);
+      const uint16_t* src = br >= 0 ? swbase + int64_t(br) * CSA2_D + 8 * cc : swa;
+      cp_async16(tile_s + sw128(kTileGroup, r, cc), src, br >= 0 ? 16 : 0);
     }
-    sm.pos[slot] = p < 0 ? -1 : p;
-    if (p >= 0) {
-      const uint8_t* cr = cbase + int64_t(p) * CSA2_CODE_BYTES;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(cr));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(cr + 128));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(sbase + int64_t(p) * CSA2_SCALE_BYTES));
-    }
+    cp_async_commit();
+  };
+
+  if (t < CSA2_H) {
+    ms.m_run[t] = -INFINITY;
+    ms.l_run[t] = 0.0f;
   }
-  if (swa) {
-    const int w0 = max(c_begin, nfp4) * kCH - nfp4 * kCH, w1 = min(c_end * kCH - nfp4 * kCH, W);
-    for (int e = t; e < max(w1 - w0, 0) * 8; e += kThreads) {   // 8 lines of 128 B per row
-      const int br = qi + w0 + (e >> 3);
-      if (br >= swa_lo) asm volatile("prefetch.global.L2 [%0];" ::"l"(swbase + int64_t(br) * CSA2_D + (e & 7) * 64));
+  if (first_live >= 0) {
+    // tensor memory, the MMA barrier, and the first window tile's rows, before anything waits
+    if (t == 0) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(mbar), "r"(kIssuers) : "memory");
+      asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
+    if (warp == 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&ms.tmem_base)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    if (first_live < nwin) copy_window(first_live);
   }
+  // ---- source rows of every tile of the split; FP4 and later window rows pulled into L2 ------------
+  for (int e = t; e < (t_end - t_begin) * kRows; e += kThreads) {
+    const int tile = t_begin + e / kRows, r = e % kRows;
+    int32_t p = -1;
+    if (tile >= nwin) {
+      const int slot = (tile - nwin) * kRows + r;
+      if (slot < n_fp4_valid) {
+        p = __ldg(irow + slot);
+        if (int64_t(p) >= cap) {
+          atomicOr(flags, CSA2_FLAG_INDEX_OOB);
+          p = -1;
+        }
+        if (p >= 0) {
+          const uint8_t* cr = cbase + int64_t(p) * CSA2_CODE_BYTES;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(cr));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(cr + 128));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(sbase + int64_t(p) * CSA2_SCALE_BYTES));
+        }
+      }
+    } else {
+      p = win_row(tile, r);
+      if (p >= 0 && tile != first_live) {
+        const uint16_t* sr = swbase + int64_t(p) * CSA2_D;
+#pragma unroll
+        for (int l = 0; l < 8; ++l) asm volatile("prefetch.global.L2 [%0];" ::"l"(sr + 64 * l));
+      }
+    }
+    ms.pos[tile - t_begin][r] = p < 0 ? -1 : p;
+  }
+  tc_fence_before();
   __syncthreads();
 
-  auto swa_row = [&](int wr) -> int {
-    if (wr >= W) return -1;
-    const int br = qi + wr;
-    return br >= swa_lo ? br : -1;
-  };
-  auto row_valid = [&](int c, int r) -> bool {
-    return (c < nfp4) ? sm.pos[c * kCH + r] >= 0 : swa_row((c - nfp4) * kCH + r) >= 0;
-  };
-
-  // gather of chunk c into buffer buf: this warp's channel slice only
-  auto issue = [&](int c, int buf) {
-    if (c < nfp4) {
+  // FP4 tile -> staging buffer (cp.async; empty rows are zero-filled).  Thread t copies 16-byte
+  // piece (t >> 3) & 15 of rows (t & 7) + 8 ((t >> 7) + 2 i), i < 4, and one half of row t >> 1's
+  // scale bytes.
+  auto stage_fp4 = [&](int tile) {
+    const int32_t* pos = ms.pos[tile - t_begin];
 #pragma unroll
-      for (int it = 0; it < 2; ++it) {  // 32 rows x 2 pieces of 16 code bytes
-        const int task = it * 32 + lane, r = task >> 1, piece = 2 * warp + (task & 1);
-        const int32_t pos = sm.pos[c * kCH + r];
-        if (pos >= 0)
-          cp_async16(smem_u32(sm.raw_codes[buf] + r * CSA2_CODE_BYTES + ((piece ^ (r & 7)) << 4)),
-                     cbase + int64_t(pos) * CSA2_CODE_BYTES + 16 * piece, 16);
-      }
-      const int32_t pos = sm.pos[c * kCH + lane];  // 4 scale bytes of row `lane`
-      if (pos >= 0)
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(
-                         smem_u32(sm.raw_scales[buf] + lane * CSA2_SCALE_BYTES + 4 * warp)),
-                     "l"(sbase + int64_t(pos) * CSA2_SCALE_BYTES + 4 * warp)
-                     : "memory");
-    } else {
-      const int cw = c - nfp4;
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {  // 32 rows x 8 pieces of 16 B (64 bf16)
-        const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
-        const int br = swa_row(cw * kCH + r);
-        const uint16_t* src = br >= 0 ? swbase + int64_t(br) * CSA2_D + 8 * cc : swa;
-        cp_async16(kv_addr(buf) + swz(r, cc), src, br >= 0 ? 16 : 0);
-      }
+    for (int i = 0; i < 4; ++i) {
+      const int r = (t & 7) + 8 * ((t >> 7) + 2 * i), piece = (t >> 3) & 15;
+      const int32_t p = pos[r];
+      const uint8_t* src = p >= 0 ? cbase + int64_t(p) * CSA2_CODE_BYTES + 16 * piece : codes;
+      cp_async16(base_s + kRawOff + raw_off(r, piece), src, p >= 0 ? 16 : 0);
     }
+    if (t < 2 * kRows) {
+      const int r = t >> 1, h2 = t & 1;
+      const int32_t p = pos[r];
+      const uint8_t* src = p >= 0 ? sbase + int64_t(p) * CSA2_SCALE_BYTES + 16 * h2 : scales;
+      cp_async16(base_s + kRawScOff + r * CSA2_SCALE_BYTES + 16 * h2, src, p >= 0 ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+  auto next_live = [&](int tile) {
+    while (tile <= last_live && !live(tile)) ++tile;
+    return tile;
   };
 
-  // this warp's slice of chunk c -> f16 rows of the KV tile; empty FP4 rows become zeros
-  auto convert = [&](int c, int buf) {
-    uint8_t* kvb = reinterpret_cast<uint8_t*>(sm.kv[buf]);
-    if (c < nfp4) {
+  bool ok = true;
+  if (first_live >= 0) {
+    tc_fence_after();
+    const uint32_t tmem = ms.tmem_base;
+    const uint32_t t_lane = tmem + (uint32_t(32 * quarter) << 16);  // this warp's lane quarter
+    const int first_fp4 = next_live(max(first_live, nwin));
+    if (first_fp4 <= last_live) stage_fp4(first_fp4);  // first FP4 tile, behind any window tile's copy
+    uint32_t phase = 0;
+    int q_kind = -1;  // 0: Q staged as f16, 1: as bf16
+    bool first = true;
+
+    for (int tile = first_live; tile <= last_live; ++tile) {
+      if (!live(tile)) continue;
+      const bool is_fp4 = tile >= nwin;
+      const int32_t* pos = ms.pos[tile - t_begin];
+      // -- a later window tile: half of its rows into registers before the operand tile is free
+      auto win_load = [&](int j) -> uint4 {
+        const int r = (t & 7) + 8 * (j & 7), cc = (t >> 3) + 32 * (j >> 3);
+        const int32_t br = pos[r];
+        return br >= 0 ? __ldg(reinterpret_cast<const uint4*>(swbase + int64_t(br) * CSA2_D + 8 * cc))
+                       : make_uint4(0, 0, 0, 0);
+      };
+      auto win_store = [&](int j, uint4 v) {
+        const int r = (t & 7) + 8 * (j & 7), cc = (t >> 3) + 32 * (j >> 3);
+        *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, cc)) = v;
+      };
+      const bool win_regs = !is_fp4 && !first;
+      uint4 wv[8];
+      if (win_regs) {
 #pragma unroll
-      for (int it = 0; it < 2; ++it) {
-        const int task = it * 32 + lane, r = task >> 1, piece = 2 * warp + (task & 1);
-        uint4 o[4];
-        if (sm.pos[c * kCH + r] >= 0) {
-          const uint4 cb = *reinterpret_cast<const uint4*>(sm.raw_codes[buf] + r * CSA2_CODE_BYTES +
-                                                           ((piece ^ (r & 7)) << 4));
-          const uint16_t s2 = *reinterpret_cast<const uint16_t*>(sm.raw_scales[buf] + r * CSA2_SCALE_BYTES + 2 * piece);
+        for (int j = 0; j < 8; ++j) wv[j] = win_load(j);
+      }
+      // -- the previous tile's O^T MMAs read the operand tile and P^T: wait for them
+      if (!first) {
+        ok = ok && mbar_wait(mbar, phase);
+        phase ^= 1u;
+      }
+      // -- Q in the tile's operand type
+      const int kind = is_fp4 ? 0 : 1;
+      if (kind != q_kind) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int h = (t & 7) + 8 * (j & 1), cc = (t >> 3) + 32 * (j >> 1);
+          uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + h * CSA2_D + 8 * cc));
+          if (kind == 0) {
+            v.x = bf16x2_to_f16x2(v.x);
+            v.y = bf16x2_to_f16x2(v.y);
+            v.z = bf16x2_to_f16x2(v.z);
+            v.w = bf16x2_to_f16x2(v.w);
+          }
+          *reinterpret_cast<uint4*>(base + kQOff + sw128(kQGroup, h, cc)) = v;
+        }
+        q_kind = kind;
+      }
+      // -- rows -> operand tile
+      if (is_fp4) {
+        cp_async_wait<0>();
+        __syncthreads();  // every thread's staged pieces are visible
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = (t & 7) + 8 * ((t >> 7) + 2 * i), piece = (t >> 3) & 15;
+          const uint4 cw = *reinterpret_cast<const uint4*>(base + kRawOff + raw_off(r, piece));
+          const uint16_t s2 = *reinterpret_cast<const uint16_t*>(base + kRawScOff + r * CSA2_SCALE_BYTES + 2 * piece);
           const __half2 sab = bits_h2(e4m3x2_to_f16x2(s2));
           const __half2 sA = __low2half2(sab), sB = __high2half2(sab);
-          const uint32_t words[4] = {cb.x, cb.y, cb.z, cb.w};
+          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
           for (int wi = 0; wi < 4; ++wi) {
             const __half2 sc = wi < 2 ? sA : sB;
             uint32_t f0, f1, f2, f3;
             e2m1x8_to_f16x2x4(words[wi], f0, f1, f2, f3);
-            o[wi].x = h2_bits(__hmul2(bits_h2(f0), sc));
-            o[wi].y = h2_bits(__hmul2(bits_h2(f1), sc));
-            o[wi].z = h2_bits(__hmul2(bits_h2(f2), sc));
-            o[wi].w = h2_bits(__hmul2(bits_h2(f3), sc));
+            uint4 o;
+            o.x = h2_bits(__hmul2(bits_h2(f0), sc));
+            o.y = h2_bits(__hmul2(bits_h2(f1), sc));
+            o.z = h2_bits(__hmul2(bits_h2(f2), sc));
+            o.w = h2_bits(__hmul2(bits_h2(f3), sc));
+            *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, 4 * piece + wi)) = o;
           }
-        } else {
-#pragma unroll
-          for (int wi = 0; wi < 4; ++wi) o[wi] = make_uint4(0, 0, 0, 0);
         }
+      } else if (win_regs) {
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) *reinterpret_cast<uint4*>(kvb + swz(r, 4 * piece + wi)) = o[wi];
-      }
-    } else {
+        for (int j = 0; j < 8; ++j) win_store(j, wv[j]);
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
-        uint4* p = reinterpret_cast<uint4*>(kvb + swz(r, cc));
-        uint4 v = *p;
-        v.x = bf16x2_to_f16x2(v.x);
-        v.y = bf16x2_to_f16x2(v.y);
-        v.z = bf16x2_to_f16x2(v.z);
-        v.w = bf16x2_to_f16x2(v.w);
-        *p = v;
-      }
-    }
-  };
-
-  float oacc[8][4];
+        for (int j = 0; j < 8; ++j) wv[j] = win_load(8 + j);  // hits L2 (prefetched)
 #pragma unroll
-  for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f;  // softmax state of head (t >> 4), same in its 16 threads
-  const int sh = t >> 4, sc2 = (t & 15) * 2;
-
-  uint32_t qa[4][4];  // this warp's Q slice (16 heads x 64 channels) as four f16 A fragments
-  if (c_begin < c_end) {
-    // Q slice of this warp: 16 rows x 128 B of bf16, staged in kv[1] (free until chunk c_begin+1
-    // is issued, and each warp touches only its own channel slice), converted to f16, then loaded
-    // into registers
-    const uint16_t* qrow = q + int64_t(inst) * CSA2_H * CSA2_D;
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
-      cp_async16(kv_addr(1) + swz(r, cc), qrow + r * CSA2_D + 8 * cc, 16);
-    }
-    cp_async_commit();
-    issue(c_begin, 0);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncwarp();
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int task = it * 32 + lane, r = task >> 3, cc = 8 * warp + (task & 7);
-      uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sm.kv[1]) + swz(r, cc));
-      uint4 v = *p;
-      v.x = bf16x2_to_f16x2(v.x);
-      v.y = bf16x2_to_f16x2(v.y);
-      v.z = bf16x2_to_f16x2(v.z);
-      v.w = bf16x2_to_f16x2(v.w);
-      *p = v;
-    }
-    __syncwarp();
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const int r = mrow + ((mat & 1) << 3);
-      ldmatrix_x4(qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kv_addr(1) + swz(r, 8 * warp + 2 * kk + (mat >> 1)));
-    }
-    __syncwarp();
-
-    for (int c = c_begin; c < c_end; ++c) {
-      const int buf = (c - c_begin) & 1;
-      if (c + 1 < c_end) {
-        issue(c + 1, buf ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();
+        for (int j = 0; j < 8; ++j) win_store(8 + j, wv[j]);
+      } else if (first_fp4 <= last_live) {
+        cp_async_wait<1>();  // the window copy; the staged FP4 tile may still be in flight
       } else {
         cp_async_wait<0>();
       }
-      __syncwarp();
-      convert(c, buf);
-      __syncwarp();
-      // ---- S_w = Q[:, slice] K[:, slice]^T for the 32 rows ------------------------------------
-      float sacc[4][4];
+      fence_async_smem();
+      __syncthreads();
+
+      // -- S^T = K Q^T (tensor core): warp i < 4 issues channels [128 i, 128 i + 128) in 8 steps
+      if (lane == 0 && warp < kIssuers) {
+        tc_fence_after();
+        const uint32_t id = instr_desc(kRows, !is_fp4, false);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.0f;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          const int kr = 16 * np + mrow + ((mat >> 1) << 3);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(b0, b1, b2, b3, kv_addr(buf) + swz(kr, 8 * warp + 2 * kk + (mat & 1)));
-          mma_f16_16816(sacc[2 * np], qa[kk], b0, b1);
-          mma_f16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
+        for (int k8 = 0; k8 < CSA2_D / 16 / kIssuers; ++k8) {
+          const int kk = warp * (CSA2_D / 16 / kIssuers) + k8;
+          const uint32_t off = uint32_t(kk & 3) * 32u;  // 16 channels = 32 B inside the swizzle atom
+          const uint64_t a = smem_desc(tile_s + uint32_t(kk >> 2) * kTileGroup + off, 0, 1024);
+          const uint64_t bq = smem_desc(q_s + uint32_t(kk >> 2) * kQGroup + off, 0, 1024);
+          umma_f16(tmem + uint32_t(16 * warp), a, bq, id, k8 > 0 ? 1u : 0u);
         }
+        umma_commit(mbar);
       }
-      float* sw = sm.s[warp];
+      // -- the staging buffer is free again: copy the next FP4 tile while this one is computed
+      if (is_fp4) {
+        const int nxt = next_live(tile + 1);
+        if (nxt <= last_live) stage_fp4(nxt);
+      }
+      ok = ok && mbar_wait(mbar, phase);
+      phase ^= 1u;
+      tc_fence_after();
+
+      // -- online softmax: warp (quarter, half) holds rows 16 quarter + lane (lanes < 16) and
+      //    heads 8 half .. 8 half + 7; S^T is the sum of the four channel-quarter partials
+      const int row = 16 * quarter + (lane & 15);
+      float x[8];
+      {
+        float sp[4][8];
+        tmem_ld8x4(t_lane + uint32_t(8 * half), sp);
+        const bool row_ok = lane < 16 && pos[row] >= 0;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        *reinterpret_cast<float2*>(sw + g * kPitchS + 8 * nt + 2 * tq) = make_float2(sacc[nt][0], sacc[nt][1]);
-        *reinterpret_cast<float2*>(sw + (g + 8) * kPitchS + 8 * nt + 2 * tq) = make_float2(sacc[nt][2], sacc[nt][3]);
+        for (int j = 0; j < 8; ++j)
+          x[j] = row_ok ? ((sp[0][j] + sp[1][j]) + (sp[2][j] + sp[3][j])) * scale_log2 : -INFINITY;
+      }
+      {
+        const float mx = reduce_scatter8<true>(x, lane);
+        if ((lane & 3) == 0) ms.red[quarter][8 * half + (lane >> 2)] = mx;
+      }
+      tc_fence_before();
+      __syncthreads();
+      if (t < CSA2_H) {
+        const float mt = fmaxf(fmaxf(ms.red[0][t], ms.red[1][t]), fmaxf(ms.red[2][t], ms.red[3][t]));
+        const float mo = ms.m_run[t], mn = fmaxf(mo, mt);
+        ms.corr[t] = mn == -INFINITY ? 1.0f : exp2f(mo - mn);
+        ms.m_run[t] = mn;
       }
       __syncthreads();
-      // ---- online softmax: thread t owns head sh, columns sc2, sc2+1 ---------------------------
-      {
-        float v[2];
-        float vmax = -INFINITY;
+      float pr[8];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int o = sh * kPitchS + sc2 + e;
-          float x = sm.s[0][o];
-#pragma unroll
-          for (int w2 = 1; w2 < kWarps; ++w2) x += sm.s[w2][o];
-          v[e] = row_valid(c, sc2 + e) ? x * scale_log2 : -INFINITY;
-          vmax = fmaxf(vmax, v[e]);
-        }
-#pragma unroll
-        for (int off = 1; off < 16; off <<= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
-        const float m_new = fmaxf(m_run, vmax);
-        float corr = 1.0f, p0 = 0.0f, p1 = 0.0f;
-        if (m_new != -INFINITY) {
-          corr = exp2f(m_run - m_new);
-          p0 = exp2f(v[0] - m_new);
-          p1 = exp2f(v[1] - m_new);
-        }
-        float rs = p0 + p1;
-#pragma unroll
-        for (int off = 1; off < 16; off <<= 1) rs += __shfl_xor_sync(0xffffffffu, rs, off);
-        l_run = l_run * corr + rs;
-        m_run = m_new;
-        *reinterpret_cast<uint32_t*>(sm.p + sh * kPitchP + sc2) = pack_f16x2(p0, p1);
-        if ((t & 15) == 0) sm.corr[sh] = corr;
+      for (int j = 0; j < 8; ++j) {
+        const float mn = ms.m_run[8 * half + j];
+        pr[j] = mn == -INFINITY ? 0.0f : exp2f(x[j] - mn);
       }
+      // P^T (heads x rows, K-major, 128-byte swizzle): element (h, row)
+      if (lane < 16) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int h = 8 * half + j;
+          const uint32_t off = uint32_t(h) * 128u + uint32_t(((row >> 3) ^ (h & 7)) << 4) + uint32_t(row & 7) * 2u;
+          const uint16_t bits = is_fp4 ? __half_as_ushort(__float2half_rn(pr[j])) : uint16_t(f2bf_bits(pr[j]));
+          *reinterpret_cast<uint16_t*>(base + kPOff + off) = bits;
+        }
+      }
+      const float sum = reduce_scatter8<false>(pr, lane);
+      // rescale the O^T accumulated so far (channel blocks 2 half, 2 half + 1 of this lane quarter)
+      if (!first) {
+        bool any = false;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) any |= ms.corr[h] != 1.0f;
+        if (any) {
+          const uint32_t ta = t_lane + kOCol + uint32_t(32 * half);
+          float o[2][16];
+          tmem_ld16x2(ta, o);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int h = 0; h < 16; ++h) o[j][h] *= ms.corr[h];
+          tmem_st16x2(ta, o);
+        }
+      }
+      if ((lane & 3) == 0) ms.red[quarter][8 * half + (lane >> 2)] = sum;
+      fence_async_smem();
+      tc_fence_before();
       __syncthreads();
-      // ---- O[:, slice] = corr * O + P V[:, slice] ---------------------------------------------
-      {
-        const float cr0 = sm.corr[g], cr1 = sm.corr[g + 8];
+      if (t < CSA2_H)
+        ms.l_run[t] = ms.l_run[t] * ms.corr[t] + ((ms.red[0][t] + ms.red[1][t]) + (ms.red[2][t] + ms.red[3][t]));
+
+      // -- O^T += V^T P^T (tensor core): warp i < 4 issues channel block i in 4 steps of 16 rows
+      if (lane == 0 && warp < kIssuers) {
+        tc_fence_after();
+        const uint32_t id = instr_desc(128, !is_fp4, true);
+        const int i = warp;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          oacc[nt][0] *= cr0;
-          oacc[nt][1] *= cr0;
-          oacc[nt][2] *= cr1;
-          oacc[nt][3] *= cr1;
+        for (int s = 0; s < kRows / 16; ++s) {
+          const uint64_t a = smem_desc(tile_s + uint32_t(2 * i) * kTileGroup + uint32_t(s) * 2048u, kTileGroup, 1024);
+          const uint64_t bp = smem_desc(p_s + uint32_t(s) * 32u, 0, 1024);
+          umma_f16(tmem + kOCol + uint32_t(16 * i), a, bp, id, (first && s == 0) ? 0u : 1u);
         }
+        umma_commit(mbar);
+      }
+      first = false;
+    }
+    // ---- last tile's MMAs, then O^T out of tensor memory ---------------------------------------------
+    ok = ok && mbar_wait(mbar, phase);
+    tc_fence_after();
+    __syncthreads();  // l_run of the last tile
+    float o[2][16];
+    tmem_ld16x2(t_lane + kOCol + uint32_t(32 * half), o);
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          uint32_t pa[4];
-          {
-            const int r = mrow + ((mat & 1) << 3);
-            ldmatrix_x4(pa[0], pa[1], pa[2], pa[3], smem_u32(sm.p + r * kPitchP + 16 * kk + ((mat >> 1) << 3)));
-          }
+    for (int j = 0; j < 2; ++j) {
+      const int ch = 128 * (2 * half + j) + 32 * quarter + lane;
+      if (n_split == 1) {
+        uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D + ch;
 #pragma unroll
-          for (int np = 0; np < 4; ++np) {
-            const int kr = 16 * kk + mrow + ((mat & 1) << 3);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(b0, b1, b2, b3, kv_addr(buf) + swz(kr, 8 * warp + 2 * np + (mat >> 1)));
-            mma_f16_16816(oacc[2 * np], pa, b0, b1);
-            mma_f16_16816(oacc[2 * np + 1], pa, b2, b3);
-          }
+        for (int h = 0; h < 16; ++h) {
+          const float l = ms.l_run[h];
+          orow[h * CSA2_D] = uint16_t(f2bf_bits(o[j][h] * (l > 0.0f ? 1.0f / l : 0.0f)));
         }
+      } else {
+        float* po = ws + (int64_t(inst) * n_split + split) * (CSA2_H * CSA2_D) + ch;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) po[h * CSA2_D] = o[j][h];
       }
     }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    if (!ok && t == 0) atomicOr(flags, CSA2_FLAG_TIMEOUT);
+  } else if (n_split == 1) {
+    uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D;
+    for (int e = t; e < CSA2_H * CSA2_D; e += kThreads) orow[e] = 0;
   }
-
-  if ((t & 15) == 0) {
-    sm.m_fin[sh] = m_run;
-    sm.l_fin[sh] = l_run;
-  }
-  __syncthreads();
 
   if (n_split == 1) {
-    const float l0 = sm.l_fin[g], l1 = sm.l_fin[g + 8];
-    const float i0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, i1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
-    uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int ch = 64 * warp + 8 * nt + 2 * tq;
-      *reinterpret_cast<uint32_t*>(orow + g * CSA2_D + ch) = pack_bf16x2(oacc[nt][0] * i0, oacc[nt][1] * i0);
-      *reinterpret_cast<uint32_t*>(orow + (g + 8) * CSA2_D + ch) = pack_bf16x2(oacc[nt][2] * i1, oacc[nt][3] * i1);
-    }
     if (lse && t < CSA2_H) {
-      const float l = sm.l_fin[t];
-      lse[int64_t(inst) * CSA2_H + t] = l > 0.0f ? (sm.m_fin[t] + log2f(l)) * kLn2 : -INFINITY;
+      const float l = ms.l_run[t];
+      lse[int64_t(inst) * CSA2_H + t] = l > 0.0f ? (ms.m_run[t] + log2f(l)) * kLn2 : -INFINITY;
     }
     return;
   }
   // ---- split partials, then the last CTA of this query merges them ------------------------------
   const int64_t instances = gridDim.y;
-  float* po = ws + (int64_t(inst) * n_split + split) * (CSA2_H * CSA2_D);
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int ch = 64 * warp + 8 * nt + 2 * tq;
-    *reinterpret_cast<float2*>(po + g * CSA2_D + ch) = make_float2(oacc[nt][0], oacc[nt][1]);
-    *reinterpret_cast<float2*>(po + (g + 8) * CSA2_D + ch) = make_float2(oacc[nt][2], oacc[nt][3]);
-  }
   float* mlb = ws + instances * n_split * (CSA2_H * CSA2_D);
   if (t < CSA2_H) {
     float* ml = mlb + (int64_t(inst) * n_split + split) * (2 * CSA2_H);
-    ml[2 * t] = sm.m_fin[t];
-    ml[2 * t + 1] = sm.l_fin[t];
+    ml[2 * t] = ms.m_run[t];
+    ml[2 * t + 1] = ms.l_run[t];
   }
   __threadfence();
   __syncthreads();
-  if (t == 0) sm.is_last = (atomicAdd(tickets + inst, 1u) == unsigned(n_split - 1));
+  if (t == 0) ms.is_last = (atomicAdd(tickets + inst, 1u) == unsigned(n_split - 1));
   __syncthreads();
-  if (!sm.is_last) return;
+  if (!ms.is_last) return;
   __threadfence();
-  // o = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j, splits in order; thread: head t>>4, 32 channels
+  // o = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j over the splits with rows, in split order.
+  // The per-head weights go through shared memory (the operand tile is free now): wgt[j][h] holds
+  // m_j then the weight, wgt[kMaxSplit + j][h] holds l_j, then 1 / L and the lse per head.  The
+  // partials are read coalesced: thread t takes float4 t + 256 v (v < 8) of the 16 x 512 block,
+  // i.e. head (t >> 7) + 2 v, channels 4 (t & 127) .. + 3.
+  float* wgt = reinterpret_cast<float*>(base + kTileOff);
   {
-    const int h = t >> 4, c0 = (t & 15) * 32;
     const float* ml = mlb + int64_t(inst) * n_split * (2 * CSA2_H);
-    float M = -INFINITY;
-    for (int j = 0; j < n_split; ++j) M = fmaxf(M, __ldcg(ml + j * 2 * CSA2_H + 2 * h));
-    float L = 0.0f;
-    float acc[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-    if (M != -INFINITY) {
+    for (int e = t; e < n_split * CSA2_H; e += kThreads) {
+      wgt[e] = __ldcg(ml + 2 * e);                            // m_j, e = j * 16 + h
+      wgt[kMaxSplit * CSA2_H + e] = __ldcg(ml + 2 * e + 1);   // l_j
+    }
+    __syncthreads();
+    if (t < CSA2_H) {
+      float M = -INFINITY;
+      for (int j = 0; j < n_split; ++j)
+        if (wgt[kMaxSplit * CSA2_H + j * CSA2_H + t] > 0.0f) M = fmaxf(M, wgt[j * CSA2_H + t]);
+      float L = 0.0f;
       for (int j = 0; j < n_split; ++j) {
-        const float a = exp2f(__ldcg(ml + j * 2 * CSA2_H + 2 * h) - M);
-        L += a * __ldcg(ml + j * 2 * CSA2_H + 2 * h + 1);
-        const float4* pj = reinterpret_cast<const float4*>(ws + (int64_t(inst) * n_split + j) * (CSA2_H * CSA2_D) +
-                                                           h * CSA2_D + c0);
+        const float lj = wgt[kMaxSplit * CSA2_H + j * CSA2_H + t];
+        const float a = (lj > 0.0f && M != -INFINITY) ? exp2f(wgt[j * CSA2_H + t] - M) : 0.0f;
+        L += a * lj;
+        wgt[j * CSA2_H + t] = a;
+      }
+      wgt[2 * kMaxSplit * CSA2_H + t] = L > 0.0f ? 1.0f / L : 0.0f;
+      wgt[2 * kMaxSplit * CSA2_H + CSA2_H + t] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+  }
+  {
+    const float4* p0 = reinterpret_cast<const float4*>(ws + int64_t(inst) * n_split * (CSA2_H * CSA2_D)) + t;
+    float4 acc[8];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const float4 x = __ldcg(pj + v);
-          acc[4 * v] += a * x.x;
-          acc[4 * v + 1] += a * x.y;
-          acc[4 * v + 2] += a * x.z;
-          acc[4 * v + 3] += a * x.w;
+    for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int j0 = 0; j0 < n_split; j0 += 2) {
+      const int j1 = min(j0 + 1, n_split - 1);
+      float4 x0[8], x1[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        x0[v] = __ldcg(p0 + int64_t(j0) * (CSA2_H * CSA2_D / 4) + kThreads * v);
+        x1[v] = __ldcg(p0 + int64_t(j1) * (CSA2_H * CSA2_D / 4) + kThreads * v);
+      }
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const int h = (t >> 7) + 2 * v;
+        // a split without rows wrote no partial: its (zero-weight) slot is never read into acc
+        const float a0 = wgt[j0 * CSA2_H + h], a1 = j1 > j0 ? wgt[j1 * CSA2_H + h] : 0.0f;
+        if (a0 != 0.0f) {
+          acc[v].x += a0 * x0[v].x;
+          acc[v].y += a0 * x0[v].y;
+          acc[v].z += a0 * x0[v].z;
+          acc[v].w += a0 * x0[v].w;
+        }
+        if (a1 != 0.0f) {
+          acc[v].x += a1 * x1[v].x;
+          acc[v].y += a1 * x1[v].y;
+          acc[v].z += a1 * x1[v].z;
+          acc[v].w += a1 * x1[v].w;
         }
       }
     }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    uint4* dst = reinterpret_cast<uint4*>(out + (int64_t(inst) * CSA2_H + h) * CSA2_D + c0);
+    uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D;
 #pragma unroll
-    for (int v = 0; v < 4; ++v)
-      dst[v] = make_uint4(pack_bf16x2(acc[8 * v] * inv, acc[8 * v + 1] * inv),
-                          pack_bf16x2(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv),
-                          pack_bf16x2(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv),
-                          pack_bf16x2(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv));
-    if (lse && (t & 15) == 0) lse[int64_t(inst) * CSA2_H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    for (int v = 0; v < 8; ++v) {
+      const int h = (t >> 7) + 2 * v;
+      const float inv = wgt[2 * kMaxSplit * CSA2_H + h];
+      *reinterpret_cast<uint2*>(orow + 4 * (t + kThreads * v)) =
+          make_uint2(pack_bf16x2(acc[v].x * inv, acc[v].y * inv), pack_bf16x2(acc[v].z * inv, acc[v].w * inv));
+    }
+    if (lse && t < CSA2_H) lse[int64_t(inst) * CSA2_H + t] = wgt[2 * kMaxSplit * CSA2_H + CSA2_H + t];
   }
   if (t == 0) tickets[inst] = 0u;  // ready for the next launch
 }
 
+int attn_tiles(int k, int W) { return (k + kRows - 1) / kRows + (W > 0 ? (W + kRows - 1) / kRows : 0); }
+
 }  // namespace
+
+// Splits actually launched: at most one per tile.
+int attn_effective_split(int k, int W, int n_split) {
+  return std::max(1, std::min(n_split, std::max(attn_tiles(k, W), 1)));
+}
 
 // partial O and (m, l) of every split, then one ticket per query (zeroed before each launch)
 size_t attn_ws_bytes(int64_t instances, int n_split) {
@@ -462,11 +715,11 @@ size_t attn_ws_bytes(int64_t instances, int n_split) {
 }
 
 int attn_auto_split(int64_t instances, int k, int W) {
-  const int nch = (k + kCH - 1) / kCH + (W + kCH - 1) / kCH;
-  if (instances <= 0 || nch <= 0) return 1;
-  const int64_t target = 2 * 152;  // two resident CTAs per SM
-  int64_t s = (target + instances - 1) / instances;
-  s = std::min<int64_t>(s, std::min(nch, kMaxSplit));
+  const int nt = attn_tiles(k, W);
+  if (instances <= 0 || nt <= 0) return 1;
+  const int64_t slots = 2 * 152;  // two resident CTAs per SM
+  int64_t s = std::max<int64_t>(slots / instances, 1);
+  s = std::min<int64_t>(s, std::min(nt, kMaxSplit));
   return int(std::max<int64_t>(s, 1));
 }
 
@@ -477,14 +730,16 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
                                float* lse, int n_split, float* ws, cudaStream_t st) {
   const int64_t instances = int64_t(B) * Nq;
   if (instances == 0) return cudaSuccess;
+  if (!swa) W = 0;
+  n_split = attn_effective_split(k, W, n_split);
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
-  const size_t smem = sizeof(AttnSmem);
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e =
+        cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -496,8 +751,8 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
     if (e != cudaSuccess) return e;
   }
   const dim3 grid{unsigned(n_split), unsigned(instances), 1u};
-  sparse_attn_kernel<<<grid, kThreads, smem, st>>>(q, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len,
-                                                   W, scale_log2, out, lse, n_split, ws, tickets, flags);
+  sparse_attn_kernel<<<grid, kThreads, kSmemBytes, st>>>(q, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len,
+                                                          W, scale_log2, out, lse, n_split, ws, tickets, flags);
   return cudaGetLastError();
 }
 
@@ -520,7 +775,7 @@ extern "C" csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq,
   if (!q || !out || !al16(q) || !al16(out)) return CSA2_ERR_INVALID_ARG;
   if (k > 0 && (!codes || !scales || !idx || !al16(codes) || !al16(scales))) return CSA2_ERR_INVALID_ARG;
   if (swa && !al16(swa)) return CSA2_ERR_INVALID_ARG;
-  const int ns = n_split ? n_split : csa2::attn_auto_split(instances, k, W);
+  const int ns = csa2::attn_effective_split(k, W, n_split ? n_split : csa2::attn_auto_split(instances, k, W));
   const size_t need = csa2::attn_ws_bytes(instances, ns);
   if (need && (!ws || ws_bytes < need || !al16(ws))) return CSA2_ERR_WORKSPACE;
   return csa2::launch_sparse_attn(q, B, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len, W,

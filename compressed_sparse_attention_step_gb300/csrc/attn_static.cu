@@ -55,7 +55,7 @@ extern "C" csa2_status csa2_sparse_attn_decode_static(const uint16_t* q, int B, 
   if (!q || !out || !al16(q) || !al16(out)) return CSA2_ERR_INVALID_ARG;
   if (k > 0 && (!codes || !scales || !idx || !al16(codes) || !al16(scales))) return CSA2_ERR_INVALID_ARG;
   if (swa && !al16(swa)) return CSA2_ERR_INVALID_ARG;
-  const int ns = n_split ? n_split : csa2::attn_auto_split(instances, k, W);
+  const int ns = csa2::attn_effective_split(k, W, n_split ? n_split : csa2::attn_auto_split(instances, k, W));
   if (csa2::attn_ws_bytes(instances, ns) > csa2::kStaticScratchBytes) return CSA2_ERR_TOO_LARGE;
   float* scratch = csa2::static_scratch();
   if (!scratch) return CSA2_ERR_CUDA;

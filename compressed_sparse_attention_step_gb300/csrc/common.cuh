@@ -148,6 +148,8 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
                                const int32_t* n_valid, int k, const uint16_t* swa,
                                const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
                                float* lse, int n_split, float* ws, cudaStream_t st);
+// Attention splits: at most one per 128-row tile; attn_ws_bytes with the effective split.
+int attn_effective_split(int k, int W, int n_split);
 size_t attn_ws_bytes(int64_t instances, int n_split);
 int attn_auto_split(int64_t instances, int k, int W);
 

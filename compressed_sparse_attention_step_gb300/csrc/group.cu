@@ -68,7 +68,7 @@ GroupWs group_ws_layout(int B, int Nq, int64_t cap, int K, int W, int hierarchic
   L.nv_off = align256(size_t(rows) * size_t(ld) * sizeof(float));
   L.topk_off = L.nv_off + align256(size_t(rows) * sizeof(int32_t));
   L.attn_off = L.topk_off + align256(topk_ws_bytes(int(rows), ld));
-  const int ns = n_split ? n_split : attn_auto_split(rows, K, W);
+  const int ns = attn_effective_split(K, W, n_split ? n_split : attn_auto_split(rows, K, W));
   L.total = L.attn_off + align256(attn_ws_bytes(rows, ns));
   return L;
 }
@@ -90,7 +90,7 @@ extern "C" size_t csa2_workspace_size(int op, const csa2_dims* d) {
     }
     case CSA2_OP_SPARSE_ATTN: {
       const int W = d->W;
-      const int ns = d->n_split ? d->n_split : csa2::attn_auto_split(rows, d->k, W);
+      const int ns = csa2::attn_effective_split(d->k, W, d->n_split ? d->n_split : csa2::attn_auto_split(rows, d->k, W));
       return csa2::attn_ws_bytes(rows, ns);
     }
     case CSA2_OP_GROUP_STEP:
@@ -216,7 +216,8 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   int32_t* nv = reinterpret_cast<int32_t*>(wsb + lay.nv_off);
   void* tws = wsb + lay.topk_off;
   float* attn_ws = reinterpret_cast<float*>(wsb + lay.attn_off);
-  const int ns_all = g->n_split ? g->n_split : csa2::attn_auto_split(rows, g->K, g->W);
+  const int ns_all =
+      csa2::attn_effective_split(g->K, g->W, g->n_split ? g->n_split : csa2::attn_auto_split(rows, g->K, g->W));
   const int64_t nb = g->cap / CSA2_BLOCK;
   const int64_t pool_w = int64_t(g->n_blocks_keep) * CSA2_BLOCK;
   const int64_t sld = lay.score_ld;
@@ -275,7 +276,8 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
     auto w_of = [&](int l) { return g->w[l] + r0 * CSA2_HI; };
     auto idx_of = [&](int l) { return g->idx[l] + r0 * K; };
     // attention split of a chunk: at most 4 when chunks overlap, and within the sized workspace
-    int ns = g->n_split ? g->n_split : std::min(csa2::attn_auto_split(rc, K, g->W), n_chunks > 1 ? 4 : 32);
+    int ns = csa2::attn_effective_split(
+        K, g->W, g->n_split ? g->n_split : std::min(csa2::attn_auto_split(rc, K, g->W), n_chunks > 1 ? 4 : 32));
     while (ns > 1 && csa2::attn_ws_bytes(rc, ns) > csa2::attn_ws_bytes(rows, ns_all)) --ns;
 
     // stage 1 (stream): the first scan over this chunk's keys (layer 0 is Full or Reindex)

@@ -80,6 +80,7 @@ typedef enum {
 /* Device flag bits (csa2_device_flags). */
 #define CSA2_FLAG_APPEND_OOB 1u /* an appended row fell outside [0, cap): row skipped   */
 #define CSA2_FLAG_INDEX_OOB 2u  /* a selected index was >= cap: row treated as empty    */
+#define CSA2_FLAG_TIMEOUT 4u    /* a kernel gave up waiting for its tensor-core work     */
 
 /*
  * FP4 quantise-and-append.  "Main key-value cache quantises to E2M1 with one E4M3 scale per
@@ -179,8 +180,12 @@ csa2_status csa2_block_pool(const uint16_t* qI, const float* w, int B, int Nq,
  *          rows >= (W-1+Nq) - swa_len[b] hold tokens (swa_len int32 [B]).  W <= 128.
  *   out    bf16 [B][Nq][16][512];  lse fp32 [B][Nq][16] (nullable), natural log; a query with
  *          no rows gets out = 0 and lse = -inf.
- *   n_split  split-KV factor, 0 = chosen from the problem size.
+ *   n_split  CTAs per query (0..32, 0 = chosen from the problem size).  A query's rows form
+ *          128-row tiles (ceil(k/128) of selected rows, one of window rows); larger splits than
+ *          tiles are clamped to the tile count.  Entries of the same query are combined in split
+ *          order, so results do not depend on scheduling.
  *   ws     csa2_workspace_size(CSA2_OP_SPARSE_ATTN, ...) bytes for the chosen split.
+ * Tensor-core waits are bounded (about one second); one that runs out sets CSA2_FLAG_TIMEOUT.
  */
 csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq, const uint8_t* codes,
                                     const uint8_t* scales, int64_t cap, const int32_t* idx,

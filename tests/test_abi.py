@@ -43,7 +43,12 @@ def test_workspace_sizes(L):
     assert csa2.workspace_size(csa2.OP_TOPK, B=4, Nq=1, n=131072, k=512) > 4 * 4096 * 4
     a = csa2.workspace_size(csa2.OP_SPARSE_ATTN, B=64, Nq=1, k=512, W=128)
     ns = L.csa2_attn_auto_split(64, 512, 128)
-    assert ns == 5 and a == 64 * ns * (16 * 512 + 32) * 4 + 64 * 4      # partials + one ticket per query
+    n_tiles = L.csa2_attn_auto_split(1, 512, 128)          # one query: one split per row tile
+    assert n_tiles >= 2 and 1 < ns <= n_tiles
+    assert a == 64 * ns * (16 * 512 + 32) * 4 + 64 * 4     # partials + one ticket per query
+    # an explicit split larger than the tile count is clamped to it
+    assert csa2.workspace_size(csa2.OP_SPARSE_ATTN, B=64, Nq=1, k=512, W=128, n_split=32) == \
+        64 * n_tiles * (16 * 512 + 32) * 4 + 64 * 4
     assert csa2.workspace_size(csa2.OP_SPARSE_ATTN, B=4096, Nq=1, k=512, W=128) == 0   # one split
     g = csa2.group_workspace_size(64, 1, 131072)
     assert g >= 64 * 131072 * 4 + a

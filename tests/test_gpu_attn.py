@@ -117,3 +117,26 @@ def test_index_out_of_range_is_flagged_not_read(orc):
     sel[0, 3] = -1
     ref, rlse = _oracle(orc, kv, q, swa, sel, None, np.array([128], np.int32), W)
     _cmp(got, glse, ref, rlse)
+
+
+@pytest.mark.parametrize("n_split", [2, 4, 10])
+def test_split_partials_of_empty_splits_are_never_read(orc, n_split):
+    """Splits whose tiles hold no rows write no partial output; the workspace is filled with NaN
+    first, so reading such a slot (even with a zero weight) would corrupt the merged result."""
+    B, Nq, cap, k, W = 3, 1, 900, 512, 128
+    kv, q, swa, idx = _case(43, B, Nq, cap, k, W)
+    nvalid = np.array([512, 300, 17], np.int32)
+    swa_len = np.array([128, 50, 0], np.int32)
+    codes = torch.empty((B, cap, 256), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((B, cap, 32), dtype=torch.uint8, device="cuda")
+    c.csa2_fp4_quantize_append(bf16_dev(kv), codes, scales)
+    nb = c.workspace_size(c.OP_SPARSE_ATTN, B=B, Nq=Nq, k=k, W=W, n_split=n_split)
+    ws = torch.full((max(nb, 256) // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.zeros((B, Nq, 16, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((B, Nq, 16), dtype=torch.float32, device="cuda")
+    c.csa2_sparse_attn_decode(bf16_dev(q), codes, scales, to_dev(idx), out, n_valid=to_dev(nvalid),
+                              swa=bf16_dev(swa), swa_len=to_dev(swa_len), W=W, softmax_scale=SCALE, lse=lse,
+                              n_split=n_split, ws=ws)
+    torch.cuda.synchronize()
+    ref, rlse = _oracle(orc, kv, q, swa, idx, nvalid, swa_len, W)
+    _cmp(bf16_host(out), lse.cpu().numpy(), ref, rlse)

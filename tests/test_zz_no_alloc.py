@@ -66,11 +66,11 @@ def test_static_scratch_matches_workspace_entry_point(seed, B):
 
 def test_static_scratch_refuses_oversized_split():
     cap_bytes = int(c.lib().csa2_sparse_attn_static_scratch_bytes())
-    B = 64
+    B = 128
     q, codes, scales, idx, swa, swa_len = _inputs(73, B, 600, 512, 128)
     out = torch.zeros((B, 1, 16, 512), dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros((B, 1, 16), dtype=torch.float32, device="cuda")
-    n_split = 20                              # 64 x 20 splits of 32 KiB exceed 16 MiB
-    assert 64 * n_split * (16 * 512 + 32) * 4 > cap_bytes
+    n_split = 5                               # 128 queries x 5 splits of 32 KiB exceed 16 MiB
+    assert B * n_split * (16 * 512 + 32) * 4 > cap_bytes
     assert _call_static(q, codes, scales, idx, swa, swa_len, out, lse, n_split=n_split) == 5
     assert c.lib().csa2_status_string(5) == b"problem exceeds the library's built-in scratch"
