@@ -5,15 +5,18 @@
 //
 // Radix select on ordered 32-bit score keys (-0 and +0 share a key), in one launch of
 // (slices x rows) CTAs so that a long row is read by several SMs at once:
-//  1. each CTA takes one slice of its row (about 32768 keys; fewer, longer slices when k is large), builds a histogram of their top 12 key
-//     bits in shared memory, finds the bin holding the slice's own k-th largest key, and appends
-//     every key of the slice in that bin or above (a superset of the slice's share of the row's
-//     Top-K) to the row's candidate list with one atomic reservation;
-//  2. the last CTA of the row to finish (an atomic ticket) loads the candidates into shared memory;
-//     radix rounds on the key bits, then on the column bits (ascending, so equal keys go to the
-//     lower column), find the exact k-th (key, column); the winners are written in column order,
-//     placed by prefix popcounts over a bitmap of the selected columns (a bitonic sort for very
-//     long rows); it then clears the row's counters for the next launch.
+//  1. each CTA takes one slice of its row (about 32768 keys; fewer, longer slices when k is large).
+//     It splits the slice's keys into groups (the 16 keys one thread reads per sweep step) and
+//     histograms the group maxima by their top 12 key bits, both in shared memory and added into
+//     the row's histogram in the workspace.  The k largest group maxima are k distinct keys, so the
+//     lower edge L of the bin holding the k-th largest maximum is at most the slice's k-th largest
+//     key: every key >= L is appended to the row's candidate list (one atomic reservation);
+//  2. the last CTA of the row to finish (an atomic ticket) takes the same bound over the whole
+//     row's histogram (a bound >= every slice's), keeps the candidates at or above it, and finds the
+//     exact k-th (key, column) by radix rounds on the key bits, then on the column bits (ascending,
+//     so equal keys go to the lower column); the winners are written in column order, placed by
+//     prefix popcounts over a bitmap of the selected columns (a bitonic sort for very long rows);
+//     it then clears the row's counters and histogram for the next launch.
 // A row whose candidates overflow the list (massive ties) is finished by that CTA with the same
 // rounds over the row in global memory and an ordered, scan-based output; rows of one slice use
 // that single-CTA path directly.  Counts are integers and every decision is a pure function of the
@@ -30,14 +33,27 @@ constexpr int64_t kSlice = 32768;      // keys per slice CTA
 constexpr int kCandCap = 10240;        // candidates per row
 constexpr int kBins = 4096;            // first-level bins (top 12 key bits)
 constexpr int64_t kBitmapCols = 262144;   // rows up to this long are ordered through a bitmap
+constexpr int kRegSteps = 4;           // sweep steps of 16 keys per thread held in registers
+constexpr int64_t kRegSlice = int64_t(kRegSteps) * 16 * kThreads;  // = kSlice
+
+constexpr int kLocCap = 4096;           // candidates of one register-held slice
 
 struct SelSmem {
   uint32_t hist[kBins];
-  uint32_t cand_key[kCandCap];
-  int32_t cand_col[kCandCap];
   union {
-    int32_t sel[CSA2_MAX_K];
-    uint32_t bits[kBitmapCols / 32];
+    struct {  // selection: the whole-row path, long slices, and the last CTA of a row
+      uint32_t cand_key[kCandCap];
+      int32_t cand_col[kCandCap];
+      union {
+        int32_t sel[CSA2_MAX_K];
+        uint32_t bits[kBitmapCols / 32];
+      };
+    };
+    struct {  // a slice held in registers: its scores (thread-major) and its candidates
+      float slice_v[kRegSlice];
+      uint32_t loc_key[kLocCap];
+      int32_t loc_col[kLocCap];
+    };
   };
   uint32_t scan_tmp[32];
   uint32_t nsel, ncand, base;
@@ -164,7 +180,7 @@ __device__ void finish_row(const RowOut& o, int64_t cnt, int row, int32_t* n_sel
 
 // The k largest of the nc candidates in shared memory (nc >= k) by (key desc, column asc), emitted
 // in column order; columns are < ncols.
-__device__ void select_candidates(SelSmem& sm, int nc, int k, int64_t ncols, const RowOut& o) {
+__device__ __noinline__ void select_candidates(SelSmem& sm, int nc, int k, int64_t ncols, const RowOut o) {
   const int t = threadIdx.x;
   uint32_t need = uint32_t(k), prefix = 0, mask = 0;
   const int kshift[3] = {21, 10, 0}, kwidth[3] = {11, 11, 10};
@@ -263,7 +279,7 @@ __device__ void select_candidates(SelSmem& sm, int nc, int k, int64_t ncols, con
 }
 
 // Whole-row selection by one CTA (short rows, and rows whose candidates overflow).
-__device__ void select_row(SelSmem& sm, const float* s, int64_t nv, int k, const RowOut& o) {
+__device__ __noinline__ void select_row(SelSmem& sm, const float* s, int64_t nv, int k, const RowOut o) {
   const int t = threadIdx.x, lane = t & 31;
   const unsigned lanes_below = (1u << lane) - 1u;
   zero(sm.hist, kBins);
@@ -346,6 +362,32 @@ __device__ void select_row(SelSmem& sm, const float* s, int64_t nv, int k, const
   }
 }
 
+// The 16 scores thread t reads in one sweep step starting at b0: float4 number u * kThreads + t
+// (u < 4) of the step, i.e. v[4 u + e] = s[b0 + 4 (u kThreads + t) + e]; past hi they are NaN,
+// which every comparison rejects and fmaxf ignores.
+__device__ __forceinline__ void load16(const float* s, int64_t b0, int64_t hi, float (&v)[16]) {
+  const int t = threadIdx.x;
+  const bool full = b0 + int64_t(16) * kThreads <= hi && ((reinterpret_cast<uintptr_t>(s + b0) & 15u) == 0);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int64_t i0 = b0 + (int64_t(u) * kThreads + t) * 4;
+    if (full) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(s + i0));
+      v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[4 * u + e] = (i0 + e < hi) ? __ldg(s + i0 + e) : __int_as_float(0x7FC00000);
+    }
+  }
+}
+
+// The smallest score whose key is >= key (the -0/+0 key gives -0, which +0 also passes).
+__device__ __forceinline__ float key_floor_score(uint32_t key) {
+  if (key <= 0x00800000u) return -INFINITY;  // at or below the key of -FLT_MAX: every finite score
+  if (key & 0x80000000u) return __uint_as_float(key & 0x7FFFFFFFu) == 0.0f ? -0.0f : __uint_as_float(key & 0x7FFFFFFFu);
+  return __uint_as_float(~key);
+}
+
 __device__ __forceinline__ int64_t row_valid(const int32_t* n_valid, int row, int64_t n) {
   return n_valid ? min(max(int64_t(n_valid[row]), int64_t(0)), n) : n;
 }
@@ -354,12 +396,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
     const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid, int k,
     const int32_t* __restrict__ map, int64_t map_ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
     int expand8, int32_t* __restrict__ pool_len, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_col,
-    uint32_t* __restrict__ row_ctl /* [rows][2]: candidate count, ticket */, int64_t slice_len) {
+    uint32_t* __restrict__ row_ctl /* [rows][2]: candidate count, ticket */,
+    uint32_t* __restrict__ row_hist /* [rows][4096]: group maxima by top 12 key bits */, int64_t slice_len) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   const int row = blockIdx.y, nslices = gridDim.x;
   const int t = threadIdx.x, lane = t & 31;
-  const unsigned lanes_below = (1u << lane) - 1u;
   const float* s = scores + int64_t(row) * ld;
   const int64_t nv = row_valid(n_valid, row, n);
   __syncthreads();  // every thread has read n_valid before pool_len (possibly the same array) is written
@@ -377,46 +419,138 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
     finish_row(o, k, row, n_sel, pool_len);
     return;
   }
+  // reserve `cnt` slots for this thread: one warp scan and one shared atomic per warp
+  auto reserve = [&](uint32_t cnt) {
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o2);
+      if (lane >= o2) incl += y;
+    }
+    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t base = 0;
+    if (lane == 31 && wtot) base = atomicAdd(&sm.ncand, wtot);
+    return __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+  };
   uint32_t* ctl = row_ctl + 2 * int64_t(row);
-  // ---- phase 1: this slice's local superset of the Top-K --------------------------------------
+  // ---- phase 1: group maxima -> the slice's bound L -> keys >= L appended to the row's list ------
+  uint32_t* ghist = row_hist + int64_t(row) * kBins;
   const int64_t lo = int64_t(blockIdx.x) * slice_len, hi = min(lo + slice_len, nv);
   if (lo < hi) {
     zero(sm.hist, kBins);
-    hist12(s, lo, hi, sm.hist);
+    // A group: the (up to) 16 keys a thread reads in one sweep step of 4 x 4 x kThreads keys.  Its
+    // maximum is taken on the floats (same order as the keys for finite scores) and keyed once.
+    // A slice of at most kRegSlice keys is read once, into registers; longer ones are read twice.
+    const bool in_regs = hi - lo <= kRegSlice;
+    float rv[kRegSteps][16];
+    uint32_t ngroups = 0;
+    if (in_regs) {
+#pragma unroll
+      for (int j = 0; j < kRegSteps; ++j) load16(s, lo + int64_t(j) * 16 * kThreads, hi, rv[j]);
+    }
+    for (int j = 0; j * int64_t(16) * kThreads < hi - lo; ++j) {
+      const int64_t b0 = lo + int64_t(j) * 16 * kThreads;
+      const int64_t firsts = (hi - b0 + 3) / 4;  // threads whose first key is < hi
+      ngroups += uint32_t(firsts < kThreads ? firsts : kThreads);
+      float v[16];
+      if (in_regs) {
+#pragma unroll
+        for (int jj = 0; jj < kRegSteps; ++jj)
+          if (jj == j) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = rv[jj][e];
+          }
+      } else {
+        load16(s, b0, hi, v);
+      }
+      float gm = v[0];
+#pragma unroll
+      for (int e = 1; e < 16; ++e) gm = fmaxf(gm, v[e]);
+      const bool has = b0 + 4 * t < hi;
+      const uint32_t bin = has ? score_key(gm) >> 20 : 0xFFFFFFFFu;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (has && (__ffs(peers) - 1) == lane) atomicAdd(&sm.hist[bin], uint32_t(__popc(peers)));
+    }
     __syncthreads();
-    const uint32_t kk = uint32_t(hi - lo < int64_t(k) ? hi - lo : int64_t(k));
-    find_bin(sm.hist, kBins, kk, true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
-    const uint32_t lb1 = sm.res_bin;
-    const uint32_t nloc = sm.res_before + sm.hist[lb1];   // keys of the slice in bins >= lb1
+    for (int i = t; i < kBins; i += kThreads)
+      if (sm.hist[i]) atomicAdd(ghist + i, sm.hist[i]);
+    uint32_t bound = 0;  // keys >= bound: a superset of the slice's Top-K
+    if (ngroups >= uint32_t(k)) {
+      find_bin(sm.hist, kBins, uint32_t(k), true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+      bound = sm.res_bin << 20;
+    }
     if (t == 0) sm.ncand = 0;
     __syncthreads();
-    if (nloc <= uint32_t(kCandCap)) {
-      for_each_key<8>(s, lo, hi, [&](int64_t i, uint32_t key, bool valid) {
-        const bool take = valid && (key >> 20) >= lb1;
-        const unsigned m = __ballot_sync(0xffffffffu, take);
-        if (!m) return;
-        uint32_t base = 0;
-        if (lane == 0) base = atomicAdd(&sm.ncand, uint32_t(__popc(m)));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (take) {
-          const uint32_t c = base + __popc(m & lanes_below);
-          sm.cand_key[c] = key;
-          sm.cand_col[c] = int32_t(i);
+    // keys >= bound <=> scores >= fb (the smallest score with that key; -0 and +0 both pass at 0)
+    const float fb = key_floor_score(bound);
+    auto mask16 = [&](const float (&v)[16]) {
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) m |= (v[e] >= fb) ? (1u << e) : 0u;
+      return m;
+    };
+    auto emit16 = [&](const float (&v)[16], uint32_t m, int64_t b0, uint32_t& base) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        if (m & (1u << e)) {
+          if (base < uint32_t(kCandCap)) {
+            sm.cand_key[base] = score_key(v[e]);
+            sm.cand_col[base] = int32_t(b0 + 4 * ((e >> 2) * kThreads + t) + (e & 3));
+          }
+          ++base;
         }
-      });
-      __syncthreads();
+      }
+    };
+    uint32_t* lkey = in_regs ? sm.loc_key : sm.cand_key;
+    int32_t* lcol = in_regs ? sm.loc_col : sm.cand_col;
+    const uint32_t lcap = in_regs ? uint32_t(kLocCap) : uint32_t(kCandCap);
+    if (in_regs) {
+      // scores to shared memory (thread-major: step j, value e of thread t at (16 j + e) kThreads + t)
+      // so that the few candidates can be read back by a dynamic index
+      uint32_t ms4[kRegSteps], cnt = 0;
+#pragma unroll
+      for (int j = 0; j < kRegSteps; ++j) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sm.slice_v[(16 * j + e) * kThreads + t] = rv[j][e];
+        ms4[j] = mask16(rv[j]);
+        cnt += __popc(ms4[j]);
+      }
+      uint32_t base = reserve(cnt);
+#pragma unroll
+      for (int j = 0; j < kRegSteps; ++j) {
+        uint32_t m = ms4[j];
+        while (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1u;
+          if (base < lcap) {
+            lkey[base] = score_key(sm.slice_v[(16 * j + e) * kThreads + t]);
+            lcol[base] = int32_t(lo + int64_t(j) * 16 * kThreads + 4 * ((e >> 2) * kThreads + t) + (e & 3));
+          }
+          ++base;
+        }
+      }
+    } else {
+      for (int64_t b0 = lo; b0 < hi; b0 += int64_t(16) * kThreads) {
+        float v[16];
+        load16(s, b0, hi, v);
+        const uint32_t m = mask16(v);
+        uint32_t base = reserve(__popc(m));
+        emit16(v, m, b0, base);
+      }
     }
-    if (t == 0)   // an oversized slice pushes the row's count past the list: whole-row path
-      sm.base = atomicAdd(ctl, nloc <= uint32_t(kCandCap) ? nloc : uint32_t(kCandCap) + 1u);
     __syncthreads();
-    if (nloc <= uint32_t(kCandCap)) {
+    const uint32_t nloc = sm.ncand;
+    if (t == 0)   // an oversized slice pushes the row's count past the list: whole-row path
+      sm.base = atomicAdd(ctl, nloc <= lcap ? nloc : uint32_t(kCandCap) + 1u);
+    __syncthreads();
+    if (nloc <= lcap) {
       uint32_t* ck = cand_key + int64_t(row) * kCandCap;
       int32_t* cc = cand_col + int64_t(row) * kCandCap;
       for (uint32_t c = t; c < nloc; c += kThreads) {
         const uint32_t dst = sm.base + c;
         if (dst < uint32_t(kCandCap)) {
-          ck[dst] = sm.cand_key[c];
-          cc[dst] = sm.cand_col[c];
+          ck[dst] = lkey[c];
+          cc[dst] = lcol[c];
         }
       }
     }
@@ -430,18 +564,57 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
   __threadfence();
   const uint32_t cnt = __ldcg(ctl);
   if (cnt <= uint32_t(kCandCap)) {
+    // the row's bound: the same rule over the whole row's group maxima (>= every slice's bound)
+    uint32_t total = 0;
+    for (int i = t; i < kBins; i += kThreads) {
+      const uint32_t h = __ldcg(ghist + i);
+      sm.hist[i] = h;
+      total += h;
+    }
+    total = __reduce_add_sync(0xffffffffu, total);
+    if (lane == 0) sm.scan_tmp[t >> 5] = total;
+    __syncthreads();
+    total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) total += sm.scan_tmp[w];
+    __syncthreads();
+    uint32_t bound = 0;
+    if (total >= uint32_t(k)) {
+      find_bin(sm.hist, kBins, uint32_t(k), true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+      bound = sm.res_bin << 20;
+    }
+    if (t == 0) sm.ncand = 0;
+    __syncthreads();
     const uint32_t* ck = cand_key + int64_t(row) * kCandCap;
     const int32_t* cc = cand_col + int64_t(row) * kCandCap;
-    for (int i = t; i < int(cnt); i += kThreads) {
-      sm.cand_key[i] = __ldcg(ck + i);
-      sm.cand_col[i] = __ldcg(cc + i);
+    constexpr int kB = 8;  // candidates per thread per batch, all loads in flight together
+    for (int i0 = 0; i0 < int(cnt); i0 += kB * kThreads) {
+      uint32_t key[kB];
+      int32_t col[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int i = i0 + u * kThreads + t;
+        key[u] = i < int(cnt) ? __ldcg(ck + i) : 0u;
+        col[u] = i < int(cnt) ? __ldcg(cc + i) : 0;
+      }
+      uint32_t m = 0;
+#pragma unroll
+      for (int u = 0; u < kB; ++u) m |= (i0 + u * kThreads + t < int(cnt) && key[u] >= bound) ? (1u << u) : 0u;
+      uint32_t base = reserve(__popc(m));
+#pragma unroll
+      for (int u = 0; u < kB; ++u)
+        if (m & (1u << u)) {
+          sm.cand_key[base] = key[u];
+          sm.cand_col[base] = col[u];
+          ++base;
+        }
     }
     __syncthreads();
-    select_candidates(sm, int(cnt), k, nv, o);
+    select_candidates(sm, int(sm.ncand), k, nv, o);
   } else {
     select_row(sm, s, nv, k, o);
   }
   finish_row(o, k, row, n_sel, pool_len);
+  for (int i = t; i < kBins; i += kThreads) ghist[i] = 0u;
   if (t == 0) {
     ctl[0] = 0u;
     ctl[1] = 0u;
@@ -456,10 +629,12 @@ int topk_slices(int64_t n, int k) {
   return int(std::max<int64_t>(1, std::min(by_len, by_cap)));
 }
 
-// workspace: candidate keys and columns per row, then (count, ticket) per row
+// workspace: candidate keys and columns per row, then (count, ticket) per row, then the row
+// histograms of group maxima (the last two zeroed before each launch)
 size_t topk_ws_bytes(int rows, int64_t n) {
   if (n <= kSlice) return 0;
-  return size_t(rows) * (kCandCap * (sizeof(uint32_t) + sizeof(int32_t)) + 2 * sizeof(uint32_t));
+  return size_t(rows) * (kCandCap * (sizeof(uint32_t) + sizeof(int32_t)) + 2 * sizeof(uint32_t) +
+                         kBins * sizeof(uint32_t));
 }
 
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
@@ -477,7 +652,7 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
   }
   int nslices = 1;
   int64_t slice_len = n;
-  uint32_t *ckey = nullptr, *ctl = nullptr;
+  uint32_t *ckey = nullptr, *ctl = nullptr, *hist = nullptr;
   int32_t* ccol = nullptr;
   if (topk_ws_bytes(rows, n) > 0) {
     if (!ws) return cudaErrorInvalidValue;
@@ -486,12 +661,13 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
     ckey = static_cast<uint32_t*>(ws);
     ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);
     ctl = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
-    cudaError_t e = cudaMemsetAsync(ctl, 0, size_t(rows) * 2 * sizeof(uint32_t), st);
+    hist = ctl + size_t(rows) * 2;
+    cudaError_t e = cudaMemsetAsync(ctl, 0, size_t(rows) * (2 + kBins) * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
   }
   const dim3 grid{unsigned(nslices), unsigned(rows), 1u};
   topk_kernel<<<grid, kThreads, smem, st>>>(scores, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len,
-                                            ckey, ccol, ctl, slice_len);
+                                            ckey, ccol, ctl, hist, slice_len);
   return cudaGetLastError();
 }
 
