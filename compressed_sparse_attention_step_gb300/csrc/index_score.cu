@@ -23,6 +23,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kU = 4;                                // 4-position groups in flight per lane
 constexpr int kPosPerWarpIt = 4 * kU;                // 16
 constexpr int kPosPerCtaIt = kWarps * kPosPerWarpIt; // 128
+constexpr int kPrefetch = 2;                         // sweeps of L2 prefetch ahead of the loads
 
 template <bool kCand>
 __global__ void __launch_bounds__(kThreads, 2) index_score_kernel(
@@ -85,6 +86,11 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_kernel(
   float* srow = scores + int64_t(row) * ld;
 
   for (int64_t base = c0 + warp * kPosPerWarpIt; base < c1; base += kPosPerCtaIt) {
+    if (!kCand) {
+      // pull this warp's rows of PF sweeps ahead into L2 (one 128-byte line per lane)
+      const int64_t tp = base + int64_t(kPrefetch) * kPosPerCtaIt + (lane >> 1);
+      if (tp < nv && tp < c1) asm volatile("prefetch.global.L2 [%0];" ::"l"(kbase - 16 * j + tp * CSA2_DI + 64 * (lane & 1)));
+    }
     uint4 kv[kU][2];
     bool ok[kU];
 #pragma unroll
