@@ -707,11 +707,13 @@ int attn_effective_split(int k, int W, int n_split) {
   return std::max(1, std::min(n_split, std::max(attn_tiles(k, W), 1)));
 }
 
-// partial O and (m, l) of every split, then one ticket per query (zeroed before each launch)
+// one ticket per query (zero before a launch; every launch leaves them zero), padded to 256 B,
+// then the partial O and (m, l) of every split
+size_t attn_ticket_bytes(int64_t instances) { return (size_t(instances) * sizeof(unsigned int) + 255) & ~size_t(255); }
 size_t attn_ws_bytes(int64_t instances, int n_split) {
   if (n_split <= 1) return 0;
-  return size_t(instances) * size_t(n_split) * (CSA2_H * CSA2_D + 2 * CSA2_H) * sizeof(float) +
-         size_t(instances) * sizeof(unsigned int);
+  return attn_ticket_bytes(instances) +
+         size_t(instances) * size_t(n_split) * (CSA2_H * CSA2_D + 2 * CSA2_H) * sizeof(float);
 }
 
 int attn_auto_split(int64_t instances, int k, int W) {
@@ -727,7 +729,7 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
                                const uint8_t* scales, int64_t cap, const int32_t* idx,
                                const int32_t* n_valid, int k, const uint16_t* swa,
                                const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
-                               float* lse, int n_split, float* ws, cudaStream_t st) {
+                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed) {
   const int64_t instances = int64_t(B) * Nq;
   if (instances == 0) return cudaSuccess;
   if (!swa) W = 0;
@@ -745,14 +747,18 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
   }
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   unsigned int* tickets = nullptr;
+  float* partials = nullptr;
   if (n_split > 1) {
-    tickets = reinterpret_cast<unsigned int*>(ws + instances * n_split * (CSA2_H * CSA2_D + 2 * CSA2_H));
-    cudaError_t e = cudaMemsetAsync(tickets, 0, size_t(instances) * sizeof(unsigned int), st);
-    if (e != cudaSuccess) return e;
+    tickets = reinterpret_cast<unsigned int*>(ws);
+    partials = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + attn_ticket_bytes(instances));
+    if (!tickets_zeroed) {
+      cudaError_t e = cudaMemsetAsync(tickets, 0, size_t(instances) * sizeof(unsigned int), st);
+      if (e != cudaSuccess) return e;
+    }
   }
   const dim3 grid{unsigned(n_split), unsigned(instances), 1u};
   sparse_attn_kernel<<<grid, kThreads, kSmemBytes, st>>>(q, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len,
-                                                          W, scale_log2, out, lse, n_split, ws, tickets, flags);
+                                                          W, scale_log2, out, lse, n_split, partials, tickets, flags);
   return cudaGetLastError();
 }
 
@@ -780,7 +786,7 @@ extern "C" csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq,
   if (need && (!ws || ws_bytes < need || !al16(ws))) return CSA2_ERR_WORKSPACE;
   return csa2::launch_sparse_attn(q, B, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len, W,
                                   softmax_scale, out, lse, ns, static_cast<float*>(ws),
-                                  reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+                                  reinterpret_cast<cudaStream_t>(stream), false) == cudaSuccess
              ? CSA2_OK
              : CSA2_ERR_CUDA;
 }

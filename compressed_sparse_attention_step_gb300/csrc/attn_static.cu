@@ -60,7 +60,7 @@ extern "C" csa2_status csa2_sparse_attn_decode_static(const uint16_t* q, int B, 
   float* scratch = csa2::static_scratch();
   if (!scratch) return CSA2_ERR_CUDA;
   return csa2::launch_sparse_attn(q, B, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len, W, softmax_scale,
-                                  out, lse, ns, scratch, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+                                  out, lse, ns, scratch, reinterpret_cast<cudaStream_t>(stream), false) == cudaSuccess
              ? CSA2_OK
              : CSA2_ERR_CUDA;
 }

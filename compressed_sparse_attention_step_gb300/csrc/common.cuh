@@ -142,12 +142,16 @@ cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq
 size_t topk_ws_bytes(int rows, int64_t n);
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
                         int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,
-                        int expand8, int32_t* pool_len, void* ws, cudaStream_t st);
+                        int expand8, int32_t* pool_len, void* ws, cudaStream_t st, bool counters_zeroed = false);
+// Bytes from the start of a Top-K workspace for `rows` rows to its counters (which run to the end of
+// topk_ws_bytes); a launch leaves them zero.
+size_t topk_counters_offset(int rows);
+size_t attn_ticket_bytes(int64_t instances);
 cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
                                const uint8_t* scales, int64_t cap, const int32_t* idx,
                                const int32_t* n_valid, int k, const uint16_t* swa,
                                const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
-                               float* lse, int n_split, float* ws, cudaStream_t st);
+                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed);
 // Attention splits: at most one per 128-row tile; attn_ws_bytes with the effective split.
 int attn_effective_split(int k, int W, int n_split);
 size_t attn_ws_bytes(int64_t instances, int n_split);

@@ -254,6 +254,18 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
         return CSA2_ERR_CUDA;
     }
   }
+  // Top-K counters and attention tickets sit back to back in the workspace; every launch leaves them
+  // zero, so one memset per step serves all layers of an unchunked step
+  const bool zeroed = n_chunks == 1;
+  if (zeroed) {
+    const size_t lo = lay.topk_off + csa2::topk_counters_offset(int(rows));
+    const size_t hi = lay.attn_off + csa2::attn_ticket_bytes(rows);
+    if (csa2::topk_ws_bytes(int(rows), lay.score_ld) > 0 && !ok(cudaMemsetAsync(wsb + lo, 0, hi - lo, st)))
+      return CSA2_ERR_CUDA;
+    if (csa2::topk_ws_bytes(int(rows), lay.score_ld) == 0 &&
+        !ok(cudaMemsetAsync(wsb + lay.attn_off, 0, csa2::attn_ticket_bytes(rows), st)))
+      return CSA2_ERR_CUDA;
+  }
   if (!rec(g->ev_score_begin, st)) return CSA2_ERR_CUDA;
 
   for (int c = 0; c < n_chunks; ++c) {
@@ -308,7 +320,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
               return CSA2_ERR_CUDA;
             if (nb > 0) {
               if (!ok(csa2::launch_topk(sc, int(rc), nb, nb, pool_len, g->n_blocks_keep, nullptr, 0, pool, nullptr, 1,
-                                        pool_len, tws, aux)))
+                                        pool_len, tws, aux, zeroed)))
                 return CSA2_ERR_CUDA;
             } else if (!ok(cudaMemsetAsync(pool_len, 0, size_t(rc) * sizeof(int32_t), aux))) {
               return CSA2_ERR_CUDA;
@@ -318,7 +330,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
                                            pool_w, g->ratio, qpos, sc, pool_w, nvc, aux)))
             return CSA2_ERR_CUDA;
           if (!ok(csa2::launch_topk(sc, int(rc), pool_w, pool_w, nvc, K, pool, pool_w, idx_of(l), nullptr, 0, nullptr,
-                                    tws, aux)))
+                                    tws, aux, zeroed)))
             return CSA2_ERR_CUDA;
         } else {
           if (l != 0 &&
@@ -326,7 +338,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
                                            g->ratio, qpos, sc, g->cap, nvc, aux)))
             return CSA2_ERR_CUDA;
           if (!ok(csa2::launch_topk(sc, int(rc), g->cap, g->cap, nvc, K, nullptr, 0, idx_of(l), nullptr, 0, nullptr,
-                                    tws, aux)))
+                                    tws, aux, zeroed)))
             return CSA2_ERR_CUDA;
         }
         latest = idx_of(l);
@@ -337,7 +349,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
       const uint16_t* swa = g->W > 0 ? g->swa[l] + int64_t(b0) * SW * CSA2_D : nullptr;
       if (!ok(csa2::launch_sparse_attn(g->q[l] + r0 * (CSA2_H * CSA2_D), Bc, Nq, codes, scl, g->cap, latest, nullptr,
                                        K, swa, swl, g->W, g->softmax_scale, g->out[l] + r0 * (CSA2_H * CSA2_D),
-                                       g->lse[l] ? g->lse[l] + r0 * CSA2_H : nullptr, ns, attn_ws, aux)))
+                                       g->lse[l] ? g->lse[l] + r0 * CSA2_H : nullptr, ns, attn_ws, aux, zeroed)))
         return CSA2_ERR_CUDA;
     }
   }

@@ -629,6 +629,8 @@ int topk_slices(int64_t n, int k) {
   return int(std::max<int64_t>(1, std::min(by_len, by_cap)));
 }
 
+size_t topk_counters_offset(int rows) { return size_t(rows) * kCandCap * (sizeof(uint32_t) + sizeof(int32_t)); }
+
 // workspace: candidate keys and columns per row, then (count, ticket) per row, then the row
 // histograms of group maxima (the last two zeroed before each launch)
 size_t topk_ws_bytes(int rows, int64_t n) {
@@ -639,7 +641,7 @@ size_t topk_ws_bytes(int rows, int64_t n) {
 
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
                         int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,
-                        int expand8, int32_t* pool_len, void* ws, cudaStream_t st) {
+                        int expand8, int32_t* pool_len, void* ws, cudaStream_t st, bool counters_zeroed) {
   if (rows == 0) return cudaSuccess;
   const size_t smem = sizeof(SelSmem);
   static bool attr_set[64] = {};
@@ -662,8 +664,10 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
     ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);
     ctl = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
     hist = ctl + size_t(rows) * 2;
-    cudaError_t e = cudaMemsetAsync(ctl, 0, size_t(rows) * (2 + kBins) * sizeof(uint32_t), st);
-    if (e != cudaSuccess) return e;
+    if (!counters_zeroed) {
+      cudaError_t e = cudaMemsetAsync(ctl, 0, size_t(rows) * (2 + kBins) * sizeof(uint32_t), st);
+      if (e != cudaSuccess) return e;
+    }
   }
   const dim3 grid{unsigned(nslices), unsigned(rows), 1u};
   topk_kernel<<<grid, kThreads, smem, st>>>(scores, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len,
