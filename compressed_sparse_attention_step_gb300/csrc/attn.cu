@@ -240,8 +240,15 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     const int32_t* __restrict__ n_valid, int k, const uint16_t* __restrict__ swa,
     const int32_t* __restrict__ swa_len, int W, float scale_log2, uint16_t* __restrict__ out,
     float* __restrict__ lse, int n_split, float* __restrict__ ws, unsigned int* __restrict__ tickets,
-    unsigned int* flags) {
+    unsigned int* flags, int inputs_ready) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  // Inputs not yet known to be complete (the selected positions may come from the kernel right
+  // before this one): wait first.  Otherwise (a layer that reuses earlier positions) wait only
+  // before the first write to the split workspace, which the kernel before this one may still read.
+  if (!inputs_ready) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
   unsigned char* base = smem_raw + (base_s - raw_s);
@@ -573,6 +580,10 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     ok = ok && mbar_wait(mbar, phase);
     tc_fence_after();
     __syncthreads();  // l_run of the last tile
+    if (inputs_ready) {
+      pdl_wait();
+      pdl_trigger();
+    }
     float o[2][16];
     tmem_ld16x2(t_lane + kOCol + uint32_t(32 * half), o);
 #pragma unroll
@@ -598,9 +609,15 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
     if (!ok && t == 0) atomicOr(flags, CSA2_FLAG_TIMEOUT);
-  } else if (n_split == 1) {
-    uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D;
-    for (int e = t; e < CSA2_H * CSA2_D; e += kThreads) orow[e] = 0;
+  } else {
+    if (inputs_ready) {
+      pdl_wait();
+      pdl_trigger();
+    }
+    if (n_split == 1) {
+      uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D;
+      for (int e = t; e < CSA2_H * CSA2_D; e += kThreads) orow[e] = 0;
+    }
   }
 
   if (n_split == 1) {
@@ -729,7 +746,8 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
                                const uint8_t* scales, int64_t cap, const int32_t* idx,
                                const int32_t* n_valid, int k, const uint16_t* swa,
                                const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
-                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed) {
+                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed,
+                               bool inputs_ready) {
   const int64_t instances = int64_t(B) * Nq;
   if (instances == 0) return cudaSuccess;
   if (!swa) W = 0;
@@ -757,9 +775,8 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
     }
   }
   const dim3 grid{unsigned(n_split), unsigned(instances), 1u};
-  sparse_attn_kernel<<<grid, kThreads, kSmemBytes, st>>>(q, Nq, codes, scales, cap, idx, n_valid, k, swa, swa_len,
-                                                          W, scale_log2, out, lse, n_split, partials, tickets, flags);
-  return cudaGetLastError();
+  return launch_pdl(sparse_attn_kernel, grid, dim3(kThreads), kSmemBytes, st, q, Nq, codes, scales, cap, idx, n_valid, k,
+                    swa, swa_len, W, scale_log2, out, lse, n_split, partials, tickets, flags, int(inputs_ready));
 }
 
 }  // namespace csa2

@@ -121,6 +121,33 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
   return warp_base + x - v;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Programmatic dependent launch.  Every library kernel is launched with programmatic stream
+// serialisation allowed: it may start while the kernel before it in the stream is still running,
+// calls pdl_wait() before it touches anything an earlier kernel writes (or writes anything an
+// earlier kernel reads), and calls pdl_trigger() only after that wait, so the next kernel can in
+// turn rely on everything before this one having completed.  Without a preceding kernel both
+// are no-ops.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 }  // namespace csa2
 
 // Internal launchers shared across translation units (all return cudaGetLastError()).
@@ -151,7 +178,8 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
                                const uint8_t* scales, int64_t cap, const int32_t* idx,
                                const int32_t* n_valid, int k, const uint16_t* swa,
                                const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
-                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed);
+                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed,
+                               bool inputs_ready = false);
 // Attention splits: at most one per 128-row tile; attn_ws_bytes with the effective split.
 int attn_effective_split(int k, int W, int n_split);
 size_t attn_ws_bytes(int64_t instances, int n_split);

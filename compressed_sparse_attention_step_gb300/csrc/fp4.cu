@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(256) fp4_quantize_kernel(
     const uint16_t* __restrict__ x, int64_t n_groups, int n_new, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, int64_t cap, const int32_t* __restrict__ offsets, int offset_bias,
     unsigned int* flags) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= n_groups) return;
   const int64_t row = gid >> 5;
@@ -88,6 +90,8 @@ __global__ void __launch_bounds__(256) fp4_dequantize_kernel(const uint8_t* __re
                                                              const uint8_t* __restrict__ scales,
                                                              int64_t n_groups,
                                                              uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= n_groups) return;
   const int64_t row = gid >> 5;
@@ -122,6 +126,8 @@ __global__ void __launch_bounds__(256) copy_rows_append_kernel(const uint16_t* _
                                                                int64_t cap,
                                                                const int32_t* __restrict__ lens,
                                                                unsigned int* flags) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = int64_t(B) * n_new * row_vecs;
   if (gid >= total) return;
@@ -146,6 +152,8 @@ __global__ void __launch_bounds__(256) block_keys_kernel(const uint16_t* __restr
                                                          uint16_t* __restrict__ bkeys,
                                                          int64_t blocks_per_seq, int only_new,
                                                          int n_new) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = int64_t(B) * blocks_per_seq * 16;
   if (gid >= total) return;
@@ -189,9 +197,8 @@ cudaError_t launch_fp4_quantize(const uint16_t* x, int B, int n_new, uint8_t* co
   if (n_groups == 0) return cudaSuccess;
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
-  fp4_quantize_kernel<<<grid_for(n_groups, 256), 256, 0, st>>>(x, n_groups, n_new, codes, scales, cap,
+  return launch_pdl(fp4_quantize_kernel, grid_for(n_groups, 256), dim3(256), 0, st, x, n_groups, n_new, codes, scales, cap,
                                                                offsets, offset_bias, flags);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_copy_rows_append(const uint16_t* src, int B, int n_new, int row_elems,
@@ -201,9 +208,8 @@ cudaError_t launch_copy_rows_append(const uint16_t* src, int B, int n_new, int r
   if (total == 0) return cudaSuccess;
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
-  copy_rows_append_kernel<<<grid_for(total, 256), 256, 0, st>>>(src, B, n_new, row_vecs, dst, cap,
+  return launch_pdl(copy_rows_append_kernel, grid_for(total, 256), dim3(256), 0, st, src, B, n_new, row_vecs, dst, cap,
                                                                 lens, flags);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_block_keys(const uint16_t* KI, int B, int64_t cap, const int32_t* lens,
@@ -211,9 +217,8 @@ cudaError_t launch_block_keys(const uint16_t* KI, int B, int64_t cap, const int3
   const int64_t bps = only_new ? int64_t(n_new / CSA2_BLOCK + 1) : cap / CSA2_BLOCK;
   const int64_t total = int64_t(B) * bps * 16;
   if (total == 0) return cudaSuccess;
-  block_keys_kernel<<<grid_for(total, 256), 256, 0, st>>>(KI, B, cap, lens, block_keys, bps, only_new,
+  return launch_pdl(block_keys_kernel, grid_for(total, 256), dim3(256), 0, st, KI, B, cap, lens, block_keys, bps, only_new,
                                                           n_new);
-  return cudaGetLastError();
 }
 
 }  // namespace csa2
@@ -246,8 +251,9 @@ extern "C" csa2_status csa2_fp4_dequantize(const uint8_t* codes, const uint8_t* 
   if (rows == 0) return CSA2_OK;
   if (!codes || !scales || !out || !al16(codes) || !al16(scales) || !al16(out)) return CSA2_ERR_INVALID_ARG;
   const int64_t n_groups = rows * (CSA2_D / CSA2_GROUP);
-  csa2::fp4_dequantize_kernel<<<csa2::grid_for(n_groups, 256), 256, 0,
-                                reinterpret_cast<cudaStream_t>(stream)>>>(codes, scales, n_groups, out);
+  const cudaError_t e = csa2::launch_pdl(csa2::fp4_dequantize_kernel, dim3(csa2::grid_for(n_groups, 256)), dim3(256), 0,
+                                        reinterpret_cast<cudaStream_t>(stream), codes, scales, n_groups, out);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
 

@@ -349,7 +349,8 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
       const uint16_t* swa = g->W > 0 ? g->swa[l] + int64_t(b0) * SW * CSA2_D : nullptr;
       if (!ok(csa2::launch_sparse_attn(g->q[l] + r0 * (CSA2_H * CSA2_D), Bc, Nq, codes, scl, g->cap, latest, nullptr,
                                        K, swa, swl, g->W, g->softmax_scale, g->out[l] + r0 * (CSA2_H * CSA2_D),
-                                       g->lse[l] ? g->lse[l] + r0 * CSA2_H : nullptr, ns, attn_ws, aux, zeroed)))
+                                       g->lse[l] ? g->lse[l] + r0 * CSA2_H : nullptr, ns, attn_ws, aux, zeroed,
+                                       mode == CSA2_MODE_REUSE)))
         return CSA2_ERR_CUDA;
     }
   }

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_kernel(
     const int32_t* __restrict__ cand_len, int64_t n_cand, int ratio,
     const int32_t* __restrict__ q_pos, float* __restrict__ scores, int64_t ld,
     int32_t* __restrict__ n_valid_out, int64_t chunk, unsigned int* flags) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.y;
   const int b = row / Nq, qi = row - b * Nq;
   const int64_t T = min(max(int64_t(lens[b]), int64_t(0)), cap_entries);
@@ -160,15 +162,11 @@ cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
   if (cand)
-    index_score_kernel<true><<<grid, kThreads, 0, st>>>(qI, w, Nq, KI, key_stride_rows, lens,
-                                                        cap_entries, block_div, cand, cand_len, n_cand,
-                                                        ratio, q_pos, scores, ld, n_valid, chunk, flags);
-  else
-    index_score_kernel<false><<<grid, kThreads, 0, st>>>(qI, w, Nq, KI, key_stride_rows, lens,
-                                                         cap_entries, block_div, nullptr, nullptr, 0,
-                                                         ratio, q_pos, scores, ld, n_valid, chunk,
-                                                         flags);
-  return cudaGetLastError();
+    return launch_pdl(index_score_kernel<true>, grid, dim3(kThreads), 0, st, qI, w, Nq, KI, key_stride_rows, lens,
+                      cap_entries, block_div, cand, cand_len, n_cand, ratio, q_pos, scores, ld, n_valid, chunk, flags);
+  return launch_pdl(index_score_kernel<false>, grid, dim3(kThreads), 0, st, qI, w, Nq, KI, key_stride_rows, lens,
+                    cap_entries, block_div, nullptr, nullptr, int64_t(0), ratio, q_pos, scores, ld, n_valid, chunk,
+                    flags);
 }
 
 }  // namespace csa2

@@ -400,6 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
     uint32_t* __restrict__ row_hist /* [rows][4096]: group maxima by top 12 key bits */, int64_t slice_len) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.y, nslices = gridDim.x;
   const int t = threadIdx.x, lane = t & 31;
   const float* s = scores + int64_t(row) * ld;
@@ -670,9 +672,8 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
     }
   }
   const dim3 grid{unsigned(nslices), unsigned(rows), 1u};
-  topk_kernel<<<grid, kThreads, smem, st>>>(scores, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len,
-                                            ckey, ccol, ctl, hist, slice_len);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, grid, dim3(kThreads), smem, st, scores, n, ld, n_valid, k, map, map_ld, idx, n_sel,
+                    expand8, pool_len, ckey, ccol, ctl, hist, slice_len);
 }
 
 }  // namespace csa2
