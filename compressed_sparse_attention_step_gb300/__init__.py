@@ -19,8 +19,8 @@ D, H, HI, DI, GROUP, BLOCK = 512, 16, 4, 128, 16, 8
 CODE_BYTES, SCALE_BYTES = 256, 32
 MAX_LAYERS = 16
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
-OP_TOPK, OP_BLOCK_POOL, OP_SPARSE_ATTN, OP_GROUP_STEP = 1, 2, 3, 4
-FLAG_APPEND_OOB, FLAG_INDEX_OOB = 1, 2
+OP_TOPK, OP_BLOCK_POOL, OP_SPARSE_ATTN, OP_GROUP_STEP, OP_INDEX_SELECT_PREFILL = 1, 2, 3, 4, 5
+FLAG_APPEND_OOB, FLAG_INDEX_OOB, FLAG_TIMEOUT = 1, 2, 4
 
 LIB_PATH = _build.LIB
 
@@ -88,6 +88,7 @@ def lib():
             "csa2_group_desc_size": [],
             "csa2_sparse_attn_decode_static": [P, I32, I32, P, P, I64, P, P, I32, P, P, I32, F32, P, P, I32, P],
             "csa2_sparse_attn_static_scratch_bytes": [],
+            "csa2_index_select_prefill": [P, P, I32, I32, P, I64, P, I32, P, I32, P, P, P, SZ, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -221,6 +222,24 @@ def _nbytes(t):
 def _ws(nbytes, device):
     torch = _torch()
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def csa2_index_select_prefill(qI, w, KI, lens, idx, *, k=512, ratio=1, q_pos=None, n_sel=None, ws=None,
+                              stream=None):
+    """Exact Top-k per query of a prefill chunk via the tensor-core filter: qI [B, Nq, 4, 128] bf16,
+    w [B, Nq, 4] fp32, KI [B, cap, 128] bf16, lens int32 [B] -> idx int32 [B*Nq, k]."""
+    torch = _torch()
+    B, Nq = qI.shape[0], qI.shape[1]
+    cap = KI.shape[1]
+    rows = B * Nq
+    need = workspace_size(OP_INDEX_SELECT_PREFILL, B=B, Nq=Nq, cap=cap)
+    if ws is None:
+        ws = _ws(need, qI.device)
+    _check("csa2_index_select_prefill", lib().csa2_index_select_prefill(
+        _ptr(qI, "qI", _bf16_types(), rows * HI * DI), _ptr(w, "w", (torch.float32,), rows * HI), B, Nq,
+        _ptr(KI, "KI", _bf16_types(), B * cap * DI), cap, _ptr(lens, "lens", (torch.int32,), B), ratio,
+        _ptr(q_pos, "q_pos", (torch.int32,), rows), k, _ptr(idx, "idx", (torch.int32,), rows * k),
+        _ptr(n_sel, "n_sel", (torch.int32,), rows), _ptr(ws, "ws"), _nbytes(ws), _stream(stream)))
 
 
 def csa2_block_pool(qI, w, block_keys, cap, lens, keep, pool, pool_len, *, ratio=1, q_pos=None, ws=None,

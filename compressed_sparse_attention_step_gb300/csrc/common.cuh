@@ -122,6 +122,41 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
 }
 
 // ---------------------------------------------------------------------------------------------
+// Canonical indexer score s = sum_h w_h relu(qI_h . KI_t) in the fixed fp32 order: per head, eight
+// fused-multiply-add chains over channels 16j..16j+15 from +0, then ((p0+p1)+(p2+p3))+((p4+p5)+
+// (p6+p7)), relu, and (w0 r0 + w1 r1) + (w2 r2 + w3 r3) with every product and sum rounded.
+// ---------------------------------------------------------------------------------------------
+// Eight lanes per key: lane j = lane & 7 owns channels 16j..16j+15 (qf: its qI slice as fp32, k0/k1:
+// its 32 key bytes) and head wh = w[2 (j & 1) + ((j >> 1) & 1)].  Every lane of the group of eight
+// returns the same bits.  All 32 lanes of the warp must call it.
+__device__ __forceinline__ float canon_score_lane8(const float (&qf)[4][16], float wh, uint4 k0, uint4 k1, int j) {
+  const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+  float P[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      acc = __fmaf_rn(qf[h][2 * e], bf16lo(kw[e]), acc);
+      acc = __fmaf_rn(qf[h][2 * e + 1], bf16hi(kw[e]), acc);
+    }
+    P[h] = acc;
+  }
+  const bool odd = (j & 1) != 0, second = (j & 2) != 0;
+  const float s0 = odd ? P[0] : P[2], s1 = odd ? P[1] : P[3];
+  const float k0v = odd ? P[2] : P[0], k1v = odd ? P[3] : P[1];
+  const float A0 = __fadd_rn(k0v, __shfl_xor_sync(0xffffffffu, s0, 1));
+  const float A1 = __fadd_rn(k1v, __shfl_xor_sync(0xffffffffu, s1, 1));
+  const float sendB = second ? A0 : A1, keepB = second ? A1 : A0;
+  const float Bv = __fadd_rn(keepB, __shfl_xor_sync(0xffffffffu, sendB, 2));
+  const float dot = __fadd_rn(Bv, __shfl_xor_sync(0xffffffffu, Bv, 4));
+  const float r = dot > 0.0f ? dot : 0.0f;
+  const float m = __fmul_rn(wh, r);
+  const float m2 = __fadd_rn(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  return __fadd_rn(m2, __shfl_xor_sync(0xffffffffu, m2, 1));
+}
+
+// ---------------------------------------------------------------------------------------------
 // Programmatic dependent launch.  Every library kernel is launched with programmatic stream
 // serialisation allowed: it may start while the kernel before it in the stream is still running,
 // calls pdl_wait() before it touches anything an earlier kernel writes (or writes anything an
@@ -183,6 +218,21 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
 // Attention splits: at most one per 128-row tile; attn_ws_bytes with the effective split.
 int attn_effective_split(int k, int W, int n_split);
 size_t attn_ws_bytes(int64_t instances, int n_split);
+// Prefill chunks: exact Top-k per query through the tensor-core filter (prefill.cu); the rescore
+// and selection over the filter's bitmap (topk.cu).
+size_t prefill_ws_bytes(int64_t rows, int64_t cap, int B);
+int64_t prefill_max_groups();  // the longest cache (in groups of 32 entries) the filter handles
+float prefill_delta_coef();
+cudaError_t launch_prefill_select(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
+                                  int64_t cap, const int32_t* lens, int ratio, const int32_t* q_pos, int k,
+                                  int32_t* idx, int32_t* n_sel, void* ws, cudaStream_t st);
+// bitmap: [rows][n_words] marked keys; ubound: per row, the score key of an upper bound on every
+// canonical score of the row (or null: no bound); order: the rows in processing order (or null).
+cudaError_t launch_bitmap_select(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
+                                 int64_t cap, const int32_t* lens, int ratio, const int32_t* q_pos, int k,
+                                 const uint32_t* bitmap, int64_t n_words, const uint32_t* ubound,
+                                 const int32_t* order, int32_t* idx, int32_t* n_sel, cudaStream_t st);
+int bitmap_list_cap();  // marked keys that one list round of the selection rescores
 int attn_auto_split(int64_t instances, int k, int W);
 
 // Library-owned side stream (highest priority) and events of the current device, created on first

@@ -53,15 +53,25 @@ namespace {
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Prefill chunks of at least 64 queries per sequence select on the tensor cores without
+// materialising scores (flat selection only; TMA row coordinates are 32-bit, and a row's group
+// maxima must fit in shared memory).
+constexpr int kPrefillMinQueries = 64;
+inline bool prefill_path(int B, int Nq, int hierarchical, int64_t cap) {
+  return Nq >= kPrefillMinQueries && !hierarchical && B <= 65535 && int64_t(B) * cap < (int64_t(1) << 31) &&
+         (cap + 31) / 32 <= prefill_max_groups();
+}
+
 struct GroupWs {
-  size_t scores_off, nv_off, topk_off, attn_off, total;
+  size_t scores_off, nv_off, topk_off, attn_off, pf_off, total;
   int64_t score_ld;
 };
 
 GroupWs group_ws_layout(int B, int Nq, int64_t cap, int K, int W, int hierarchical, int keep, int n_split) {
   GroupWs L{};
   const int64_t rows = int64_t(B) * Nq;
-  int64_t ld = cap;
+  const bool pf = prefill_path(B, Nq, hierarchical, cap);
+  int64_t ld = pf ? 0 : cap;
   if (hierarchical) ld = std::max<int64_t>(cap / CSA2_BLOCK, int64_t(keep) * CSA2_BLOCK);
   L.score_ld = ld;
   L.scores_off = 0;
@@ -69,7 +79,8 @@ GroupWs group_ws_layout(int B, int Nq, int64_t cap, int K, int W, int hierarchic
   L.topk_off = L.nv_off + align256(size_t(rows) * sizeof(int32_t));
   L.attn_off = L.topk_off + align256(topk_ws_bytes(int(rows), ld));
   const int ns = attn_effective_split(K, W, n_split ? n_split : attn_auto_split(rows, K, W));
-  L.total = L.attn_off + align256(attn_ws_bytes(rows, ns));
+  L.pf_off = L.attn_off + align256(attn_ws_bytes(rows, ns));
+  L.total = L.pf_off + (pf ? align256(prefill_ws_bytes(rows, cap, B)) : 0);
   return L;
 }
 
@@ -93,6 +104,8 @@ extern "C" size_t csa2_workspace_size(int op, const csa2_dims* d) {
       const int ns = csa2::attn_effective_split(d->k, W, d->n_split ? d->n_split : csa2::attn_auto_split(rows, d->k, W));
       return csa2::attn_ws_bytes(rows, ns);
     }
+    case CSA2_OP_INDEX_SELECT_PREFILL:
+      return csa2::prefill_ws_bytes(rows, d->cap, d->B);
     case CSA2_OP_GROUP_STEP:
       return csa2::group_ws_layout(d->B, d->Nq, d->cap, d->k, d->W, d->hierarchical, d->n_blocks_keep,
                                    d->n_split)
@@ -198,6 +211,8 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
     if (g->W > 0 && (!g->swa[l] || !al16(g->swa[l]))) return CSA2_ERR_INVALID_ARG;
     if (m != CSA2_MODE_REUSE) {
       if (!g->qI[l] || !g->w[l] || !g->idx[l] || !al16(g->qI[l])) return CSA2_ERR_INVALID_ARG;
+      if (csa2::prefill_path(g->B, g->Nq, g->hierarchical, g->cap) && (!al16(g->w[l]) || !al16(g->idx[l])))
+        return CSA2_ERR_INVALID_ARG;
       any_full |= (m == CSA2_MODE_FULL);
     }
   }
@@ -216,6 +231,8 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   int32_t* nv = reinterpret_cast<int32_t*>(wsb + lay.nv_off);
   void* tws = wsb + lay.topk_off;
   float* attn_ws = reinterpret_cast<float*>(wsb + lay.attn_off);
+  void* pf_ws = wsb + lay.pf_off;
+  const bool pf = csa2::prefill_path(g->B, g->Nq, g->hierarchical, g->cap);
   const int ns_all =
       csa2::attn_effective_split(g->K, g->W, g->n_split ? g->n_split : csa2::attn_auto_split(rows, g->K, g->W));
   const int64_t nb = g->cap / CSA2_BLOCK;
@@ -292,8 +309,10 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
         K, g->W, g->n_split ? g->n_split : std::min(csa2::attn_auto_split(rc, K, g->W), n_chunks > 1 ? 4 : 32));
     while (ns > 1 && csa2::attn_ws_bytes(rc, ns) > csa2::attn_ws_bytes(rows, ns_all)) --ns;
 
-    // stage 1 (stream): the first scan over this chunk's keys (layer 0 is Full or Reindex)
-    if (g->hierarchical && g->modes[0] == CSA2_MODE_FULL) {
+    // stage 1 (stream): the first scan over this chunk's keys (layer 0 is Full or Reindex); prefill
+    // chunks select on the tensor cores in stage 2 instead
+    if (pf) {
+    } else if (g->hierarchical && g->modes[0] == CSA2_MODE_FULL) {
       if (nb > 0 &&
           !ok(csa2::launch_index_score(qI_of(0), w_of(0), Bc, Nq, bkeys, nb, lens, g->cap, CSA2_BLOCK, nullptr,
                                        nullptr, 0, g->ratio, qpos, sc, nb, pool_len, st)))
@@ -331,6 +350,10 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
             return CSA2_ERR_CUDA;
           if (!ok(csa2::launch_topk(sc, int(rc), pool_w, pool_w, nvc, K, pool, pool_w, idx_of(l), nullptr, 0, nullptr,
                                     tws, aux, zeroed)))
+            return CSA2_ERR_CUDA;
+        } else if (pf) {
+          if (!ok(csa2::launch_prefill_select(qI_of(l), w_of(l), Bc, Nq, KI, g->cap, lens, g->ratio, qpos, K,
+                                              idx_of(l), nullptr, pf_ws, aux)))
             return CSA2_ERR_CUDA;
         } else {
           if (l != 0 &&

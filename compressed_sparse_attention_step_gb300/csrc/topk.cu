@@ -39,6 +39,7 @@ constexpr int64_t kRegSlice = int64_t(kRegSteps) * 16 * kThreads;  // = kSlice
 constexpr int kLocCap = 4096;           // candidates of one register-held slice
 
 struct SelSmem {
+  static constexpr int kNT = kThreads;
   uint32_t hist[kBins];
   union {
     struct {  // selection: the whole-row path, long slices, and the last CTA of a row
@@ -60,6 +61,21 @@ struct SelSmem {
   uint32_t res_bin, res_before;
   uint32_t run_g, run_e;
   int is_last;
+};
+
+// The prefill rows' selection (bitmap_select_kernel): a shorter candidate list (marked keys beyond
+// it stream through keep_top), kept in column order, so that two CTAs share an SM.
+constexpr int kBmThreads = 256;
+constexpr int kBmCap = 4096;  // > CSA2_MAX_K
+struct BmSmem {
+  static constexpr int kNT = kBmThreads;
+  uint32_t hist[2048];
+  uint32_t cand_key[kBmCap];
+  int32_t cand_col[kBmCap];  // always in column order
+  uint32_t scan_tmp[32];
+  uint32_t nsel, ncand, base;
+  uint32_t res_bin, res_before;
+  uint32_t run_g, run_e;
 };
 
 // Visit keys [lo, hi) of a row in tiles of 4 * U * blockDim.x (each thread takes U groups of 4
@@ -90,11 +106,11 @@ __device__ __forceinline__ void for_each_key(const float* s, int64_t lo, int64_t
   }
 }
 
-template <int NB>
+template <int NB, int NT>
 __device__ void find_bin_n(const uint32_t* hist, uint32_t need, bool from_top, uint32_t* scan_tmp,
                            uint32_t* res_bin, uint32_t* res_before) {
-  constexpr int per = NB / kThreads;   // 8, 4 or 2 bins per thread
-  static_assert(per * kThreads == NB && (per == 8 || per == 4 || per == 2), "bin count");
+  constexpr int per = NB / NT;   // 2 .. 16 bins per thread (NT threads in the block)
+  static_assert(per * NT == NB && (per == 16 || per == 8 || per == 4 || per == 2), "bin count");
   const int t = threadIdx.x;
   // the run of walk positions [t*per, t*per + per) covers bins [lo_bin, lo_bin + per)
   const int lo_bin = from_top ? NB - (t + 1) * per : t * per;
@@ -132,13 +148,19 @@ __device__ void find_bin_n(const uint32_t* hist, uint32_t need, bool from_top, u
 
 // Bin where the cumulative count, walking from the highest bin down (from_top) or from the lowest
 // bin up, first reaches need (1 <= need <= total).  Result in *res_bin / *res_before (count
-// strictly before that bin in walking order).  All threads of the block call it.  Each thread
+// strictly before that bin in walking order).  All NT threads of the block call it.  Each thread
 // reads its run of bins with vector loads (a strided scalar walk would hit one bank per warp).
+template <int NT = kThreads>
 __device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, bool from_top,
                                          uint32_t* scan_tmp, uint32_t* res_bin, uint32_t* res_before) {
-  if (nbins == 4096) find_bin_n<4096>(hist, need, from_top, scan_tmp, res_bin, res_before);
-  else if (nbins == 2048) find_bin_n<2048>(hist, need, from_top, scan_tmp, res_bin, res_before);
-  else find_bin_n<1024>(hist, need, from_top, scan_tmp, res_bin, res_before);
+  if constexpr (4096 / NT <= 16) {
+    if (nbins == 4096) {
+      find_bin_n<4096, NT>(hist, need, from_top, scan_tmp, res_bin, res_before);
+      return;
+    }
+  }
+  if (nbins == 2048) find_bin_n<2048, NT>(hist, need, from_top, scan_tmp, res_bin, res_before);
+  else find_bin_n<1024, NT>(hist, need, from_top, scan_tmp, res_bin, res_before);
 }
 
 __device__ __forceinline__ void zero(uint32_t* h, int n) {
@@ -178,9 +200,10 @@ __device__ void finish_row(const RowOut& o, int64_t cnt, int row, int32_t* n_sel
   for (int i = int(cnt) * (o.expand8 ? CSA2_BLOCK : 1) + threadIdx.x; i < o.out_w; i += blockDim.x) o.out[i] = -1;
 }
 
-// The k largest of the nc candidates in shared memory (nc >= k) by (key desc, column asc), emitted
-// in column order; columns are < ncols.
-__device__ __noinline__ void select_candidates(SelSmem& sm, int nc, int k, int64_t ncols, const RowOut o) {
+// The cut of the k largest of the nc candidates in shared memory (nc >= k) by (key desc, column
+// asc): a candidate is among them iff key > tau, or key == tau and column <= col_cut.
+template <class S>
+__device__ __forceinline__ void candidate_cut(S& sm, int nc, int k, uint32_t& tau_out, int32_t& cut_out) {
   const int t = threadIdx.x;
   uint32_t need = uint32_t(k), prefix = 0, mask = 0;
   const int kshift[3] = {21, 10, 0}, kwidth[3] = {11, 11, 10};
@@ -192,7 +215,7 @@ __device__ __noinline__ void select_candidates(SelSmem& sm, int nc, int k, int64
       if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> kshift[r]) & uint32_t(nb - 1)], 1u);
     }
     __syncthreads();
-    find_bin(sm.hist, nb, need, true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+    find_bin<S::kNT>(sm.hist, nb, need, true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
     prefix |= sm.res_bin << kshift[r];
     mask |= uint32_t(nb - 1) << kshift[r];
     need -= sm.res_before;
@@ -215,13 +238,25 @@ __device__ __noinline__ void select_candidates(SelSmem& sm, int nc, int k, int64
           atomicAdd(&sm.hist[(col >> cshift[r]) & uint32_t(nb - 1)], 1u);
       }
       __syncthreads();
-      find_bin(sm.hist, nb, need, false, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+      find_bin<S::kNT>(sm.hist, nb, need, false, sm.scan_tmp, &sm.res_bin, &sm.res_before);
       cpre |= sm.res_bin << cshift[r];
       need -= sm.res_before;
       __syncthreads();
     }
     col_cut = int32_t(cpre);
   }
+  tau_out = tau;
+  cut_out = col_cut;
+}
+
+// The k largest of the nc candidates in shared memory (nc >= k) by (key desc, column asc), emitted
+// in column order; columns are < ncols.
+template <class S>
+__device__ __noinline__ void select_candidates(S& sm, int nc, int k, int64_t ncols, const RowOut o) {
+  const int t = threadIdx.x;
+  uint32_t tau;
+  int32_t col_cut;
+  candidate_cut(sm, nc, k, tau, col_cut);
   if (ncols <= kBitmapCols) {
     // slot of a winner = number of winners in lower columns: bitmap + prefix popcounts
     const int nwords = int((ncols + 31) / 32);
@@ -276,6 +311,56 @@ __device__ __noinline__ void select_candidates(SelSmem& sm, int nc, int k, int64
     }
   }
   for (int i = t; i < k; i += blockDim.x) o.emit(i, sm.sel[i]);
+}
+
+// Visits the winners (key > tau, or key == tau and column <= col_cut) of the nc listed candidates in
+// list order: f(slot, key, col) with slot = the number of winners before it.  All threads call it.
+template <class S, class F>
+__device__ __forceinline__ void for_each_winner(S& sm, int nc, uint32_t tau, int32_t col_cut, F&& f) {
+  const int t = threadIdx.x;
+  if (t == 0) sm.run_g = 0;
+  __syncthreads();
+  for (int base = 0; base < nc; base += blockDim.x) {
+    const int c = base + t;
+    uint32_t key = 0;
+    int32_t col = 0;
+    bool win = false;
+    if (c < nc) {
+      key = sm.cand_key[c];
+      col = sm.cand_col[c];
+      win = key > tau || (key == tau && col <= col_cut);
+    }
+    uint32_t tot;
+    const uint32_t slot = sm.run_g + block_exclusive_scan(win ? 1u : 0u, sm.scan_tmp, &tot);  // reads done
+    if (win) f(slot, key, col);
+    __syncthreads();
+    if (t == 0) sm.run_g += tot;
+    __syncthreads();
+  }
+}
+
+// Keeps the k largest of the nc candidates (nc >= k) by (key desc, column asc) at the front of the
+// list, in their list order (a stable compaction); returns the k-th largest key.
+template <class S>
+__device__ __noinline__ uint32_t keep_top(S& sm, int nc, int k) {
+  uint32_t tau;
+  int32_t col_cut;
+  candidate_cut(sm, nc, k, tau, col_cut);
+  for_each_winner(sm, nc, tau, col_cut, [&](uint32_t slot, uint32_t key, int32_t col) {
+    sm.cand_key[slot] = key;
+    sm.cand_col[slot] = col;
+  });
+  return tau;
+}
+
+// The k largest of the nc listed candidates (nc >= k), emitted in list order (the list is in
+// column order).
+template <class S>
+__device__ __noinline__ void select_listed(S& sm, int nc, int k, const RowOut o) {
+  uint32_t tau;
+  int32_t col_cut;
+  candidate_cut(sm, nc, k, tau, col_cut);
+  for_each_winner(sm, nc, tau, col_cut, [&](uint32_t slot, uint32_t, int32_t col) { o.emit(int(slot), col); });
 }
 
 // Whole-row selection by one CTA (short rows, and rows whose candidates overflow).
@@ -623,6 +708,133 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
   }
 }
 
+// Prefill rows: the keys marked in the tensor-core filter's bitmap are rescored in the canonical
+// order (eight lanes per key, the query slice in registers) and the exact Top-k is selected among
+// them.  One CTA per query row.
+__global__ void __launch_bounds__(kBmThreads, 2) bitmap_select_kernel(
+    const uint16_t* __restrict__ qI, const float* __restrict__ w, int Nq, const uint16_t* __restrict__ KI,
+    int64_t cap, const int32_t* __restrict__ lens, int ratio, const int32_t* __restrict__ q_pos, int k,
+    const uint32_t* __restrict__ bitmap, int64_t n_words, const uint32_t* __restrict__ ubound,
+    const int32_t* __restrict__ order, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  BmSmem& sm = *reinterpret_cast<BmSmem*>(smem_raw);
+  pdl_wait();
+  pdl_trigger();
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int64_t row = order ? int64_t(__ldg(order + blockIdx.x)) : int64_t(blockIdx.x), b = row / Nq, qi = row - b * Nq;
+  const int64_t T = min(max(int64_t(lens[b]), int64_t(0)), cap);
+  const int64_t p = q_pos ? int64_t(q_pos[row]) : int64_t(ratio) * T - Nq + qi;
+  const int64_t vis = (p + 1 < 0) ? 0 : min((p + 1) / ratio, T);
+  RowOut o{nullptr, idx + row * k, k, 0};
+  if (vis <= k) {
+    for (int64_t i = t; i < vis; i += kBmThreads) o.emit(int(i), int32_t(i));
+    finish_row(o, vis, int(row), n_sel, nullptr);
+    return;
+  }
+  const uint32_t* bm = bitmap + row * n_words;
+  const uint16_t* qrow = qI + row * (CSA2_HI * CSA2_DI);
+  const uint16_t* kseq = KI + b * cap * CSA2_DI;
+  const int64_t nw = min((vis + 31) / 32, n_words);
+  const int per = int((nw + kBmThreads - 1) / kBmThreads);
+  auto word = [&](int64_t wi) -> uint32_t {
+    uint32_t v = __ldg(bm + wi);
+    const int64_t valid = vis - 32 * wi;  // bits of this word that are visible positions
+    if (valid < 32) v &= (1u << valid) - 1u;
+    return v;
+  };
+  uint32_t local = 0;
+  for (int e = 0; e < per; ++e) {
+    const int64_t wi = int64_t(t) * per + e;
+    if (wi < nw) local += __popc(word(wi));
+  }
+  uint32_t total;
+  const uint32_t first = block_exclusive_scan(local, sm.scan_tmp, &total);  // rank of this thread's first key
+  const int j = lane & 7, sub = lane >> 3;  // eight lanes per candidate, four candidates per warp step
+  float qf[4][16];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint4 a = *reinterpret_cast<const uint4*>(qrow + h * CSA2_DI + 16 * j);
+    const uint4 c = *reinterpret_cast<const uint4*>(qrow + h * CSA2_DI + 16 * j + 8);
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      qf[h][2 * e] = bf16lo(v[e]);
+      qf[h][2 * e + 1] = bf16hi(v[e]);
+    }
+  }
+  const float wh = w[row * CSA2_HI + 2 * (j & 1) + ((j >> 1) & 1)];
+  // Marked keys in rank (= position) order, a chunk at a time: the chunk is appended to the list
+  // and rescored; while keys remain, the list is cut back to its k best (in position order), so
+  // any number of marked keys (ties at the threshold) is selected exactly.  Once the k-th best key
+  // reaches the row's score bound ubound[row] no later key can enter (a later tie loses on
+  // position).  A row whose marked keys overflow the list and whose bound is <= 0 (all head
+  // weights negative: typically thousands of exact zeros tie) takes chunks of max(2k, 1024) keys
+  // and stops after the first.
+  const uint32_t ub = ubound ? __ldg(ubound + row) : 0xFFFFFFFFu;
+  const uint32_t lim = (total > uint32_t(kBmCap) && ub <= score_key(0.0f)) ? uint32_t(max(2 * k, 1024))
+                                                                          : uint32_t(kBmCap);
+  uint32_t n = 0;
+  for (uint32_t lo = 0; lo < total;) {
+    const uint32_t hi = min(total, lo + min(uint32_t(kBmCap) - n, lim));
+    uint32_t slot = first;
+    for (int e = 0; e < per && slot < hi; ++e) {
+      const int64_t wi = int64_t(t) * per + e;
+      if (wi >= nw) break;
+      uint32_t v = word(wi);
+      const uint32_t pc = __popc(v);
+      if (slot + pc <= lo) {  // the whole word lies before this chunk
+        slot += pc;
+        continue;
+      }
+      while (v && slot < hi) {
+        const int bit = __ffs(v) - 1;
+        if (slot >= lo) sm.cand_col[n + slot - lo] = int32_t(wi * 32 + bit);
+        ++slot;
+        v &= v - 1u;
+      }
+    }
+    __syncthreads();
+    const uint32_t n_end = n + (hi - lo);
+    // the next step's key rows load while this step's are scored
+    constexpr uint32_t kStep = 4 * (kBmThreads / 32);
+    auto load_key = [&](uint32_t c, uint4& k0, uint4& k1) {
+      k0 = make_uint4(0, 0, 0, 0);
+      k1 = k0;
+      if (c < n_end) {
+        const uint4* kp = reinterpret_cast<const uint4*>(kseq + int64_t(sm.cand_col[c]) * CSA2_DI + 16 * j);
+        k0 = __ldg(kp);
+        k1 = __ldg(kp + 1);
+      }
+    };
+    uint4 k0, k1;
+    load_key(n + uint32_t(warp) * 4 + sub, k0, k1);
+    for (uint32_t c0 = n + uint32_t(warp) * 4; c0 < n_end; c0 += kStep) {
+      const uint32_t c = c0 + sub;
+      uint4 n0, n1;
+      load_key(c + kStep, n0, n1);
+      const float sc = canon_score_lane8(qf, wh, k0, k1, j);
+      if (j == 0 && c < n_end) sm.cand_key[c] = score_key(sc);
+      k0 = n0;
+      k1 = n1;
+    }
+    __syncthreads();
+    n = n_end;
+    lo = hi;
+    if (lo < total) {
+      const uint32_t tau = keep_top(sm, int(n), k);
+      n = uint32_t(k);
+      if (tau >= ub) break;
+    }
+  }
+  if (n < uint32_t(k)) {  // not reached: at least k groups hold a key at or above the threshold
+    for (uint32_t i = t; i < n; i += kBmThreads) o.emit(int(i), sm.cand_col[i]);
+    finish_row(o, n, int(row), n_sel, nullptr);
+    return;
+  }
+  select_listed(sm, int(n), k, o);
+  finish_row(o, k, int(row), n_sel, nullptr);
+}
+
 }  // namespace
 
 int topk_slices(int64_t n, int k) {
@@ -675,6 +887,27 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
   return launch_pdl(topk_kernel, grid, dim3(kThreads), smem, st, scores, n, ld, n_valid, k, map, map_ld, idx, n_sel,
                     expand8, pool_len, ckey, ccol, ctl, hist, slice_len);
 }
+
+cudaError_t launch_bitmap_select(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
+                                 int64_t cap, const int32_t* lens, int ratio, const int32_t* q_pos, int k,
+                                 const uint32_t* bitmap, int64_t n_words, const uint32_t* ubound,
+                                 const int32_t* order, int32_t* idx, int32_t* n_sel, cudaStream_t st) {
+  const int64_t rows = int64_t(B) * Nq;
+  if (rows == 0) return cudaSuccess;
+  const size_t smem = sizeof(BmSmem);
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(bitmap_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  return launch_pdl(bitmap_select_kernel, dim3(unsigned(rows)), dim3(kBmThreads), smem, st, qI, w, Nq, KI, cap, lens,
+                    ratio, q_pos, k, bitmap, n_words, ubound, order, idx, n_sel);
+}
+
+int bitmap_list_cap() { return kBmCap; }
 
 }  // namespace csa2
 

@@ -168,6 +168,27 @@ csa2_status csa2_block_pool(const uint16_t* qI, const float* w, int B, int Nq,
                             void* ws, size_t ws_bytes, csa2_stream_t stream);
 
 /*
+ * Exact Top-k cache positions for every query of a prefill chunk, by the indexer score
+ * s_t = sum_h w_h relu(qI_h . KI_t) in the canonical fp32 order (ai-maestro "Compressed Sparse
+ * Attention 2"; the causal compressed positions of "Causal Encoder-Decoder architecture"), without
+ * materialising the scores.  The dense [B*Nq*4 x 128] x [128 x T] product runs on the tensor cores
+ * twice: first to bound each query's k-th score from below, then to mark every key whose
+ * tensor-core score is within twice a rigorous error bound of that bound; the marked keys are
+ * rescored canonically and selected exactly.  The result is identical to csa2_index_score followed
+ * by csa2_topk (same tie rule, same visibility).
+ *   qI bf16 [B][Nq][4][128], w fp32 [B][Nq][4] (16-byte aligned), KI bf16 [B][cap][128], lens,
+ *   ratio, q_pos as csa2_index_score.  k in 1..2048.
+ *   idx int32 [B*Nq][k] ascending, -1 padded when fewer than k positions are visible;
+ *   n_sel int32 [B*Nq] (nullable): the number selected.
+ *   ws csa2_workspace_size(CSA2_OP_INDEX_SELECT_PREFILL, {B, Nq, cap}) bytes.
+ * Tensor-core waits are bounded; one that runs out sets CSA2_FLAG_TIMEOUT.
+ */
+csa2_status csa2_index_select_prefill(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
+                                      int64_t cap, const int32_t* lens, int ratio, const int32_t* q_pos, int k,
+                                      int32_t* idx, int32_t* n_sel, void* ws, size_t ws_bytes,
+                                      csa2_stream_t stream);
+
+/*
  * Sparse attention of each query's 16 heads over its selected FP4 rows plus its sliding-window
  * rows ("Every layer retains its own main Q and sliding-window key-value cache", ai-maestro
  * "Compressed Sparse Attention 2"; 128-token window, "Causal Encoder-Decoder architecture").
@@ -283,6 +304,7 @@ csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_t ws_bytes,
 #define CSA2_OP_BLOCK_POOL 2
 #define CSA2_OP_SPARSE_ATTN 3
 #define CSA2_OP_GROUP_STEP 4
+#define CSA2_OP_INDEX_SELECT_PREFILL 5
 
 typedef struct csa2_dims {
   int B, Nq;
