@@ -46,6 +46,19 @@ def assert_attn_close(got_bf16_bits, ref, what=""):
     assert err.max() <= ATOL and rel <= RTOL, f"{what}: max abs {err.max():.3e}, rel {rel:.3e}"
 
 
+def one_query_oracle(orc, modes, T, codes, scales, KI, q, qI, w, swa, swa_len, i, q_pos_i, *, K, W, ratio):
+    """The oracle group step of query i of a chunk alone: one sequence of T entries (codes, scales,
+    KI), per-layer chunk inputs q [L,Nq,16,512], qI [L,Nq,4,128], w [L,Nq,4], swa [L,W-1+Nq,512]
+    with its last swa_len rows valid; query i at position q_pos_i attends rows i .. i+W-1 of its
+    layer's window buffer, so it runs as a one-query chunk over those W rows (the valid ones among
+    them)."""
+    SW = swa.shape[1]
+    valid = int(min(W, max(0, W - max(0, SW - int(swa_len) - i))))
+    return orc.group_step(modes, [T], codes[None], scales[None], KI[None], q[:, i][:, None, None],
+                          qI[:, i][:, None, None], w[:, i][:, None, None], swa[:, i:i + W][:, None], [valid],
+                          Nq=1, K=K, W=W, ratio=ratio, q_pos=np.array([[q_pos_i]], np.int32), softmax_scale=SCALE)
+
+
 class GroupCase:
     """One CSA2 layer group: inputs on host (per sequence) and on the device.
 
@@ -188,6 +201,31 @@ class GroupCase:
         return orc.group_step(self.modes, Ts, codes, scales, KI, q, qI, w, swa, self.swa_len_np[seqs],
                               Nq=Nq, K=self.K, W=self.W, ratio=self.ratio, hierarchical=self.hierarchical,
                               keep=self.keep, q_pos=qp, softmax_scale=SCALE, threads=threads)
+
+    def check_queries(self, orc, b, queries):
+        """Compare single queries of sequence b with the oracle run on each alone (one_query_oracle).
+        Indices bit-exact, outputs and lse as in check()."""
+        L, Nq = self.L, self.Nq
+        Tb = self.T[b]
+        codes, scales = orc.fp4_quantize(self.h_kv(b)[:Tb])
+        KI = self.h_ki(b)[:Tb]
+        qs = np.stack([self.h_q(l, b) for l in range(L)])
+        qIs = np.stack([self.h_qI(l, b) for l in range(L)])
+        ws = np.stack([self.h_w(l, b) for l in range(L)])
+        swas = np.stack([self.h_swa(l, b) for l in range(L)])
+        qp_all = (np.asarray(self.q_pos, np.int32).reshape(self.B, Nq)[b] if self.q_pos is not None
+                  else self.ratio * Tb - Nq + np.arange(Nq, dtype=np.int32))
+        for i in queries:
+            ref = one_query_oracle(orc, self.modes, Tb, codes, scales, KI, qs, qIs, ws, swas,
+                                   int(self.swa_len_np[b]), i, int(qp_all[i]), K=self.K, W=self.W, ratio=self.ratio)
+            r = b * Nq + i
+            for l in range(L):
+                assert np.array_equal(self.idx[l][r].cpu().numpy(), ref["idx"][l, 0, 0]), f"query {i} layer {l}: indices"
+                assert_attn_close(bf16_host(self.out[l][b, i]), ref["out"][l, 0, 0], f"query {i} layer {l} out")
+                lse = self.lse[l][b, i].cpu().numpy()
+                fin = np.isfinite(ref["lse"][l, 0, 0])
+                assert np.array_equal(np.isfinite(lse), fin)
+                assert np.all(np.abs(lse[fin] - ref["lse"][l, 0, 0][fin]) <= 1e-2), f"query {i} layer {l} lse"
 
     def check(self, orc, seqs=None, threads=1):
         """Compare the device results of `seqs` with the oracle: bit-exact indices (and pools),

@@ -134,3 +134,22 @@ def test_prefill_select_full_chunk_2048x131072(orc):
     exp = _expected(orc, KI, qI, w, T, Nq, 2, None, k, [(0, 0), (0, 1023), (0, 2047)])
     for (b, i), e in exp.items():
         assert np.array_equal(got[i], e), f"row {i}"
+
+
+def test_prefill_group_full_size_1f5r_q2048_t131072(orc):
+    """The encoder prefill chunk through the group step: 1 Full + 5 Reuse layers, ratio 2, 2048
+    queries at the end of 262144 tokens (131072 compressed entries), Top-512, 128-token window.
+    Sampled queries (first, middle, last, and one whose Full-layer head weights are all negative)
+    against the oracle run on each query alone; every row of every layer well formed."""
+    Nq, T = 2048, 131072
+    q_pos = np.arange(2 * T - Nq, 2 * T, dtype=np.int32)[None]
+    gc = GroupCase(syn.SEEDS["prefill_group_1f5r_ratio2_q2048"], [T], [F, R, R, R, R, R], Nq=Nq, ratio=2,
+                   append=False, q_pos=q_pos)
+    gc.run()
+    idx = gc.idx[0].cpu().numpy()
+    assert np.all(np.diff(idx, axis=1) > 0) and idx.min() >= 0
+    assert np.all(idx.max(axis=1) < (q_pos[0] + 1) // 2)
+    neg = np.nonzero((gc.h_w(0, 0) < 0).all(axis=1))[0]
+    assert neg.size > 0
+    gc.check_queries(orc, 0, [0, 1023, 2047, int(neg[len(neg) // 2])])
+
