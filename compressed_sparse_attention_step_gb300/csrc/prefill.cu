@@ -28,6 +28,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -101,16 +102,17 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 // 16 accumulator columns of this warp's lane quarter into r, asynchronously: r is valid only after
-// tmem_wait(r), which names r so that no use of it moves above the wait.
+// a wait that names r (tmem_wait4), so that no use of it moves above the wait.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                : "r"(taddr)
                : "memory");
 }
-__device__ __forceinline__ void tmem_wait(uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_wait4(uint32_t (&a)[16], uint32_t (&b)[16], uint32_t (&c)[16],
+                                           uint32_t (&d)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]), "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3]), "+r"(c[4]), "+r"(c[5]), "+r"(c[6]), "+r"(c[7]), "+r"(c[8]), "+r"(c[9]), "+r"(c[10]), "+r"(c[11]), "+r"(c[12]), "+r"(c[13]), "+r"(c[14]), "+r"(c[15]), "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3]), "+r"(d[4]), "+r"(d[5]), "+r"(d[6]), "+r"(d[7]), "+r"(d[8]), "+r"(d[9]), "+r"(d[10]), "+r"(d[11]), "+r"(d[12]), "+r"(d[13]), "+r"(d[14]), "+r"(d[15])
                :
                : "memory");
 }
@@ -130,8 +132,8 @@ struct PfItems {
   int64_t n_items;
 };
 
-// Pass A (kMark = false): group maxima of the tensor-core scores.  Pass B (kMark = true): bitmap of
-// the keys with score >= thr[row].
+// Pass A (kMark = false): group maxima of the tensor-core scores (float bits).  Pass B (kMark =
+// true): bitmap of the keys with score >= thr[row].
 template <bool kMark>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_score_kernel(
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_score_kernel(
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ __align__(8) unsigned long long fullA[kStages], emptyA[kStages], fullB, emptyB, accF[2], accE[2];
   __shared__ uint32_t tmem_base;
-  __shared__ float4 s_w[kQPerTile];     // the current item's queries: head weights,
+  __shared__ float4 s_w[kQPerTile];     // the current item's queries: halved head weights,
   __shared__ int32_t s_vis[kQPerTile];  // visible entries (0 past the chunk's end),
   __shared__ float s_thr[kQPerTile];    // and pass-B thresholds
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -263,51 +265,68 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_score_kernel(
       if (et < kQPerTile) {
         const bool qv = et < qlim;
         const int64_t row = qv ? row0 + et : row0;
-        s_w[et] = qv ? __ldg(reinterpret_cast<const float4*>(w + row * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 wq = qv ? __ldg(reinterpret_cast<const float4*>(w + row * 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        s_w[et] = make_float4(0.5f * wq.x, 0.5f * wq.y, 0.5f * wq.z, 0.5f * wq.w);
         s_vis[et] = qv ? int32_t(pf_visible(row, Nq, lens, cap, ratio, q_pos)) : 0;
         s_thr[et] = (kMark && qv) ? __ldg(thr + row) : 0.0f;
       }
       asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiWarps * 32) : "memory");
+      int32_t vmin = 0x7FFFFFFF;  // the fewest entries any of the warp's 16 queries sees
+#pragma unroll
+      for (int qi = 0; qi < 16; ++qi) vmin = min(vmin, s_vis[16 * colq + qi]);
       for (int kt = kt0; kt < kt1; ++kt, ++tile) {
         const int a = int(tile & 1u);
         ok = ok && pf_wait(smem_u32(&accF[a]), (tile >> 1) & 1u);
         asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
         const int32_t key = kt * kKeyTile + 32 * quarter + lane;  // this lane's key
         const int64_t grp = (int64_t(kt) * kKeyTile + 32 * quarter) / kGroup;
-        uint32_t* outp = out + (row0 + 16 * colq) * n_groups + grp;
-        const bool grp_ok = lane == 0 && grp < n_groups;
-        // four chunks of 16 columns (4 queries), the next chunk's load in flight while one is used
+        // four chunks of 16 columns (4 queries each), loaded together; query qi's result (pass A: the
+        // group's largest score, pass B: its mask) ends in lane qi.  On a tile that every key of is
+        // visible to all 16 queries (all of them in the chunk) no per-query test remains.  The score
+        // is sum_h w_h relu(d_h), with w_h relu(d) computed as (w_h / 2) (d + |d|): the same product
+        // (halving and doubling are exact), on the FMA pipe rather than the ALU.
         const uint32_t tq = tmem + (uint32_t(32 * quarter) << 16) + uint32_t(256 * a + 64 * colq);
-        uint32_t da[16], db[16];
-        auto use = [&](const uint32_t (&d)[16], int c) {
+        uint32_t res = 0u;
+        auto tile_body = [&](auto full_c) {
+          constexpr bool kFull = decltype(full_c)::value;  // every key of the tile visible to all 16
+          uint32_t da[16], db[16], dc[16], dd[16];
+          auto use = [&](const uint32_t (&d)[16], int c) {
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const int qi = 4 * c + qq;     // query within the warp's 16
-            const int q = 16 * colq + qi;  // query within the item
-            const float4 wq = s_w[q];
-            const float s = fmaf(wq.w, fmaxf(__uint_as_float(d[4 * qq + 3]), 0.0f),
-                                 fmaf(wq.z, fmaxf(__uint_as_float(d[4 * qq + 2]), 0.0f),
-                                      fmaf(wq.y, fmaxf(__uint_as_float(d[4 * qq + 1]), 0.0f),
-                                           wq.x * fmaxf(__uint_as_float(d[4 * qq]), 0.0f))));
-            const bool v = key < s_vis[q];
-            uint32_t m;
-            if (kMark) m = __ballot_sync(0xffffffffu, v && s >= s_thr[q]);
-            else m = __reduce_max_sync(0xffffffffu, v ? score_key(s) : 0u);
-            if (grp_ok && q < qlim) outp[int64_t(qi) * n_groups] = m;
-          }
+            for (int qq = 0; qq < 4; ++qq) {
+              const int qi = 4 * c + qq;     // query within the warp's 16
+              const int q = 16 * colq + qi;  // query within the item
+              const float4 hw = s_w[q];
+              auto r2 = [&](int h) {  // 2 relu(d_h), exactly
+                const float x = __uint_as_float(d[4 * qq + h]);
+                return __fadd_rn(x, fabsf(x));
+              };
+              const float s = fmaf(hw.w, r2(3), fmaf(hw.z, r2(2), fmaf(hw.y, r2(1), hw.x * r2(0))));
+              const bool v = kFull || key < s_vis[q];
+              uint32_t m;
+              if (kMark) {
+                m = __ballot_sync(0xffffffffu, v && s >= s_thr[q]);
+              } else {
+                float mf;
+                asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mf) : "f"(v ? s : -INFINITY));
+                m = __float_as_uint(mf);
+              }
+              res = lane == qi ? m : res;
+            }
+          };
+          tmem_ld16(tq, da);
+          tmem_ld16(tq + 16u, db);
+          tmem_ld16(tq + 32u, dc);
+          tmem_ld16(tq + 48u, dd);
+          tmem_wait4(da, db, dc, dd);
+          use(da, 0);
+          use(db, 1);
+          use(dc, 2);
+          use(dd, 3);
         };
-        tmem_ld16(tq, da);
-        tmem_wait(da);
-        tmem_ld16(tq + 16u, db);
-        use(da, 0);
-        tmem_wait(db);
-        tmem_ld16(tq + 32u, da);
-        use(db, 1);
-        tmem_wait(da);
-        tmem_ld16(tq + 48u, db);
-        use(da, 2);
-        tmem_wait(db);
-        use(db, 3);
+        if ((kt + 1) * kKeyTile <= vmin) tile_body(std::true_type{});
+        else tile_body(std::false_type{});
+        if (lane < 16 && 16 * colq + lane < qlim && grp < n_groups)  // pass A: float bits of the maximum
+          out[(row0 + 16 * colq + lane) * n_groups + grp] = res;
         asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
         __syncwarp();
         if (lane == 0) bar_arrive(smem_u32(&accE[a]));
@@ -402,8 +421,8 @@ __global__ void __launch_bounds__(kThThreads) prefill_threshold_kernel(
     return;
   }
   uint32_t kmx = 0u;
-  for (int64_t i = t; i < ng; i += kThThreads) {
-    keys[i] = __ldg(gmax + row * n_groups + i);
+  for (int64_t i = t; i < ng; i += kThThreads) {  // group maxima: float bits -> score keys
+    keys[i] = score_key(__uint_as_float(__ldg(gmax + row * n_groups + i)));
     kmx = max(kmx, keys[i]);
   }
   kmx = __reduce_max_sync(0xffffffffu, kmx);
