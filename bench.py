@@ -233,9 +233,9 @@ def make_desc(c, wl, events=None, q=None, qI=None, w=None, kv_new=None, ki_new=N
 
 
 def launches_per_step(c):
-    ns = int(c.lib().csa2_attn_auto_split(B_PER_GPU, K_SEL, W_WIN))
-    # quantise-append + indexer-K append + score + select + per layer (attention [+ combine])
-    return 4 + N_LAYERS * (2 if ns > 1 else 1)
+    # quantise-append + indexer-K append + score + select + one attention launch for the four layers
+    # (they attend the same selected rows; split partials are merged inside that launch)
+    return 5
 
 
 def run_gpu(args, rank, world, local_rank):

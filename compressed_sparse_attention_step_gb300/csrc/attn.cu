@@ -235,12 +235,10 @@ __device__ __forceinline__ float reduce_scatter8(const float (&v)[8], int lane) 
 }
 
 __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
-    const uint16_t* __restrict__ q, int Nq, const uint8_t* __restrict__ codes,
+    const __grid_constant__ AttnLayers layers, int Nq, const uint8_t* __restrict__ codes,
     const uint8_t* __restrict__ scales, int64_t cap, const int32_t* __restrict__ idx,
-    const int32_t* __restrict__ n_valid, int k, const uint16_t* __restrict__ swa,
-    const int32_t* __restrict__ swa_len, int W, float scale_log2, uint16_t* __restrict__ out,
-    float* __restrict__ lse, int n_split, float* __restrict__ ws, unsigned int* __restrict__ tickets,
-    unsigned int* flags, int inputs_ready) {
+    const int32_t* __restrict__ n_valid, int k, const int32_t* __restrict__ swa_len, int W, float scale_log2,
+    int n_split, float* __restrict__ ws, unsigned int* __restrict__ tickets, unsigned int* flags, int inputs_ready) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // Inputs not yet known to be complete (the selected positions may come from the kernel right
   // before this one): wait first.  Otherwise (a layer that reuses earlier positions) wait only
@@ -256,7 +254,14 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   const uint32_t tile_s = base_s + kTileOff, q_s = base_s + kQOff, p_s = base_s + kPOff;
   const uint32_t mbar = smem_u32(&ms.mbar);
 
+  // blockIdx.z: the layer; blockIdx.y: the query (its selected rows are the same in every layer);
+  // ginst: the instance's slot in the split workspace and tickets
   const int inst = blockIdx.y, split = blockIdx.x;
+  const int64_t ginst = int64_t(blockIdx.z) * gridDim.y + inst;
+  const uint16_t* __restrict__ q = layers.q[blockIdx.z];
+  const uint16_t* __restrict__ swa = layers.swa[blockIdx.z];
+  uint16_t* __restrict__ out = layers.out[blockIdx.z];
+  float* __restrict__ lse = layers.lse[blockIdx.z];
   const int b = inst / Nq, qi = inst - b * Nq;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter; heads / channel blocks half
@@ -597,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
           orow[h * CSA2_D] = uint16_t(f2bf_bits(o[j][h] * (l > 0.0f ? 1.0f / l : 0.0f)));
         }
       } else {
-        float* po = ws + (int64_t(inst) * n_split + split) * (CSA2_H * CSA2_D) + ch;
+        float* po = ws + (ginst * n_split + split) * (CSA2_H * CSA2_D) + ch;
 #pragma unroll
         for (int h = 0; h < 16; ++h) po[h * CSA2_D] = o[j][h];
       }
@@ -628,16 +633,16 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     return;
   }
   // ---- split partials, then the last CTA of this query merges them ------------------------------
-  const int64_t instances = gridDim.y;
+  const int64_t instances = int64_t(gridDim.y) * gridDim.z;
   float* mlb = ws + instances * n_split * (CSA2_H * CSA2_D);
   if (t < CSA2_H) {
-    float* ml = mlb + (int64_t(inst) * n_split + split) * (2 * CSA2_H);
+    float* ml = mlb + (ginst * n_split + split) * (2 * CSA2_H);
     ml[2 * t] = ms.m_run[t];
     ml[2 * t + 1] = ms.l_run[t];
   }
   __threadfence();
   __syncthreads();
-  if (t == 0) ms.is_last = (atomicAdd(tickets + inst, 1u) == unsigned(n_split - 1));
+  if (t == 0) ms.is_last = (atomicAdd(tickets + ginst, 1u) == unsigned(n_split - 1));
   __syncthreads();
   if (!ms.is_last) return;
   __threadfence();
@@ -648,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   // i.e. head (t >> 7) + 2 v, channels 4 (t & 127) .. + 3.
   float* wgt = reinterpret_cast<float*>(base + kTileOff);
   {
-    const float* ml = mlb + int64_t(inst) * n_split * (2 * CSA2_H);
+    const float* ml = mlb + ginst * n_split * (2 * CSA2_H);
     for (int e = t; e < n_split * CSA2_H; e += kThreads) {
       wgt[e] = __ldcg(ml + 2 * e);                            // m_j, e = j * 16 + h
       wgt[kMaxSplit * CSA2_H + e] = __ldcg(ml + 2 * e + 1);   // l_j
@@ -671,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     __syncthreads();
   }
   {
-    const float4* p0 = reinterpret_cast<const float4*>(ws + int64_t(inst) * n_split * (CSA2_H * CSA2_D)) + t;
+    const float4* p0 = reinterpret_cast<const float4*>(ws + ginst * n_split * (CSA2_H * CSA2_D)) + t;
     float4 acc[8];
 #pragma unroll
     for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -712,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     }
     if (lse && t < CSA2_H) lse[int64_t(inst) * CSA2_H + t] = wgt[2 * kMaxSplit * CSA2_H + CSA2_H + t];
   }
-  if (t == 0) tickets[inst] = 0u;  // ready for the next launch
+  if (t == 0) tickets[ginst] = 0u;  // ready for the next launch
 }
 
 int attn_tiles(int k, int W) { return (k + kRows - 1) / kRows + (W > 0 ? (W + kRows - 1) / kRows : 0); }
@@ -742,15 +747,15 @@ int attn_auto_split(int64_t instances, int k, int W) {
   return int(std::max<int64_t>(s, 1));
 }
 
-cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
-                               const uint8_t* scales, int64_t cap, const int32_t* idx,
-                               const int32_t* n_valid, int k, const uint16_t* swa,
-                               const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
-                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed,
-                               bool inputs_ready) {
-  const int64_t instances = int64_t(B) * Nq;
+cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, int B, int Nq, const uint8_t* codes,
+                                      const uint8_t* scales, int64_t cap, const int32_t* idx,
+                                      const int32_t* n_valid, int k, const int32_t* swa_len, int W,
+                                      float softmax_scale, int n_split, float* ws, cudaStream_t st,
+                                      bool tickets_zeroed, bool inputs_ready) {
+  const int64_t per_layer = int64_t(B) * Nq, instances = per_layer * n_layers;
   if (instances == 0) return cudaSuccess;
-  if (!swa) W = 0;
+  if (n_layers < 1 || n_layers > CSA2_MAX_LAYERS || per_layer > 65535) return cudaErrorInvalidValue;
+  if (!layers.swa[0]) W = 0;
   n_split = attn_effective_split(k, W, n_split);
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
@@ -774,9 +779,24 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
       if (e != cudaSuccess) return e;
     }
   }
-  const dim3 grid{unsigned(n_split), unsigned(instances), 1u};
-  return launch_pdl(sparse_attn_kernel, grid, dim3(kThreads), kSmemBytes, st, q, Nq, codes, scales, cap, idx, n_valid, k,
-                    swa, swa_len, W, scale_log2, out, lse, n_split, partials, tickets, flags, int(inputs_ready));
+  const dim3 grid{unsigned(n_split), unsigned(per_layer), unsigned(n_layers)};
+  return launch_pdl(sparse_attn_kernel, grid, dim3(kThreads), kSmemBytes, st, layers, Nq, codes, scales, cap, idx,
+                    n_valid, k, swa_len, W, scale_log2, n_split, partials, tickets, flags, int(inputs_ready));
+}
+
+cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
+                               const uint8_t* scales, int64_t cap, const int32_t* idx,
+                               const int32_t* n_valid, int k, const uint16_t* swa,
+                               const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
+                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed,
+                               bool inputs_ready) {
+  AttnLayers layers{};
+  layers.q[0] = q;
+  layers.swa[0] = swa;
+  layers.out[0] = out;
+  layers.lse[0] = lse;
+  return launch_sparse_attn_layers(layers, 1, B, Nq, codes, scales, cap, idx, n_valid, k, swa_len, W, softmax_scale,
+                                   n_split, ws, st, tickets_zeroed, inputs_ready);
 }
 
 }  // namespace csa2

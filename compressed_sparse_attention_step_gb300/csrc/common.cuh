@@ -209,6 +209,21 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
 // topk_ws_bytes); a launch leaves them zero.
 size_t topk_counters_offset(int rows);
 size_t attn_ticket_bytes(int64_t instances);
+// Per-layer operands of one attention launch over layers that attend the same selected rows (a
+// Full or Reindex layer and the Reuse layers after it): query, window buffer, output, lse.
+struct AttnLayers {
+  const uint16_t* q[CSA2_MAX_LAYERS];
+  const uint16_t* swa[CSA2_MAX_LAYERS];
+  uint16_t* out[CSA2_MAX_LAYERS];
+  float* lse[CSA2_MAX_LAYERS];
+};
+// n_layers layers of B*Nq queries each in one launch; the split workspace holds
+// n_layers * B * Nq instances (attn_ws_bytes), tickets first.
+cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, int B, int Nq, const uint8_t* codes,
+                                      const uint8_t* scales, int64_t cap, const int32_t* idx,
+                                      const int32_t* n_valid, int k, const int32_t* swa_len, int W,
+                                      float softmax_scale, int n_split, float* ws, cudaStream_t st,
+                                      bool tickets_zeroed, bool inputs_ready);
 cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
                                const uint8_t* scales, int64_t cap, const int32_t* idx,
                                const int32_t* n_valid, int k, const uint16_t* swa,

@@ -62,6 +62,20 @@ inline bool prefill_path(int B, int Nq, int hierarchical, int64_t cap) {
          (cap + 31) / 32 <= prefill_max_groups();
 }
 
+// Attention workspace of a group step: tickets for rows * ns instances, then the split partials of
+// rows * ns instance-splits, ns being the split of one layer's rows.  A launch over several layers
+// that share their selected rows takes a split that fits (attn_ws_bytes(instances, split) within
+// these bytes); with a split above 1 its instances are at most rows * ns / 2, so its tickets fit.
+size_t group_attn_ws_bytes(int64_t rows, int K, int W, int n_split) {
+  const int ns = attn_effective_split(K, W, n_split ? n_split : attn_auto_split(rows, K, W));
+  if (ns <= 1) return attn_ticket_bytes(rows);
+  return attn_ticket_bytes(rows * ns) + (attn_ws_bytes(rows, ns) - attn_ticket_bytes(rows));
+}
+size_t group_attn_ticket_bytes(int64_t rows, int K, int W, int n_split) {
+  const int ns = attn_effective_split(K, W, n_split ? n_split : attn_auto_split(rows, K, W));
+  return attn_ticket_bytes(rows * std::max(ns, 1));
+}
+
 struct GroupWs {
   size_t scores_off, nv_off, topk_off, attn_off, pf_off, total;
   int64_t score_ld;
@@ -78,8 +92,7 @@ GroupWs group_ws_layout(int B, int Nq, int64_t cap, int K, int W, int hierarchic
   L.nv_off = align256(size_t(rows) * size_t(ld) * sizeof(float));
   L.topk_off = L.nv_off + align256(size_t(rows) * sizeof(int32_t));
   L.attn_off = L.topk_off + align256(topk_ws_bytes(int(rows), ld));
-  const int ns = attn_effective_split(K, W, n_split ? n_split : attn_auto_split(rows, K, W));
-  L.pf_off = L.attn_off + align256(attn_ws_bytes(rows, ns));
+  L.pf_off = L.attn_off + align256(group_attn_ws_bytes(rows, K, W, n_split));
   L.total = L.pf_off + (pf ? align256(prefill_ws_bytes(rows, cap, B)) : 0);
   return L;
 }
@@ -233,8 +246,6 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   float* attn_ws = reinterpret_cast<float*>(wsb + lay.attn_off);
   void* pf_ws = wsb + lay.pf_off;
   const bool pf = csa2::prefill_path(g->B, g->Nq, g->hierarchical, g->cap);
-  const int ns_all =
-      csa2::attn_effective_split(g->K, g->W, g->n_split ? g->n_split : csa2::attn_auto_split(rows, g->K, g->W));
   const int64_t nb = g->cap / CSA2_BLOCK;
   const int64_t pool_w = int64_t(g->n_blocks_keep) * CSA2_BLOCK;
   const int64_t sld = lay.score_ld;
@@ -276,11 +287,11 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   const bool zeroed = n_chunks == 1;
   if (zeroed) {
     const size_t lo = lay.topk_off + csa2::topk_counters_offset(int(rows));
-    const size_t hi = lay.attn_off + csa2::attn_ticket_bytes(rows);
+    const size_t hi = lay.attn_off + csa2::group_attn_ticket_bytes(rows, K, g->W, g->n_split);
     if (csa2::topk_ws_bytes(int(rows), lay.score_ld) > 0 && !ok(cudaMemsetAsync(wsb + lo, 0, hi - lo, st)))
       return CSA2_ERR_CUDA;
     if (csa2::topk_ws_bytes(int(rows), lay.score_ld) == 0 &&
-        !ok(cudaMemsetAsync(wsb + lay.attn_off, 0, csa2::attn_ticket_bytes(rows), st)))
+        !ok(cudaMemsetAsync(wsb + lay.attn_off, 0, csa2::group_attn_ticket_bytes(rows, K, g->W, g->n_split), st)))
       return CSA2_ERR_CUDA;
   }
   if (!rec(g->ev_score_begin, st)) return CSA2_ERR_CUDA;
@@ -304,10 +315,26 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
     auto qI_of = [&](int l) { return g->qI[l] + r0 * (CSA2_HI * CSA2_DI); };
     auto w_of = [&](int l) { return g->w[l] + r0 * CSA2_HI; };
     auto idx_of = [&](int l) { return g->idx[l] + r0 * K; };
-    // attention split of a chunk: at most 4 when chunks overlap, and within the sized workspace
-    int ns = csa2::attn_effective_split(
-        K, g->W, g->n_split ? g->n_split : std::min(csa2::attn_auto_split(rc, K, g->W), n_chunks > 1 ? 4 : 32));
-    while (ns > 1 && csa2::attn_ws_bytes(rc, ns) > csa2::attn_ws_bytes(rows, ns_all)) --ns;
+    // One attention launch per run of layers that attend the same selected rows (a Full or Reindex
+    // layer and the Reuse layers after it), issued before the next layer's selection.  Its split:
+    // the forced one, else the automatic one for all the run's queries (at most 4 when chunks
+    // overlap), within the sized workspace.
+    const size_t attn_cap = csa2::group_attn_ws_bytes(rows, K, g->W, g->n_split);
+    csa2::AttnLayers run{};
+    int run_n = 0;
+    const int32_t* run_idx = nullptr;
+    auto flush_run = [&]() -> bool {
+      if (run_n == 0) return true;
+      const int64_t inst = int64_t(run_n) * rc;
+      int ns = csa2::attn_effective_split(
+          K, g->W, g->n_split ? g->n_split : std::min(csa2::attn_auto_split(inst, K, g->W), n_chunks > 1 ? 4 : 32));
+      while (ns > 1 && csa2::attn_ws_bytes(inst, ns) > attn_cap) --ns;
+      const bool r = ok(csa2::launch_sparse_attn_layers(run, run_n, Bc, Nq, codes, scl, g->cap, run_idx, nullptr, K,
+                                                         swl, g->W, g->softmax_scale, ns, attn_ws, aux, zeroed,
+                                                         false));
+      run_n = 0;
+      return r;
+    };
 
     // stage 1 (stream): the first scan over this chunk's keys (layer 0 is Full or Reindex); prefill
     // chunks select on the tensor cores in stage 2 instead
@@ -331,6 +358,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
     for (int l = 0; l < L; ++l) {
       const int mode = g->modes[l];
       if (mode != CSA2_MODE_REUSE) {
+        if (!flush_run()) return CSA2_ERR_CUDA;
         if (g->hierarchical) {
           if (mode == CSA2_MODE_FULL) {
             if (nb > 0 && l != 0 &&
@@ -369,13 +397,14 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
         if (!ok(cudaMemcpyAsync(idx_of(l), latest, size_t(rc) * K * sizeof(int32_t), cudaMemcpyDeviceToDevice, aux)))
           return CSA2_ERR_CUDA;
       }
-      const uint16_t* swa = g->W > 0 ? g->swa[l] + int64_t(b0) * SW * CSA2_D : nullptr;
-      if (!ok(csa2::launch_sparse_attn(g->q[l] + r0 * (CSA2_H * CSA2_D), Bc, Nq, codes, scl, g->cap, latest, nullptr,
-                                       K, swa, swl, g->W, g->softmax_scale, g->out[l] + r0 * (CSA2_H * CSA2_D),
-                                       g->lse[l] ? g->lse[l] + r0 * CSA2_H : nullptr, ns, attn_ws, aux, zeroed,
-                                       mode == CSA2_MODE_REUSE)))
-        return CSA2_ERR_CUDA;
+      run.q[run_n] = g->q[l] + r0 * (CSA2_H * CSA2_D);
+      run.swa[run_n] = g->W > 0 ? g->swa[l] + int64_t(b0) * SW * CSA2_D : nullptr;
+      run.out[run_n] = g->out[l] + r0 * (CSA2_H * CSA2_D);
+      run.lse[run_n] = g->lse[l] ? g->lse[l] + r0 * CSA2_H : nullptr;
+      run_idx = latest;
+      ++run_n;
     }
+    if (!flush_run()) return CSA2_ERR_CUDA;
   }
   if (ds && (!ok(cudaEventRecord(ds->join, aux)) || !ok(cudaStreamWaitEvent(st, ds->join, 0))))
     return CSA2_ERR_CUDA;
