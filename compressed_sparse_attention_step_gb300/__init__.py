@@ -21,6 +21,7 @@ MAX_LAYERS = 16
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 OP_TOPK, OP_BLOCK_POOL, OP_SPARSE_ATTN, OP_GROUP_STEP, OP_INDEX_SELECT_PREFILL = 1, 2, 3, 4, 5
 FLAG_APPEND_OOB, FLAG_INDEX_OOB, FLAG_TIMEOUT = 1, 2, 4
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TOO_LARGE = 0, 1, 2, 3, 4, 5
 
 LIB_PATH = _build.LIB
 
@@ -81,6 +82,7 @@ def lib():
             "csa2_sparse_attn_decode": [P, I32, I32, P, P, I64, P, P, I32, P, P, I32, F32, P, P, I32, P,
                                         SZ, P],
             "csa2_group_step": [ctypes.POINTER(GroupDesc), P, SZ, P],
+            "csa2_stack_step": [ctypes.POINTER(GroupDesc), I32, P, SZ, P],
             "csa2_workspace_size": [I32, ctypes.POINTER(Dims)],
             "csa2_attn_auto_split": [I64, I32, I32],
             "csa2_status_string": [I32],
@@ -339,6 +341,13 @@ def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa
 def csa2_group_step(desc, ws, stream=None):
     _check("csa2_group_step", lib().csa2_group_step(ctypes.byref(desc), _ptr(ws, "ws"), _nbytes(ws),
                                                     _stream(stream)))
+
+
+def csa2_stack_step(descs, ws, stream=None):
+    """The groups of a decoder stack in order (csa2_stack_step): descs is a list of group
+    descriptors sharing one batch and cache; ws is sized for the largest group."""
+    arr = (GroupDesc * len(descs))(*descs)
+    _check("csa2_stack_step", lib().csa2_stack_step(arr, len(descs), _ptr(ws, "ws"), _nbytes(ws), _stream(stream)))
 
 
 def csa2_device_flags(clear=True, stream=None):

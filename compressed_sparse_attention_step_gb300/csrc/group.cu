@@ -198,8 +198,11 @@ extern "C" csa2_status csa2_block_pool(const uint16_t* qI, const float* w, int B
 
 extern "C" size_t csa2_group_desc_size(void) { return sizeof(csa2_group_desc); }
 
-extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_t ws_bytes,
-                                       csa2_stream_t stream) {
+namespace {
+// The argument checks of a group step, made before anything is launched.  *empty: the step has no
+// queries (nothing to launch; the remaining checks are skipped).
+csa2_status group_check(const csa2_group_desc* g, const void* ws, size_t ws_bytes, bool* empty) {
+  *empty = false;
   if (!g) return CSA2_ERR_INVALID_ARG;
   const int L = g->n_layers;
   if (L < 1 || L > CSA2_MAX_LAYERS) return CSA2_ERR_INVALID_ARG;
@@ -208,7 +211,10 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   if (g->n_split < 0 || g->n_split > 32 || g->n_new < 0) return CSA2_ERR_INVALID_ARG;
   if (g->hierarchical && (g->n_blocks_keep < 1 || g->n_blocks_keep > CSA2_MAX_K)) return CSA2_ERR_INVALID_ARG;
   const int64_t rows = int64_t(g->B) * g->Nq;
-  if (rows == 0) return CSA2_OK;
+  if (rows == 0) {
+    *empty = true;
+    return CSA2_OK;
+  }
   if (rows > 65535) return CSA2_ERR_UNSUPPORTED;
   if (g->modes[0] != CSA2_MODE_FULL && g->modes[0] != CSA2_MODE_REINDEX) return CSA2_ERR_INVALID_ARG;
   if (!g->lens || !g->codes || !g->scales || !g->KI || !al16(g->codes) || !al16(g->scales) || !al16(g->KI))
@@ -237,6 +243,19 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   const csa2::GroupWs lay = csa2::group_ws_layout(g->B, g->Nq, g->cap, g->K, g->W, g->hierarchical,
                                                   g->n_blocks_keep, g->n_split);
   if (!ws || ws_bytes < lay.total || !al16(ws)) return CSA2_ERR_WORKSPACE;
+  return CSA2_OK;
+}
+}  // namespace
+
+extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_t ws_bytes,
+                                       csa2_stream_t stream) {
+  bool empty = false;
+  const csa2_status chk = group_check(g, ws, ws_bytes, &empty);
+  if (chk != CSA2_OK || empty) return chk;
+  const int L = g->n_layers;
+  const int64_t rows = int64_t(g->B) * g->Nq;
+  const csa2::GroupWs lay = csa2::group_ws_layout(g->B, g->Nq, g->cap, g->K, g->W, g->hierarchical,
+                                                  g->n_blocks_keep, g->n_split);
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* wsb = static_cast<char*>(ws);
@@ -408,5 +427,33 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   }
   if (ds && (!ok(cudaEventRecord(ds->join, aux)) || !ok(cudaStreamWaitEvent(st, ds->join, 0))))
     return CSA2_ERR_CUDA;
+  return CSA2_OK;
+}
+
+// A decoder stack's step: its layer groups in order over one cache.  Every group is checked before
+// anything is launched.
+extern "C" csa2_status csa2_stack_step(const csa2_group_desc* groups, int n_groups, void* ws, size_t ws_bytes,
+                                       csa2_stream_t stream) {
+  if (!groups || n_groups < 1) return CSA2_ERR_INVALID_ARG;
+  const csa2_group_desc& g0 = groups[0];
+  for (int i = 0; i < n_groups; ++i) {
+    const csa2_group_desc* g = groups + i;
+    bool empty = false;
+    const csa2_status chk = group_check(g, ws, ws_bytes, &empty);
+    if (chk != CSA2_OK) return chk;
+    if (i == 0) continue;
+    // one batch, one cache, one append (by the first group), one pool
+    if (g->B != g0.B || g->Nq != g0.Nq || g->cap != g0.cap || g->lens != g0.lens || g->q_pos != g0.q_pos ||
+        g->ratio != g0.ratio || g->codes != g0.codes || g->scales != g0.scales || g->KI != g0.KI ||
+        g->hierarchical != g0.hierarchical)
+      return CSA2_ERR_INVALID_ARG;
+    if (g->n_new > 0 && (g->kv_new || g->ki_new)) return CSA2_ERR_INVALID_ARG;
+    if (g->hierarchical && (g->block_keys != g0.block_keys || g->pool != g0.pool || g->pool_len != g0.pool_len))
+      return CSA2_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n_groups; ++i) {
+    const csa2_status st = csa2_group_step(groups + i, ws, ws_bytes, stream);
+    if (st != CSA2_OK) return st;
+  }
   return CSA2_OK;
 }

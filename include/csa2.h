@@ -299,6 +299,20 @@ typedef struct csa2_group_desc {
 csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_t ws_bytes,
                             csa2_stream_t stream);
 
+/*
+ * One token's pass through a decoder stack of layer groups (ai-maestro "Compressed Sparse
+ * Attention 2": Reindex layers "reuse the most recent Full layer's KV and indexer keys"; the
+ * 20-layer decoder as 5 groups of 4, the first led by a Full layer, the rest by Reindex layers).
+ * groups[0 .. n_groups-1] run in order, each exactly as csa2_group_step, on one workspace (the
+ * largest group's csa2_workspace_size).  All groups share B, Nq, cap, lens, q_pos, ratio, the
+ * cache (codes, scales, KI) and, when hierarchical, block_keys and the pool buffers (a Reindex-led
+ * group rescores the pool kept by the latest Full layer of an earlier group).  Only groups[0] may
+ * append (kv_new / ki_new).  Every group is checked before anything is launched: a mismatch, or
+ * any check of csa2_group_step failing, returns its status with nothing enqueued.
+ */
+csa2_status csa2_stack_step(const csa2_group_desc* groups, int n_groups, void* ws, size_t ws_bytes,
+                            csa2_stream_t stream);
+
 /* Workspace sizing. */
 #define CSA2_OP_TOPK 1
 #define CSA2_OP_BLOCK_POOL 2

@@ -68,7 +68,10 @@ class GroupCase:
     """
 
     def __init__(self, seed, T, modes, *, Nq=1, K=512, W=128, ratio=1, hierarchical=False, keep=2048,
-                 cap=None, append=True, host_seqs=None, q_pos=None):
+                 cap=None, append=True, host_seqs=None, q_pos=None, share=None, layer0=0):
+        """share: a case whose cache, lengths, block keys and pool this one uses (a later group of
+        a decoder stack: no append of its own); layer0: the stack index of this group's first
+        layer (its per-layer draws use tensor ids offset by it)."""
         import torch
         import compressed_sparse_attention_step_gb300 as c
         self.c = c
@@ -77,7 +80,8 @@ class GroupCase:
         self.Nq, self.K, self.W, self.ratio = Nq, K, W, ratio
         self.hierarchical, self.keep = hierarchical, keep
         self.cap = cap if cap is not None else max(T)
-        self.append = append and Nq == 1
+        self.append = append and Nq == 1 and share is None
+        self.layer0 = layer0
         self.host_seqs = list(range(self.B)) if host_seqs is None else list(host_seqs)
         self.q_pos = q_pos
         B, L, cap, SW = self.B, self.L, self.cap, W - 1 + Nq
@@ -96,10 +100,11 @@ class GroupCase:
             self.w = [to_dev(np.stack([self.h_w(l, b) for b in range(B)])) for l in range(L)]
             self.swa = [bf16_dev(np.stack([self.h_swa(l, b) for b in range(B)])) for l in range(L)]
         else:
-            self.q = [syn.device_normal_bf16((B, Nq, H, D), seed, syn.T_Q + l) for l in range(L)]
-            self.qI = [syn.device_normal_bf16((B, Nq, HI, DI), seed, syn.T_QI + l) for l in range(L)]
-            self.w = [syn.device_normal_bf16((B, Nq, HI), seed, syn.T_W + l).float() for l in range(L)]
-            self.swa = [syn.device_normal_bf16((B, SW, D), seed, syn.T_SWA + l) for l in range(L)]
+            l0 = layer0
+            self.q = [syn.device_normal_bf16((B, Nq, H, D), seed, syn.T_Q + l0 + l) for l in range(L)]
+            self.qI = [syn.device_normal_bf16((B, Nq, HI, DI), seed, syn.T_QI + l0 + l) for l in range(L)]
+            self.w = [syn.device_normal_bf16((B, Nq, HI), seed, syn.T_W + l0 + l).float() for l in range(L)]
+            self.swa = [syn.device_normal_bf16((B, SW, D), seed, syn.T_SWA + l0 + l) for l in range(L)]
             for b in self.host_seqs:
                 for l in range(L):
                     self.q[l][b].copy_(bf16_dev(self.h_q(l, b)))
@@ -109,7 +114,11 @@ class GroupCase:
         # cache rows (kept before the step; the last row comes from the step's append)
         self.kv_new = torch.zeros((B, 1, D), dtype=torch.bfloat16, device=dev)
         self.ki_new = torch.zeros((B, 1, DI), dtype=torch.bfloat16, device=dev)
-        for b in range(B):
+        if share is not None:
+            self.codes, self.scales, self.KI, self.lens = share.codes, share.scales, share.KI, share.lens
+            self.__dict__["_kv"] = share.__dict__.setdefault("_kv", {})
+            self.__dict__["_ki"] = share.__dict__.setdefault("_ki", {})
+        for b in (range(B) if share is None else ()):
             Tb = self.T[b]
             pre = Tb - 1 if self.append else Tb
             if b in self.host_seqs:
@@ -131,7 +140,9 @@ class GroupCase:
                 self.scales[b, self.T[b] - 1].fill_(0x7E)
                 self.KI[b, self.T[b] - 1].fill_(7.0)
         self.block_keys = None
-        if hierarchical:
+        if share is not None and hierarchical:
+            self.block_keys, self.pool, self.pool_len = share.block_keys, share.pool, share.pool_len
+        elif hierarchical:
             self.block_keys = torch.zeros((B, cap // 8, DI), dtype=torch.bfloat16, device=dev)
             pre_lens = self.lens - (1 if self.append else 0)
             c.csa2_block_keys_build(self.KI, pre_lens.contiguous(), self.block_keys)
@@ -159,10 +170,11 @@ class GroupCase:
             cache[b] = syn.normal_bf16(self.seed, syn.T_KI, b, (self.cap, DI))
         return cache[b]
 
-    def h_q(self, l, b): return syn.normal_bf16(self.seed, syn.T_Q + l, b, (self.Nq, H, D))
-    def h_qI(self, l, b): return syn.normal_bf16(self.seed, syn.T_QI + l, b, (self.Nq, HI, DI))
-    def h_w(self, l, b): return syn.normal_f32(self.seed, syn.T_W + l, b, (self.Nq, HI))
-    def h_swa(self, l, b): return syn.normal_bf16(self.seed, syn.T_SWA + l, b, (self.W - 1 + self.Nq, D))
+    def h_q(self, l, b): return syn.normal_bf16(self.seed, syn.T_Q + self.layer0 + l, b, (self.Nq, H, D))
+    def h_qI(self, l, b): return syn.normal_bf16(self.seed, syn.T_QI + self.layer0 + l, b, (self.Nq, HI, DI))
+    def h_w(self, l, b): return syn.normal_f32(self.seed, syn.T_W + self.layer0 + l, b, (self.Nq, HI))
+    def h_swa(self, l, b):
+        return syn.normal_bf16(self.seed, syn.T_SWA + self.layer0 + l, b, (self.W - 1 + self.Nq, D))
 
     def desc(self, events=None, n_split=0, seq_chunks=0):
         c = self.c
@@ -182,25 +194,7 @@ class GroupCase:
 
     def oracle(self, orc, seqs=None, threads=1):
         """Oracle of the sequences `seqs` (host draws only)."""
-        seqs = self.host_seqs if seqs is None else seqs
-        L, Nq = self.L, self.Nq
-        Ts = [self.T[b] for b in seqs]
-        cap = max(Ts)
-        codes = np.zeros((len(seqs), cap, 256), np.uint8)
-        scales = np.zeros((len(seqs), cap, 32), np.uint8)
-        KI = np.zeros((len(seqs), cap, DI), np.uint16)
-        for i, b in enumerate(seqs):
-            kv = self.h_kv(b)[:self.T[b]]
-            codes[i, :self.T[b]], scales[i, :self.T[b]] = orc.fp4_quantize(kv)
-            KI[i, :self.T[b]] = self.h_ki(b)[:self.T[b]]
-        q = np.stack([np.stack([self.h_q(l, b) for b in seqs]) for l in range(L)])
-        qI = np.stack([np.stack([self.h_qI(l, b) for b in seqs]) for l in range(L)])
-        w = np.stack([np.stack([self.h_w(l, b) for b in seqs]) for l in range(L)])
-        swa = np.stack([np.stack([self.h_swa(l, b) for b in seqs]) for l in range(L)])
-        qp = None if self.q_pos is None else np.asarray(self.q_pos, np.int32).reshape(self.B, Nq)[seqs]
-        return orc.group_step(self.modes, Ts, codes, scales, KI, q, qI, w, swa, self.swa_len_np[seqs],
-                              Nq=Nq, K=self.K, W=self.W, ratio=self.ratio, hierarchical=self.hierarchical,
-                              keep=self.keep, q_pos=qp, softmax_scale=SCALE, threads=threads)
+        return stack_oracle(orc, [self], seqs, threads)
 
     def check_queries(self, orc, b, queries):
         """Compare single queries of sequence b with the oracle run on each alone (one_query_oracle).
@@ -230,24 +224,61 @@ class GroupCase:
     def check(self, orc, seqs=None, threads=1):
         """Compare the device results of `seqs` with the oracle: bit-exact indices (and pools),
         attention outputs within the tolerance, lse within 1e-2 absolute."""
-        seqs = self.host_seqs if seqs is None else seqs
-        ref = self.oracle(orc, seqs, threads)
-        Nq = self.Nq
-        rows = np.concatenate([np.arange(b * Nq, (b + 1) * Nq) for b in seqs])
-        for l in range(self.L):
-            gi = self.idx[l].cpu().numpy()[rows].reshape(len(seqs), Nq, self.K)
-            assert np.array_equal(gi, ref["idx"][l]), f"layer {l}: indices differ"
-            out = bf16_host(self.out[l])[seqs]
-            assert_attn_close(out, ref["out"][l], f"layer {l} out")
-            lse = self.lse[l].cpu().numpy()[seqs]
-            fin = np.isfinite(ref["lse"][l])
-            assert np.array_equal(np.isfinite(lse), fin)
-            assert np.all(np.abs(lse[fin] - ref["lse"][l][fin]) <= 1e-2), f"layer {l} lse"
-        if self.hierarchical:
-            gp = self.pool.cpu().numpy()[rows]
-            gl = self.pool_len.cpu().numpy()[rows]
-            assert np.array_equal(gl, ref["pool_len"].reshape(-1))
-            for i in range(len(rows)):
-                n = gl[i]
-                assert np.array_equal(gp[i, :n], ref["pool"].reshape(len(rows), -1)[i, :n])
-        return ref
+        return check_stack(orc, [self], seqs, threads)
+
+
+def stack_oracle(orc, groups, seqs=None, threads=1):
+    """The oracle of the groups of a decoder stack, run in order on the first group's cache: one
+    group step over all their layers (a Reindex layer rescores the latest Full layer's pool)."""
+    g0 = groups[0]
+    seqs = g0.host_seqs if seqs is None else seqs
+    Nq = g0.Nq
+    Ts = [g0.T[b] for b in seqs]
+    cap = max(Ts)
+    codes = np.zeros((len(seqs), cap, 256), np.uint8)
+    scales = np.zeros((len(seqs), cap, 32), np.uint8)
+    KI = np.zeros((len(seqs), cap, DI), np.uint16)
+    for i, b in enumerate(seqs):
+        kv = g0.h_kv(b)[:g0.T[b]]
+        codes[i, :g0.T[b]], scales[i, :g0.T[b]] = orc.fp4_quantize(kv)
+        KI[i, :g0.T[b]] = g0.h_ki(b)[:g0.T[b]]
+    layers = [(g, l) for g in groups for l in range(g.L)]
+    modes = [g.modes[l] for g, l in layers]
+    q = np.stack([np.stack([g.h_q(l, b) for b in seqs]) for g, l in layers])
+    qI = np.stack([np.stack([g.h_qI(l, b) for b in seqs]) for g, l in layers])
+    w = np.stack([np.stack([g.h_w(l, b) for b in seqs]) for g, l in layers])
+    swa = np.stack([np.stack([g.h_swa(l, b) for b in seqs]) for g, l in layers])
+    qp = None if g0.q_pos is None else np.asarray(g0.q_pos, np.int32).reshape(g0.B, Nq)[seqs]
+    return orc.group_step(modes, Ts, codes, scales, KI, q, qI, w, swa, g0.swa_len_np[seqs],
+                          Nq=Nq, K=g0.K, W=g0.W, ratio=g0.ratio, hierarchical=g0.hierarchical,
+                          keep=g0.keep, q_pos=qp, softmax_scale=SCALE, threads=threads)
+
+
+def check_stack(orc, groups, seqs=None, threads=1):
+    """Compare the device results of the groups of a stack (run in order) for the sequences `seqs`
+    with stack_oracle: bit-exact indices (and pools), attention outputs within the tolerance, lse
+    within 1e-2 absolute."""
+    g0 = groups[0]
+    seqs = g0.host_seqs if seqs is None else seqs
+    ref = stack_oracle(orc, groups, seqs, threads)
+    Nq = g0.Nq
+    rows = np.concatenate([np.arange(b * Nq, (b + 1) * Nq) for b in seqs])
+    layers = [(g, l) for g in groups for l in range(g.L)]
+    for j, (g, l) in enumerate(layers):
+        gi = g.idx[l].cpu().numpy()[rows].reshape(len(seqs), Nq, g.K)
+        assert np.array_equal(gi, ref["idx"][j]), f"layer {j}: indices differ"
+        out = bf16_host(g.out[l])[seqs]
+        assert_attn_close(out, ref["out"][j], f"layer {j} out")
+        lse = g.lse[l].cpu().numpy()[seqs]
+        fin = np.isfinite(ref["lse"][j])
+        assert np.array_equal(np.isfinite(lse), fin)
+        assert np.all(np.abs(lse[fin] - ref["lse"][j][fin]) <= 1e-2), f"layer {j} lse"
+    if g0.hierarchical:
+        gp = g0.pool.cpu().numpy()[rows]
+        gl = g0.pool_len.cpu().numpy()[rows]
+        assert np.array_equal(gl, ref["pool_len"].reshape(-1))
+        for i in range(len(rows)):
+            n = gl[i]
+            assert np.array_equal(gp[i, :n], ref["pool"].reshape(len(rows), -1)[i, :n])
+    return ref
+
