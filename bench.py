@@ -386,6 +386,127 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------------------------
+# other workloads (`--workload`): the 20-layer decoder stack and the encoder prefill chunk
+# ----------------------------------------------------------------------------------------------
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def time_steps(torch, fn, K, Wm):
+    for _ in range(Wm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / K
+
+
+def run_stack20(args):
+    """One token through the 20-layer decoder: 5 groups of 4 (Full + 3 Reuse, then 4 x Reindex +
+    3 Reuse) over one cache, B = 64, T = 131072; one csa2_stack_step per step."""
+    import torch
+
+    import csa2_synth as syn
+    import compressed_sparse_attention_step_gb300 as c
+    dev = torch.device("cuda")
+    wl = build_workload(torch, c, syn, dev)
+    seed = syn.SEEDS["decode_group_1f3r_b64_t131072"]
+    B, T = B_PER_GPU, T_CTX
+    descs = [make_desc(c, wl)]
+    keep = []
+    for g in range(1, 5):
+        L0 = 4 * g
+        q = [syn.device_normal_bf16((B, 1, 16, 512), seed, syn.T_Q + L0 + l, device=dev) for l in range(4)]
+        qI = [syn.device_normal_bf16((B, 1, 4, 128), seed, syn.T_QI + L0, device=dev), None, None, None]
+        w = [syn.device_normal_bf16((B, 1, 4), seed, syn.T_W + L0, device=dev).float(), None, None, None]
+        swa = [syn.device_normal_bf16((B, W_WIN, 512), seed, syn.T_SWA + L0 + l, device=dev) for l in range(4)]
+        out = [torch.empty((B, 1, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        idx = [torch.empty((B, K_SEL), dtype=torch.int32, device=dev), None, None, None]
+        keep += [q, qI, w, swa, out, idx]
+        descs.append(c.make_group_desc(
+            [c.MODE_REINDEX, c.MODE_REUSE, c.MODE_REUSE, c.MODE_REUSE], B=B, Nq=1, cap=T, lens=wl["lens"],
+            codes=wl["codes"], scales=wl["scales"], KI=wl["KI"], q=q, qI=qI, w=w, swa=swa, swa_len=wl["swa_len"],
+            out=out, idx=idx, K=K_SEL, W=W_WIN))
+    ms = time_steps(torch, lambda: c.csa2_stack_step(descs, wl["ws"]), args.steps, max(args.warmup, 3))
+    # algorithmic bytes: 5 indexer-K scans + 20 layers of attention + the append, per sequence
+    per_seq = 5 * BYTES_KI_PER_SEQ + 20 * BYTES_ATTN_PER_SEQ_LAYER + BYTES_APPEND_PER_SEQ
+    peak, kind = peaks()
+    gbs = per_seq * B / (ms / 1e3) / 1e9
+    return {"metric": "CSA2 20-layer decoder stack tokens/s at 128K ctx", "value": B / (ms / 1e3),
+            "unit": "tokens/s", "ms_per_step": ms, "higher_is_better": True,
+            "config": {"workload": "csa2_decoder_stack_5x4_b64_t131072", "global_batch": B, "seq_len": T,
+                       "layers": "Full+3 Reuse, then 4 x (Reindex + 3 Reuse)", "top_k": K_SEL, "window": W_WIN},
+            "kv_gbs": gbs, "hbm_frac_step": gbs / peak, "peak_kind": f"{kind} (hbm copy)",
+            # group 1: append (2) + score + Top-K + attention; groups 2-5: score + Top-K + attention
+            "gpu_launches": (5 + 4 * 3) * args.steps}
+
+
+def run_prefill(args):
+    """The encoder prefill chunk: 2048 queries at the end of 262144 tokens (131072 compressed
+    entries, ratio 2), 1 Full + 5 Reuse, Top-512, 128-token window; one csa2_group_step per step."""
+    import torch
+
+    import csa2_synth as syn
+    import compressed_sparse_attention_step_gb300 as c
+    dev = torch.device("cuda")
+    seed = syn.SEEDS["prefill_group_1f5r_ratio2_q2048"]
+    T, Nq, L = 131072, 2048, 6
+    codes = torch.empty((1, T, 256), dtype=torch.uint8, device=dev)
+    scales = torch.empty((1, T, 32), dtype=torch.uint8, device=dev)
+    kv = syn.device_normal_bf16((1, T, 512), seed, syn.T_KV * 1000, device=dev)
+    c.csa2_fp4_quantize_append(kv, codes, scales)
+    del kv
+    KI = syn.device_normal_bf16((1, T, 128), seed, syn.T_KI * 1000, device=dev)
+    q = [syn.device_normal_bf16((1, Nq, 16, 512), seed, syn.T_Q + l, device=dev) for l in range(L)]
+    qI = [syn.device_normal_bf16((1, Nq, 4, 128), seed, syn.T_QI, device=dev)] + [None] * (L - 1)
+    w = [syn.device_normal_bf16((1, Nq, 4), seed, syn.T_W, device=dev).float()] + [None] * (L - 1)
+    swa = [syn.device_normal_bf16((1, W_WIN - 1 + Nq, 512), seed, syn.T_SWA + l, device=dev) for l in range(L)]
+    out = [torch.empty((1, Nq, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    idx = [torch.empty((Nq, K_SEL), dtype=torch.int32, device=dev)] + [None] * (L - 1)
+    lens = torch.tensor([T], dtype=torch.int32, device=dev)
+    swa_len = torch.tensor([W_WIN - 1 + Nq], dtype=torch.int32, device=dev)
+    q_pos = torch.arange(2 * T - Nq, 2 * T, dtype=torch.int32, device=dev)
+    d = c.make_group_desc([c.MODE_FULL] + [c.MODE_REUSE] * (L - 1), B=1, Nq=Nq, cap=T, lens=lens, codes=codes,
+                          scales=scales, KI=KI, q=q, qI=qI, w=w, swa=swa, swa_len=swa_len, out=out, idx=idx,
+                          K=K_SEL, W=W_WIN, ratio=2, q_pos=q_pos)
+    ws = torch.empty(c.group_workspace_size(1, Nq, T, K_SEL, W_WIN), dtype=torch.uint8, device=dev)
+    ms = time_steps(torch, lambda: c.csa2_group_step(d, ws), args.steps, max(args.warmup, 3))
+    # dense work: the indexer contraction over each query's visible entries (1024 flop per pair)
+    # and 6 layers of attention (2 x 16 heads x 512 x 640 rows x 2 flop per query)
+    vis = (np.arange(2 * T - Nq, 2 * T) + 1) // 2
+    gflop = (float(vis.sum()) * 1024 + L * Nq * 2 * 16 * 512 * (K_SEL + W_WIN) * 2) / 1e9
+    peak, kind = bf16_peak()
+    tflops = gflop / ms
+    return {"metric": "CSA2 encoder prefill chunk queries/s (2048 q x 131072 entries, 6 layers)",
+            "value": Nq / (ms / 1e3), "unit": "queries/s", "ms_per_step": ms, "higher_is_better": True,
+            "config": {"workload": "csa2_prefill_1f5r_ratio2_q2048_t131072", "global_batch": Nq, "seq_len": 2 * T,
+                       "layers": "1 Full + 5 Reuse", "top_k": K_SEL, "window": W_WIN},
+            "dense_gflop_per_step": gflop, "tflops_step": tflops, "bf16_peak_tflops": peak,
+            "frac_of_bf16_peak": tflops / peak, "peak_kind": kind,
+            # key norms, two tensor-core passes, threshold, count, order, rescore/select, attention
+            "gpu_launches": 8 * args.steps}
+
+
+def run_extra(args):
+    import torch
+    torch.cuda.set_device(0)
+    fn = run_stack20 if args.workload == "decoder_stack_20" else run_prefill
+    line = fn(args)
+    line.update({"n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "scaling": "weak",
+                 "vs_baseline": None, "dtype": "bf16/fp4 in, fp32 accumulate", "data": "synthetic",
+                 "cpu_baseline": None})
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -396,6 +517,8 @@ def main():
     ap.add_argument("--batch", type=int, default=64,
                     help="sequences per GPU (64 is the workload; smaller values are for profiling)")
     ap.add_argument("--n-split", type=int, default=0, help="force the attention split-KV factor (profiling)")
+    ap.add_argument("--workload", default="decode_group", choices=["decode_group", "decoder_stack_20", "prefill_chunk"],
+                    help="decode_group (default): the headline line; the others print their own line on one GPU")
     args = ap.parse_args()
     global B_PER_GPU, N_SPLIT
     B_PER_GPU = args.batch
@@ -406,6 +529,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload != "decode_group":
+        if rank == 0:
+            run_extra(args)
         return
     if world > 1:
         import torch
