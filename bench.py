@@ -496,10 +496,43 @@ def run_prefill(args):
             "gpu_launches": 8 * args.steps}
 
 
+def run_fp8win(args):
+    """The decode workload with 8-bit windows: the same group step, every layer's 128 window rows
+    held as E4M3 bytes (csa2_fp8_quantize at set-up)."""
+    import torch
+
+    import csa2_synth as syn
+    import compressed_sparse_attention_step_gb300 as c
+    dev = torch.device("cuda")
+    wl = build_workload(torch, c, syn, dev)
+    swa8 = []
+    for x in wl["swa"]:
+        y = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        c.csa2_fp8_quantize(x, y)
+        swa8.append(y)
+    d = c.make_group_desc(
+        [c.MODE_FULL, c.MODE_REUSE, c.MODE_REUSE, c.MODE_REUSE], B=B_PER_GPU, Nq=1, cap=T_CTX, lens=wl["lens"],
+        codes=wl["codes"], scales=wl["scales"], KI=wl["KI"], q=wl["q"], qI=wl["qI"], w=wl["w"], swa=swa8,
+        swa_len=wl["swa_len"], out=wl["out"], idx=wl["idx"], K=K_SEL, W=W_WIN, kv_new=wl["kv_new"],
+        ki_new=wl["ki_new"], swa_fp8=True)
+    ms = time_steps(torch, lambda: c.csa2_group_step(d, wl["ws"]), args.steps, max(args.warmup, 3))
+    per_seq = BYTES_PER_SEQ - N_LAYERS * W_WIN * 512   # window rows of 512 B instead of 1 KiB
+    peak, kind = peaks()
+    gbs = per_seq * B_PER_GPU / (ms / 1e3) / 1e9
+    return {"metric": "CSA2 decode tokens/s at 128K ctx with 8-bit (E4M3) windows", "value": B_PER_GPU / (ms / 1e3),
+            "unit": "tokens/s", "ms_per_step": ms, "higher_is_better": True,
+            "config": {"workload": "csa2_decode_group_1full_3reuse_b64_t131072_fp8win", "global_batch": B_PER_GPU,
+                       "seq_len": T_CTX, "layers": "1 Full + 3 Reuse", "top_k": K_SEL, "window": W_WIN,
+                       "window_format": "E4M3, one byte per channel"},
+            "kv_gbs": gbs, "hbm_frac_step": gbs / peak, "bytes_per_step": per_seq * B_PER_GPU,
+            "peak_kind": f"{kind} (hbm copy)", "gpu_launches": launches_per_step(c) * args.steps}
+
+
 def run_extra(args):
     import torch
     torch.cuda.set_device(0)
-    fn = run_stack20 if args.workload == "decoder_stack_20" else run_prefill
+    fn = {"decoder_stack_20": run_stack20, "prefill_chunk": run_prefill,
+          "decode_group_fp8win": run_fp8win}[args.workload]
     line = fn(args)
     line.update({"n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "scaling": "weak",
                  "vs_baseline": None, "dtype": "bf16/fp4 in, fp32 accumulate", "data": "synthetic",
@@ -517,7 +550,8 @@ def main():
     ap.add_argument("--batch", type=int, default=64,
                     help="sequences per GPU (64 is the workload; smaller values are for profiling)")
     ap.add_argument("--n-split", type=int, default=0, help="force the attention split-KV factor (profiling)")
-    ap.add_argument("--workload", default="decode_group", choices=["decode_group", "decoder_stack_20", "prefill_chunk"],
+    ap.add_argument("--workload", default="decode_group",
+                    choices=["decode_group", "decoder_stack_20", "prefill_chunk", "decode_group_fp8win"],
                     help="decode_group (default): the headline line; the others print their own line on one GPU")
     args = ap.parse_args()
     global B_PER_GPU, N_SPLIT

@@ -22,6 +22,7 @@ MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 OP_TOPK, OP_BLOCK_POOL, OP_SPARSE_ATTN, OP_GROUP_STEP, OP_INDEX_SELECT_PREFILL = 1, 2, 3, 4, 5
 FLAG_APPEND_OOB, FLAG_INDEX_OOB, FLAG_TIMEOUT = 1, 2, 4
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TOO_LARGE = 0, 1, 2, 3, 4, 5
+SWA_BF16, SWA_E4M3 = 0, 1
 
 LIB_PATH = _build.LIB
 
@@ -45,7 +46,7 @@ class GroupDesc(ctypes.Structure):
         ("n_layers", I32), ("modes", I32 * MAX_LAYERS),
         ("B", I32), ("Nq", I32), ("K", I32), ("W", I32), ("ratio", I32),
         ("hierarchical", I32), ("n_blocks_keep", I32), ("n_split", I32), ("n_new", I32), ("seq_chunks", I32),
-        ("cap", I64), ("lens", P), ("q_pos", P),
+        ("swa_format", I32), ("cap", I64), ("lens", P), ("q_pos", P),
         ("codes", P), ("scales", P), ("KI", P), ("block_keys", P),
         ("kv_new", P), ("ki_new", P),
         ("q", P * MAX_LAYERS), ("qI", P * MAX_LAYERS), ("w", P * MAX_LAYERS),
@@ -83,6 +84,7 @@ def lib():
                                         SZ, P],
             "csa2_group_step": [ctypes.POINTER(GroupDesc), P, SZ, P],
             "csa2_stack_step": [ctypes.POINTER(GroupDesc), I32, P, SZ, P],
+            "csa2_fp8_quantize": [P, I64, P, P],
             "csa2_workspace_size": [I32, ctypes.POINTER(Dims)],
             "csa2_attn_auto_split": [I64, I32, I32],
             "csa2_status_string": [I32],
@@ -290,9 +292,10 @@ def group_workspace_size(B, Nq, cap, K=512, W=128, hierarchical=False, keep=2048
 def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa, swa_len, out, idx,
                     K=512, W=128, ratio=1, hierarchical=False, keep=2048, n_split=0, q_pos=None,
                     block_keys=None, pool=None, pool_len=None, kv_new=None, ki_new=None, lse=None,
-                    softmax_scale=None, events=None, seq_chunks=0):
+                    softmax_scale=None, events=None, seq_chunks=0, swa_fp8=False):
     """Build a csa2_group_desc from torch tensors (per-layer arguments are lists; entries of
-    qI/w/idx may be None for Reuse layers).  Keeps references to the tensors on the result."""
+    qI/w/idx may be None for Reuse layers; swa_fp8: the window buffers are uint8 E4M3 rows, as
+    csa2_fp8_quantize writes them)."""
     torch = _torch()
     L = len(modes)
     if not 1 <= L <= MAX_LAYERS:
@@ -310,6 +313,7 @@ def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa
         n_new = ki_new.shape[1]
     g.n_new = n_new
     g.seq_chunks = int(seq_chunks)
+    g.swa_format = SWA_E4M3 if swa_fp8 else SWA_BF16
     g.cap = cap
     bf = _bf16_types()
     g.lens = _ptr(lens, "lens", (torch.int32,), B)
@@ -324,7 +328,8 @@ def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa
         g.q[l] = _ptr(q[l], f"q[{l}]", bf, B * Nq * H * D)
         g.qI[l] = _ptr(qI[l], f"qI[{l}]", bf) if qI[l] is not None else None
         g.w[l] = _ptr(w[l], f"w[{l}]", (torch.float32,)) if w[l] is not None else None
-        g.swa[l] = _ptr(swa[l], f"swa[{l}]", bf) if (swa is not None and swa[l] is not None) else None
+        g.swa[l] = (_ptr(swa[l], f"swa[{l}]", (torch.uint8,) if swa_fp8 else bf)
+                    if (swa is not None and swa[l] is not None) else None)
         g.out[l] = _ptr(out[l], f"out[{l}]", bf, B * Nq * H * D)
         g.lse[l] = _ptr(lse[l], f"lse[{l}]", (torch.float32,)) if (lse is not None and lse[l] is not None) else None
         g.idx[l] = _ptr(idx[l], f"idx[{l}]", (torch.int32,), B * Nq * K) if idx[l] is not None else None
@@ -341,6 +346,14 @@ def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa
 def csa2_group_step(desc, ws, stream=None):
     _check("csa2_group_step", lib().csa2_group_step(ctypes.byref(desc), _ptr(ws, "ws"), _nbytes(ws),
                                                     _stream(stream)))
+
+
+def csa2_fp8_quantize(x, out, stream=None):
+    """8-bit window rows: bf16 tensor x -> uint8 E4M3 tensor out of the same number of elements."""
+    torch = _torch()
+    n = x.numel()
+    _check("csa2_fp8_quantize", lib().csa2_fp8_quantize(_ptr(x, "x", _bf16_types(), n), n,
+                                                        _ptr(out, "out", (torch.uint8,), n), _stream(stream)))
 
 
 def csa2_stack_step(descs, ws, stream=None):

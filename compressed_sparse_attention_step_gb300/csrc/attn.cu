@@ -238,7 +238,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     const __grid_constant__ AttnLayers layers, int Nq, const uint8_t* __restrict__ codes,
     const uint8_t* __restrict__ scales, int64_t cap, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ n_valid, int k, const int32_t* __restrict__ swa_len, int W, float scale_log2,
-    int n_split, float* __restrict__ ws, unsigned int* __restrict__ tickets, unsigned int* flags, int inputs_ready) {
+    int n_split, float* __restrict__ ws, unsigned int* __restrict__ tickets, unsigned int* flags, int inputs_ready,
+    int win_fp8) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // Inputs not yet known to be complete (the selected positions may come from the kernel right
   // before this one): wait first.  Otherwise (a layer that reuses earlier positions) wait only
@@ -289,6 +290,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   const uint8_t* cbase = codes + int64_t(b) * cap * CSA2_CODE_BYTES;
   const uint8_t* sbase = scales + int64_t(b) * cap * CSA2_SCALE_BYTES;
   const uint16_t* swbase = swa ? swa + int64_t(b) * SW * CSA2_D : nullptr;
+  // 8-bit window: E4M3 bytes, rows of 512 B
+  const uint8_t* sw8 = swa ? reinterpret_cast<const uint8_t*>(swa) + int64_t(b) * SW * CSA2_D : nullptr;
   const uint16_t* qrow = q + int64_t(inst) * CSA2_H * CSA2_D;
 
   // window row of tile row r of window tile `tile`, or -1
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
                    : "memory");
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
-    if (first_live < nwin) copy_window(first_live);
+    if (first_live < nwin && !win_fp8) copy_window(first_live);
   }
   // ---- source rows of every tile of the split; FP4 and later window rows pulled into L2 ------------
   for (int e = t; e < (t_end - t_begin) * kRows; e += kThreads) {
@@ -348,7 +351,11 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
       }
     } else {
       p = win_row(tile, r);
-      if (p >= 0 && tile != first_live) {
+      if (p >= 0 && win_fp8) {
+        const uint8_t* sr = sw8 + int64_t(p) * CSA2_D;
+#pragma unroll
+        for (int l = 0; l < 4; ++l) asm volatile("prefetch.global.L2 [%0];" ::"l"(sr + 128 * l));
+      } else if (p >= 0 && tile != first_live) {
         const uint16_t* sr = swbase + int64_t(p) * CSA2_D;
 #pragma unroll
         for (int l = 0; l < 8; ++l) asm volatile("prefetch.global.L2 [%0];" ::"l"(sr + 64 * l));
@@ -410,11 +417,21 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         const int r = (t & 7) + 8 * (j & 7), cc = (t >> 3) + 32 * (j >> 3);
         *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, cc)) = v;
       };
-      const bool win_regs = !is_fp4 && !first;
+      const bool f16_tile = is_fp4 || win_fp8;  // operands in f16 (FP4 rows, 8-bit window rows)
+      const bool win8 = !is_fp4 && win_fp8;
+      const bool win_regs = !is_fp4 && !win_fp8 && !first;
       uint4 wv[8];
       if (win_regs) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) wv[j] = win_load(j);
+      } else if (win8) {
+        // 8-bit window tile: thread t loads 16 channels (16 B, piece t >> 3) of rows (t & 7) + 8 j
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int32_t br = pos[(t & 7) + 8 * j];
+          wv[j] = br >= 0 ? __ldg(reinterpret_cast<const uint4*>(sw8 + int64_t(br) * CSA2_D + 16 * (t >> 3)))
+                          : make_uint4(0, 0, 0, 0);
+        }
       }
       // -- the previous tile's O^T MMAs read the operand tile and P^T: wait for them
       if (!first) {
@@ -422,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         phase ^= 1u;
       }
       // -- Q in the tile's operand type
-      const int kind = is_fp4 ? 0 : 1;
+      const int kind = f16_tile ? 0 : 1;
       if (kind != q_kind) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -463,6 +480,20 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
             *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, 4 * piece + wi)) = o;
           }
         }
+      } else if (win8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = (t & 7) + 8 * j, cc = 2 * (t >> 3);
+          const uint32_t bw[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+          uint32_t h[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            h[2 * e] = e4m3x2_to_f16x2(uint16_t(bw[e] & 0xFFFFu));
+            h[2 * e + 1] = e4m3x2_to_f16x2(uint16_t(bw[e] >> 16));
+          }
+          *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, cc)) = make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, cc + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
       } else if (win_regs) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) win_store(j, wv[j]);
@@ -481,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
       // -- S^T = K Q^T (tensor core): warp i < 4 issues channels [128 i, 128 i + 128) in 8 steps
       if (lane == 0 && warp < kIssuers) {
         tc_fence_after();
-        const uint32_t id = instr_desc(kRows, !is_fp4, false);
+        const uint32_t id = instr_desc(kRows, !f16_tile, false);
 #pragma unroll
         for (int k8 = 0; k8 < CSA2_D / 16 / kIssuers; ++k8) {
           const int kk = warp * (CSA2_D / 16 / kIssuers) + k8;
@@ -538,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         for (int j = 0; j < 8; ++j) {
           const int h = 8 * half + j;
           const uint32_t off = uint32_t(h) * 128u + uint32_t(((row >> 3) ^ (h & 7)) << 4) + uint32_t(row & 7) * 2u;
-          const uint16_t bits = is_fp4 ? __half_as_ushort(__float2half_rn(pr[j])) : uint16_t(f2bf_bits(pr[j]));
+          const uint16_t bits = f16_tile ? __half_as_ushort(__float2half_rn(pr[j])) : uint16_t(f2bf_bits(pr[j]));
           *reinterpret_cast<uint16_t*>(base + kPOff + off) = bits;
         }
       }
@@ -569,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
       // -- O^T += V^T P^T (tensor core): warp i < 4 issues channel block i in 4 steps of 16 rows
       if (lane == 0 && warp < kIssuers) {
         tc_fence_after();
-        const uint32_t id = instr_desc(128, !is_fp4, true);
+        const uint32_t id = instr_desc(128, !f16_tile, true);
         const int i = warp;
 #pragma unroll
         for (int s = 0; s < kRows / 16; ++s) {
@@ -751,7 +782,7 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
                                       const uint8_t* scales, int64_t cap, const int32_t* idx,
                                       const int32_t* n_valid, int k, const int32_t* swa_len, int W,
                                       float softmax_scale, int n_split, float* ws, cudaStream_t st,
-                                      bool tickets_zeroed, bool inputs_ready) {
+                                      bool tickets_zeroed, bool inputs_ready, bool win_fp8) {
   const int64_t per_layer = int64_t(B) * Nq, instances = per_layer * n_layers;
   if (instances == 0) return cudaSuccess;
   if (n_layers < 1 || n_layers > CSA2_MAX_LAYERS || per_layer > 65535) return cudaErrorInvalidValue;
@@ -781,7 +812,8 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
   }
   const dim3 grid{unsigned(n_split), unsigned(per_layer), unsigned(n_layers)};
   return launch_pdl(sparse_attn_kernel, grid, dim3(kThreads), kSmemBytes, st, layers, Nq, codes, scales, cap, idx,
-                    n_valid, k, swa_len, W, scale_log2, n_split, partials, tickets, flags, int(inputs_ready));
+                    n_valid, k, swa_len, W, scale_log2, n_split, partials, tickets, flags, int(inputs_ready),
+                    int(win_fp8));
 }
 
 cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
@@ -796,7 +828,7 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
   layers.out[0] = out;
   layers.lse[0] = lse;
   return launch_sparse_attn_layers(layers, 1, B, Nq, codes, scales, cap, idx, n_valid, k, swa_len, W, softmax_scale,
-                                   n_split, ws, st, tickets_zeroed, inputs_ready);
+                                   n_split, ws, st, tickets_zeroed, inputs_ready, false);
 }
 
 }  // namespace csa2

@@ -218,12 +218,15 @@ struct AttnLayers {
   float* lse[CSA2_MAX_LAYERS];
 };
 // n_layers layers of B*Nq queries each in one launch; the split workspace holds
-// n_layers * B * Nq instances (attn_ws_bytes), tickets first.
+// n_layers * B * Nq instances (attn_ws_bytes), tickets first.  win_fp8: the window buffers hold
+// E4M3 bytes (rows of 512 B) instead of bf16.
 cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, int B, int Nq, const uint8_t* codes,
                                       const uint8_t* scales, int64_t cap, const int32_t* idx,
                                       const int32_t* n_valid, int k, const int32_t* swa_len, int W,
                                       float softmax_scale, int n_split, float* ws, cudaStream_t st,
-                                      bool tickets_zeroed, bool inputs_ready);
+                                      bool tickets_zeroed, bool inputs_ready, bool win_fp8);
+// 8-bit window rows: n bf16 values -> E4M3 bytes (RNE, saturating to +-448).
+cudaError_t launch_fp8_quantize(const uint16_t* x, int64_t n, uint8_t* out, cudaStream_t st);
 cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
                                const uint8_t* scales, int64_t cap, const int32_t* idx,
                                const int32_t* n_valid, int k, const uint16_t* swa,

@@ -119,6 +119,30 @@ __global__ void __launch_bounds__(256) fp4_dequantize_kernel(const uint8_t* __re
   __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
 }
 
+// 8-bit window rows (kongchang.com "DeepSeek V4.1 Flash Deep Dive", section "Compressed Absorption
+// Attention (2nd Gen)": the sliding window is kept in 8-bit precision): every bf16 value to E4M3FN
+// with round-to-nearest-even, saturating to +-448, by the hardware conversion; 8 values per thread.
+__global__ void __launch_bounds__(256) fp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                           uint8_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+  if (i >= n) return;
+  auto cvt2 = [](float lo, float hi) -> uint32_t {  // two E4M3 bytes, lo's in the low byte
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+  };
+  if (i + 8 <= n) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + i));
+    const uint32_t o0 = cvt2(bf16lo(v.x), bf16hi(v.x)) | (cvt2(bf16lo(v.y), bf16hi(v.y)) << 16);
+    const uint32_t o1 = cvt2(bf16lo(v.z), bf16hi(v.z)) | (cvt2(bf16lo(v.w), bf16hi(v.w)) << 16);
+    *reinterpret_cast<uint2*>(out + i) = make_uint2(o0, o1);
+  } else {
+    for (int64_t j = i; j < n; ++j) out[j] = uint8_t(cvt2(bf16f(x[j]), 0.0f) & 0xFFu);
+  }
+}
+
 // dst row (lens[b] - n_new + r) of sequence b <- src row r of sequence b; 16 B per thread.
 __global__ void __launch_bounds__(256) copy_rows_append_kernel(const uint16_t* __restrict__ src,
                                                                int B, int n_new, int row_vecs,
@@ -201,6 +225,11 @@ cudaError_t launch_fp4_quantize(const uint16_t* x, int B, int n_new, uint8_t* co
                                                                offsets, offset_bias, flags);
 }
 
+cudaError_t launch_fp8_quantize(const uint16_t* x, int64_t n, uint8_t* out, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  return launch_pdl(fp8_quantize_kernel, grid_for((n + 7) / 8, 256), dim3(256), 0, st, x, n, out);
+}
+
 cudaError_t launch_copy_rows_append(const uint16_t* src, int B, int n_new, int row_elems,
                                     uint16_t* dst, int64_t cap, const int32_t* lens, cudaStream_t st) {
   const int row_vecs = row_elems / 8;
@@ -242,6 +271,14 @@ extern "C" csa2_status csa2_fp4_quantize_append(const uint16_t* x, int B, int n_
                                    reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? CSA2_OK
              : CSA2_ERR_CUDA;
+}
+
+extern "C" csa2_status csa2_fp8_quantize(const uint16_t* x, int64_t n, uint8_t* out, csa2_stream_t stream) {
+  if (n < 0) return CSA2_ERR_INVALID_ARG;
+  if (n == 0) return CSA2_OK;
+  if (!x || !out || !al16(x) || !al16(out)) return CSA2_ERR_INVALID_ARG;
+  return csa2::launch_fp8_quantize(x, n, out, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? CSA2_OK
+                                                                                                   : CSA2_ERR_CUDA;
 }
 
 extern "C" csa2_status csa2_fp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows,

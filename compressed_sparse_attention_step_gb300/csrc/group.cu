@@ -222,6 +222,7 @@ csa2_status group_check(const csa2_group_desc* g, const void* ws, size_t ws_byte
   if (g->hierarchical && (!g->block_keys || !g->pool || !g->pool_len || !al16(g->block_keys)))
     return CSA2_ERR_INVALID_ARG;
   if (g->W > 0 && !g->swa_len) return CSA2_ERR_INVALID_ARG;
+  if (g->swa_format != CSA2_SWA_BF16 && g->swa_format != CSA2_SWA_E4M3) return CSA2_ERR_INVALID_ARG;
   bool any_full = false;
   for (int l = 0; l < L; ++l) {
     const int m = g->modes[l];
@@ -350,7 +351,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
       while (ns > 1 && csa2::attn_ws_bytes(inst, ns) > attn_cap) --ns;
       const bool r = ok(csa2::launch_sparse_attn_layers(run, run_n, Bc, Nq, codes, scl, g->cap, run_idx, nullptr, K,
                                                          swl, g->W, g->softmax_scale, ns, attn_ws, aux, zeroed,
-                                                         false));
+                                                         false, g->swa_format == CSA2_SWA_E4M3));
       run_n = 0;
       return r;
     };
@@ -417,7 +418,12 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
           return CSA2_ERR_CUDA;
       }
       run.q[run_n] = g->q[l] + r0 * (CSA2_H * CSA2_D);
-      run.swa[run_n] = g->W > 0 ? g->swa[l] + int64_t(b0) * SW * CSA2_D : nullptr;
+      // window rows: 512 bf16 values, or 512 E4M3 bytes (the same pointer arithmetic in bytes)
+      const int64_t win_off = int64_t(b0) * SW * CSA2_D;
+      run.swa[run_n] = g->W <= 0 ? nullptr
+                       : g->swa_format == CSA2_SWA_E4M3
+                           ? reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(g->swa[l]) + win_off)
+                           : g->swa[l] + win_off;
       run.out[run_n] = g->out[l] + r0 * (CSA2_H * CSA2_D);
       run.lse[run_n] = g->lse[l] ? g->lse[l] + r0 * CSA2_H : nullptr;
       run_idx = latest;

@@ -77,6 +77,10 @@ typedef enum {
 #define CSA2_MODE_REINDEX 1
 #define CSA2_MODE_REUSE 2
 
+/* Window row formats of csa2_group_desc.swa_format. */
+#define CSA2_SWA_BF16 0
+#define CSA2_SWA_E4M3 1
+
 /* Device flag bits (csa2_device_flags). */
 #define CSA2_FLAG_APPEND_OOB 1u /* an appended row fell outside [0, cap): row skipped   */
 #define CSA2_FLAG_INDEX_OOB 2u  /* a selected index was >= cap: row treated as empty    */
@@ -98,6 +102,15 @@ typedef enum {
 csa2_status csa2_fp4_quantize_append(const uint16_t* x, int B, int n_new, int d, uint8_t* codes,
                                      uint8_t* scales, int64_t cap, const int32_t* offsets,
                                      csa2_stream_t stream);
+
+/*
+ * 8-bit window rows (kongchang.com "DeepSeek V4.1 Flash Deep Dive", section "Compressed Absorption
+ * Attention (2nd Gen)": the sliding window is kept in 8-bit precision): out[i] = E4M3FN(x[i]) for
+ * n bf16 values, round-to-nearest-even, saturating to +-448, a zero result keeping x's sign; no
+ * scale.  Fills the window buffers of groups with swa_format = CSA2_SWA_E4M3.  x and out 16-byte
+ * aligned.  Asynchronous on `stream`.
+ */
+csa2_status csa2_fp8_quantize(const uint16_t* x, int64_t n, uint8_t* out, csa2_stream_t stream);
 
 /*
  * FP4 dequantisation of `rows` cache rows: out[r][c] = E2M1(code) * E4M3(scale), exact in bf16.
@@ -250,7 +263,9 @@ size_t csa2_sparse_attn_static_scratch_bytes(void);
  *            (pool / pool_len hold it, possibly from an earlier group), else all visible
  *            entries; selects Top-K.
  *   REUSE    attends with the latest layer's indices; no scoring.
- * Every layer attends with its own q and window.  The first layer must be FULL or REINDEX.
+ * Every layer attends with its own q and window; window rows are bf16, or one E4M3 byte per
+ * channel with swa_format = CSA2_SWA_E4M3 (csa2_fp8_quantize).  The first layer must be FULL or
+ * REINDEX.
  * Execution: the batch is cut into `seq_chunks` groups of whole sequences (0: one group).  With
  * more than one group, the first indexer scan of group c runs on `stream` while the remaining
  * work of group c-1 runs on a library-owned, highest-priority stream of the current device
@@ -271,6 +286,8 @@ typedef struct csa2_group_desc {
   int n_split;                        /* attention split, 0 = automatic                  */
   int n_new;                          /* rows appended by the Full layer (0: none)       */
   int seq_chunks;                     /* sequence chunks pipelined over two streams, 0 = 1 */
+  int swa_format;                     /* CSA2_SWA_BF16, or CSA2_SWA_E4M3: swa[l] holds one
+                                         E4M3 byte per channel (rows of 512 B)           */
   int64_t cap;                        /* cache capacity (entries) per sequence           */
   const int32_t* lens;                /* [B] entries present (after the append)          */
   const int32_t* q_pos;               /* [B*Nq] query token positions, or NULL           */

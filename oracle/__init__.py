@@ -66,7 +66,9 @@ def lib():
         _lib.oracle_sparse_attn.argtypes = [P, P, P, P, i32, P, i32, f32, P, P]
         _lib.oracle_group_step.restype = i32
         _lib.oracle_group_step.argtypes = [i32, i32, P, i32, i32, i32, i32, i32, i32, P, i64,
-                                           P, P, P, P, P, P, P, P, P, f32, P, P, P, P, P, i32]
+                                           P, P, P, P, P, P, P, P, P, f32, P, P, P, P, P, i32, i32]
+        _lib.oracle_fp8_quantize.argtypes = [P, i64, P]
+        _lib.oracle_fp8_dequantize.argtypes = [P, i64, P]
     return _lib
 
 
@@ -108,6 +110,22 @@ def fp4_quantize(x_bf16: np.ndarray):
     scales = np.empty(x.shape[:-1] + (D // GROUP,), np.uint8)
     lib().oracle_fp4_quantize(_p(x), rows, _p(codes), _p(scales))
     return codes, scales
+
+
+def fp8_quantize(x_bf16: np.ndarray) -> np.ndarray:
+    """8-bit window rows: bf16 bits -> E4M3 bytes (RNE, saturating to +-448), same shape."""
+    x = _c(x_bf16, np.uint16)
+    out = np.empty(x.shape, np.uint8)
+    lib().oracle_fp8_quantize(_p(x), x.size, _p(out))
+    return out
+
+
+def fp8_dequantize(b: np.ndarray) -> np.ndarray:
+    """E4M3 bytes -> bf16 bits (exact), same shape."""
+    b = _c(b, np.uint8)
+    out = np.empty(b.shape, np.uint16)
+    lib().oracle_fp8_dequantize(_p(b), b.size, _p(out))
+    return out
 
 
 def fp4_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
@@ -178,11 +196,11 @@ def sparse_attn(q, codes, scales, idx, swa_rows, softmax_scale: float):
 
 def group_step(modes, T, codes, scales, KI, q, qI, w, swa, swa_len, *, Nq=1, K=512, W=128,
                ratio=1, hierarchical=False, keep=2048, q_pos=None, softmax_scale=None,
-               threads=1):
+               threads=1, swa_fp8=False):
     """One layer group over a batch.  Shapes: codes [B,cap,256], scales [B,cap,32],
     KI [B,cap,128]; q [L,B,Nq,16,512]; qI [L,B,Nq,4,128]; w [L,B,Nq,4];
-    swa [L,B,W-1+Nq,512]; T and swa_len [B].  Returns dict of out (fp64), lse, idx,
-    pool, pool_len."""
+    swa [L,B,W-1+Nq,512] (bf16 bits, or E4M3 bytes when swa_fp8); T and swa_len [B].
+    Returns dict of out (fp64), lse, idx, pool, pool_len."""
     modes = _c(modes, np.int32)
     L = modes.size
     codes = _c(codes, np.uint8)
@@ -193,7 +211,7 @@ def group_step(modes, T, codes, scales, KI, q, qI, w, swa, swa_len, *, Nq=1, K=5
     q = _c(q, np.uint16)
     qI = _c(qI, np.uint16)
     w = _c(w, np.float32)
-    swa = _c(swa, np.uint16)
+    swa = _c(swa, np.uint8 if swa_fp8 else np.uint16)
     swa_len = _c(swa_len, np.int32)
     qp = None if q_pos is None else _c(q_pos, np.int32)
     if softmax_scale is None:
@@ -206,7 +224,7 @@ def group_step(modes, T, codes, scales, KI, q, qI, w, swa, swa_len, *, Nq=1, K=5
     rc = lib().oracle_group_step(B, L, _p(modes), Nq, K, W, ratio, int(bool(hierarchical)), keep,
                                  _p(T), cap, _p(codes), _p(scales), _p(KI), _p(qp), _p(q), _p(qI),
                                  _p(w), _p(swa), _p(swa_len), float(softmax_scale), _p(out),
-                                 _p(lse), _p(idx), _p(pool), _p(pool_len), int(threads))
+                                 _p(lse), _p(idx), _p(pool), _p(pool_len), int(threads), int(bool(swa_fp8)))
     if rc != 0:
         raise ValueError("oracle_group_step: bad arguments")
     return {"out": out, "lse": lse, "idx": idx, "pool": pool, "pool_len": pool_len}

@@ -292,6 +292,14 @@ std::vector<double> bf16_row(const uint16_t* r) {
   return v;
 }
 
+// A window row kept in 8 bits ([KCH] "Compressed Absorption Attention (2nd Gen)": the sliding
+// window is retained in 8-bit precision): every channel one E4M3 value, no scale (READING).
+std::vector<double> fp8_row(const uint8_t* r) {
+  std::vector<double> v(kD);
+  for (int c = 0; c < kD; ++c) v[size_t(c)] = e4m3_value(r[c]);
+  return v;
+}
+
 // Entries visible to a query at absolute token position p when each cache entry merges
 // `ratio` tokens: entry j covers tokens ratio*j .. ratio*j+ratio-1 and is visible iff its last
 // token is <= p (READING, causal mask over compressed positions).
@@ -311,6 +319,14 @@ uint8_t oracle_e2m1_encode(float v) { return e2m1_encode(v); }
 void oracle_fp4_quantize(const uint16_t* x, int64_t rows, uint8_t* codes, uint8_t* scales) {
   for (int64_t r = 0; r < rows; ++r)
     quantize_row(x + r * kD, codes + r * kCodeBytes, scales + r * kScaleBytes);
+}
+
+// 8-bit window rows: each bf16 element to E4M3 (RNE, saturating to +-448), and back (exact).
+void oracle_fp8_quantize(const uint16_t* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_encode(bf16_to_f32(x[i]));
+}
+void oracle_fp8_dequantize(const uint8_t* in, int64_t n, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f32_to_bf16(float(e4m3_value(in[i])));
 }
 
 void oracle_fp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows, uint16_t* out) {
@@ -359,7 +375,8 @@ void oracle_sparse_attn(const uint16_t* q, const uint8_t* codes, const uint8_t* 
 // Every layer attends with its own main Q and its own window rows over the shared FP4 cache.
 // Layout (contiguous): codes [B][cap][256], scales [B][cap][32], KI [B][cap][128];
 // per-layer tensors are layer-major: q [L][B][Nq][16][512], qI [L][B][Nq][4][128],
-// w [L][B][Nq][4], swa [L][B][W-1+Nq][512]; outputs out [L][B][Nq][16][512] (fp64),
+// w [L][B][Nq][4], swa [L][B][W-1+Nq][512] (bf16, or E4M3 bytes when swa_fp8); outputs
+// out [L][B][Nq][16][512] (fp64),
 // lse [L][B][Nq][16] (nullable), idx [L][B][Nq][K], pool [B][Nq][keep*8] and pool_len [B][Nq]
 // (nullable unless hierarchical).  Query i of sequence b sits at token position
 // q_pos[b*Nq+i], or ratio*T_b - Nq + i when q_pos is NULL.  Window rows of query i are rows
@@ -369,9 +386,9 @@ int oracle_group_step(int B, int L, const int32_t* modes, int Nq, int K, int W, 
                       int hierarchical, int keep, const int64_t* T, int64_t cap,
                       const uint8_t* codes, const uint8_t* scales, const uint16_t* KI,
                       const int32_t* q_pos, const uint16_t* q, const uint16_t* qI, const float* w,
-                      const uint16_t* swa, const int32_t* swa_len, float softmax_scale,
+                      const void* swa, const int32_t* swa_len, float softmax_scale,
                       double* out, double* lse, int32_t* idx, int32_t* pool, int32_t* pool_len,
-                      int threads) {
+                      int threads, int swa_fp8) {
   if (B <= 0 || L <= 0 || Nq <= 0 || K <= 0 || W < 0 || ratio <= 0) return -1;
   if (modes[0] == MODE_REUSE) return -1;
   if (hierarchical && (modes[0] != MODE_FULL || keep <= 0 || !pool || !pool_len)) return -1;
@@ -423,9 +440,12 @@ int oracle_group_step(int B, int L, const int32_t* modes, int Nq, int K, int W, 
         std::vector<std::vector<double>> rows;
         for (int j = 0; j < K; ++j)
           if (il[j] >= 0) rows.push_back(fp4_row(cb, sb, il[j]));
-        const uint16_t* swl = swa + (int64_t(l) * B + b) * SW * kD;
-        for (int r = i; r < i + W; ++r)
-          if (r >= SW - swa_len[b]) rows.push_back(bf16_row(swl + int64_t(r) * kD));
+        const int64_t wrow0 = (int64_t(l) * B + b) * SW;
+        for (int r = i; r < i + W; ++r) {
+          if (r < SW - swa_len[b]) continue;
+          if (swa_fp8) rows.push_back(fp8_row(static_cast<const uint8_t*>(swa) + (wrow0 + r) * kD));
+          else rows.push_back(bf16_row(static_cast<const uint16_t*>(swa) + (wrow0 + r) * kD));
+        }
         attend(q + lr * kH * kD, rows, softmax_scale, out + lr * kH * kD, lse ? lse + lr * kH : nullptr);
       }
     }

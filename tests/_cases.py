@@ -46,7 +46,8 @@ def assert_attn_close(got_bf16_bits, ref, what=""):
     assert err.max() <= ATOL and rel <= RTOL, f"{what}: max abs {err.max():.3e}, rel {rel:.3e}"
 
 
-def one_query_oracle(orc, modes, T, codes, scales, KI, q, qI, w, swa, swa_len, i, q_pos_i, *, K, W, ratio):
+def one_query_oracle(orc, modes, T, codes, scales, KI, q, qI, w, swa, swa_len, i, q_pos_i, *, K, W, ratio,
+                     swa_fp8=False):
     """The oracle group step of query i of a chunk alone: one sequence of T entries (codes, scales,
     KI), per-layer chunk inputs q [L,Nq,16,512], qI [L,Nq,4,128], w [L,Nq,4], swa [L,W-1+Nq,512]
     with its last swa_len rows valid; query i at position q_pos_i attends rows i .. i+W-1 of its
@@ -56,7 +57,8 @@ def one_query_oracle(orc, modes, T, codes, scales, KI, q, qI, w, swa, swa_len, i
     valid = int(min(W, max(0, W - max(0, SW - int(swa_len) - i))))
     return orc.group_step(modes, [T], codes[None], scales[None], KI[None], q[:, i][:, None, None],
                           qI[:, i][:, None, None], w[:, i][:, None, None], swa[:, i:i + W][:, None], [valid],
-                          Nq=1, K=K, W=W, ratio=ratio, q_pos=np.array([[q_pos_i]], np.int32), softmax_scale=SCALE)
+                          Nq=1, K=K, W=W, ratio=ratio, q_pos=np.array([[q_pos_i]], np.int32), softmax_scale=SCALE,
+                          swa_fp8=swa_fp8)
 
 
 class GroupCase:
@@ -68,10 +70,12 @@ class GroupCase:
     """
 
     def __init__(self, seed, T, modes, *, Nq=1, K=512, W=128, ratio=1, hierarchical=False, keep=2048,
-                 cap=None, append=True, host_seqs=None, q_pos=None, share=None, layer0=0):
+                 cap=None, append=True, host_seqs=None, q_pos=None, share=None, layer0=0, swa_fp8=False):
         """share: a case whose cache, lengths, block keys and pool this one uses (a later group of
         a decoder stack: no append of its own); layer0: the stack index of this group's first
-        layer (its per-layer draws use tensor ids offset by it)."""
+        layer (its per-layer draws use tensor ids offset by it); swa_fp8: 8-bit (E4M3) window rows,
+        quantised from the bf16 draws by the oracle for host-drawn sequences (both sides see the
+        same bytes) and by the library elsewhere."""
         import torch
         import compressed_sparse_attention_step_gb300 as c
         self.c = c
@@ -82,6 +86,7 @@ class GroupCase:
         self.cap = cap if cap is not None else max(T)
         self.append = append and Nq == 1 and share is None
         self.layer0 = layer0
+        self.swa_fp8 = swa_fp8
         self.host_seqs = list(range(self.B)) if host_seqs is None else list(host_seqs)
         self.q_pos = q_pos
         B, L, cap, SW = self.B, self.L, self.cap, W - 1 + Nq
@@ -98,19 +103,20 @@ class GroupCase:
             self.q = [bf16_dev(np.stack([self.h_q(l, b) for b in range(B)])) for l in range(L)]
             self.qI = [bf16_dev(np.stack([self.h_qI(l, b) for b in range(B)])) for l in range(L)]
             self.w = [to_dev(np.stack([self.h_w(l, b) for b in range(B)])) for l in range(L)]
-            self.swa = [bf16_dev(np.stack([self.h_swa(l, b) for b in range(B)])) for l in range(L)]
+            self.swa = [self._dev_win(np.stack([self.h_swa(l, b) for b in range(B)])) for l in range(L)]
         else:
             l0 = layer0
             self.q = [syn.device_normal_bf16((B, Nq, H, D), seed, syn.T_Q + l0 + l) for l in range(L)]
             self.qI = [syn.device_normal_bf16((B, Nq, HI, DI), seed, syn.T_QI + l0 + l) for l in range(L)]
             self.w = [syn.device_normal_bf16((B, Nq, HI), seed, syn.T_W + l0 + l).float() for l in range(L)]
-            self.swa = [syn.device_normal_bf16((B, SW, D), seed, syn.T_SWA + l0 + l) for l in range(L)]
+            self.swa = [self._dev_win_device(syn.device_normal_bf16((B, SW, D), seed, syn.T_SWA + l0 + l))
+                        for l in range(L)]
             for b in self.host_seqs:
                 for l in range(L):
                     self.q[l][b].copy_(bf16_dev(self.h_q(l, b)))
                     self.qI[l][b].copy_(bf16_dev(self.h_qI(l, b)))
                     self.w[l][b].copy_(to_dev(self.h_w(l, b)))
-                    self.swa[l][b].copy_(bf16_dev(self.h_swa(l, b)))
+                    self.swa[l][b].copy_(self._dev_win(self.h_swa(l, b)))
         # cache rows (kept before the step; the last row comes from the step's append)
         self.kv_new = torch.zeros((B, 1, D), dtype=torch.bfloat16, device=dev)
         self.ki_new = torch.zeros((B, 1, DI), dtype=torch.bfloat16, device=dev)
@@ -176,6 +182,29 @@ class GroupCase:
     def h_swa(self, l, b):
         return syn.normal_bf16(self.seed, syn.T_SWA + self.layer0 + l, b, (self.W - 1 + self.Nq, D))
 
+    def h_win(self, l, b):
+        """Window rows as the step reads them: bf16 bits, or the oracle's E4M3 bytes."""
+        if not self.swa_fp8:
+            return self.h_swa(l, b)
+        import oracle
+        oracle.build()
+        return oracle.fp8_quantize(self.h_swa(l, b))
+
+    def _dev_win(self, host_bf16):
+        if not self.swa_fp8:
+            return bf16_dev(host_bf16)
+        import oracle
+        oracle.build()
+        return to_dev(oracle.fp8_quantize(host_bf16))
+
+    def _dev_win_device(self, dev_bf16):
+        if not self.swa_fp8:
+            return dev_bf16
+        import torch
+        out = torch.empty(dev_bf16.shape, dtype=torch.uint8, device=dev_bf16.device)
+        self.c.csa2_fp8_quantize(dev_bf16, out)
+        return out
+
     def desc(self, events=None, n_split=0, seq_chunks=0):
         c = self.c
         return c.make_group_desc(
@@ -184,7 +213,8 @@ class GroupCase:
             idx=self.idx, K=self.K, W=self.W, ratio=self.ratio, hierarchical=self.hierarchical, keep=self.keep,
             n_split=n_split, q_pos=self.qp_dev, block_keys=self.block_keys, pool=self.pool,
             pool_len=self.pool_len, kv_new=self.kv_new if self.append else None,
-            ki_new=self.ki_new if self.append else None, lse=self.lse, events=events, seq_chunks=seq_chunks)
+            ki_new=self.ki_new if self.append else None, lse=self.lse, events=events, seq_chunks=seq_chunks,
+            swa_fp8=self.swa_fp8)
 
     def run(self, n_split=0, seq_chunks=0):
         import torch
@@ -206,12 +236,13 @@ class GroupCase:
         qs = np.stack([self.h_q(l, b) for l in range(L)])
         qIs = np.stack([self.h_qI(l, b) for l in range(L)])
         ws = np.stack([self.h_w(l, b) for l in range(L)])
-        swas = np.stack([self.h_swa(l, b) for l in range(L)])
+        swas = np.stack([self.h_win(l, b) for l in range(L)])
         qp_all = (np.asarray(self.q_pos, np.int32).reshape(self.B, Nq)[b] if self.q_pos is not None
                   else self.ratio * Tb - Nq + np.arange(Nq, dtype=np.int32))
         for i in queries:
             ref = one_query_oracle(orc, self.modes, Tb, codes, scales, KI, qs, qIs, ws, swas,
-                                   int(self.swa_len_np[b]), i, int(qp_all[i]), K=self.K, W=self.W, ratio=self.ratio)
+                                   int(self.swa_len_np[b]), i, int(qp_all[i]), K=self.K, W=self.W, ratio=self.ratio,
+                                   swa_fp8=self.swa_fp8)
             r = b * Nq + i
             for l in range(L):
                 assert np.array_equal(self.idx[l][r].cpu().numpy(), ref["idx"][l, 0, 0]), f"query {i} layer {l}: indices"
@@ -247,11 +278,11 @@ def stack_oracle(orc, groups, seqs=None, threads=1):
     q = np.stack([np.stack([g.h_q(l, b) for b in seqs]) for g, l in layers])
     qI = np.stack([np.stack([g.h_qI(l, b) for b in seqs]) for g, l in layers])
     w = np.stack([np.stack([g.h_w(l, b) for b in seqs]) for g, l in layers])
-    swa = np.stack([np.stack([g.h_swa(l, b) for b in seqs]) for g, l in layers])
+    swa = np.stack([np.stack([g.h_win(l, b) for b in seqs]) for g, l in layers])
     qp = None if g0.q_pos is None else np.asarray(g0.q_pos, np.int32).reshape(g0.B, Nq)[seqs]
     return orc.group_step(modes, Ts, codes, scales, KI, q, qI, w, swa, g0.swa_len_np[seqs],
                           Nq=Nq, K=g0.K, W=g0.W, ratio=g0.ratio, hierarchical=g0.hierarchical,
-                          keep=g0.keep, q_pos=qp, softmax_scale=SCALE, threads=threads)
+                          keep=g0.keep, q_pos=qp, softmax_scale=SCALE, threads=threads, swa_fp8=g0.swa_fp8)
 
 
 def check_stack(orc, groups, seqs=None, threads=1):

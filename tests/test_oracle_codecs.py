@@ -225,3 +225,20 @@ def test_nibble_order_and_layout(orc):
     assert codes[0, 8] == (0x07 | (0x0D << 4))     # channels 16 (6.0) and 17 (-3.0)
     assert scales[0, 0] == 0x38 and scales[0, 1] == 0x38
     assert np.all(scales[0, 2:] == 0) and np.all(codes[0, 9:] == 0)
+
+
+def test_fp8_window_rows_every_bf16_value(orc):
+    """8-bit window rows: every finite bf16 value quantises to the nearest E4M3 value of its
+    magnitude (exact rationals; ties to the even code; saturating at 448) with its sign, a zero
+    result keeping the sign; dequantisation returns the E4M3 value exactly (in bf16)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f = syn.bf16_bits_to_f32(bits)
+    bits = bits[np.isfinite(f)]
+    f = f[np.isfinite(f)]
+    got = orc.fp8_quantize(bits)
+    sign = ((bits >> 15).astype(np.uint8) << 7)
+    exp = np.array([_e4m3_nearest_exact(Fraction(abs(float(v)))) for v in f], np.uint8) | sign
+    assert np.array_equal(got, exp)
+    back = syn.bf16_bits_to_f32(orc.fp8_dequantize(got)).astype(np.float64)
+    ref = _torch_e4m3(got)
+    assert np.array_equal(back, ref)
