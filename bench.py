@@ -238,6 +238,20 @@ def launches_per_step(c):
     return 5
 
 
+def max_over_ranks(torch, dist, value, world, device):
+    """The largest of a rank's `value` (a timed region in ms) over all ranks; every rank gets it."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(units_per_rank, world, ms_per_step):
+    """Whole-job rate: the units all ranks processed in one step over the (max-over-ranks) step time."""
+    return units_per_rank * world / (ms_per_step / 1e3)
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -285,10 +299,7 @@ def run_gpu(args, rank, world, local_rank):
     ms_total = e0.elapsed_time(e1)
     score_ms = [a.elapsed_time(b) for a, b in ev_pairs]
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(torch, dist, ms_total, world, dev)
 
     # ---- end to end through host buffers ---------------------------------------------------------
     L = N_LAYERS
@@ -329,10 +340,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = f0.elapsed_time(f1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(torch, dist, e2e_ms, world, dev)
     if sampler:
         sampler.stop()
     if rank != 0:
@@ -340,7 +348,7 @@ def run_gpu(args, rank, world, local_rank):
 
     ms_step = ms_total / K
     tokens = B_PER_GPU * world
-    value = tokens / (ms_step / 1e3)
+    value = throughput(B_PER_GPU, world, ms_step)
     kv_gbs = BYTES_PER_SEQ * B_PER_GPU * world / (ms_step / 1e3) / 1e9
     peak, peak_kind = peaks()
     score_avg = statistics.mean(score_ms)
@@ -377,7 +385,7 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": {"kernel": "index_score_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} (hbm copy)",
                      "traffic": traffic, "algorithmic_bytes": score_bytes, "avg_launch_ms": score_avg},
-        "e2e": {"value": tokens / (e2e_ms / K / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d * world,
+        "e2e": {"value": throughput(B_PER_GPU, world, e2e_ms / K), "unit": "tokens/s", "h2d_bytes_per_step": h2d * world,
                 "d2h_bytes_per_step": d2h * world, "ms_per_step": e2e_ms / K},
         "gpu_launches": launches_per_step(c) * K,
         "clocks": clocks,
