@@ -30,7 +30,8 @@ def nvcc() -> str:
 
 def _deps():
     files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, "common.cuh"), os.path.join(ROOT, "include", "csa2.h")]
+    files += [os.path.join(CSRC, h) for h in ("common.cuh", "attn_common.cuh")]
+    files += [os.path.join(ROOT, "include", "csa2.h")]
     return files
 
 
