@@ -62,18 +62,26 @@ inline bool prefill_path(int B, int Nq, int hierarchical, int64_t cap) {
          (cap + 31) / 32 <= prefill_max_groups();
 }
 
-// Attention workspace of a group step: tickets for rows * ns instances, then the split partials of
-// rows * ns instance-splits, ns being the split of one layer's rows.  A launch over several layers
-// that share their selected rows takes a split that fits (attn_ws_bytes(instances, split) within
-// these bytes); with a split above 1 its instances are at most rows * ns / 2, so its tickets fit.
-size_t group_attn_ws_bytes(int64_t rows, int K, int W, int n_split) {
-  const int ns = attn_effective_split(K, W, n_split ? n_split : attn_auto_split(rows, K, W));
-  if (ns <= 1) return attn_ticket_bytes(rows);
-  return attn_ticket_bytes(rows * ns) + (attn_ws_bytes(rows, ns) - attn_ticket_bytes(rows));
-}
+// Attention workspace of a group step.  One launch serves a run of L' layers that share their
+// selected rows, L' * rows instances at a split.  Tickets: for rows * max(ns, CSA2_MAX_LAYERS)
+// instances (ns: one layer's split).  Partials: with the automatic split, enough for a run of any
+// length L' <= CSA2_MAX_LAYERS at its own automatic split (about max(304, L' rows) instance-splits,
+// a few MB); with a forced split, for one layer's rows at that split (a longer run takes the
+// largest split that fits).
 size_t group_attn_ticket_bytes(int64_t rows, int K, int W, int n_split) {
   const int ns = attn_effective_split(K, W, n_split ? n_split : attn_auto_split(rows, K, W));
-  return attn_ticket_bytes(rows * std::max(ns, 1));
+  return attn_ticket_bytes(rows * std::max(ns, CSA2_MAX_LAYERS));
+}
+size_t group_attn_ws_bytes(int64_t rows, int K, int W, int n_split) {
+  auto partials = [&](int64_t inst, int ns) { return ns <= 1 ? size_t(0) : attn_ws_bytes(inst, ns) - attn_ticket_bytes(inst); };
+  size_t part = 0;
+  if (n_split) {
+    part = partials(rows, attn_effective_split(K, W, n_split));
+  } else {
+    for (int l = 1; l <= CSA2_MAX_LAYERS; ++l)
+      part = std::max(part, partials(l * rows, attn_effective_split(K, W, attn_auto_split(l * rows, K, W))));
+  }
+  return group_attn_ticket_bytes(rows, K, W, n_split) + part;
 }
 
 struct GroupWs {
