@@ -536,11 +536,63 @@ def run_fp8win(args):
             "peak_kind": f"{kind} (hbm copy)", "gpu_launches": launches_per_step(c) * args.steps}
 
 
+def run_hier1m(args):
+    """The hierarchical indexer at 1M context: batch 8, T = 2^20, ratio 1; Full (top 2048 blocks of 8
+    by block key, then Top-512 in the 16384-position pool) + Reindex (the same pool, its own indexer
+    Q) + 3 Reuse; each step appends the new token (refreshing the block it completes)."""
+    import torch
+
+    import csa2_synth as syn
+    import compressed_sparse_attention_step_gb300 as c
+    dev = torch.device("cuda")
+    seed = syn.SEEDS["hier_decode_b8_t1m"]
+    B, T, L, keep = 8, 1 << 20, 5, 2048
+    codes = torch.empty((B, T, 256), dtype=torch.uint8, device=dev)
+    scales = torch.empty((B, T, 32), dtype=torch.uint8, device=dev)
+    for b in range(B):
+        kv = syn.device_normal_bf16((1, T, 512), seed, syn.T_KV * 1000 + b, device=dev)
+        c.csa2_fp4_quantize_append(kv, codes[b:b + 1], scales[b:b + 1])
+        del kv
+    KI = syn.device_normal_bf16((B, T, 128), seed, syn.T_KI * 1000, device=dev)
+    lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+    block_keys = torch.empty((B, T // 8, 128), dtype=torch.bfloat16, device=dev)
+    c.csa2_block_keys_build(KI, lens, block_keys)
+    q = [syn.device_normal_bf16((B, 1, 16, 512), seed, syn.T_Q + l, device=dev) for l in range(L)]
+    qI = [syn.device_normal_bf16((B, 1, 4, 128), seed, syn.T_QI + l, device=dev) if l < 2 else None for l in range(L)]
+    w = [syn.device_normal_bf16((B, 1, 4), seed, syn.T_W + l, device=dev).float() if l < 2 else None for l in range(L)]
+    swa = [syn.device_normal_bf16((B, W_WIN, 512), seed, syn.T_SWA + l, device=dev) for l in range(L)]
+    out = [torch.empty((B, 1, 16, 512), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    idx = [torch.empty((B, K_SEL), dtype=torch.int32, device=dev) if l < 2 else None for l in range(L)]
+    swa_len = torch.full((B,), W_WIN, dtype=torch.int32, device=dev)
+    pool = torch.empty((B, keep * 8), dtype=torch.int32, device=dev)
+    pool_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    kv_new = syn.device_normal_bf16((B, 1, 512), seed, syn.T_KV_NEW, device=dev)
+    ki_new = syn.device_normal_bf16((B, 1, 128), seed, syn.T_KI_NEW, device=dev)
+    d = c.make_group_desc([c.MODE_FULL, c.MODE_REINDEX, c.MODE_REUSE, c.MODE_REUSE, c.MODE_REUSE], B=B, Nq=1, cap=T,
+                          lens=lens, codes=codes, scales=scales, KI=KI, q=q, qI=qI, w=w, swa=swa, swa_len=swa_len,
+                          out=out, idx=idx, K=K_SEL, W=W_WIN, hierarchical=True, keep=keep, block_keys=block_keys,
+                          pool=pool, pool_len=pool_len, kv_new=kv_new, ki_new=ki_new)
+    ws = torch.empty(c.group_workspace_size(B, 1, T, K_SEL, W_WIN, hierarchical=True, keep=keep), dtype=torch.uint8,
+                     device=dev)
+    ms = time_steps(torch, lambda: c.csa2_group_step(d, ws), args.steps, max(args.warmup, 3))
+    # algorithmic bytes per sequence: the block-key scan, the pool's indexer keys for Full and Reindex,
+    # five layers of attention, the append
+    per_seq = (T // 8) * 256 + 2 * keep * 8 * 256 + L * BYTES_ATTN_PER_SEQ_LAYER + BYTES_APPEND_PER_SEQ
+    peak, kind = peaks()
+    gbs = per_seq * B / (ms / 1e3) / 1e9
+    return {"metric": "CSA2 hierarchical decode tokens/s at 1M ctx", "value": B / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "higher_is_better": True,
+            "config": {"workload": "csa2_hier_decode_full_reindex_3reuse_b8_t1m", "global_batch": B, "seq_len": T,
+                       "layers": "Full + Reindex + 3 Reuse", "blocks_kept": keep, "pool": keep * 8, "top_k": K_SEL,
+                       "window": W_WIN},
+            "kv_gbs": gbs, "hbm_frac_step": gbs / peak, "bytes_per_step": per_seq * B, "peak_kind": f"{kind} (hbm copy)"}
+
+
 def run_extra(args):
     import torch
     torch.cuda.set_device(0)
     fn = {"decoder_stack_20": run_stack20, "prefill_chunk": run_prefill,
-          "decode_group_fp8win": run_fp8win}[args.workload]
+          "decode_group_fp8win": run_fp8win, "hier_decode_1m": run_hier1m}[args.workload]
     line = fn(args)
     line.update({"n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "scaling": "weak",
                  "vs_baseline": None, "dtype": "bf16/fp4 in, fp32 accumulate", "data": "synthetic",
@@ -559,7 +611,8 @@ def main():
                     help="sequences per GPU (64 is the workload; smaller values are for profiling)")
     ap.add_argument("--n-split", type=int, default=0, help="force the attention split-KV factor (profiling)")
     ap.add_argument("--workload", default="decode_group",
-                    choices=["decode_group", "decoder_stack_20", "prefill_chunk", "decode_group_fp8win"],
+                    choices=["decode_group", "decoder_stack_20", "prefill_chunk", "decode_group_fp8win",
+                             "hier_decode_1m"],
                     help="decode_group (default): the headline line; the others print their own line on one GPU")
     args = ap.parse_args()
     global B_PER_GPU, N_SPLIT
