@@ -28,33 +28,19 @@
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 512;          // CTA size
-constexpr int64_t kSlice = 32768;      // keys per slice CTA
+constexpr int kThreads = 512;          // CTA size of the one-CTA-per-row selections
 constexpr int kCandCap = 10240;        // candidates per row
 constexpr int kBins = 4096;            // first-level bins (top 12 key bits)
 constexpr int64_t kBitmapCols = 262144;   // rows up to this long are ordered through a bitmap
-constexpr int kRegSteps = 4;           // sweep steps of 16 keys per thread held in registers
-constexpr int64_t kRegSlice = int64_t(kRegSteps) * 16 * kThreads;  // = kSlice
-
-constexpr int kLocCap = 4096;           // candidates of one register-held slice
 
 struct SelSmem {
   static constexpr int kNT = kThreads;
   uint32_t hist[kBins];
+  uint32_t cand_key[kCandCap];
+  int32_t cand_col[kCandCap];
   union {
-    struct {  // selection: the whole-row path, long slices, and the last CTA of a row
-      uint32_t cand_key[kCandCap];
-      int32_t cand_col[kCandCap];
-      union {
-        int32_t sel[CSA2_MAX_K];
-        uint32_t bits[kBitmapCols / 32];
-      };
-    };
-    struct {  // a slice held in registers: its scores (thread-major) and its candidates
-      float slice_v[kRegSlice];
-      uint32_t loc_key[kLocCap];
-      int32_t loc_col[kLocCap];
-    };
+    int32_t sel[CSA2_MAX_K];
+    uint32_t bits[kBitmapCols / 32];
   };
   uint32_t scan_tmp[32];
   uint32_t nsel, ncand, base;
@@ -450,12 +436,13 @@ __device__ __noinline__ void select_row(SelSmem& sm, const float* s, int64_t nv,
 // The 16 scores thread t reads in one sweep step starting at b0: float4 number u * kThreads + t
 // (u < 4) of the step, i.e. v[4 u + e] = s[b0 + 4 (u kThreads + t) + e]; past hi they are NaN,
 // which every comparison rejects and fmaxf ignores.
+template <int NT = kThreads>
 __device__ __forceinline__ void load16(const float* s, int64_t b0, int64_t hi, float (&v)[16]) {
   const int t = threadIdx.x;
-  const bool full = b0 + int64_t(16) * kThreads <= hi && ((reinterpret_cast<uintptr_t>(s + b0) & 15u) == 0);
+  const bool full = b0 + int64_t(16) * NT <= hi && ((reinterpret_cast<uintptr_t>(s + b0) & 15u) == 0);
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    const int64_t i0 = b0 + (int64_t(u) * kThreads + t) * 4;
+    const int64_t i0 = b0 + (int64_t(u) * NT + t) * 4;
     if (full) {
       const float4 x = __ldg(reinterpret_cast<const float4*>(s + i0));
       v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
@@ -477,37 +464,117 @@ __device__ __forceinline__ int64_t row_valid(const int32_t* n_valid, int row, in
   return n_valid ? min(max(int64_t(n_valid[row]), int64_t(0)), n) : n;
 }
 
+// Rows up to kSmallRow entries: one CTA selects over the whole row.
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
     const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid, int k,
     const int32_t* __restrict__ map, int64_t map_ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
-    int expand8, int32_t* __restrict__ pool_len, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_col,
-    uint32_t* __restrict__ row_ctl /* [rows][2]: candidate count, ticket */,
-    uint32_t* __restrict__ row_hist /* [rows][4096]: group maxima by top 12 key bits */, int64_t slice_len) {
+    int expand8, int32_t* __restrict__ pool_len) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   pdl_wait();
   pdl_trigger();
-  const int row = blockIdx.y, nslices = gridDim.x;
-  const int t = threadIdx.x, lane = t & 31;
+  const int row = blockIdx.y, t = threadIdx.x;
   const float* s = scores + int64_t(row) * ld;
   const int64_t nv = row_valid(n_valid, row, n);
   __syncthreads();  // every thread has read n_valid before pool_len (possibly the same array) is written
   RowOut o{map ? map + int64_t(row) * map_ld : nullptr, idx + int64_t(row) * (expand8 ? k * CSA2_BLOCK : k),
            expand8 ? k * CSA2_BLOCK : k, expand8};
   if (nv <= k) {  // everything valid is selected, already ascending
-    if (blockIdx.x == 0) {
-      for (int i = t; i < nv; i += kThreads) o.emit(i, i);
-      finish_row(o, nv, row, n_sel, pool_len);
-    }
+    for (int i = t; i < nv; i += kThreads) o.emit(i, i);
+    finish_row(o, nv, row, n_sel, pool_len);
     return;
   }
-  if (nslices == 1) {
-    select_row(sm, s, nv, k, o);
-    finish_row(o, k, row, n_sel, pool_len);
-    return;
+  select_row(sm, s, nv, k, o);
+  finish_row(o, k, row, n_sel, pool_len);
+}
+
+// ---- rows longer than kSmallRow: the row's bound first, then only the keys above it are listed -----
+// 1. topk_hist_kernel: every CTA of a row adds the maxima of its slice's 16-key groups (the 16 keys a
+//    thread reads in one sweep step) to the row's histogram of the top 12 key bits;
+// 2. topk_filter_kernel: every CTA of the row takes the bin of the k-th largest group maximum (a
+//    lower bound on the k-th largest key: those k maxima are k distinct keys) from the complete
+//    histogram and appends the keys of its slice at or above that bin to the row's list, a superset
+//    of the Top-k;
+// 3. topk_select_kernel: one CTA per row selects among them (the whole row instead, should they
+//    overflow the list) and clears the histogram and counters for the next launch.
+constexpr int kHThreads = 256;
+constexpr int64_t kSmallRow = 8192;  // rows up to this long: one CTA selects over the whole row
+
+__global__ void __launch_bounds__(kHThreads) topk_hist_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
+                                                              const int32_t* __restrict__ n_valid, int k,
+                                                              int64_t slice_len, uint32_t* __restrict__ row_hist) {
+  __shared__ uint32_t h[kBins];
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.y, t = threadIdx.x, lane = t & 31;
+  const int64_t nv = row_valid(n_valid, row, n);
+  const int64_t lo = int64_t(blockIdx.x) * slice_len, hi = min(lo + slice_len, nv);
+  if (nv <= k || lo >= hi) return;
+  for (int i = t; i < kBins; i += kHThreads) h[i] = 0u;
+  __syncthreads();
+  const float* s = scores + int64_t(row) * ld;
+  for (int64_t b0 = lo; b0 < hi; b0 += int64_t(16) * kHThreads) {  // the same trip count for every thread
+    float v[16];
+    load16<kHThreads>(s, b0, hi, v);  // NaN past hi: fmaxf skips it
+    float gm = v[0];
+#pragma unroll
+    for (int e = 1; e < 16; ++e) gm = fmaxf(gm, v[e]);
+    const bool has = b0 + 4 * t < hi;
+    const uint32_t bin = has ? score_key(gm) >> 20 : 0xFFFFFFFFu;
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (has && (__ffs(peers) - 1) == lane) atomicAdd(&h[bin], uint32_t(__popc(peers)));
   }
-  // reserve `cnt` slots for this thread: one warp scan and one shared atomic per warp
-  auto reserve = [&](uint32_t cnt) {
+  __syncthreads();
+  uint32_t* gh = row_hist + int64_t(row) * kBins;
+  for (int i = t; i < kBins; i += kHThreads)
+    if (h[i]) atomicAdd(gh + i, h[i]);
+}
+
+__global__ void __launch_bounds__(kHThreads) topk_filter_kernel(const float* __restrict__ scores, int64_t n,
+                                                                int64_t ld, const int32_t* __restrict__ n_valid, int k,
+                                                                int64_t slice_len, const uint32_t* __restrict__ row_hist,
+                                                                uint32_t* __restrict__ cand_key,
+                                                                int32_t* __restrict__ cand_col,
+                                                                uint32_t* __restrict__ row_ctl) {
+  __shared__ __align__(16) uint32_t h[kBins];
+  __shared__ uint32_t scan_tmp[32];
+  __shared__ uint32_t res_bin, res_before;
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.y, t = threadIdx.x, lane = t & 31;
+  const int64_t nv = row_valid(n_valid, row, n);
+  const int64_t lo = int64_t(blockIdx.x) * slice_len, hi = min(lo + slice_len, nv);
+  if (nv <= k || lo >= hi) return;
+  const uint32_t* gh = row_hist + int64_t(row) * kBins;
+  uint32_t groups = 0;
+  for (int i = t; i < kBins; i += kHThreads) {
+    h[i] = __ldcg(gh + i);
+    groups += h[i];
+  }
+  groups = __reduce_add_sync(0xffffffffu, groups);
+  if (lane == 0) scan_tmp[t >> 5] = groups;
+  __syncthreads();
+  groups = 0;
+  for (int w = 0; w < kHThreads / 32; ++w) groups += scan_tmp[w];
+  __syncthreads();
+  uint32_t bound = 0;  // keys >= bound: a superset of the row's Top-k
+  if (groups >= uint32_t(k)) {
+    find_bin<kHThreads>(h, kBins, uint32_t(k), true, scan_tmp, &res_bin, &res_before);
+    bound = res_bin << 20;
+  }
+  const float fb = key_floor_score(bound);
+  const float* s = scores + int64_t(row) * ld;
+  uint32_t* ctl = row_ctl + 2 * int64_t(row);
+  uint32_t* ck = cand_key + int64_t(row) * kCandCap;
+  int32_t* cc = cand_col + int64_t(row) * kCandCap;
+  for (int64_t b0 = lo; b0 < hi; b0 += int64_t(16) * kHThreads) {
+    float v[16];
+    load16<kHThreads>(s, b0, hi, v);
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) m |= (v[e] >= fb) ? (1u << e) : 0u;  // NaN (past hi) fails
+    // one reservation per warp: a warp scan of the counts and one global add
+    const uint32_t cnt = __popc(m);
     uint32_t incl = cnt;
 #pragma unroll
     for (int o2 = 1; o2 < 32; o2 <<= 1) {
@@ -515,196 +582,63 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
       if (lane >= o2) incl += y;
     }
     const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+    if (!wtot) continue;
     uint32_t base = 0;
-    if (lane == 31 && wtot) base = atomicAdd(&sm.ncand, wtot);
-    return __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
-  };
-  uint32_t* ctl = row_ctl + 2 * int64_t(row);
-  // ---- phase 1: group maxima -> the slice's bound L -> keys >= L appended to the row's list ------
-  uint32_t* ghist = row_hist + int64_t(row) * kBins;
-  const int64_t lo = int64_t(blockIdx.x) * slice_len, hi = min(lo + slice_len, nv);
-  if (lo < hi) {
-    zero(sm.hist, kBins);
-    // A group: the (up to) 16 keys a thread reads in one sweep step of 4 x 4 x kThreads keys.  Its
-    // maximum is taken on the floats (same order as the keys for finite scores) and keyed once.
-    // A slice of at most kRegSlice keys is read once, into registers; longer ones are read twice.
-    const bool in_regs = hi - lo <= kRegSlice;
-    float rv[kRegSteps][16];
-    uint32_t ngroups = 0;
-    if (in_regs) {
+    if (lane == 31) base = atomicAdd(ctl, wtot);
+    base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
 #pragma unroll
-      for (int j = 0; j < kRegSteps; ++j) load16(s, lo + int64_t(j) * 16 * kThreads, hi, rv[j]);
-    }
-    for (int j = 0; j * int64_t(16) * kThreads < hi - lo; ++j) {
-      const int64_t b0 = lo + int64_t(j) * 16 * kThreads;
-      const int64_t firsts = (hi - b0 + 3) / 4;  // threads whose first key is < hi
-      ngroups += uint32_t(firsts < kThreads ? firsts : kThreads);
-      float v[16];
-      if (in_regs) {
-#pragma unroll
-        for (int jj = 0; jj < kRegSteps; ++jj)
-          if (jj == j) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = rv[jj][e];
-          }
-      } else {
-        load16(s, b0, hi, v);
-      }
-      float gm = v[0];
-#pragma unroll
-      for (int e = 1; e < 16; ++e) gm = fmaxf(gm, v[e]);
-      const bool has = b0 + 4 * t < hi;
-      const uint32_t bin = has ? score_key(gm) >> 20 : 0xFFFFFFFFu;
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (has && (__ffs(peers) - 1) == lane) atomicAdd(&sm.hist[bin], uint32_t(__popc(peers)));
-    }
-    __syncthreads();
-    for (int i = t; i < kBins; i += kThreads)
-      if (sm.hist[i]) atomicAdd(ghist + i, sm.hist[i]);
-    uint32_t bound = 0;  // keys >= bound: a superset of the slice's Top-K
-    if (ngroups >= uint32_t(k)) {
-      find_bin(sm.hist, kBins, uint32_t(k), true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
-      bound = sm.res_bin << 20;
-    }
-    if (t == 0) sm.ncand = 0;
-    __syncthreads();
-    // keys >= bound <=> scores >= fb (the smallest score with that key; -0 and +0 both pass at 0)
-    const float fb = key_floor_score(bound);
-    auto mask16 = [&](const float (&v)[16]) {
-      uint32_t m = 0;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) m |= (v[e] >= fb) ? (1u << e) : 0u;
-      return m;
-    };
-    auto emit16 = [&](const float (&v)[16], uint32_t m, int64_t b0, uint32_t& base) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        if (m & (1u << e)) {
-          if (base < uint32_t(kCandCap)) {
-            sm.cand_key[base] = score_key(v[e]);
-            sm.cand_col[base] = int32_t(b0 + 4 * ((e >> 2) * kThreads + t) + (e & 3));
-          }
-          ++base;
+    for (int e = 0; e < 16; ++e) {
+      if (m & (1u << e)) {
+        if (base < uint32_t(kCandCap)) {
+          ck[base] = score_key(v[e]);
+          cc[base] = int32_t(b0 + 4 * ((e >> 2) * kHThreads + t) + (e & 3));
         }
-      }
-    };
-    uint32_t* lkey = in_regs ? sm.loc_key : sm.cand_key;
-    int32_t* lcol = in_regs ? sm.loc_col : sm.cand_col;
-    const uint32_t lcap = in_regs ? uint32_t(kLocCap) : uint32_t(kCandCap);
-    if (in_regs) {
-      // scores to shared memory (thread-major: step j, value e of thread t at (16 j + e) kThreads + t)
-      // so that the few candidates can be read back by a dynamic index
-      uint32_t ms4[kRegSteps], cnt = 0;
-#pragma unroll
-      for (int j = 0; j < kRegSteps; ++j) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sm.slice_v[(16 * j + e) * kThreads + t] = rv[j][e];
-        ms4[j] = mask16(rv[j]);
-        cnt += __popc(ms4[j]);
-      }
-      uint32_t base = reserve(cnt);
-#pragma unroll
-      for (int j = 0; j < kRegSteps; ++j) {
-        uint32_t m = ms4[j];
-        while (m) {
-          const int e = __ffs(m) - 1;
-          m &= m - 1u;
-          if (base < lcap) {
-            lkey[base] = score_key(sm.slice_v[(16 * j + e) * kThreads + t]);
-            lcol[base] = int32_t(lo + int64_t(j) * 16 * kThreads + 4 * ((e >> 2) * kThreads + t) + (e & 3));
-          }
-          ++base;
-        }
-      }
-    } else {
-      for (int64_t b0 = lo; b0 < hi; b0 += int64_t(16) * kThreads) {
-        float v[16];
-        load16(s, b0, hi, v);
-        const uint32_t m = mask16(v);
-        uint32_t base = reserve(__popc(m));
-        emit16(v, m, b0, base);
-      }
-    }
-    __syncthreads();
-    const uint32_t nloc = sm.ncand;
-    if (t == 0)   // an oversized slice pushes the row's count past the list: whole-row path
-      sm.base = atomicAdd(ctl, nloc <= lcap ? nloc : uint32_t(kCandCap) + 1u);
-    __syncthreads();
-    if (nloc <= lcap) {
-      uint32_t* ck = cand_key + int64_t(row) * kCandCap;
-      int32_t* cc = cand_col + int64_t(row) * kCandCap;
-      for (uint32_t c = t; c < nloc; c += kThreads) {
-        const uint32_t dst = sm.base + c;
-        if (dst < uint32_t(kCandCap)) {
-          ck[dst] = lkey[c];
-          cc[dst] = lcol[c];
-        }
+        ++base;
       }
     }
   }
-  // ---- phase 2: the last slice CTA of the row selects ------------------------------------------
-  __threadfence();
-  __syncthreads();
-  if (t == 0) sm.is_last = (atomicAdd(ctl + 1, 1u) == unsigned(nslices - 1));
-  __syncthreads();
-  if (!sm.is_last) return;
-  __threadfence();
-  const uint32_t cnt = __ldcg(ctl);
-  if (cnt <= uint32_t(kCandCap)) {
-    // the row's bound: the same rule over the whole row's group maxima (>= every slice's bound)
-    uint32_t total = 0;
-    for (int i = t; i < kBins; i += kThreads) {
-      const uint32_t h = __ldcg(ghist + i);
-      sm.hist[i] = h;
-      total += h;
-    }
-    total = __reduce_add_sync(0xffffffffu, total);
-    if (lane == 0) sm.scan_tmp[t >> 5] = total;
-    __syncthreads();
-    total = 0;
-    for (int w = 0; w < kThreads / 32; ++w) total += sm.scan_tmp[w];
-    __syncthreads();
-    uint32_t bound = 0;
-    if (total >= uint32_t(k)) {
-      find_bin(sm.hist, kBins, uint32_t(k), true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
-      bound = sm.res_bin << 20;
-    }
-    if (t == 0) sm.ncand = 0;
-    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(
+    const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid, int k,
+    const int32_t* __restrict__ map, int64_t map_ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
+    int expand8, int32_t* __restrict__ pool_len, uint32_t* __restrict__ row_hist,
+    const uint32_t* __restrict__ cand_key, const int32_t* __restrict__ cand_col, uint32_t* __restrict__ row_ctl) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x, t = threadIdx.x;
+  const float* s = scores + int64_t(row) * ld;
+  const int64_t nv = row_valid(n_valid, row, n);
+  __syncthreads();  // every thread has read n_valid before pool_len (possibly the same array) is written
+  RowOut o{map ? map + int64_t(row) * map_ld : nullptr, idx + int64_t(row) * (expand8 ? k * CSA2_BLOCK : k),
+           expand8 ? k * CSA2_BLOCK : k, expand8};
+  if (nv <= k) {  // everything valid is selected, already ascending
+    for (int i = t; i < nv; i += kThreads) o.emit(i, i);
+    finish_row(o, nv, row, n_sel, pool_len);
+    return;
+  }
+  const uint32_t total = __ldcg(row_ctl + 2 * int64_t(row));
+  if (total <= uint32_t(kCandCap)) {
     const uint32_t* ck = cand_key + int64_t(row) * kCandCap;
     const int32_t* cc = cand_col + int64_t(row) * kCandCap;
-    constexpr int kB = 8;  // candidates per thread per batch, all loads in flight together
-    for (int i0 = 0; i0 < int(cnt); i0 += kB * kThreads) {
-      uint32_t key[kB];
-      int32_t col[kB];
-#pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        const int i = i0 + u * kThreads + t;
-        key[u] = i < int(cnt) ? __ldcg(ck + i) : 0u;
-        col[u] = i < int(cnt) ? __ldcg(cc + i) : 0;
-      }
-      uint32_t m = 0;
-#pragma unroll
-      for (int u = 0; u < kB; ++u) m |= (i0 + u * kThreads + t < int(cnt) && key[u] >= bound) ? (1u << u) : 0u;
-      uint32_t base = reserve(__popc(m));
-#pragma unroll
-      for (int u = 0; u < kB; ++u)
-        if (m & (1u << u)) {
-          sm.cand_key[base] = key[u];
-          sm.cand_col[base] = col[u];
-          ++base;
-        }
+    for (uint32_t c = t; c < total; c += kThreads) {
+      sm.cand_key[c] = __ldcg(ck + c);
+      sm.cand_col[c] = __ldcg(cc + c);
     }
     __syncthreads();
-    select_candidates(sm, int(sm.ncand), k, nv, o);
+    select_candidates(sm, int(total), k, nv, o);
   } else {
     select_row(sm, s, nv, k, o);
   }
   finish_row(o, k, row, n_sel, pool_len);
-  for (int i = t; i < kBins; i += kThreads) ghist[i] = 0u;
+  // the next launch finds the histogram and the counters zero
+  uint32_t* gh = row_hist + int64_t(row) * kBins;
+  for (int i = t; i < kBins; i += kThreads) gh[i] = 0u;
   if (t == 0) {
-    ctl[0] = 0u;
-    ctl[1] = 0u;
+    row_ctl[2 * int64_t(row)] = 0u;
+    row_ctl[2 * int64_t(row) + 1] = 0u;
   }
 }
 
@@ -837,18 +771,13 @@ __global__ void __launch_bounds__(kBmThreads, 2) bitmap_select_kernel(
 
 }  // namespace
 
-int topk_slices(int64_t n, int k) {
-  const int64_t by_len = (n + kSlice - 1) / kSlice;
-  const int64_t by_cap = std::max<int64_t>(1, kCandCap / (int64_t(k) + 1024));  // k - 1 + |bin| per slice
-  return int(std::max<int64_t>(1, std::min(by_len, by_cap)));
-}
-
 size_t topk_counters_offset(int rows) { return size_t(rows) * kCandCap * (sizeof(uint32_t) + sizeof(int32_t)); }
 
-// workspace: candidate keys and columns per row, then (count, ticket) per row, then the row
-// histograms of group maxima (the last two zeroed before each launch)
+// workspace (rows longer than kSmallRow): candidate keys and columns per row, then (count, ticket)
+// per row, then the row histograms of group maxima (the last two zero before each launch; every
+// launch leaves them zero)
 size_t topk_ws_bytes(int rows, int64_t n) {
-  if (n <= kSlice) return 0;
+  if (n <= kSmallRow) return 0;
   return size_t(rows) * (kCandCap * (sizeof(uint32_t) + sizeof(int32_t)) + 2 * sizeof(uint32_t) +
                          kBins * sizeof(uint32_t));
 }
@@ -866,26 +795,37 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  int nslices = 1;
-  int64_t slice_len = n;
-  uint32_t *ckey = nullptr, *ctl = nullptr, *hist = nullptr;
-  int32_t* ccol = nullptr;
-  if (topk_ws_bytes(rows, n) > 0) {
-    if (!ws) return cudaErrorInvalidValue;
-    nslices = topk_slices(n, k);
-    slice_len = ((n + nslices - 1) / nslices + 3) / 4 * 4;   // the slices cover the row; 16-byte starts
-    ckey = static_cast<uint32_t*>(ws);
-    ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);
-    ctl = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
-    hist = ctl + size_t(rows) * 2;
-    if (!counters_zeroed) {
-      cudaError_t e = cudaMemsetAsync(ctl, 0, size_t(rows) * (2 + kBins) * sizeof(uint32_t), st);
-      if (e != cudaSuccess) return e;
-    }
+  if (topk_ws_bytes(rows, n) == 0)  // one CTA per row over the whole row
+    return launch_pdl(topk_kernel, dim3(1u, unsigned(rows), 1u), dim3(kThreads), smem, st, scores, n, ld, n_valid, k,
+                      map, map_ld, idx, n_sel, expand8, pool_len);
+  if (!ws) return cudaErrorInvalidValue;
+  uint32_t* ckey = static_cast<uint32_t*>(ws);
+  int32_t* ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);
+  uint32_t* ctl = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
+  uint32_t* hist = ctl + size_t(rows) * 2;
+  if (!counters_zeroed) {
+    cudaError_t e = cudaMemsetAsync(ctl, 0, size_t(rows) * (2 + kBins) * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
   }
-  const dim3 grid{unsigned(nslices), unsigned(rows), 1u};
-  return launch_pdl(topk_kernel, grid, dim3(kThreads), smem, st, scores, n, ld, n_valid, k, map, map_ld, idx, n_sel,
-                    expand8, pool_len, ckey, ccol, ctl, hist, slice_len);
+  static bool sel_attr[64] = {};
+  if (dev < 64 && !sel_attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    sel_attr[dev] = true;
+  }
+  // slices: about four CTAs of 256 threads per SM over all rows, at least 2048 keys each
+  const int64_t want = std::max<int64_t>(1, (4 * 152 + rows - 1) / rows);
+  const int64_t nsl = std::max<int64_t>(1, std::min(want, (n + 2047) / 2048));
+  const int64_t slice_len = ((n + nsl - 1) / nsl + 63) / 64 * 64;  // 16-byte aligned slice starts
+  const dim3 grid{unsigned(nsl), unsigned(rows), 1u};
+  cudaError_t e = launch_pdl(topk_hist_kernel, grid, dim3(kHThreads), 0, st, scores, n, ld, n_valid, k, slice_len, hist);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(topk_filter_kernel, grid, dim3(kHThreads), 0, st, scores, n, ld, n_valid, k, slice_len,
+                 static_cast<const uint32_t*>(hist), ckey, ccol, ctl);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(topk_select_kernel, dim3(unsigned(rows)), dim3(kThreads), smem, st, scores, n, ld, n_valid, k, map,
+                    map_ld, idx, n_sel, expand8, pool_len, hist, static_cast<const uint32_t*>(ckey),
+                    static_cast<const int32_t*>(ccol), ctl);
 }
 
 cudaError_t launch_bitmap_select(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
