@@ -545,11 +545,16 @@ __global__ void __launch_bounds__(kHThreads) topk_filter_kernel(const float* __r
   const int64_t nv = row_valid(n_valid, row, n);
   const int64_t lo = int64_t(blockIdx.x) * slice_len, hi = min(lo + slice_len, nv);
   if (nv <= k || lo >= hi) return;
-  const uint32_t* gh = row_hist + int64_t(row) * kBins;
+  // the row's histogram: four 16-byte loads per thread, all in flight together
+  const uint4* gh4 = reinterpret_cast<const uint4*>(row_hist + int64_t(row) * kBins);
+  uint4 hv[kBins / 4 / kHThreads];
+#pragma unroll
+  for (int u = 0; u < kBins / 4 / kHThreads; ++u) hv[u] = __ldcg(gh4 + u * kHThreads + t);
   uint32_t groups = 0;
-  for (int i = t; i < kBins; i += kHThreads) {
-    h[i] = __ldcg(gh + i);
-    groups += h[i];
+#pragma unroll
+  for (int u = 0; u < kBins / 4 / kHThreads; ++u) {
+    reinterpret_cast<uint4*>(h)[u * kHThreads + t] = hv[u];
+    groups += hv[u].x + hv[u].y + hv[u].z + hv[u].w;
   }
   groups = __reduce_add_sync(0xffffffffu, groups);
   if (lane == 0) scan_tmp[t >> 5] = groups;
@@ -772,14 +777,17 @@ __global__ void __launch_bounds__(kBmThreads, 2) bitmap_select_kernel(
 }  // namespace
 
 size_t topk_counters_offset(int rows) { return size_t(rows) * kCandCap * (sizeof(uint32_t) + sizeof(int32_t)); }
+// (count, ticket) per row, padded to a multiple of four words so that the histograms after them
+// start on a 16-byte boundary
+inline size_t topk_ctl_words(int rows) { return (size_t(rows) * 2 + 3) / 4 * 4; }
 
 // workspace (rows longer than kSmallRow): candidate keys and columns per row, then (count, ticket)
 // per row, then the row histograms of group maxima (the last two zero before each launch; every
 // launch leaves them zero)
 size_t topk_ws_bytes(int rows, int64_t n) {
   if (n <= kSmallRow) return 0;
-  return size_t(rows) * (kCandCap * (sizeof(uint32_t) + sizeof(int32_t)) + 2 * sizeof(uint32_t) +
-                         kBins * sizeof(uint32_t));
+  return size_t(rows) * (kCandCap * (sizeof(uint32_t) + sizeof(int32_t)) + kBins * sizeof(uint32_t)) +
+         topk_ctl_words(rows) * sizeof(uint32_t);
 }
 
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
@@ -802,9 +810,9 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
   uint32_t* ckey = static_cast<uint32_t*>(ws);
   int32_t* ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);
   uint32_t* ctl = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
-  uint32_t* hist = ctl + size_t(rows) * 2;
+  uint32_t* hist = ctl + topk_ctl_words(rows);
   if (!counters_zeroed) {
-    cudaError_t e = cudaMemsetAsync(ctl, 0, size_t(rows) * (2 + kBins) * sizeof(uint32_t), st);
+    cudaError_t e = cudaMemsetAsync(ctl, 0, (topk_ctl_words(rows) + size_t(rows) * kBins) * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
   }
   static bool sel_attr[64] = {};
