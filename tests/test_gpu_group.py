@@ -49,6 +49,16 @@ def test_decode_group_pipelined_sequence_chunks(orc):
         gc.check(orc)
 
 
+def test_decode_group_long_rows_ragged(orc):
+    """Contexts above 8192 entries (the score scan also writes the Top-K's group keys), ragged,
+    some below k groups of 16, with a Reindex layer; unchunked and in three sequence chunks (each
+    chunk's rows of the group keys are its own)."""
+    gc = GroupCase(58, [20000, 9000, 8193, 3000, 12345], [F, R, RX, R])
+    for chunks in (1, 3):
+        gc.run(seq_chunks=chunks)
+        gc.check(orc)
+
+
 def test_hierarchical_group_pipelined_sequence_chunks(orc):
     gc = GroupCase(57, [8 * 3000, 8 * 2300 + 5, 8 * 900 + 1], [F, RX, R], hierarchical=True)
     gc.run(seq_chunks=2)

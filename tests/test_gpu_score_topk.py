@@ -110,6 +110,26 @@ def test_topk_matches_oracle(orc, n, k):
         assert np.array_equal(idx[r], exp), r
 
 
+def test_topk_long_rows_bound_and_overflow(orc):
+    """Rows longer than 8192 columns, at the edges of the group-key bound: fewer than k groups of
+    16 (every key is a candidate; the list holds them, or overflows to the whole-row selection),
+    a valid prefix one past a group, all keys equal over 262144 columns (more groups at the bound
+    than the group list holds), and a row where only the top group keys' bin survives."""
+    g = np.random.default_rng(11)
+    n, k = 262144, 2048
+    s = np.stack([g.standard_normal(n).astype(np.float32) for _ in range(4)] +
+                 [np.full(n, -1.25, np.float32), (g.standard_normal(n) * 1e-4).astype(np.float32)])
+    nvalid = np.array([9000, 20000, 16 * 2048 + 1, 8193, n, n - 3], np.int32)
+    idx = torch.full((s.shape[0], k), -5, dtype=torch.int32, device="cuda")
+    nsel = torch.zeros(s.shape[0], dtype=torch.int32, device="cuda")
+    c.csa2_topk(to_dev(s), k, idx, n_valid=to_dev(nvalid), n_sel=nsel)
+    idx, nsel = idx.cpu().numpy(), nsel.cpu().numpy()
+    for r in range(s.shape[0]):
+        exp, cnt = orc.topk(s[r, :nvalid[r]], k)
+        assert nsel[r] == cnt
+        assert np.array_equal(idx[r], exp), r
+
+
 def test_topk_with_map(orc):
     g = np.random.default_rng(5)
     n, k = 16384, 512
