@@ -235,17 +235,118 @@ __device__ __forceinline__ void candidate_cut(S& sm, int nc, int k, uint32_t& ta
   cut_out = col_cut;
 }
 
+// Position of the n-th set bit (from 0) of m (n < popcount(m)), by halving.
+__device__ __forceinline__ int nth_set_bit(uint32_t m, int n) {
+  int pos = 0;
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) {
+    const uint32_t low = (1u << s) - 1u;
+    const int c = __popc(m & low);
+    if (n >= c) {
+      n -= c;
+      m >>= s;
+      pos += s;
+    } else {
+      m &= low;
+    }
+  }
+  return pos;
+}
+
+// Emits the first cnt set columns of the bitmap sm.bits (nwords words, zero up to per * NT words,
+// per a power of two <= 8) in column order: out slot r gets the column of rank r.  Each thread
+// owns a run of per words; the words' exclusive prefix counts go to sm.hist, and every rank is
+// placed by a binary search over them, so the work does not depend on where the columns lie.
+template <class S>
+__device__ __forceinline__ void emit_by_rank(S& sm, int nwords, int per, int cnt, const RowOut& o) {
+  const int t = threadIdx.x;
+  uint32_t wv[8];
+  const uint32_t* run = sm.bits + t * per;
+  if (per >= 4) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (4 * q < per) {
+        const uint4 a = reinterpret_cast<const uint4*>(run)[q];
+        wv[4 * q] = a.x; wv[4 * q + 1] = a.y; wv[4 * q + 2] = a.z; wv[4 * q + 3] = a.w;
+      }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      if (e < per) wv[e] = run[e];
+  }
+  uint32_t local = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (e < per) local += __popc(wv[e]);
+  uint32_t pre = block_exclusive_scan(local, sm.scan_tmp, nullptr);
+  uint32_t* pw = sm.hist;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (e < per) {
+      pw[t * per + e] = pre;
+      pre += __popc(wv[e]);
+    }
+  __syncthreads();
+  for (int r = t; r < cnt; r += blockDim.x) {
+    int lo = 0, hi = nwords - 1;  // the last word whose prefix is <= r holds rank r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pw[mid] <= uint32_t(r)) lo = mid;
+      else hi = mid - 1;
+    }
+    o.emit(r, int32_t(lo * 32 + nth_set_bit(sm.bits[lo], r - int(pw[lo]))));
+  }
+}
+
 // The k largest of the nc candidates in shared memory (nc >= k) by (key desc, column asc), emitted
 // in column order; columns are < ncols.
 template <class S>
 __device__ __noinline__ void select_candidates(S& sm, int nc, int k, int64_t ncols, const RowOut o) {
-  const int t = threadIdx.x;
-  uint32_t tau;
-  int32_t col_cut;
-  candidate_cut(sm, nc, k, tau, col_cut);
+  const int t = threadIdx.x, lane = t & 31;
+  // A list of one key (all candidates tie, as the exact zeros of a row whose head weights are all
+  // negative do): the k lowest columns win, with no radix rounds.
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int c = t; c < nc; c += blockDim.x) {
+    const uint32_t key = sm.cand_key[c];
+    kmin = min(kmin, key);
+    kmax = max(kmax, key);
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (t == 0) {
+    sm.run_g = 0xFFFFFFFFu;
+    sm.run_e = 0u;
+  }
+  __syncthreads();
+  if (lane == 0) {
+    atomicMin(&sm.run_g, kmin);
+    atomicMax(&sm.run_e, kmax);
+  }
+  __syncthreads();
+  const bool one_key = sm.run_g == sm.run_e;
+  uint32_t tau = sm.run_g;
+  int32_t col_cut = 0x7FFFFFFF;
+  __syncthreads();
+  const int nwords = int((ncols + 31) / 32);
+  int per = 1;
+  while (per * int(blockDim.x) < nwords) per <<= 1;
+  const bool rank_emit = per <= 8 && per * int(blockDim.x) <= kBins;
+  if (!(one_key && rank_emit)) candidate_cut(sm, nc, k, tau, col_cut);
+  if (rank_emit) {
+    // bitmap of the winners (of every candidate for one key), then the first k ranks
+    for (int i = t; i < per * int(blockDim.x); i += blockDim.x) sm.bits[i] = 0u;
+    __syncthreads();
+    for (int c = t; c < nc; c += blockDim.x) {
+      const uint32_t key = sm.cand_key[c];
+      const int32_t col = sm.cand_col[c];
+      if (key > tau || (key == tau && col <= col_cut)) atomicOr(&sm.bits[col >> 5], 1u << (col & 31));
+    }
+    __syncthreads();
+    emit_by_rank(sm, nwords, per, k, o);
+    return;
+  }
   if (ncols <= kBitmapCols) {
     // slot of a winner = number of winners in lower columns: bitmap + prefix popcounts
-    const int nwords = int((ncols + 31) / 32);
     for (int i = t; i < nwords; i += blockDim.x) sm.bits[i] = 0u;
     __syncthreads();
     for (int c = t; c < nc; c += blockDim.x) {
@@ -254,15 +355,15 @@ __device__ __noinline__ void select_candidates(S& sm, int nc, int k, int64_t nco
       if (key > tau || (key == tau && col <= col_cut)) atomicOr(&sm.bits[col >> 5], 1u << (col & 31));
     }
     __syncthreads();
-    const int per = (nwords + int(blockDim.x) - 1) / int(blockDim.x);
+    const int per2 = (nwords + int(blockDim.x) - 1) / int(blockDim.x);
     uint32_t local = 0;
-    for (int e = 0; e < per; ++e) {
-      const int wi = t * per + e;
+    for (int e = 0; e < per2; ++e) {
+      const int wi = t * per2 + e;
       if (wi < nwords) local += __popc(sm.bits[wi]);
     }
     uint32_t slot = block_exclusive_scan(local, sm.scan_tmp, nullptr);
-    for (int e = 0; e < per; ++e) {
-      const int wi = t * per + e;
+    for (int e = 0; e < per2; ++e) {
+      const int wi = t * per2 + e;
       if (wi >= nwords) break;
       uint32_t wv = sm.bits[wi];
       while (wv) {
@@ -628,9 +729,26 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(
   if (total <= uint32_t(kCandCap)) {
     const uint32_t* ck = cand_key + int64_t(row) * kCandCap;
     const int32_t* cc = cand_col + int64_t(row) * kCandCap;
-    for (uint32_t c = t; c < total; c += kThreads) {
-      sm.cand_key[c] = __ldcg(ck + c);
-      sm.cand_col[c] = __ldcg(cc + c);
+    // the list in 16-byte pieces, all of a thread's loads in flight together (rows start 16-byte
+    // aligned: kCandCap is a multiple of 4)
+    constexpr int kPieces = (kCandCap / 4 + kThreads - 1) / kThreads;
+    const uint32_t np = (total + 3) / 4;
+    uint4 pa[kPieces], pb[kPieces];
+#pragma unroll
+    for (int u = 0; u < kPieces; ++u) {
+      const uint32_t pi = u * kThreads + t;
+      if (pi < np) {
+        pa[u] = __ldcg(reinterpret_cast<const uint4*>(ck) + pi);
+        pb[u] = __ldcg(reinterpret_cast<const uint4*>(cc) + pi);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPieces; ++u) {
+      const uint32_t pi = u * kThreads + t;
+      if (pi < np) {
+        reinterpret_cast<uint4*>(sm.cand_key)[pi] = pa[u];
+        reinterpret_cast<uint4*>(sm.cand_col)[pi] = pb[u];
+      }
     }
     __syncthreads();
     select_candidates(sm, int(total), k, nv, o);
