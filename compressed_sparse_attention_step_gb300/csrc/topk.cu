@@ -595,15 +595,19 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(
 // 2. topk_filter_kernel: every CTA of the row takes the bin of the k-th largest group maximum (a
 //    lower bound on the k-th largest key: those k maxima are k distinct keys) from the complete
 //    histogram and appends the keys of its slice at or above that bin to the row's list, a superset
-//    of the Top-k;
+//    of the Top-k.  It reads the scores of only the groups whose maximum (kept by the histogram
+//    kernel) reaches the bound: every key at or above it lies in one of them;
 // 3. topk_select_kernel: one CTA per row selects among them (the whole row instead, should they
 //    overflow the list) and clears the histogram and counters for the next launch.
 constexpr int kHThreads = 256;
 constexpr int64_t kSmallRow = 8192;  // rows up to this long: one CTA selects over the whole row
+constexpr int64_t kSweep = int64_t(16) * kHThreads;  // keys of one sweep step of a slice CTA
+constexpr int kFSweeps = 4;          // sweeps whose groups the filter lists at once (4 * kHThreads <= kBins)
 
 __global__ void __launch_bounds__(kHThreads) topk_hist_kernel(const float* __restrict__ scores, int64_t n, int64_t ld,
                                                               const int32_t* __restrict__ n_valid, int k,
-                                                              int64_t slice_len, uint32_t* __restrict__ row_hist) {
+                                                              int64_t slice_len, uint32_t* __restrict__ row_hist,
+                                                              uint32_t* __restrict__ gkey, int64_t gld) {
   __shared__ uint32_t h[kBins];
   pdl_wait();
   pdl_trigger();
@@ -621,7 +625,9 @@ __global__ void __launch_bounds__(kHThreads) topk_hist_kernel(const float* __res
 #pragma unroll
     for (int e = 1; e < 16; ++e) gm = fmaxf(gm, v[e]);
     const bool has = b0 + 4 * t < hi;
-    const uint32_t bin = has ? score_key(gm) >> 20 : 0xFFFFFFFFu;
+    const uint32_t gmk = score_key(gm);
+    if (has) gkey[int64_t(row) * gld + (b0 / kSweep) * kHThreads + t] = gmk;
+    const uint32_t bin = has ? gmk >> 20 : 0xFFFFFFFFu;
     const unsigned peers = __match_any_sync(0xffffffffu, bin);
     if (has && (__ffs(peers) - 1) == lane) atomicAdd(&h[bin], uint32_t(__popc(peers)));
   }
@@ -634,12 +640,13 @@ __global__ void __launch_bounds__(kHThreads) topk_hist_kernel(const float* __res
 __global__ void __launch_bounds__(kHThreads) topk_filter_kernel(const float* __restrict__ scores, int64_t n,
                                                                 int64_t ld, const int32_t* __restrict__ n_valid, int k,
                                                                 int64_t slice_len, const uint32_t* __restrict__ row_hist,
+                                                                const uint32_t* __restrict__ gkey, int64_t gld,
                                                                 uint32_t* __restrict__ cand_key,
                                                                 int32_t* __restrict__ cand_col,
                                                                 uint32_t* __restrict__ row_ctl) {
-  __shared__ __align__(16) uint32_t h[kBins];
+  __shared__ __align__(16) uint32_t h[kBins];  // the row histogram, then the chunk's group list
   __shared__ uint32_t scan_tmp[32];
-  __shared__ uint32_t res_bin, res_before;
+  __shared__ uint32_t res_bin, res_before, s_base;
   pdl_wait();
   pdl_trigger();
   const int row = blockIdx.y, t = threadIdx.x, lane = t & 31;
@@ -670,38 +677,73 @@ __global__ void __launch_bounds__(kHThreads) topk_filter_kernel(const float* __r
   }
   const float fb = key_floor_score(bound);
   const float* s = scores + int64_t(row) * ld;
+  const bool vec = (reinterpret_cast<uintptr_t>(s) & 15u) == 0;  // slices start at multiples of kSweep keys
+  const uint32_t* gk = gkey + int64_t(row) * gld;
   uint32_t* ctl = row_ctl + 2 * int64_t(row);
   uint32_t* ck = cand_key + int64_t(row) * kCandCap;
   int32_t* cc = cand_col + int64_t(row) * kCandCap;
-  for (int64_t b0 = lo; b0 < hi; b0 += int64_t(16) * kHThreads) {
-    float v[16];
-    load16<kHThreads>(s, b0, hi, v);
-    uint32_t m = 0;
+  for (int64_t c0 = lo; c0 < hi; c0 += int64_t(kFSweeps) * kSweep) {  // the same trip count for every thread
+    // 1. the chunk's groups whose key reaches the bound (group q * kHThreads + t: the 16 keys thread t
+    //    of the histogram kernel took in sweep q), listed in shared memory
+    uint32_t take = 0;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) m |= (v[e] >= fb) ? (1u << e) : 0u;  // NaN (past hi) fails
-    // one reservation per warp: a warp scan of the counts and one global add
-    const uint32_t cnt = __popc(m);
-    uint32_t incl = cnt;
-#pragma unroll
-    for (int o2 = 1; o2 < 32; o2 <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o2);
-      if (lane >= o2) incl += y;
+    for (int q = 0; q < kFSweeps; ++q) {
+      const int64_t b0 = c0 + int64_t(q) * kSweep;
+      if (b0 + 4 * t < hi && __ldcg(gk + (b0 / kSweep) * kHThreads + t) >= bound) take |= 1u << q;
     }
-    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
-    if (!wtot) continue;
-    uint32_t base = 0;
-    if (lane == 31) base = atomicAdd(ctl, wtot);
-    base = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+    uint32_t nlist;
+    uint32_t slot = block_exclusive_scan(uint32_t(__popc(take)), scan_tmp, &nlist);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      if (m & (1u << e)) {
-        if (base < uint32_t(kCandCap)) {
-          ck[base] = score_key(v[e]);
-          cc[base] = int32_t(b0 + 4 * ((e >> 2) * kHThreads + t) + (e & 3));
+    for (int q = 0; q < kFSweeps; ++q)
+      if ((take >> q) & 1u) h[slot++] = uint32_t(q * kHThreads + t);
+    __syncthreads();
+    // 2. their keys, a quarter group (four consecutive keys) per item and four items per thread in
+    //    flight; one reservation per CTA and batch
+    const int items = int(nlist) * 4;
+    for (int i0 = 0; i0 < items; i0 += 4 * kHThreads) {
+      float v[4][4];
+      int64_t col[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = i0 + u * kHThreads + t;
+        col[u] = hi;
+        if (it < items) {
+          const uint32_t g = h[it >> 2];
+          col[u] = c0 + int64_t(g / kHThreads) * kSweep + 4 * (int64_t(it & 3) * kHThreads + (g % kHThreads));
         }
-        ++base;
+        if (vec && col[u] + 3 < hi) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(s + col[u]));
+          v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[u][e] = (col[u] + e < hi) ? __ldcg(s + col[u] + e) : __int_as_float(0x7FC00000);
+        }
       }
+      uint32_t m = 0;  // bit 4u+e: key v[u][e] is listed (NaN, past hi, fails)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) m |= (v[u][e] >= fb) ? 1u << (4 * u + e) : 0u;
+      uint32_t tot;
+      uint32_t base = block_exclusive_scan(uint32_t(__popc(m)), scan_tmp, &tot);
+      if (tot == 0) continue;
+      if (t == 0) s_base = atomicAdd(ctl, tot);
+      __syncthreads();
+      base += s_base;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((m >> (4 * u + e)) & 1u) {
+            if (base < uint32_t(kCandCap)) {
+              ck[base] = score_key(v[u][e]);
+              cc[base] = int32_t(col[u] + e);
+            }
+            ++base;
+          }
+      __syncthreads();  // s_base is read by every thread before the next reservation
     }
+    __syncthreads();  // the group list is rewritten by the next chunk
   }
 }
 
@@ -899,13 +941,16 @@ size_t topk_counters_offset(int rows) { return size_t(rows) * kCandCap * (sizeof
 // start on a 16-byte boundary
 inline size_t topk_ctl_words(int rows) { return (size_t(rows) * 2 + 3) / 4 * 4; }
 
+// group keys per row: one per thread and sweep step
+inline int64_t topk_group_ld(int64_t n) { return (n + kSweep - 1) / kSweep * kHThreads; }
+
 // workspace (rows longer than kSmallRow): candidate keys and columns per row, then (count, ticket)
 // per row, then the row histograms of group maxima (the last two zero before each launch; every
-// launch leaves them zero)
+// launch leaves them zero), then the group keys (written before they are read in every launch)
 size_t topk_ws_bytes(int rows, int64_t n) {
   if (n <= kSmallRow) return 0;
   return size_t(rows) * (kCandCap * (sizeof(uint32_t) + sizeof(int32_t)) + kBins * sizeof(uint32_t)) +
-         topk_ctl_words(rows) * sizeof(uint32_t);
+         topk_ctl_words(rows) * sizeof(uint32_t) + size_t(rows) * size_t(topk_group_ld(n)) * sizeof(uint32_t);
 }
 
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
@@ -929,6 +974,8 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
   int32_t* ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);
   uint32_t* ctl = reinterpret_cast<uint32_t*>(ccol + size_t(rows) * kCandCap);
   uint32_t* hist = ctl + topk_ctl_words(rows);
+  uint32_t* gkey = hist + size_t(rows) * kBins;
+  const int64_t gld = topk_group_ld(n);
   if (!counters_zeroed) {
     cudaError_t e = cudaMemsetAsync(ctl, 0, (topk_ctl_words(rows) + size_t(rows) * kBins) * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
@@ -939,15 +986,17 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
     if (e != cudaSuccess) return e;
     sel_attr[dev] = true;
   }
-  // slices: about four CTAs of 256 threads per SM over all rows, at least 2048 keys each
+  // slices: about four CTAs of 256 threads per SM over all rows, whole sweep steps of kSweep keys
   const int64_t want = std::max<int64_t>(1, (4 * 152 + rows - 1) / rows);
-  const int64_t nsl = std::max<int64_t>(1, std::min(want, (n + 2047) / 2048));
-  const int64_t slice_len = ((n + nsl - 1) / nsl + 63) / 64 * 64;  // 16-byte aligned slice starts
+  const int64_t sweeps = (n + kSweep - 1) / kSweep;
+  const int64_t slice_len = (sweeps + want - 1) / want * kSweep;
+  const int64_t nsl = (n + slice_len - 1) / slice_len;
   const dim3 grid{unsigned(nsl), unsigned(rows), 1u};
-  cudaError_t e = launch_pdl(topk_hist_kernel, grid, dim3(kHThreads), 0, st, scores, n, ld, n_valid, k, slice_len, hist);
+  cudaError_t e = launch_pdl(topk_hist_kernel, grid, dim3(kHThreads), 0, st, scores, n, ld, n_valid, k, slice_len, hist,
+                             gkey, gld);
   if (e != cudaSuccess) return e;
   e = launch_pdl(topk_filter_kernel, grid, dim3(kHThreads), 0, st, scores, n, ld, n_valid, k, slice_len,
-                 static_cast<const uint32_t*>(hist), ckey, ccol, ctl);
+                 static_cast<const uint32_t*>(hist), static_cast<const uint32_t*>(gkey), gld, ckey, ccol, ctl);
   if (e != cudaSuccess) return e;
   return launch_pdl(topk_select_kernel, dim3(unsigned(rows)), dim3(kThreads), smem, st, scores, n, ld, n_valid, k, map,
                     map_ld, idx, n_sel, expand8, pool_len, hist, static_cast<const uint32_t*>(ckey),
