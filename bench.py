@@ -234,10 +234,10 @@ def make_desc(c, wl, events=None, q=None, qI=None, w=None, kv_new=None, ki_new=N
 
 
 def launches_per_step(c):
-    # quantise-append + indexer-K append + score + Top-K (row histogram, filter, select) + one
-    # attention launch for the four layers (they attend the same selected rows; split partials are
-    # merged inside that launch)
-    return 7
+    # the append (quantise the new KV row, copy the new indexer-K row: one launch) + score + Top-K
+    # (row histogram, filter, select) + one attention launch for the four layers (they attend the
+    # same selected rows; split partials are merged inside that launch)
+    return 6
 
 
 def max_over_ranks(torch, dist, value, world, device):
@@ -492,8 +492,8 @@ def run_stack20(args):
             "config": {"workload": "csa2_decoder_stack_5x4_b64_t131072", "global_batch": B, "seq_len": T,
                        "layers": "Full+3 Reuse, then 4 x (Reindex + 3 Reuse)", "top_k": K_SEL, "window": W_WIN},
             "kv_gbs": gbs, "hbm_frac_step": gbs / peak, "peak_kind": f"{kind} (hbm copy)",
-            # group 1: append (2) + score + Top-K (3) + attention; groups 2-5: score + Top-K (3) + attention
-            "gpu_launches": (7 + 4 * 5) * args.steps}
+            # group 1: append + score + Top-K (3) + attention; groups 2-5: score + Top-K (3) + attention
+            "gpu_launches": (6 + 4 * 5) * args.steps}
 
 
 def run_prefill(args):

@@ -60,14 +60,11 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&wv)[8], uint32_t
   }
 }
 
-__global__ void __launch_bounds__(256) fp4_quantize_kernel(
-    const uint16_t* __restrict__ x, int64_t n_groups, int n_new, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, int64_t cap, const int32_t* __restrict__ offsets, int offset_bias,
-    unsigned int* flags) {
-  pdl_wait();
-  pdl_trigger();
-  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (gid >= n_groups) return;
+// One 16-value group (gid = row * 32 + group) of the rows being appended: FP4 codes and its scale.
+__device__ __forceinline__ void quantize_append_group(const uint16_t* __restrict__ x, int64_t gid, int n_new,
+                                                      uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                      int64_t cap, const int32_t* __restrict__ offsets,
+                                                      int offset_bias, unsigned int* flags) {
   const int64_t row = gid >> 5;
   const int g = int(gid & 31);
   const int64_t b = row / n_new, r = row - b * n_new;
@@ -84,6 +81,62 @@ __global__ void __launch_bounds__(256) fp4_quantize_kernel(
   const int64_t crow = b * cap + pos;
   *reinterpret_cast<uint2*>(codes + crow * CSA2_CODE_BYTES + g * 8) = make_uint2(lo, hi);
   scales[crow * CSA2_SCALE_BYTES + g] = uint8_t(sb);
+}
+
+// 16 bytes (vector v of row `row`) of the rows being appended: dst row (lens[b] - n_new + r) of
+// sequence b <- src row r of sequence b.
+__device__ __forceinline__ void copy_append_vec(const uint16_t* __restrict__ src, int64_t row, int v, int n_new,
+                                                int row_vecs, uint16_t* __restrict__ dst, int64_t cap,
+                                                const int32_t* __restrict__ lens, unsigned int* flags) {
+  const int64_t b = row / n_new, r = row - b * n_new;
+  const int64_t pos = int64_t(lens[b]) - n_new + r;
+  if (pos < 0 || pos >= cap) {
+    if (v == 0) atomicOr(flags, CSA2_FLAG_APPEND_OOB);
+    return;
+  }
+  const uint4 val = reinterpret_cast<const uint4*>(src)[row * row_vecs + v];
+  reinterpret_cast<uint4*>(dst)[(b * cap + pos) * row_vecs + v] = val;
+}
+
+__global__ void __launch_bounds__(256) fp4_quantize_kernel(
+    const uint16_t* __restrict__ x, int64_t n_groups, int n_new, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, int64_t cap, const int32_t* __restrict__ offsets, int offset_bias,
+    unsigned int* flags) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= n_groups) return;
+  quantize_append_group(x, gid, n_new, codes, scales, cap, offsets, offset_bias, flags);
+}
+
+// The decode append in one launch: threads [0, n_groups) quantise the new main-KV rows, the next
+// n_vecs copy the new indexer-K rows (16 bytes each), and the last n_zero clear 16 bytes each of
+// `zero` (a step's counters, which must start at zero).
+__global__ void __launch_bounds__(256) append_kernel(const uint16_t* __restrict__ kv_new,
+                                                     const uint16_t* __restrict__ ki_new, int64_t n_groups,
+                                                     int64_t n_vecs, int n_new, int ki_vecs,
+                                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                     uint16_t* __restrict__ KI, int64_t cap,
+                                                     const int32_t* __restrict__ lens, uint4* __restrict__ zero,
+                                                     int64_t n_zero, unsigned int* flags) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid < n_groups) {
+    quantize_append_group(kv_new, gid, n_new, codes, scales, cap, lens, -n_new, flags);
+  } else if (gid - n_groups < n_vecs) {
+    const int64_t q = gid - n_groups, row = q / ki_vecs;
+    copy_append_vec(ki_new, row, int(q - row * ki_vecs), n_new, ki_vecs, KI, cap, lens, flags);
+  } else if (gid - n_groups - n_vecs < n_zero) {
+    zero[gid - n_groups - n_vecs] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__global__ void __launch_bounds__(256) zero_kernel(uint4* __restrict__ p, int64_t n16) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n16) p[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 __global__ void __launch_bounds__(256) fp4_dequantize_kernel(const uint8_t* __restrict__ codes,
@@ -156,15 +209,7 @@ __global__ void __launch_bounds__(256) copy_rows_append_kernel(const uint16_t* _
   const int64_t total = int64_t(B) * n_new * row_vecs;
   if (gid >= total) return;
   const int64_t row = gid / row_vecs;
-  const int v = int(gid - row * row_vecs);
-  const int64_t b = row / n_new, r = row - b * n_new;
-  const int64_t pos = int64_t(lens[b]) - n_new + r;
-  if (pos < 0 || pos >= cap) {
-    if (v == 0) atomicOr(flags, CSA2_FLAG_APPEND_OOB);
-    return;
-  }
-  const uint4 val = reinterpret_cast<const uint4*>(src)[row * row_vecs + v];
-  reinterpret_cast<uint4*>(dst)[(b * cap + pos) * row_vecs + v] = val;
+  copy_append_vec(src, row, int(gid - row * row_vecs), n_new, row_vecs, dst, cap, lens, flags);
 }
 
 // Block keys: key of block j = bf16_RNE(0.125 * sum_{i<8} KI[8j+i]) with the sum in token order
@@ -239,6 +284,29 @@ cudaError_t launch_copy_rows_append(const uint16_t* src, int B, int n_new, int r
   if (!flags) return cudaErrorUnknown;
   return launch_pdl(copy_rows_append_kernel, grid_for(total, 256), dim3(256), 0, st, src, B, n_new, row_vecs, dst, cap,
                                                                 lens, flags);
+}
+
+cudaError_t launch_append(const uint16_t* kv_new, const uint16_t* ki_new, int B, int n_new, uint8_t* codes,
+                          uint8_t* scales, uint16_t* KI, int64_t cap, const int32_t* lens, void* zero,
+                          size_t zero_bytes, cudaStream_t st) {
+  const int64_t n_groups = int64_t(B) * n_new * (CSA2_D / CSA2_GROUP);
+  const int ki_vecs = CSA2_DI / 8;
+  const int64_t n_vecs = int64_t(B) * n_new * ki_vecs;
+  if ((reinterpret_cast<uintptr_t>(zero) | zero_bytes) & 15u) return cudaErrorInvalidValue;
+  const int64_t n_zero = zero ? int64_t(zero_bytes / 16) : 0;
+  if (n_groups + n_vecs + n_zero == 0) return cudaSuccess;
+  unsigned int* flags = device_flags_ptr();
+  if (!flags) return cudaErrorUnknown;
+  return launch_pdl(append_kernel, grid_for(n_groups + n_vecs + n_zero, 256), dim3(256), 0, st, kv_new, ki_new,
+                    n_groups, n_vecs, n_new, ki_vecs, codes, scales, KI, cap, lens, static_cast<uint4*>(zero), n_zero,
+                    flags);
+}
+
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st) {
+  if (bytes == 0) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(p) | bytes) & 15u) return cudaMemsetAsync(p, 0, bytes, st);
+  const int64_t n16 = int64_t(bytes / 16);
+  return launch_pdl(zero_kernel, grid_for(n16, 256), dim3(256), 0, st, static_cast<uint4*>(p), n16);
 }
 
 cudaError_t launch_block_keys(const uint16_t* KI, int B, int64_t cap, const int32_t* lens,

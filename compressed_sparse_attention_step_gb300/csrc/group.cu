@@ -296,32 +296,38 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   if (ds) lock = std::unique_lock<std::mutex>(ds->mu);
   cudaStream_t aux = ds ? ds->aux : st;
 
+  // Top-K counters and attention tickets sit back to back in the workspace; every launch leaves them
+  // zero, so clearing them once per step serves all layers of an unchunked step (by the append's
+  // launch when the step has one)
+  const bool zeroed = n_chunks == 1;
+  const size_t zero_lo = csa2::topk_ws_bytes(int(rows), lay.score_ld) > 0
+                             ? lay.topk_off + csa2::topk_counters_offset(int(rows))
+                             : lay.attn_off;
+  const size_t zero_hi = lay.attn_off + csa2::group_attn_ticket_bytes(rows, K, g->W, g->n_split);
+  bool zero_done = false;
+
   // ---- append (Full layer of a decode step), before any scoring --------------------------------
   if (g->n_new > 0) {
-    if (g->kv_new &&
-        !ok(csa2::launch_fp4_quantize(g->kv_new, g->B, g->n_new, g->codes, g->scales, g->cap, g->lens,
-                                      -g->n_new, st)))
+    if (g->kv_new && g->ki_new) {
+      if (!ok(csa2::launch_append(g->kv_new, g->ki_new, g->B, g->n_new, g->codes, g->scales, g->KI, g->cap, g->lens,
+                                  zeroed ? wsb + zero_lo : nullptr, zeroed ? zero_hi - zero_lo : 0, st)))
+        return CSA2_ERR_CUDA;
+      zero_done = zeroed;
+    } else if (g->kv_new &&
+               !ok(csa2::launch_fp4_quantize(g->kv_new, g->B, g->n_new, g->codes, g->scales, g->cap, g->lens,
+                                             -g->n_new, st))) {
       return CSA2_ERR_CUDA;
+    }
     if (g->ki_new) {
-      if (!ok(csa2::launch_copy_rows_append(g->ki_new, g->B, g->n_new, CSA2_DI, g->KI, g->cap, g->lens, st)))
+      if (!g->kv_new &&
+          !ok(csa2::launch_copy_rows_append(g->ki_new, g->B, g->n_new, CSA2_DI, g->KI, g->cap, g->lens, st)))
         return CSA2_ERR_CUDA;
       if (g->hierarchical &&
           !ok(csa2::launch_block_keys(g->KI, g->B, g->cap, g->lens, g->block_keys, 1, g->n_new, st)))
         return CSA2_ERR_CUDA;
     }
   }
-  // Top-K counters and attention tickets sit back to back in the workspace; every launch leaves them
-  // zero, so one memset per step serves all layers of an unchunked step
-  const bool zeroed = n_chunks == 1;
-  if (zeroed) {
-    const size_t lo = lay.topk_off + csa2::topk_counters_offset(int(rows));
-    const size_t hi = lay.attn_off + csa2::group_attn_ticket_bytes(rows, K, g->W, g->n_split);
-    if (csa2::topk_ws_bytes(int(rows), lay.score_ld) > 0 && !ok(cudaMemsetAsync(wsb + lo, 0, hi - lo, st)))
-      return CSA2_ERR_CUDA;
-    if (csa2::topk_ws_bytes(int(rows), lay.score_ld) == 0 &&
-        !ok(cudaMemsetAsync(wsb + lay.attn_off, 0, csa2::group_attn_ticket_bytes(rows, K, g->W, g->n_split), st)))
-      return CSA2_ERR_CUDA;
-  }
+  if (zeroed && !zero_done && !ok(csa2::launch_zero(wsb + zero_lo, zero_hi - zero_lo, st))) return CSA2_ERR_CUDA;
   if (!rec(g->ev_score_begin, st)) return CSA2_ERR_CUDA;
 
   for (int c = 0; c < n_chunks; ++c) {
