@@ -145,6 +145,163 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_kernel(
   }
 }
 
+// ---- contiguous keys (a sequence's cache or its block keys): staged by bulk asynchronous copies --
+// Each warp streams its own 16-position steps (4 KiB of contiguous keys) through a ring of
+// kStages shared-memory buffers: lane 0 issues one cp.async.bulk per step, completing on the
+// stage's mbarrier, kStages steps ahead of the arithmetic.  The copies in flight hold no registers,
+// so an SM keeps 2 CTAs x 8 warps x kStages x 4 KiB of keys requested, far more than the
+// register-staged loads allow at this kernel's occupancy.  The arithmetic (the same lanes, order
+// and rounding as above) reads each position's 32 bytes per lane from shared memory.
+constexpr int kStages = 3;
+constexpr uint32_t kStepBytes = uint32_t(kPosPerWarpIt) * CSA2_DI * 2;  // 4096
+constexpr size_t kStreamSmem = size_t(kWarps) * kStages * kStepBytes + size_t(kWarps) * kStages * 8;
+
+// Waits for phase `parity` of a shared-memory mbarrier, for at most about one second.
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p; }\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 63u) == 0u) {
+      uint64_t now;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+      if (it == 0u) t0 = now;
+      else if (now - t0 > 1000000000ull) return false;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
+    const uint16_t* __restrict__ qI, const float* __restrict__ w, int Nq,
+    const uint16_t* __restrict__ KI, int64_t key_stride_rows, const int32_t* __restrict__ lens,
+    int64_t cap_entries, int block_div, int ratio, const int32_t* __restrict__ q_pos,
+    float* __restrict__ scores, int64_t ld, int32_t* __restrict__ n_valid_out, int64_t chunk,
+    unsigned int* flags) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.y;
+  const int b = row / Nq, qi = row - b * Nq;
+  const int64_t T = min(max(int64_t(lens[b]), int64_t(0)), cap_entries);
+  const int64_t p = q_pos ? int64_t(q_pos[row]) : int64_t(ratio) * T - Nq + qi;
+  const int64_t nvis = (p + 1 < 0) ? 0 : min((p + 1) / ratio, T);
+  const int64_t nv = nvis / block_div;  // scored prefix of this row
+  if (n_valid_out && blockIdx.x == 0 && threadIdx.x == 0) n_valid_out[row] = int32_t(nv);
+
+  const int64_t c0 = int64_t(blockIdx.x) * chunk;
+  const int64_t c1 = min(c0 + chunk, ld);
+  if (c0 >= c1) return;
+  const int64_t lend = min(min(nv, c1), key_stride_rows);  // positions below this are read
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane >> 3;
+  const int j = lane & 7;
+  const uint32_t ring = smem_u32(smem) + uint32_t(warp) * kStages * kStepBytes;
+  const uint32_t bars = smem_u32(smem) + uint32_t(kWarps) * kStages * kStepBytes + uint32_t(warp) * kStages * 8u;
+  const unsigned char* ring_p = smem + size_t(warp) * kStages * kStepBytes;
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(bars + 8u * st) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncwarp();
+
+  const uint16_t* kseq = KI + int64_t(b) * key_stride_rows * CSA2_DI;
+  const int64_t first = c0 + int64_t(warp) * kPosPerWarpIt;
+  const int n_steps = first < c1 ? int((c1 - first + kPosPerCtaIt - 1) / kPosPerCtaIt) : 0;
+  // step i covers positions first + i * kPosPerCtaIt + [0, 16); the keys of those below lend
+  auto issue = [&](int i) {
+    const int64_t base = first + int64_t(i) * kPosPerCtaIt;
+    const int64_t cnt = min(max(lend - base, int64_t(0)), int64_t(kPosPerWarpIt));
+    const uint32_t bytes = uint32_t(cnt) * CSA2_DI * 2u;
+    const uint32_t bar = bars + 8u * uint32_t(i % kStages);
+    const uint32_t dst = ring + uint32_t(i % kStages) * kStepBytes;
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+    if (bytes)
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+          "l"(kseq + base * CSA2_DI), "r"(bytes), "r"(bar)
+          : "memory");
+  };
+  if (lane == 0)
+    for (int i = 0; i < min(n_steps, kStages); ++i) issue(i);
+
+  float qf[4][16];
+  const uint16_t* qrow = qI + int64_t(row) * (CSA2_HI * CSA2_DI);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint4 a = *reinterpret_cast<const uint4*>(qrow + h * CSA2_DI + 16 * j);
+    const uint4 c = *reinterpret_cast<const uint4*>(qrow + h * CSA2_DI + 16 * j + 8);
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      qf[h][2 * e] = bf16lo(v[e]);
+      qf[h][2 * e + 1] = bf16hi(v[e]);
+    }
+  }
+  const int my_head = 2 * (j & 1) + ((j >> 1) & 1);
+  const float wh = w[int64_t(row) * CSA2_HI + my_head];
+  const bool odd = (j & 1) != 0, second = (j & 2) != 0;
+  float* srow = scores + int64_t(row) * ld;
+
+  int done = n_steps;
+  for (int i = 0; i < n_steps; ++i) {
+    const int64_t base = first + int64_t(i) * kPosPerCtaIt;
+    if (!stage_wait(bars + 8u * uint32_t(i % kStages), uint32_t(i / kStages) & 1u)) {
+      if (lane == 0) atomicOr(flags, CSA2_FLAG_TIMEOUT);
+      done = i;
+      break;
+    }
+    const unsigned char* stg = ring_p + size_t(i % kStages) * kStepBytes;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t t = base + u * 4 + sub;
+      const bool ok = t < lend;
+      const uint4* kp = reinterpret_cast<const uint4*>(stg + (u * 4 + sub) * (CSA2_DI * 2) + 32 * j);
+      const uint4 k0 = kp[0], k1 = kp[1];
+      const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+      float P[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc = __fmaf_rn(qf[h][2 * e], bf16lo(kw[e]), acc);
+          acc = __fmaf_rn(qf[h][2 * e + 1], bf16hi(kw[e]), acc);
+        }
+        P[h] = acc;
+      }
+      const float s0 = odd ? P[0] : P[2], s1 = odd ? P[1] : P[3];
+      const float k0f = odd ? P[2] : P[0], k1f = odd ? P[3] : P[1];
+      const float A0 = __fadd_rn(k0f, __shfl_xor_sync(0xffffffffu, s0, 1));
+      const float A1 = __fadd_rn(k1f, __shfl_xor_sync(0xffffffffu, s1, 1));
+      const float sendB = second ? A0 : A1, keepB = second ? A1 : A0;
+      const float Bv = __fadd_rn(keepB, __shfl_xor_sync(0xffffffffu, sendB, 2));
+      const float dot = __fadd_rn(Bv, __shfl_xor_sync(0xffffffffu, Bv, 4));
+      const float r = dot > 0.0f ? dot : 0.0f;
+      const float m = __fmul_rn(wh, r);
+      const float m2 = __fadd_rn(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      const float sc = __fadd_rn(m2, __shfl_xor_sync(0xffffffffu, m2, 1));
+      if (j == 0 && t < c1) srow[t] = ok ? sc : -INFINITY;
+    }
+    __syncwarp();  // every lane has read the stage before it is refilled
+    if (lane == 0 && i + kStages < n_steps) issue(i + kStages);
+  }
+  if (done < n_steps) {
+    // gave up waiting: wait (bounded) for the copies still in flight before the CTA leaves
+    for (int i = done; i < min(n_steps, done + kStages); ++i)
+      stage_wait(bars + 8u * uint32_t(i % kStages), uint32_t(i / kStages) & 1u);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
@@ -161,6 +318,22 @@ cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq
   const dim3 grid(unsigned((ld + chunk - 1) / chunk), unsigned(rows));
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
+  if (!cand) {
+    // contiguous keys: the bulk-copy streaming kernel
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_set[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(index_score_stream_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kStreamSmem));
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+    if ((reinterpret_cast<uintptr_t>(KI) & 15u) == 0)
+      return launch_pdl(index_score_stream_kernel, grid, dim3(kThreads), kStreamSmem, st, qI, w, Nq, KI,
+                        key_stride_rows, lens, cap_entries, block_div, ratio, q_pos, scores, ld, n_valid, chunk,
+                        flags);
+  }
   if (cand)
     return launch_pdl(index_score_kernel<true>, grid, dim3(kThreads), 0, st, qI, w, Nq, KI, key_stride_rows, lens,
                       cap_entries, block_div, cand, cand_len, n_cand, ratio, q_pos, scores, ld, n_valid, chunk, flags);
