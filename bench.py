@@ -418,7 +418,7 @@ def run_gpu(args, rank, world, local_rank):
                    "layers": "1 Full + 3 Reuse", "top_k": K_SEL, "window": W_WIN,
                    "l2": "inputs larger than L2 (2.1 GB indexer-K scan per step)"},
         "kv_gbs": kv_gbs, "hbm_frac_step": kv_gbs / peak, "bytes_per_step": BYTES_PER_SEQ * B_PER_GPU * world,
-        "roofline": {"kernel": "index_score_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": "index_score_stream_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": f"{peak_kind} (hbm copy)",
                      "traffic": traffic, "algorithmic_bytes": score_bytes, "avg_launch_ms": score_avg},
         "e2e": {"value": throughput(B_PER_GPU, world, e2e_ms / K), "unit": "tokens/s", "h2d_bytes_per_step": h2d * world,

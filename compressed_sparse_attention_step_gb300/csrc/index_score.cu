@@ -12,7 +12,8 @@
 // fused-multiply-add chain p_j over channels 16j..16j+15 from +0; the 8-lane reduction is a
 // reduce-scatter whose additions are exactly ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)) (IEEE addition
 // is commutative, so either operand order gives the same bits); then relu, w_h * r_h, and
-// (m0 + m1) + (m2 + m3).  Only _rn intrinsics are used, so nothing is contracted or reordered.
+// (m0 + m1) + (m2 + m3).  Only _rn intrinsics (and the packed fma.rn.f32x2, whose two lanes each
+// round like one fmaf) are used, so nothing is contracted or reordered.
 #include "common.cuh"
 
 namespace csa2 {
@@ -156,6 +157,18 @@ constexpr int kStages = 3;
 constexpr uint32_t kStepBytes = uint32_t(kPosPerWarpIt) * CSA2_DI * 2;  // 4096
 constexpr size_t kStreamSmem = size_t(kWarps) * kStages * kStepBytes + size_t(kWarps) * kStages * 8;
 
+// (x, y) <- (a * k + x, b * k + y), each rounded once to nearest (one packed fp32 FMA).
+__device__ __forceinline__ void fma2_rn(float& x, float& y, float a, float b, float k) {
+  asm("{ .reg .b64 ab, kk, xy;\n\t"
+      "mov.b64 ab, {%2, %3};\n\t"
+      "mov.b64 kk, {%4, %4};\n\t"
+      "mov.b64 xy, {%0, %1};\n\t"
+      "fma.rn.f32x2 xy, ab, kk, xy;\n\t"
+      "mov.b64 {%0, %1}, xy; }\n"
+      : "+f"(x), "+f"(y)
+      : "f"(a), "f"(b), "f"(k));
+}
+
 // Waits for phase `parity` of a shared-memory mbarrier, for at most about one second.
 __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity) {
   uint64_t t0 = 0;
@@ -268,16 +281,17 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
       const uint4* kp = reinterpret_cast<const uint4*>(stg + (u * 4 + sub) * (CSA2_DI * 2) + 32 * j);
       const uint4 k0 = kp[0], k1 = kp[1];
       const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-      float P[4];
+      // the four heads' chains two at a time (packed fp32 FMA: each lane of the pair rounds as one
+      // fmaf would), channels in the same order
+      float P[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float acc = 0.0f;
+      for (int e = 0; e < 8; ++e) {
+        const float klo = bf16lo(kw[e]), khi = bf16hi(kw[e]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          acc = __fmaf_rn(qf[h][2 * e], bf16lo(kw[e]), acc);
-          acc = __fmaf_rn(qf[h][2 * e + 1], bf16hi(kw[e]), acc);
+        for (int hp = 0; hp < 2; ++hp) {
+          fma2_rn(P[2 * hp], P[2 * hp + 1], qf[2 * hp][2 * e], qf[2 * hp + 1][2 * e], klo);
+          fma2_rn(P[2 * hp], P[2 * hp + 1], qf[2 * hp][2 * e + 1], qf[2 * hp + 1][2 * e + 1], khi);
         }
-        P[h] = acc;
       }
       const float s0 = odd ? P[0] : P[2], s1 = odd ? P[1] : P[3];
       const float k0f = odd ? P[2] : P[0], k1f = odd ? P[3] : P[1];
