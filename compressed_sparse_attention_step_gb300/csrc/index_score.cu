@@ -3,10 +3,13 @@
 // layers rescore with their own indexer Q (ai-maestro.online "DeepSeek AI released
 // DeepSeek-V4.1-Flash with 1M context, FP4", section "Compressed Sparse Attention 2").
 //
-// HBM-bound streaming kernel (256 B of indexer K per position, ~2 FMA per byte): eight lanes
-// share one position, each lane owning 16 consecutive channels (two 16-byte loads), so a warp
-// reads four whole 256-byte rows per step and four steps are kept in flight per lane.  The
-// indexer query slice (4 heads x 16 channels) stays in registers for the whole CTA.
+// HBM-bound streaming kernels (256 B of indexer K per position, ~2 FMA per byte): eight lanes
+// share one position, each lane owning 16 consecutive channels (32 bytes), so a warp covers four
+// whole 256-byte rows per step.  The indexer query slice (4 heads x 16 channels) stays in
+// registers for the whole CTA.  Contiguous keys (a sequence's cache or its block keys) stream
+// through shared memory by bulk asynchronous copies (index_score_stream_kernel, below); candidate
+// pools, whose positions are gathered, use register loads with four steps in flight per lane
+// (index_score_kernel).
 //
 // The fp32 result is bit-identical to the canonical order: per head, lane j computes the
 // fused-multiply-add chain p_j over channels 16j..16j+15 from +0; the 8-lane reduction is a
