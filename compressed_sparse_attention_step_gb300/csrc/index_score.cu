@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_kernel(
     crow = cand + int64_t(row) * n_cand;
     const int64_t cl = min(max(int64_t(cand_len[row]), int64_t(0)), n_cand);
     int64_t lo = 0, hi = cl;  // first pool entry not visible (the pool is ascending)
+    if (cl > 0 && int64_t(crow[cl - 1]) < nvis) lo = hi;  // all visible (every decode query): no search
     while (lo < hi) {
       const int64_t mid = (lo + hi) >> 1;
       if (int64_t(crow[mid]) < nvis) lo = mid + 1;
