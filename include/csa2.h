@@ -152,7 +152,10 @@ csa2_status csa2_index_score(const uint16_t* qI, const float* w, int B, int Nq, 
  *   map     NULL, or int32 [rows][map_ld]: output map[r][col] instead of col (an ascending map
  *           such as a pool keeps the output ascending).
  *   idx     int32 [rows][k];  n_sel int32 [rows] (nullable): min(k, valid columns).
- *   ws      workspace of csa2_workspace_size(CSA2_OP_TOPK, ...) bytes (currently 0: may be NULL).
+ *   ws      workspace of csa2_workspace_size(CSA2_OP_TOPK, ...) bytes, 16-byte aligned: for rows
+ *           longer than 8192 columns the candidate lists, per-row counters, histograms and
+ *           16-column group keys of the multi-CTA selection (the call clears what must start at
+ *           zero); 0 bytes, and ws may be NULL, otherwise.
  */
 csa2_status csa2_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
                       int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,
