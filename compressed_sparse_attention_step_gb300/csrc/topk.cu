@@ -3,24 +3,22 @@
 // blocks for the hierarchical pool).  Order: larger score first, equal scores by lower column;
 // the k selected columns are returned in ascending order.
 //
-// Radix select on ordered 32-bit score keys (-0 and +0 share a key), in one launch of
-// (slices x rows) CTAs so that a long row is read by several SMs at once:
-//  1. each CTA takes one slice of its row (about 32768 keys; fewer, longer slices when k is large).
-//     It splits the slice's keys into groups (the 16 keys one thread reads per sweep step) and
-//     histograms the group maxima by their top 12 key bits, both in shared memory and added into
-//     the row's histogram in the workspace.  The k largest group maxima are k distinct keys, so the
-//     lower edge L of the bin holding the k-th largest maximum is at most the slice's k-th largest
-//     key: every key >= L is appended to the row's candidate list (one atomic reservation);
-//  2. the last CTA of the row to finish (an atomic ticket) takes the same bound over the whole
-//     row's histogram (a bound >= every slice's), keeps the candidates at or above it, and finds the
-//     exact k-th (key, column) by radix rounds on the key bits, then on the column bits (ascending,
-//     so equal keys go to the lower column); the winners are written in column order, placed by
-//     prefix popcounts over a bitmap of the selected columns (a bitonic sort for very long rows);
-//     it then clears the row's counters and histogram for the next launch.
-// A row whose candidates overflow the list (massive ties) is finished by that CTA with the same
-// rounds over the row in global memory and an ordered, scan-based output; rows of one slice use
-// that single-CTA path directly.  Counts are integers and every decision is a pure function of the
-// scores, so the result is deterministic.
+// Radix select on ordered 32-bit score keys (-0 and +0 share a key):
+//  * rows up to 8192 columns (topk_kernel): one CTA per row histograms the top 12 key bits, lists
+//    the keys in and above the bin of the k-th largest key, and selects among them;
+//  * longer rows, three launches over (slices x rows) CTAs and then one CTA per row:
+//    topk_hist_kernel histograms the rows' 16-key group maxima and keeps every group's key;
+//    topk_filter_kernel takes the bin of the k-th largest group maximum as a lower bound on the
+//    k-th largest key (those k maxima are k distinct keys) and lists the keys at or above it,
+//    reading only the groups whose key reaches it; topk_select_kernel selects among the list.
+// Among the candidates, a list of one key takes its k lowest columns directly; otherwise radix
+// rounds on the key bits, then on the column bits (ascending, so equal keys go to the lower
+// column), find the exact k-th (key, column).  The winners are written in column order by rank,
+// each found by a binary search over the per-word prefix counts of the winners' column bitmap (a
+// bitonic sort for very long rows).  A row whose candidates overflow the list (massive ties) is
+// selected by one CTA with the same rounds over the row in global memory and an ordered,
+// scan-based output.  Counts are integers and every decision is a pure function of the scores,
+// so the result is deterministic.
 #include <algorithm>
 
 #include "common.cuh"
