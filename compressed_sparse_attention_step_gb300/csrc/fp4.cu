@@ -1,7 +1,9 @@
 // FP4 main-KV codec: E2M1 codes with one E4M3 scale per 16 channels, NVFP4 without the global
 // scale (ai-maestro.online "DeepSeek AI released DeepSeek-V4.1-Flash with 1M context, FP4",
-// section "FP4 KV, Bounded Replay, and other extensions").  Also the plain row-append copy and
-// the block-key builder of the hierarchical indexer.
+// section "FP4 KV, Bounded Replay, and other extensions").  Also the plain row-append copy, the
+// decode append in one launch (new KV rows quantised, new indexer-K rows copied, the step's
+// counters cleared), the 8-bit window encoder and the block-key builder of the hierarchical
+// indexer.
 //
 // All kernels here stream: one thread per 16-channel group (32 B of bf16 in, 8 B of codes and
 // 1 B of scale out), so a warp covers one 512-channel row with fully coalesced accesses.
