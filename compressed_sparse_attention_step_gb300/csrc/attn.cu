@@ -627,7 +627,7 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
   n_split = attn_effective_split(k, W, n_split);
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; set once, by any host thread
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {

@@ -8,7 +8,7 @@
 // caller's stream at the start of every call; the partials are written before they are read.
 #include <mutex>
 
-#include "common.cuh"
+#include "attn_common.cuh"
 
 namespace csa2 {
 namespace {
@@ -18,7 +18,9 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];
 
-// Device address of g_attn_scratch for the current device (looked up once per device), or NULL.
+// Device address of g_attn_scratch for the current device (looked up once per device and kept for
+// the life of the process, so a device reset or context teardown while the library is loaded is not
+// supported), or NULL.
 float* static_scratch() {
   static float* ptrs[64] = {};
   static std::mutex mu;
@@ -45,7 +47,7 @@ extern "C" csa2_status csa2_sparse_attn_decode_static(const uint16_t* q, int B, 
                                                       uint16_t* out, float* lse, int n_split,
                                                       csa2_stream_t stream) {
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  if (B < 0 || Nq < 0 || cap < 0 || k < 0 || k > CSA2_MAX_ATTN_K || n_split < 0 || n_split > 32)
+  if (B < 0 || Nq < 0 || cap < 0 || k < 0 || k > CSA2_MAX_ATTN_K || n_split < 0 || n_split > csa2::attn::kMaxSplit)
     return CSA2_ERR_INVALID_ARG;
   if (swa && (W < 1 || W > CSA2_MAX_W || !swa_len)) return CSA2_ERR_INVALID_ARG;
   if (!swa) W = 0;

@@ -338,7 +338,7 @@ cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq
   if (!flags) return cudaErrorUnknown;
   if (!cand) {
     // contiguous keys: the bulk-copy streaming kernel
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];  // per device; set once, by any host thread
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {

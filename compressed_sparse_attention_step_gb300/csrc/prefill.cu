@@ -643,7 +643,7 @@ cudaError_t launch_prefill_select(const uint16_t* qI, const float* w, int B, int
   CUtensorMap map_k, map_q;
   if (!make_map(&map_k, KI, int64_t(B) * cap, kKeyTile) || !make_map(&map_q, qI, rows * 4, 4 * kQPerTile))
     return cudaErrorUnknown;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; set once, by any host thread
   static int n_sm[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);

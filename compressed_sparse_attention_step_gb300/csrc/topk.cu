@@ -956,7 +956,7 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
                         int expand8, int32_t* pool_len, void* ws, cudaStream_t st, bool counters_zeroed) {
   if (rows == 0) return cudaSuccess;
   const size_t smem = sizeof(SelSmem);
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; set once, by any host thread
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
@@ -978,7 +978,7 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
     cudaError_t e = cudaMemsetAsync(ctl, 0, (topk_ctl_words(rows) + size_t(rows) * kBins) * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
   }
-  static bool sel_attr[64] = {};
+  static std::atomic<bool> sel_attr[64];
   if (dev < 64 && !sel_attr[dev]) {
     cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
@@ -1008,7 +1008,7 @@ cudaError_t launch_bitmap_select(const uint16_t* qI, const float* w, int B, int 
   const int64_t rows = int64_t(B) * Nq;
   if (rows == 0) return cudaSuccess;
   const size_t smem = sizeof(BmSmem);
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; set once, by any host thread
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {

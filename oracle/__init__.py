@@ -55,7 +55,7 @@ def lib():
         _lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
         _lib.oracle_e2m1_encode.restype = ctypes.c_uint8
         _lib.oracle_e2m1_encode.argtypes = [f32]
-        _lib.oracle_fp4_quantize.argtypes = [P, i64, P, P]
+        _lib.oracle_fp4_quantize.argtypes = [P, i64, P, P, i32]
         _lib.oracle_fp4_dequantize.argtypes = [P, P, i64, P]
         _lib.oracle_index_score.argtypes = [P, P, P, P, i64, P]
         _lib.oracle_topk.restype = i32
@@ -68,6 +68,7 @@ def lib():
         _lib.oracle_group_step.argtypes = [i32, i32, P, i32, i32, i32, i32, i32, i32, P, i64,
                                            P, P, P, P, P, P, P, P, P, f32, P, P, P, P, P, i32, i32]
         _lib.oracle_fp8_quantize.argtypes = [P, i64, P]
+        _lib.oracle_index_select.argtypes = [i32, i32, P, i64, P, P, P, i32, P, i32, P, P, i32]
         _lib.oracle_fp8_dequantize.argtypes = [P, i64, P]
     return _lib
 
@@ -102,13 +103,14 @@ def e2m1_encode(v: float) -> int:
 # ---------------------------------------------------------------------------
 # Array functions
 # ---------------------------------------------------------------------------
-def fp4_quantize(x_bf16: np.ndarray):
-    """x: uint16 bf16 bits [..., 512] -> (codes uint8 [..., 256], scales uint8 [..., 32])."""
+def fp4_quantize(x_bf16: np.ndarray, threads: int = 1):
+    """x: uint16 bf16 bits [..., 512] -> (codes uint8 [..., 256], scales uint8 [..., 32]).
+    Rows are quantised independently, on up to `threads` host threads."""
     x = _c(x_bf16, np.uint16)
     rows = x.size // D
     codes = np.empty(x.shape[:-1] + (D // 2,), np.uint8)
     scales = np.empty(x.shape[:-1] + (D // GROUP,), np.uint8)
-    lib().oracle_fp4_quantize(_p(x), rows, _p(codes), _p(scales))
+    lib().oracle_fp4_quantize(_p(x), rows, _p(codes), _p(scales), int(threads))
     return codes, scales
 
 
@@ -160,6 +162,25 @@ def topk(scores: np.ndarray, k: int, map_=None):
     out = np.empty(k, np.int32)
     cnt = lib().oracle_topk(_p(s), s.size, int(k), _p(m), _p(out))
     return out, cnt
+
+
+def index_select(KI, qI, w, T, k: int, *, ratio=1, q_pos=None, threads=1):
+    """Flat Top-k of every query row of a batch, as a flat Full layer selects: KI [B,cap,128] bf16
+    bits, qI [B,Nq,4,128] bf16 bits, w [B,Nq,4] fp32, T [B] entries present; query i of sequence b
+    at q_pos[b,i] (or ratio*T_b - Nq + i).  Returns (idx int32 [B,Nq,k] ascending, -1 padded;
+    n_sel int32 [B,Nq])."""
+    KI = _c(KI, np.uint16)
+    qI = _c(qI, np.uint16)
+    w = _c(w, np.float32)
+    B, cap = KI.shape[0], KI.shape[1]
+    Nq = qI.shape[1]
+    T = _c(T, np.int64)
+    qp = None if q_pos is None else _c(q_pos, np.int32)
+    idx = np.empty((B, Nq, k), np.int32)
+    n_sel = np.empty((B, Nq), np.int32)
+    lib().oracle_index_select(B, Nq, _p(T), cap, _p(KI), _p(qI), _p(w), int(ratio), _p(qp), int(k), _p(idx),
+                              _p(n_sel), int(threads))
+    return idx, n_sel
 
 
 def block_keys(KI: np.ndarray) -> np.ndarray:

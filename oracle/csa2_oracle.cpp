@@ -307,6 +307,21 @@ int64_t visible_entries(int64_t T, int64_t p, int ratio) {
   return std::max<int64_t>(0, std::min<int64_t>(T, (p + 1) / ratio));
 }
 
+// Runs f(0) .. f(n-1) on up to `threads` host threads (interleaved); the order of the calls does
+// not matter to any caller (each index writes only its own outputs).
+template <typename F>
+void parallel_for(int64_t n, int threads, F f) {
+  const int nt = int(std::max<int64_t>(1, std::min<int64_t>(threads, n)));
+  if (nt == 1) {
+    for (int64_t i = 0; i < n; ++i) f(i);
+    return;
+  }
+  std::vector<std::thread> pool_t;
+  for (int t = 0; t < nt; ++t)
+    pool_t.emplace_back([&, t] { for (int64_t i = t; i < n; i += nt) f(i); });
+  for (auto& th : pool_t) th.join();
+}
+
 }  // namespace
 
 extern "C" {
@@ -316,9 +331,13 @@ uint8_t oracle_e4m3_encode(float v) { return e4m3_encode(v); }
 float oracle_e2m1_value(uint8_t n) { return e2m1_value(n); }
 uint8_t oracle_e2m1_encode(float v) { return e2m1_encode(v); }
 
-void oracle_fp4_quantize(const uint16_t* x, int64_t rows, uint8_t* codes, uint8_t* scales) {
-  for (int64_t r = 0; r < rows; ++r)
-    quantize_row(x + r * kD, codes + r * kCodeBytes, scales + r * kScaleBytes);
+void oracle_fp4_quantize(const uint16_t* x, int64_t rows, uint8_t* codes, uint8_t* scales, int threads) {
+  // rows are independent: chunks of 1024 rows on the host threads
+  const int64_t chunks = (rows + 1023) / 1024;
+  parallel_for(chunks, threads, [&](int64_t ch) {
+    for (int64_t r = ch * 1024; r < std::min(rows, ch * 1024 + 1024); ++r)
+      quantize_row(x + r * kD, codes + r * kCodeBytes, scales + r * kScaleBytes);
+  });
 }
 
 // 8-bit window rows: each bf16 element to E4M3 (RNE, saturating to +-448), and back (exact).
@@ -343,6 +362,25 @@ void oracle_index_score(const uint16_t* qI, const float* w, const uint16_t* KI, 
 
 int oracle_topk(const float* scores, int64_t n, int k, const int32_t* map, int32_t* out) {
   return topk(scores, n, k, map, out);
+}
+
+// Flat selection of a Full layer for every query row of a batch: the scores of the row's visible
+// entries (score_one), then their exact Top-k (topk), exactly as a flat Full layer of
+// oracle_group_step selects.  KI [B][cap][128]; qI [B*Nq][4][128]; w [B*Nq][4]; query i of
+// sequence b sits at q_pos[b*Nq+i] (or ratio*T_b - Nq + i when q_pos is NULL).  idx [B*Nq][k],
+// n_sel [B*Nq] (nullable).  Rows run on up to `threads` host threads.
+void oracle_index_select(int B, int Nq, const int64_t* T, int64_t cap, const uint16_t* KI, const uint16_t* qI,
+                         const float* w, int ratio, const int32_t* q_pos, int k, int32_t* idx, int32_t* n_sel,
+                         int threads) {
+  parallel_for(int64_t(B) * Nq, threads, [&](int64_t row) {
+    const int64_t b = row / Nq, i = row - b * Nq;
+    const int64_t p = q_pos ? q_pos[row] : int64_t(ratio) * T[b] - Nq + i;
+    const int64_t nvis = visible_entries(T[b], p, ratio);
+    std::vector<float> s(size_t(std::max<int64_t>(nvis, 1)));
+    for (int64_t t = 0; t < nvis; ++t) s[size_t(t)] = score_one(qI + row * kHI * kDI, w + row * kHI, KI + (b * cap + t) * kDI);
+    const int m = topk(s.data(), nvis, k, nullptr, idx + row * k);
+    if (n_sel) n_sel[row] = m;
+  });
 }
 
 void oracle_block_keys(const uint16_t* KI, int64_t T, uint16_t* out) { block_keys(KI, T, out); }
@@ -395,71 +433,65 @@ int oracle_group_step(int B, int L, const int32_t* modes, int Nq, int K, int W, 
   const int SW = W - 1 + Nq;
   const int64_t pool_cap = int64_t(keep) * kBlock;
 
-  auto run_seq = [&](int b) {
+  // Block keys of every sequence first (hierarchical), then every query row on its own: a row's
+  // layers depend only on its sequence's cache and block keys, so rows may run in any order.
+  std::vector<std::vector<uint16_t>> bk(static_cast<size_t>(B));
+  if (hierarchical)
+    parallel_for(B, threads, [&](int64_t b) {
+      const int64_t Tb = T[b];
+      bk[size_t(b)].resize(size_t(std::max<int64_t>(Tb / kBlock, 1)) * kDI);
+      block_keys(KI + b * cap * kDI, Tb, bk[size_t(b)].data());
+    });
+
+  auto run_row = [&](int64_t row) {
+    const int64_t b = row / Nq, i = row - b * Nq;
     const int64_t Tb = T[b];
-    const uint8_t* cb = codes + int64_t(b) * cap * kCodeBytes;
-    const uint8_t* sb = scales + int64_t(b) * cap * kScaleBytes;
-    const uint16_t* kb = KI + int64_t(b) * cap * kDI;
-    std::vector<uint16_t> bk;
-    if (hierarchical) {
-      bk.resize(size_t(std::max<int64_t>(Tb / kBlock, 1)) * kDI);
-      block_keys(kb, Tb, bk.data());
-    }
-    for (int i = 0; i < Nq; ++i) {
-      const int64_t row = int64_t(b) * Nq + i;
-      const int64_t p = q_pos ? q_pos[row] : int64_t(ratio) * Tb - Nq + i;
-      const int64_t nvis = visible_entries(Tb, p, ratio);
-      int32_t* prow = hierarchical ? pool + row * pool_cap : nullptr;
-      int64_t plen = 0;
-      int latest = -1;  // layer whose indices are the latest
-      for (int l = 0; l < L; ++l) {
-        const int64_t lr = int64_t(l) * B * Nq + row;
-        int32_t* il = idx + lr * K;
-        const int mode = modes[l];
-        if (mode == MODE_FULL || mode == MODE_REINDEX) {
-          const uint16_t* qil = qI + lr * kHI * kDI;
-          const float* wl = w + lr * kHI;
-          if (hierarchical) {
-            if (mode == MODE_FULL) {
-              plen = block_pool(qil, wl, bk.data(), nvis / kBlock, keep, prow);
-              pool_len[row] = int32_t(plen);
-            }
-            std::vector<float> s(size_t(std::max<int64_t>(plen, 1)));
-            for (int64_t t = 0; t < plen; ++t) s[size_t(t)] = score_one(qil, wl, kb + int64_t(prow[t]) * kDI);
-            topk(s.data(), plen, K, prow, il);
-          } else {
-            std::vector<float> s(size_t(std::max<int64_t>(nvis, 1)));
-            for (int64_t t = 0; t < nvis; ++t) s[size_t(t)] = score_one(qil, wl, kb + t * kDI);
-            topk(s.data(), nvis, K, nullptr, il);
+    const uint8_t* cb = codes + b * cap * kCodeBytes;
+    const uint8_t* sb = scales + b * cap * kScaleBytes;
+    const uint16_t* kb = KI + b * cap * kDI;
+    const int64_t p = q_pos ? q_pos[row] : int64_t(ratio) * Tb - Nq + i;
+    const int64_t nvis = visible_entries(Tb, p, ratio);
+    int32_t* prow = hierarchical ? pool + row * pool_cap : nullptr;
+    int64_t plen = 0;
+    int latest = -1;  // layer whose indices are the latest
+    for (int l = 0; l < L; ++l) {
+      const int64_t lr = int64_t(l) * B * Nq + row;
+      int32_t* il = idx + lr * K;
+      const int mode = modes[l];
+      if (mode == MODE_FULL || mode == MODE_REINDEX) {
+        const uint16_t* qil = qI + lr * kHI * kDI;
+        const float* wl = w + lr * kHI;
+        if (hierarchical) {
+          if (mode == MODE_FULL) {
+            plen = block_pool(qil, wl, bk[size_t(b)].data(), nvis / kBlock, keep, prow);
+            pool_len[row] = int32_t(plen);
           }
-          latest = l;
+          std::vector<float> s(size_t(std::max<int64_t>(plen, 1)));
+          for (int64_t t = 0; t < plen; ++t) s[size_t(t)] = score_one(qil, wl, kb + int64_t(prow[t]) * kDI);
+          topk(s.data(), plen, K, prow, il);
         } else {
-          std::memcpy(il, idx + (int64_t(latest) * B * Nq + row) * K, sizeof(int32_t) * size_t(K));
+          std::vector<float> s(size_t(std::max<int64_t>(nvis, 1)));
+          for (int64_t t = 0; t < nvis; ++t) s[size_t(t)] = score_one(qil, wl, kb + t * kDI);
+          topk(s.data(), nvis, K, nullptr, il);
         }
-        // attention rows: selected FP4 entries, then the query's window rows
-        std::vector<std::vector<double>> rows;
-        for (int j = 0; j < K; ++j)
-          if (il[j] >= 0) rows.push_back(fp4_row(cb, sb, il[j]));
-        const int64_t wrow0 = (int64_t(l) * B + b) * SW;
-        for (int r = i; r < i + W; ++r) {
-          if (r < SW - swa_len[b]) continue;
-          if (swa_fp8) rows.push_back(fp8_row(static_cast<const uint8_t*>(swa) + (wrow0 + r) * kD));
-          else rows.push_back(bf16_row(static_cast<const uint16_t*>(swa) + (wrow0 + r) * kD));
-        }
-        attend(q + lr * kH * kD, rows, softmax_scale, out + lr * kH * kD, lse ? lse + lr * kH : nullptr);
+        latest = l;
+      } else {
+        std::memcpy(il, idx + (int64_t(latest) * B * Nq + row) * K, sizeof(int32_t) * size_t(K));
       }
+      // attention rows: selected FP4 entries, then the query's window rows
+      std::vector<std::vector<double>> rows;
+      for (int j = 0; j < K; ++j)
+        if (il[j] >= 0) rows.push_back(fp4_row(cb, sb, il[j]));
+      const int64_t wrow0 = (int64_t(l) * B + b) * SW;
+      for (int64_t r = i; r < i + W; ++r) {
+        if (r < SW - swa_len[b]) continue;
+        if (swa_fp8) rows.push_back(fp8_row(static_cast<const uint8_t*>(swa) + (wrow0 + r) * kD));
+        else rows.push_back(bf16_row(static_cast<const uint16_t*>(swa) + (wrow0 + r) * kD));
+      }
+      attend(q + lr * kH * kD, rows, softmax_scale, out + lr * kH * kD, lse ? lse + lr * kH : nullptr);
     }
   };
-
-  const int nt = std::max(1, std::min(threads, B));
-  if (nt == 1) {
-    for (int b = 0; b < B; ++b) run_seq(b);
-  } else {
-    std::vector<std::thread> pool_t;
-    for (int t = 0; t < nt; ++t)
-      pool_t.emplace_back([&, t] { for (int b = t; b < B; b += nt) run_seq(b); });
-    for (auto& th : pool_t) th.join();
-  }
+  parallel_for(int64_t(B) * Nq, threads, run_row);
   return 0;
 }
 

@@ -9,14 +9,21 @@ oracle's.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+
 import numpy as np
 
 import csa2_synth as syn
 
+# host threads for the oracle and for drawing many sequences (numpy's generators release the GIL)
+HOST_THREADS = max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1))
+
 D, H, HI, DI = 512, 16, 4, 128
 SCALE = float(np.float32(1.0 / np.sqrt(D)))
 
-# attention outputs: |gpu - oracle| <= ATOL everywhere and ||gpu - oracle|| <= RTOL ||oracle||
+# attention outputs: |gpu - oracle| <= ATOL everywhere, and ||gpu - oracle|| <= RTOL ||oracle|| for
+# every (query, head) row of 512 channels on its own as well as over the whole tensor
 ATOL, RTOL = 2e-2, 1e-2
 
 
@@ -39,26 +46,23 @@ def bf16_host(t):
 
 
 def assert_attn_close(got_bf16_bits, ref, what=""):
+    """Attention outputs [..., 512] against the oracle: element-wise max-abs ATOL, and relative
+    error RTOL per (query, head) row and over the whole tensor.  A row the oracle gives as exactly
+    zero (a query with no rows) must be exactly zero."""
     got = syn.bf16_bits_to_f32(got_bf16_bits).astype(np.float64)
     ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, f"{what}: shape {got.shape} vs {ref.shape}"
     err = np.abs(got - ref)
     rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
-    assert err.max() <= ATOL and rel <= RTOL, f"{what}: max abs {err.max():.3e}, rel {rel:.3e}"
-
-
-def one_query_oracle(orc, modes, T, codes, scales, KI, q, qI, w, swa, swa_len, i, q_pos_i, *, K, W, ratio,
-                     swa_fp8=False):
-    """The oracle group step of query i of a chunk alone: one sequence of T entries (codes, scales,
-    KI), per-layer chunk inputs q [L,Nq,16,512], qI [L,Nq,4,128], w [L,Nq,4], swa [L,W-1+Nq,512]
-    with its last swa_len rows valid; query i at position q_pos_i attends rows i .. i+W-1 of its
-    layer's window buffer, so it runs as a one-query chunk over those W rows (the valid ones among
-    them)."""
-    SW = swa.shape[1]
-    valid = int(min(W, max(0, W - max(0, SW - int(swa_len) - i))))
-    return orc.group_step(modes, [T], codes[None], scales[None], KI[None], q[:, i][:, None, None],
-                          qI[:, i][:, None, None], w[:, i][:, None, None], swa[:, i:i + W][:, None], [valid],
-                          Nq=1, K=K, W=W, ratio=ratio, q_pos=np.array([[q_pos_i]], np.int32), softmax_scale=SCALE,
-                          swa_fp8=swa_fp8)
+    g2, r2 = got.reshape(-1, got.shape[-1]), ref.reshape(-1, ref.shape[-1])
+    rn = np.linalg.norm(r2, axis=1)
+    en = np.linalg.norm(g2 - r2, axis=1)
+    zero = rn == 0.0
+    assert not np.any(en[zero] > 0.0), f"{what}: {int(np.sum(en[zero] > 0))} rows should be exactly zero"
+    row_rel = en[~zero] / rn[~zero]
+    worst = float(row_rel.max()) if row_rel.size else 0.0
+    assert err.max() <= ATOL and rel <= RTOL and worst <= RTOL, \
+        f"{what}: max abs {err.max():.3e}, rel {rel:.3e}, worst row rel {worst:.3e}"
 
 
 class GroupCase:
@@ -70,12 +74,17 @@ class GroupCase:
     """
 
     def __init__(self, seed, T, modes, *, Nq=1, K=512, W=128, ratio=1, hierarchical=False, keep=2048,
-                 cap=None, append=True, host_seqs=None, q_pos=None, share=None, layer0=0, swa_fp8=False):
+                 cap=None, append=True, host_seqs=None, q_pos=None, share=None, layer0=0, swa_fp8=False,
+                 integer_index=False):
         """share: a case whose cache, lengths, block keys and pool this one uses (a later group of
         a decoder stack: no append of its own); layer0: the stack index of this group's first
         layer (its per-layer draws use tensor ids offset by it); swa_fp8: 8-bit (E4M3) window rows,
         quantised from the bf16 draws by the oracle for host-drawn sequences (both sides see the
-        same bytes) and by the library elsewhere."""
+        same bytes) and by the library elsewhere; integer_index: indexer keys and queries are small
+        integers in [-8, 8] and head weights integers in [-4, 4] (every indexer score is then exact
+        in fp32 in any summation order, and ties are plentiful); host-drawn sequences only."""
+        self.integer_index = integer_index
+        assert not integer_index or host_seqs is None
         import torch
         import compressed_sparse_attention_step_gb300 as c
         self.c = c
@@ -124,6 +133,9 @@ class GroupCase:
             self.codes, self.scales, self.KI, self.lens = share.codes, share.scales, share.KI, share.lens
             self.__dict__["_kv"] = share.__dict__.setdefault("_kv", {})
             self.__dict__["_ki"] = share.__dict__.setdefault("_ki", {})
+        if share is None and len(self.host_seqs) > 2:   # draw the host sequences' caches in parallel
+            with cf.ThreadPoolExecutor(HOST_THREADS) as ex:
+                list(ex.map(lambda b: (self.h_kv(b), self.h_ki(b)), self.host_seqs))
         for b in (range(B) if share is None else ()):
             Tb = self.T[b]
             pre = Tb - 1 if self.append else Tb
@@ -173,12 +185,23 @@ class GroupCase:
     def h_ki(self, b):
         cache = self.__dict__.setdefault("_ki", {})
         if b not in cache:
-            cache[b] = syn.normal_bf16(self.seed, syn.T_KI, b, (self.cap, DI))
+            cache[b] = (syn.integer_bf16(self.seed, syn.T_KI, b, (self.cap, DI), -8, 8) if self.integer_index
+                        else syn.normal_bf16(self.seed, syn.T_KI, b, (self.cap, DI)))
         return cache[b]
 
     def h_q(self, l, b): return syn.normal_bf16(self.seed, syn.T_Q + self.layer0 + l, b, (self.Nq, H, D))
-    def h_qI(self, l, b): return syn.normal_bf16(self.seed, syn.T_QI + self.layer0 + l, b, (self.Nq, HI, DI))
-    def h_w(self, l, b): return syn.normal_f32(self.seed, syn.T_W + self.layer0 + l, b, (self.Nq, HI))
+
+    def h_qI(self, l, b):
+        tid = syn.T_QI + self.layer0 + l
+        if self.integer_index:
+            return syn.integer_bf16(self.seed, tid, b, (self.Nq, HI, DI), -8, 8)
+        return syn.normal_bf16(self.seed, tid, b, (self.Nq, HI, DI))
+
+    def h_w(self, l, b):
+        tid = syn.T_W + self.layer0 + l
+        if self.integer_index:
+            return syn.bf16_bits_to_f32(syn.integer_bf16(self.seed, tid, b, (self.Nq, HI), -4, 4))
+        return syn.normal_f32(self.seed, tid, b, (self.Nq, HI))
     def h_swa(self, l, b):
         return syn.normal_bf16(self.seed, syn.T_SWA + self.layer0 + l, b, (self.W - 1 + self.Nq, D))
 
@@ -222,43 +245,17 @@ class GroupCase:
         self.c.csa2_group_step(d, self.ws)
         torch.cuda.synchronize()
 
-    def oracle(self, orc, seqs=None, threads=1):
+    def oracle(self, orc, seqs=None, threads=HOST_THREADS):
         """Oracle of the sequences `seqs` (host draws only)."""
         return stack_oracle(orc, [self], seqs, threads)
 
-    def check_queries(self, orc, b, queries):
-        """Compare single queries of sequence b with the oracle run on each alone (one_query_oracle).
-        Indices bit-exact, outputs and lse as in check()."""
-        L, Nq = self.L, self.Nq
-        Tb = self.T[b]
-        codes, scales = orc.fp4_quantize(self.h_kv(b)[:Tb])
-        KI = self.h_ki(b)[:Tb]
-        qs = np.stack([self.h_q(l, b) for l in range(L)])
-        qIs = np.stack([self.h_qI(l, b) for l in range(L)])
-        ws = np.stack([self.h_w(l, b) for l in range(L)])
-        swas = np.stack([self.h_win(l, b) for l in range(L)])
-        qp_all = (np.asarray(self.q_pos, np.int32).reshape(self.B, Nq)[b] if self.q_pos is not None
-                  else self.ratio * Tb - Nq + np.arange(Nq, dtype=np.int32))
-        for i in queries:
-            ref = one_query_oracle(orc, self.modes, Tb, codes, scales, KI, qs, qIs, ws, swas,
-                                   int(self.swa_len_np[b]), i, int(qp_all[i]), K=self.K, W=self.W, ratio=self.ratio,
-                                   swa_fp8=self.swa_fp8)
-            r = b * Nq + i
-            for l in range(L):
-                assert np.array_equal(self.idx[l][r].cpu().numpy(), ref["idx"][l, 0, 0]), f"query {i} layer {l}: indices"
-                assert_attn_close(bf16_host(self.out[l][b, i]), ref["out"][l, 0, 0], f"query {i} layer {l} out")
-                lse = self.lse[l][b, i].cpu().numpy()
-                fin = np.isfinite(ref["lse"][l, 0, 0])
-                assert np.array_equal(np.isfinite(lse), fin)
-                assert np.all(np.abs(lse[fin] - ref["lse"][l, 0, 0][fin]) <= 1e-2), f"query {i} layer {l} lse"
-
-    def check(self, orc, seqs=None, threads=1):
+    def check(self, orc, seqs=None, threads=HOST_THREADS):
         """Compare the device results of `seqs` with the oracle: bit-exact indices (and pools),
         attention outputs within the tolerance, lse within 1e-2 absolute."""
         return check_stack(orc, [self], seqs, threads)
 
 
-def stack_oracle(orc, groups, seqs=None, threads=1):
+def stack_oracle(orc, groups, seqs=None, threads=HOST_THREADS):
     """The oracle of the groups of a decoder stack, run in order on the first group's cache: one
     group step over all their layers (a Reindex layer rescores the latest Full layer's pool)."""
     g0 = groups[0]
@@ -271,7 +268,7 @@ def stack_oracle(orc, groups, seqs=None, threads=1):
     KI = np.zeros((len(seqs), cap, DI), np.uint16)
     for i, b in enumerate(seqs):
         kv = g0.h_kv(b)[:g0.T[b]]
-        codes[i, :g0.T[b]], scales[i, :g0.T[b]] = orc.fp4_quantize(kv)
+        codes[i, :g0.T[b]], scales[i, :g0.T[b]] = orc.fp4_quantize(kv, threads=threads)
         KI[i, :g0.T[b]] = g0.h_ki(b)[:g0.T[b]]
     layers = [(g, l) for g in groups for l in range(g.L)]
     modes = [g.modes[l] for g, l in layers]
@@ -285,7 +282,7 @@ def stack_oracle(orc, groups, seqs=None, threads=1):
                           keep=g0.keep, q_pos=qp, softmax_scale=SCALE, threads=threads, swa_fp8=g0.swa_fp8)
 
 
-def check_stack(orc, groups, seqs=None, threads=1):
+def check_stack(orc, groups, seqs=None, threads=HOST_THREADS):
     """Compare the device results of the groups of a stack (run in order) for the sequences `seqs`
     with stack_oracle: bit-exact indices (and pools), attention outputs within the tolerance, lse
     within 1e-2 absolute."""

@@ -23,6 +23,35 @@ def _score_inputs(seed, B, Nq, cap):
     return qI, w, KI
 
 
+def _adversarial(seed, shape):
+    """bf16 values from {0, +-1, +-2, +-2^12}: products of 2^24, 2^13, 2^12 and small integers make
+    fp32 sums absorb and tie, so any summation order other than the canonical one changes bits."""
+    g = np.random.default_rng(seed)
+    vals = np.array([0.0, 1.0, -1.0, 2.0, -2.0, 4096.0, -4096.0], np.float32)
+    p = np.array([0.6, 0.12, 0.12, 0.05, 0.05, 0.03, 0.03])
+    return syn.f32_to_bf16_bits(g.choice(vals, size=shape, p=p).astype(np.float32))
+
+
+def test_scores_rounding_order_adversarial(orc):
+    """Scores of crafted keys and queries whose fp32 sums depend on the order of every addition (see
+    _adversarial) are bit-identical to the oracle's canonical order; head weights include 1 + 2^-23
+    and 3 so that each weighted product's own rounding matters."""
+    B, Nq, cap = 2, 3, 4096
+    qI = _adversarial(1, (B, Nq, 4, 128))
+    KI = _adversarial(2, (B, cap, 128))
+    w = np.array([[1.0, -1.0, np.float32(1.0 + 2.0 ** -23), 3.0], [0.5, 1.0, 1.0, 1.0], [-1.0, 2.0, 0.25, 1.0]],
+                 np.float32)
+    w = np.broadcast_to(w[None], (B, Nq, 4)).copy()
+    sc = torch.zeros((B * Nq, cap), device="cuda")
+    c.csa2_index_score(bf16_dev(qI), to_dev(w), bf16_dev(KI), to_dev(np.full(B, cap, np.int32)), sc)
+    sc = sc.cpu().numpy()
+    for b in range(B):
+        for i in range(Nq):
+            n = cap - Nq + i + 1
+            exp = orc.index_score(qI[b, i], w[b, i], KI[b], n=n)
+            assert np.array_equal(sc[b * Nq + i, :n].view(np.uint32), exp.view(np.uint32)), (b, i)
+
+
 def test_scores_flat_ragged(orc):
     B, Nq, cap = 3, 2, 1000
     lens = [1000, 517, 3]

@@ -251,21 +251,15 @@ def test_causal_prefill_indices_and_windows(orc):
         assert np.array_equal(out, r["out"][1, 0, i])
 
 
-@pytest.mark.parametrize("swa_len", [23, 10])
-def test_one_query_decomposition_matches_chunk(orc, swa_len):
-    """The single-query oracle the full-size prefill parity test compares against (one query of a
-    chunk run alone over its own window rows) equals the oracle's chunk step query by query, with
-    the whole window valid and with only its last rows valid."""
-    from tests._cases import one_query_oracle
-    Nq, W, T = 8, 16, [700]
-    codes, scales, KI, q, qI, w, swa, _ = _group_inputs(orc, 9, 1, T, 3, Nq=Nq, W=W)
-    q_pos = (np.arange(Nq) + 2 * T[0] - Nq).astype(np.int32)[None]
-    modes = [0, 2, 2]
-    full = orc.group_step(modes, T, codes, scales, KI, q, qI, w, swa, [swa_len], Nq=Nq, K=64, W=W, ratio=2,
-                          q_pos=q_pos, softmax_scale=SCALE)
-    for i in range(Nq):
-        r = one_query_oracle(orc, modes, T[0], codes[0], scales[0], KI[0], q[:, 0], qI[:, 0], w[:, 0], swa[:, 0],
-                             swa_len, i, int(q_pos[0, i]), K=64, W=W, ratio=2)
-        assert np.array_equal(r["idx"][:, 0, 0], full["idx"][:, 0, i])
-        assert np.array_equal(r["out"][:, 0, 0], full["out"][:, 0, i])
-        assert np.array_equal(r["lse"][:, 0, 0], full["lse"][:, 0, i])
+@pytest.mark.parametrize("hier", [False, True])
+def test_group_step_rows_are_independent_of_thread_count(orc, hier):
+    """The group step runs its query rows on host threads; a chunk of queries over ragged
+    sequences gives identical indices, pools, outputs and lse on 1 and on 5 threads."""
+    Nq, W = 6, 16
+    T = [8 * 700 + 5, 8 * 300] if hier else [700, 333]
+    codes, scales, KI, q, qI, w, swa, swa_len = _group_inputs(orc, 15, 2, T, 3, Nq=Nq, W=W)
+    kw = dict(Nq=Nq, K=64, W=W, ratio=1 if hier else 2, hierarchical=hier, keep=256)
+    r1 = orc.group_step([0, 1, 2], T, codes, scales, KI, q, qI, w, swa, swa_len, threads=1, **kw)
+    r5 = orc.group_step([0, 1, 2], T, codes, scales, KI, q, qI, w, swa, swa_len, threads=5, **kw)
+    for key in ("idx", "out", "lse") + (("pool", "pool_len") if hier else ()):
+        assert np.array_equal(r1[key], r5[key]), key

@@ -57,6 +57,132 @@ def test_score_positions_and_error_bound(orc):
 
 
 # ---------------------------------------------------------------------------
+# Rounding order of the score.  bf16 x bf16 products are exact in fp32 (8-bit significands give a
+# 16-bit product), so each fused multiply-add of a chain is exactly one fp32 addition of an exact
+# product.  With products of 2^24 and 1 an addition of 1 to 2^24 is a tie that rounds to even
+# (back to 2^24), while 2^24 + 2 and 2^24 + 4 are exact: the cases below give different bits for
+# every plausible reordering, and their canonical values follow by hand.
+# ---------------------------------------------------------------------------
+BIG = 2.0 ** 12          # BIG * BIG = 2^24
+
+
+def _crafted(products, w):
+    """qI / KI rows whose per-(head, channel) products are the given values: products[h] maps a
+    channel to (q, k) with q * k the product."""
+    q = np.zeros((4, 128), np.float32)
+    k = np.zeros(128, np.float32)
+    for h, chans in products.items():
+        for ch, (qv, kv) in chans.items():
+            q[h, ch] = qv
+            k[ch] = kv
+    return syn.f32_to_bf16_bits(q), np.asarray(w, np.float32), syn.f32_to_bf16_bits(k[None])
+
+
+def test_score_chain_runs_in_increasing_channel_order(orc):
+    # head 0, chain 0: 2^24 at channel 0, then 1 at channels 1..15.  In increasing order every +1 is a
+    # tie that rounds back to 2^24; summed the other way round the ones reach 15 first and
+    # 2^24 + 15 rounds (tie, to even) to 2^24 + 16.
+    prods = {0: {0: (BIG, BIG), **{c: (1.0, 1.0) for c in range(1, 16)}}}
+    qI, w, k = _crafted(prods, [1.0, 0.0, 0.0, 0.0])
+    assert orc.index_score(qI, w, k)[0] == np.float32(2.0 ** 24)
+
+
+def test_score_chain_partials_combine_as_a_fixed_tree(orc):
+    # p0 = 2^24, p1 = p2 = p3 = 1: ((p0 + p1) + (p2 + p3)) = 2^24 + 2, whereas one running sum
+    # gives 2^24 and the reversed running sum 2^24 + 4.
+    prods = {0: {0: (BIG, BIG), 16: (1.0, 1.0), 32: (1.0, 1.0), 48: (1.0, 1.0)}}
+    qI, w, k = _crafted(prods, [1.0, 0.0, 0.0, 0.0])
+    assert orc.index_score(qI, w, k)[0] == np.float32(2.0 ** 24 + 2)
+    # p0 = 2^24 and p4 = p5 = p6 = 1: (2^24) + ((1 + 1) + (1 + 0)) = 2^24 + 3, a tie that rounds
+    # to 2^24 + 4; a running sum keeps 2^24.
+    prods = {0: {0: (BIG, BIG), 64: (1.0, 1.0), 80: (1.0, 1.0), 96: (1.0, 1.0)}}
+    qI, w, k = _crafted(prods, [1.0, 0.0, 0.0, 0.0])
+    assert orc.index_score(qI, w, k)[0] == np.float32(2.0 ** 24 + 4)
+
+
+def test_score_heads_combine_in_pairs(orc):
+    # r0 = 2^24, r1 = r2 = r3 = 1 with unit weights: (w0 r0 + w1 r1) + (w2 r2 + w3 r3) = 2^24 + 2;
+    # a running sum over the heads gives 2^24.
+    prods = {0: {0: (BIG, BIG)}, 1: {1: (1.0, 1.0)}, 2: {2: (1.0, 1.0)}, 3: {3: (1.0, 1.0)}}
+    qI, w, k = _crafted(prods, [1.0, 1.0, 1.0, 1.0])
+    assert orc.index_score(qI, w, k)[0] == np.float32(2.0 ** 24 + 2)
+    # each weighted product is rounded on its own before the sums: with r0 = r1 = 3, w0 = -1 and
+    # w1 = 1 + 2^-23, w1 r1 = 3 + 1.5 * 2^-22 is a tie between 3 + 2^-22 and 3 + 2^-21 (spacing 2^-22
+    # above 2) and rounds to the even 3 + 2^-21, so the score is -3 + (3 + 2^-21) = 2^-21 exactly.
+    # Fusing w1 r1 into the sum with w0 r0 would give 1.5 * 2^-22 instead.
+    prods = {0: {0: (3.0, 1.0)}, 1: {1: (3.0, 1.0)}}
+    w1 = np.float32(1.0 + 2.0 ** -23)
+    qI, w, k = _crafted(prods, [-1.0, w1, 0.0, 0.0])
+    assert orc.index_score(qI, w, k)[0] == np.float32(2.0 ** -21)
+
+
+def test_score_relu_and_signed_zero(orc):
+    # a negative head dot contributes w * (+0); all heads negative with negative weights give -0,
+    # which is an exact zero (Top-K treats -0 and +0 alike)
+    prods = {h: {h: (-1.0, 2.0)} for h in range(4)}
+    qI, w, k = _crafted(prods, [-1.0, -2.0, -3.0, -4.0])
+    s = orc.index_score(qI, w, k)[0]
+    assert s == 0.0
+    # one positive head: only it counts
+    prods = {0: {0: (3.0, 2.0)}, 1: {1: (-1.0, 2.0)}, 2: {2: (-5.0, 1.0)}, 3: {3: (-1.0, 1.0)}}
+    qI, w, k = _crafted(prods, [0.5, 100.0, 100.0, 100.0])
+    assert orc.index_score(qI, w, k)[0] == np.float32(3.0)
+
+
+def _numpy_score(qI, w, KI):
+    """The canonical score restated with numpy fp32 array arithmetic: every product of two bf16
+    values is exact in fp32, so adding it to the chain's running sum is the fused multiply-add."""
+    q = syn.bf16_bits_to_f32(qI)
+    k = syn.bf16_bits_to_f32(KI)
+    w = np.asarray(w, np.float32)
+    r = []
+    for h in range(4):
+        p = []
+        for j in range(8):
+            acc = np.zeros(k.shape[0], np.float32)
+            for ch in range(16 * j, 16 * j + 16):
+                acc = acc + q[h, ch] * k[:, ch]
+            p.append(acc)
+        dot = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]))
+        r.append(np.where(dot > 0, dot, np.float32(0.0)))
+    m = [w[h] * r[h] for h in range(4)]
+    return (m[0] + m[1]) + (m[2] + m[3])
+
+
+def test_score_matches_numpy_restatement_bitwise(orc):
+    for seed in (11, 12):
+        qI = syn.normal_bf16(seed, 1, 0, (4, 128))
+        KI = syn.normal_bf16(seed, 2, 0, (3000, 128))
+        w = syn.normal_f32(seed, 3, 0, (4,))
+        exp = _numpy_score(qI, w, KI)
+        assert exp.dtype == np.float32
+        got = orc.index_score(qI, w, KI)
+        assert np.array_equal(got.view(np.uint32), exp.view(np.uint32)), seed
+
+
+def test_index_select_is_rowwise_score_then_topk(orc):
+    """The batched flat selection equals index_score + topk per row (ragged, causal ratio 2, explicit
+    positions, fewer visible entries than k) and does not depend on the thread count."""
+    B, Nq, cap, k = 3, 5, 900, 64
+    T = np.array([900, 401, 30], np.int64)
+    KI = np.stack([syn.normal_bf16(21, syn.T_KI, b, (cap, 128)) for b in range(B)])
+    qI = np.stack([syn.normal_bf16(21, syn.T_QI, b, (Nq, 4, 128)) for b in range(B)])
+    w = np.stack([syn.normal_f32(21, syn.T_W, b, (Nq, 4)) for b in range(B)])
+    q_pos = np.array([[0, 1, 500, 1700, 1799], [3, 100, 700, 801, 900], [1, 9, 59, 61, 3000]], np.int32)
+    for qp in (None, q_pos):
+        idx1, n1 = orc.index_select(KI, qI, w, T, k, ratio=2, q_pos=qp, threads=1)
+        idx4, n4 = orc.index_select(KI, qI, w, T, k, ratio=2, q_pos=qp, threads=4)
+        assert np.array_equal(idx1, idx4) and np.array_equal(n1, n4)
+        for b in range(B):
+            for i in range(Nq):
+                p = int(qp[b, i]) if qp is not None else 2 * int(T[b]) - Nq + i
+                nv = max(0, min(int(T[b]), (p + 1) // 2))
+                s = orc.index_score(qI[b, i], w[b, i], KI[b], n=nv) if nv else np.zeros(0, np.float32)
+                e, cnt = orc.topk(s, k) if nv else (np.full(k, -1, np.int32), 0)
+                assert np.array_equal(idx1[b, i], e) and n1[b, i] == cnt
+
+
+# ---------------------------------------------------------------------------
 # Top-K
 # ---------------------------------------------------------------------------
 def _check_topk(scores, k, idx, cnt, n_valid=None):

@@ -4,7 +4,7 @@ csa2_sparse_attn_decode_static serves callers that cannot allocate device memory
 (for instance code running inside a memory allocator's callbacks, or a plugin that is handed only
 its input and output buffers): it keeps its split-KV scratch in a fixed array inside the library.
 These tests call it through the C ABI and check that it reproduces csa2_sparse_attn_decode (which
-takes a caller workspace) within the attention tolerance, on two calls in a row (the array keeps the
+takes a caller workspace) bit for bit, on calls in a row of different sizes (the array keeps the
 previous call's contents), and that an oversized problem is refused.  The file is collected last so
 that a run stopping at the first failure has already run every other test.
 """
@@ -46,22 +46,33 @@ def _call_static(q, codes, scales, idx, swa, swa_len, out, lse, n_split=0):
     return st
 
 
-@pytest.mark.parametrize("seed,B", [(71, 7), (72, 64)])
-def test_static_scratch_matches_workspace_entry_point(seed, B):
-    q, codes, scales, idx, swa, swa_len = _inputs(seed, B, 2000, 512, 128)
-    ref = torch.empty((B, 1, 16, 512), dtype=torch.bfloat16, device="cuda")
-    ref_lse = torch.empty((B, 1, 16), dtype=torch.float32, device="cuda")
-    c.csa2_sparse_attn_decode(q, codes, scales, idx, ref, swa=swa, swa_len=swa_len, W=128,
-                              softmax_scale=SCALE, lse=ref_lse)
+def test_static_scratch_matches_workspace_entry_point():
+    """Calls alternate between a batch of 7 queries (automatic split 10) and one of 64 (split 4), so
+    each call starts from the previous call's partials and tickets, over a different ticket range.
+    Both entry points run the same kernel at the same split, so outputs and lse must be identical
+    bit for bit; the first case is also checked against the attention tolerance of the oracle tests'
+    reference, the workspace entry point."""
+    cases = []
+    for seed, B in ((71, 7), (72, 64)):
+        q, codes, scales, idx, swa, swa_len = _inputs(seed, B, 2000, 512, 128)
+        ref = torch.empty((B, 1, 16, 512), dtype=torch.bfloat16, device="cuda")
+        ref_lse = torch.empty((B, 1, 16), dtype=torch.float32, device="cuda")
+        c.csa2_sparse_attn_decode(q, codes, scales, idx, ref, swa=swa, swa_len=swa_len, W=128,
+                                  softmax_scale=SCALE, lse=ref_lse)
+        cases.append(((q, codes, scales, idx, swa, swa_len), ref, ref_lse))
     torch.cuda.synchronize()
-    want = syn.bf16_bits_to_f32(bf16_host(ref)).astype(np.float64)
-    for _ in range(2):   # the second call starts from the first call's leftovers
+    assert c.lib().csa2_attn_auto_split(7, 512, 128) > 1 and c.lib().csa2_attn_auto_split(64, 512, 128) > 1
+    for call in (0, 1, 0, 1, 1, 0):
+        args, ref, ref_lse = cases[call]
+        B = ref.shape[0]
         out = torch.full((B, 1, 16, 512), 9.0, dtype=torch.bfloat16, device="cuda")
         lse = torch.zeros((B, 1, 16), dtype=torch.float32, device="cuda")
-        assert _call_static(q, codes, scales, idx, swa, swa_len, out, lse) == 0
+        assert _call_static(*args, out, lse) == 0
         torch.cuda.synchronize()
-        assert_attn_close(bf16_host(out), want, "static-scratch attention")
-        assert np.allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), atol=1e-2)
+        assert torch.equal(out, ref), f"call of batch {B}: outputs differ from the workspace entry point"
+        assert torch.equal(lse, ref_lse), f"call of batch {B}: lse differs from the workspace entry point"
+        assert_attn_close(bf16_host(out), syn.bf16_bits_to_f32(bf16_host(ref)).astype(np.float64),
+                          "static-scratch attention")
 
 
 def test_static_scratch_refuses_oversized_split():
