@@ -19,7 +19,7 @@ D, H, HI, DI, GROUP, BLOCK = 512, 16, 4, 128, 16, 8
 CODE_BYTES, SCALE_BYTES = 256, 32
 MAX_LAYERS = 16
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
-OP_TOPK, OP_BLOCK_POOL, OP_SPARSE_ATTN, OP_GROUP_STEP, OP_INDEX_SELECT_PREFILL = 1, 2, 3, 4, 5
+OP_TOPK, OP_BLOCK_POOL, OP_SPARSE_ATTN, OP_GROUP_STEP, OP_INDEX_SELECT_PREFILL, OP_MERGE_PAIRS = 1, 2, 3, 4, 5, 6
 FLAG_APPEND_OOB, FLAG_INDEX_OOB, FLAG_TIMEOUT = 1, 2, 4
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TOO_LARGE = 0, 1, 2, 3, 4, 5
 SWA_BF16, SWA_E4M3 = 0, 1
@@ -55,6 +55,7 @@ class GroupDesc(ctypes.Structure):
         ("pool", P), ("pool_len", P),
         ("softmax_scale", F32),
         ("ev_score_begin", P), ("ev_score_end", P),
+        ("ev_attn_begin", P), ("ev_attn_end", P),
     ]
 
 
@@ -93,6 +94,10 @@ def lib():
             "csa2_sparse_attn_decode_static": [P, I32, I32, P, P, I64, P, P, I32, P, P, I32, F32, P, P, I32, P],
             "csa2_sparse_attn_static_scratch_bytes": [],
             "csa2_index_select_prefill": [P, P, I32, I32, P, I64, P, I32, P, I32, P, P, P, SZ, P],
+            "csa2_shard_topk_pairs": [P, I32, I64, I64, P, I32, P, I64, I64, P, P, P, P, SZ, P],
+            "csa2_merge_topk_pairs": [P, P, P, I32, I32, I32, P, P, P, SZ, P],
+            "csa2_shard_indices": [P, I32, I32, I64, I64, P, P],
+            "csa2_attn_merge_shards": [P, P, I32, I32, P, P, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -292,10 +297,11 @@ def group_workspace_size(B, Nq, cap, K=512, W=128, hierarchical=False, keep=2048
 def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa, swa_len, out, idx,
                     K=512, W=128, ratio=1, hierarchical=False, keep=2048, n_split=0, q_pos=None,
                     block_keys=None, pool=None, pool_len=None, kv_new=None, ki_new=None, lse=None,
-                    softmax_scale=None, events=None, seq_chunks=0, swa_fp8=False):
+                    softmax_scale=None, events=None, seq_chunks=0, swa_fp8=False, attn_events=None):
     """Build a csa2_group_desc from torch tensors (per-layer arguments are lists; entries of
     qI/w/idx may be None for Reuse layers; swa_fp8: the window buffers are uint8 E4M3 rows, as
-    csa2_fp8_quantize writes them)."""
+    csa2_fp8_quantize writes them; events / attn_events: (begin, end) torch.cuda.Event pairs
+    recorded around the step's first indexer scan / first attention launch)."""
     torch = _torch()
     L = len(modes)
     if not 1 <= L <= MAX_LAYERS:
@@ -340,6 +346,9 @@ def make_group_desc(modes, *, B, Nq, cap, lens, codes, scales, KI, q, qI, w, swa
     if events is not None:
         g.ev_score_begin = events[0].cuda_event
         g.ev_score_end = events[1].cuda_event
+    if attn_events is not None:
+        g.ev_attn_begin = attn_events[0].cuda_event
+        g.ev_attn_end = attn_events[1].cuda_event
     return g
 
 
@@ -367,3 +376,59 @@ def csa2_device_flags(clear=True, stream=None):
     v = ctypes.c_uint32(0)
     _check("csa2_device_flags", lib().csa2_device_flags(ctypes.byref(v), int(clear), _stream(stream)))
     return int(v.value)
+
+
+# ---------------------------------------------------------------------------------------------
+# context split of one sequence over G shards
+# ---------------------------------------------------------------------------------------------
+def csa2_shard_topk_pairs(scores, k, pair_score, pair_pos, *, n_valid=None, n=None, pos_offset=0, map_=None,
+                          pair_n=None, ws=None, stream=None):
+    """A shard's local Top-k of scores fp32 [rows, ld] as (score, global position) pairs: pair_score
+    fp32 [rows, k], pair_pos int32 [rows, k] (ascending, -1 padded), pair_n int32 [rows]."""
+    torch = _torch()
+    rows, ld = scores.shape
+    n = ld if n is None else n
+    map_ld = map_.shape[-1] if map_ is not None else 0
+    need = workspace_size(OP_TOPK, B=rows, Nq=1, n=n, k=k)
+    if ws is None and need:
+        ws = _ws(need, scores.device)
+    _check("csa2_shard_topk_pairs", lib().csa2_shard_topk_pairs(
+        _ptr(scores, "scores", (torch.float32,)), rows, n, ld, _ptr(n_valid, "n_valid", (torch.int32,), rows), k,
+        _ptr(map_, "map", (torch.int32,)), map_ld, int(pos_offset),
+        _ptr(pair_score, "pair_score", (torch.float32,), rows * k), _ptr(pair_pos, "pair_pos", (torch.int32,), rows * k),
+        _ptr(pair_n, "pair_n", (torch.int32,), rows), _ptr(ws, "ws"), _nbytes(ws), _stream(stream)))
+
+
+def csa2_merge_topk_pairs(pair_score, pair_pos, idx, *, pair_n=None, n_sel=None, ws=None, stream=None):
+    """The exact Top-k of G shards' pairs: pair_score fp32 [G, rows, k], pair_pos int32 [G, rows, k],
+    pair_n int32 [G, rows] (shards in ascending order of their position ranges) -> idx int32 [rows, k]."""
+    torch = _torch()
+    G, rows, k = pair_score.shape
+    need = workspace_size(OP_MERGE_PAIRS, B=rows, Nq=1, n=G, k=k)
+    if ws is None:
+        ws = _ws(need, pair_score.device)
+    _check("csa2_merge_topk_pairs", lib().csa2_merge_topk_pairs(
+        _ptr(pair_score, "pair_score", (torch.float32,), G * rows * k),
+        _ptr(pair_pos, "pair_pos", (torch.int32,), G * rows * k), _ptr(pair_n, "pair_n", (torch.int32,), G * rows),
+        G, rows, k, _ptr(idx, "idx", (torch.int32,), rows * k), _ptr(n_sel, "n_sel", (torch.int32,), rows),
+        _ptr(ws, "ws"), _nbytes(ws), _stream(stream)))
+
+
+def csa2_shard_indices(idx, lo, hi, idx_local, stream=None):
+    """The selected positions a shard holding entries [lo, hi) attends, as its local rows (-1 elsewhere)."""
+    torch = _torch()
+    rows, k = idx.shape
+    _check("csa2_shard_indices", lib().csa2_shard_indices(
+        _ptr(idx, "idx", (torch.int32,)), rows, k, int(lo), int(hi),
+        _ptr(idx_local, "idx_local", (torch.int32,), rows * k), _stream(stream)))
+
+
+def csa2_attn_merge_shards(out_g, lse_g, out, lse=None, stream=None):
+    """out_g [G, rows, 16, 512] bf16 and lse_g fp32 [G, rows, 16] -> out [rows, 16, 512], lse [rows, 16]."""
+    torch = _torch()
+    G = out_g.shape[0]
+    rows = out_g[0].numel() // (H * D)
+    _check("csa2_attn_merge_shards", lib().csa2_attn_merge_shards(
+        _ptr(out_g, "out_g", _bf16_types(), G * rows * H * D), _ptr(lse_g, "lse_g", (torch.float32,), G * rows * H),
+        G, rows, _ptr(out, "out", _bf16_types(), rows * H * D), _ptr(lse, "lse", (torch.float32,), rows * H),
+        _stream(stream)))

@@ -45,9 +45,14 @@ namespace {
 using namespace attn;
 
 constexpr int kMaxTiles = (CSA2_MAX_ATTN_K + kRows - 1) / kRows + (CSA2_MAX_W + kRows - 1) / kRows;
-constexpr int kIssuers = 4;          // warps whose lane 0 issues tensor-core work (independent chains)
-constexpr uint32_t kOCol = 16 * kIssuers;  // S^T partial i in columns [16 i, 16 i + 16); O^T block i at kOCol + 16 i
-constexpr uint32_t kTmemCols = 128;
+constexpr int kSIssuers = 8;         // warps whose lane 0 issues a 64-channel eighth of S^T (independent chains)
+constexpr int kOIssuers = 4;         // warps whose lane 0 issues a 128-channel block of O^T
+constexpr uint32_t kOCol = 16 * kSIssuers;  // S^T partial i in columns [16 i, 16 i + 16); O^T block i at kOCol + 16 i
+constexpr uint32_t kTmemCols = 256;
+// Lazy rescaling: a head's running offset moves only when a tile's maximum exceeds it by more than
+// this many (log2 units), so P = 2^(x - m) stays below 2^8 and the accumulated O^T and sums are
+// rescaled only on such a jump.
+constexpr float kLazy = 8.0f;
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr uint32_t kTileGroup = kRows * 128;                 // 8 KiB per 64-channel group
@@ -60,14 +65,15 @@ constexpr uint32_t kRawScOff = kRawOff + kRows * CSA2_CODE_BYTES;  // staged sca
 constexpr uint32_t kMiscOff = kRawScOff + kRows * CSA2_SCALE_BYTES;
 
 struct Misc {
-  unsigned long long mbar;
+  unsigned long long mbar_s;      // S^T of a tile complete (one arrival per S issuer)
+  unsigned long long mbar_o;      // O^T of a tile complete (one arrival per O issuer)
   uint32_t tmem_base;
   int is_last;
   int32_t pos[kMaxTiles][kRows];  // source row of each row of the CTA's tiles, -1 if empty
-  float red[4][CSA2_H];           // per-quarter partial max / sum
-  float m_run[CSA2_H];            // running maximum (log2 units), per head
-  float l_run[CSA2_H];            // running sum, per head
-  float corr[CSA2_H];             // rescale factor of the current tile, per head
+  float red[4][CSA2_H];           // per-quarter tile maximum, then (at the end) partial sums
+  float m_run[2][CSA2_H];         // running offset (log2 units) per head, by tile parity
+  float corr[CSA2_H];             // rescale factor of a tile that moved an offset, per head
+  float l_fin[CSA2_H];            // final sum per head
 };
 constexpr size_t kSmemBytes = 1024 + kMiscOff + sizeof(Misc);
 
@@ -90,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   unsigned char* base = smem_raw + (base_s - raw_s);
   Misc& ms = *reinterpret_cast<Misc*>(base + kMiscOff);
   const uint32_t tile_s = base_s + kTileOff, q_s = base_s + kQOff, p_s = base_s + kPOff;
-  const uint32_t mbar = smem_u32(&ms.mbar);
+  const uint32_t mbar_s = smem_u32(&ms.mbar_s), mbar_o = smem_u32(&ms.mbar_o);
 
   // blockIdx.z: the layer; blockIdx.y: the query (its selected rows are the same in every layer);
   // ginst: the instance's slot in the split workspace and tickets
@@ -150,13 +156,14 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   };
 
   if (t < CSA2_H) {
-    ms.m_run[t] = -INFINITY;
-    ms.l_run[t] = 0.0f;
+    ms.m_run[0][t] = -INFINITY;
+    ms.l_fin[t] = 0.0f;
   }
   if (first_live >= 0) {
-    // tensor memory, the MMA barrier, and the first window tile's rows, before anything waits
+    // tensor memory, the MMA barriers, and the first window tile's rows, before anything waits
     if (t == 0) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(mbar), "r"(kIssuers) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(mbar_s), "r"(kSIssuers) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(mbar_o), "r"(kOIssuers) : "memory");
       asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (warp == 0) {
@@ -229,15 +236,18 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   };
 
   bool ok = true;
+  int par = 0;  // parity of the running offsets in use
   if (first_live >= 0) {
     tc_fence_after();
     const uint32_t tmem = ms.tmem_base;
     const uint32_t t_lane = tmem + (uint32_t(32 * quarter) << 16);  // this warp's lane quarter
     const int first_fp4 = next_live(max(first_live, nwin));
     if (first_fp4 <= last_live) stage_fp4(first_fp4);  // first FP4 tile, behind any window tile's copy
-    uint32_t phase = 0;
+    uint32_t ph_s = 0, ph_o = 0;
     int q_kind = -1;  // 0: Q staged as f16, 1: as bf16
     bool first = true;
+    // running sum of this lane's head (8 half + lane / 4) over this warp's rows
+    float l_w = 0.0f;
 
     for (int tile = first_live; tile <= last_live; ++tile) {
       if (!live(tile)) continue;
@@ -272,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
       }
       // -- the previous tile's O^T MMAs read the operand tile and P^T: wait for them
       if (!first) {
-        ok = ok && mbar_wait(mbar, phase);
-        phase ^= 1u;
+        ok = ok && mbar_wait(mbar_o, ph_o);
+        ph_o ^= 1u;
       }
       // -- Q in the tile's operand type
       const int kind = f16_tile ? 0 : 1;
@@ -346,40 +356,43 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
       fence_async_smem();
       __syncthreads();
 
-      // -- S^T = K Q^T (tensor core): warp i < 4 issues channels [128 i, 128 i + 128) in 8 steps
-      if (lane == 0 && warp < kIssuers) {
+      // -- S^T = K Q^T (tensor core): warp i < 8 issues the 64 channels [64 i, 64 i + 64) in 4 steps
+      if (lane == 0 && warp < kSIssuers) {
         tc_fence_after();
         const uint32_t id = instr_desc(kRows, !f16_tile, false);
 #pragma unroll
-        for (int k8 = 0; k8 < CSA2_D / 16 / kIssuers; ++k8) {
-          const int kk = warp * (CSA2_D / 16 / kIssuers) + k8;
-          const uint32_t off = uint32_t(kk & 3) * 32u;  // 16 channels = 32 B inside the swizzle atom
-          const uint64_t a = smem_desc(tile_s + uint32_t(kk >> 2) * kTileGroup + off, 0, 1024);
-          const uint64_t bq = smem_desc(q_s + uint32_t(kk >> 2) * kQGroup + off, 0, 1024);
-          umma_f16(tmem + uint32_t(16 * warp), a, bq, id, k8 > 0 ? 1u : 0u);
+        for (int k4 = 0; k4 < CSA2_D / 16 / kSIssuers; ++k4) {
+          const uint32_t off = uint32_t(k4) * 32u;  // 16 channels = 32 B inside the swizzle atom
+          const uint64_t a = smem_desc(tile_s + uint32_t(warp) * kTileGroup + off, 0, 1024);
+          const uint64_t bq = smem_desc(q_s + uint32_t(warp) * kQGroup + off, 0, 1024);
+          umma_f16(tmem + uint32_t(16 * warp), a, bq, id, k4 > 0 ? 1u : 0u);
         }
-        umma_commit(mbar);
+        umma_commit(mbar_s);
       }
       // -- the staging buffer is free again: copy the next FP4 tile while this one is computed
       if (is_fp4) {
         const int nxt = next_live(tile + 1);
         if (nxt <= last_live) stage_fp4(nxt);
       }
-      ok = ok && mbar_wait(mbar, phase);
-      phase ^= 1u;
+      ok = ok && mbar_wait(mbar_s, ph_s);
+      ph_s ^= 1u;
       tc_fence_after();
 
       // -- online softmax: warp (quarter, half) holds rows 16 quarter + lane (lanes < 16) and
-      //    heads 8 half .. 8 half + 7; S^T is the sum of the four channel-quarter partials
+      //    heads 8 half .. 8 half + 7; S^T is the sum of the eight channel-eighth partials
       const int row = 16 * quarter + (lane & 15);
       float x[8];
       {
-        float sp[4][8];
-        tmem_ld8x4(t_lane + uint32_t(8 * half), sp);
+        // ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)), the first half summed before the second loads
+        float sp[4][8], lo4[8];
+        tmem_ld8x4(t_lane + uint32_t(8 * half), sp);  // partials 0..3
+#pragma unroll
+        for (int j = 0; j < 8; ++j) lo4[j] = (sp[0][j] + sp[1][j]) + (sp[2][j] + sp[3][j]);
+        tmem_ld8x4(t_lane + 64u + uint32_t(8 * half), sp);  // partials 4..7
         const bool row_ok = lane < 16 && pos[row] >= 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          x[j] = row_ok ? ((sp[0][j] + sp[1][j]) + (sp[2][j] + sp[3][j])) * scale_log2 : -INFINITY;
+          x[j] = row_ok ? (lo4[j] + ((sp[0][j] + sp[1][j]) + (sp[2][j] + sp[3][j]))) * scale_log2 : -INFINITY;
       }
       {
         const float mx = reduce_scatter8<true>(x, lane);
@@ -387,19 +400,26 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
       }
       tc_fence_before();
       __syncthreads();
-      if (t < CSA2_H) {
-        const float mt = fmaxf(fmaxf(ms.red[0][t], ms.red[1][t]), fmaxf(ms.red[2][t], ms.red[3][t]));
-        const float mo = ms.m_run[t], mn = fmaxf(mo, mt);
-        ms.corr[t] = mn == -INFINITY ? 1.0f : exp2f(mo - mn);
-        ms.m_run[t] = mn;
-      }
-      __syncthreads();
-      float pr[8];
+      // every thread derives the new offsets of its half's heads itself from the four quarters'
+      // maxima; threads t < 16 publish head t's offset and correction factor
+      const float* m_old = ms.m_run[par];
+      float* m_new = ms.m_run[par ^ 1];
+      float mj[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float mn = ms.m_run[8 * half + j];
-        pr[j] = mn == -INFINITY ? 0.0f : exp2f(x[j] - mn);
+        const int h = 8 * half + j;
+        const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+        mj[j] = mt > m_old[h] + kLazy ? mt : m_old[h];
       }
+      if (t < CSA2_H) {
+        const float mt = fmaxf(fmaxf(ms.red[0][t], ms.red[1][t]), fmaxf(ms.red[2][t], ms.red[3][t]));
+        const float mo = m_old[t], mn = mt > mo + kLazy ? mt : mo;
+        m_new[t] = mn;
+        ms.corr[t] = (mn != mo && mo != -INFINITY) ? exp2f(mo - mn) : 1.0f;
+      }
+      float pr[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) pr[j] = mj[j] == -INFINITY ? 0.0f : exp2f(x[j] - mj[j]);
       // P^T (heads x rows, K-major, 128-byte swizzle): element (h, row)
       if (lane < 16) {
 #pragma unroll
@@ -410,32 +430,39 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
           *reinterpret_cast<uint16_t*>(base + kPOff + off) = bits;
         }
       }
-      const float sum = reduce_scatter8<false>(pr, lane);
-      // rescale the O^T accumulated so far (channel blocks 2 half, 2 half + 1 of this lane quarter)
-      if (!first) {
-        bool any = false;
-#pragma unroll
-        for (int h = 0; h < 16; ++h) any |= ms.corr[h] != 1.0f;
-        if (any) {
-          const uint32_t ta = t_lane + kOCol + uint32_t(32 * half);
-          float o[2][16];
-          tmem_ld16x2(ta, o);
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int h = 0; h < 16; ++h) o[j][h] *= ms.corr[h];
-          tmem_st16x2(ta, o);
-        }
+      const float sum = reduce_scatter8<false>(pr, lane);  // this warp's rows, head 8 half + lane / 4
+      {
+        const int h = 8 * half + (lane >> 2);
+        const float mo = m_old[h];
+        const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+        const float mn = mt > mo + kLazy ? mt : mo;
+        const float cr = (mn != mo && mo != -INFINITY) ? exp2f(mo - mn) : 1.0f;
+        l_w = l_w * cr + sum;
       }
-      if ((lane & 3) == 0) ms.red[quarter][8 * half + (lane >> 2)] = sum;
       fence_async_smem();
       tc_fence_before();
       __syncthreads();
-      if (t < CSA2_H)
-        ms.l_run[t] = ms.l_run[t] * ms.corr[t] + ((ms.red[0][t] + ms.red[1][t]) + (ms.red[2][t] + ms.red[3][t]));
+      par ^= 1;
+      bool moved = false;  // an offset moved: the accumulated O^T is rescaled (the same on every thread)
+#pragma unroll
+      for (int h = 0; h < CSA2_H; ++h) moved |= ms.corr[h] != 1.0f;
+      if (moved) {
+        // rescale the O^T accumulated so far (channel blocks 2 half, 2 half + 1 of this lane quarter)
+        tc_fence_after();
+        const uint32_t ta = t_lane + kOCol + uint32_t(32 * half);
+        float o[2][16];
+        tmem_ld16x2(ta, o);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int h = 0; h < 16; ++h) o[j][h] *= ms.corr[h];
+        tmem_st16x2(ta, o);
+        tc_fence_before();
+        __syncthreads();
+      }
 
       // -- O^T += V^T P^T (tensor core): warp i < 4 issues channel block i in 4 steps of 16 rows
-      if (lane == 0 && warp < kIssuers) {
+      if (lane == 0 && warp < kOIssuers) {
         tc_fence_after();
         const uint32_t id = instr_desc(128, !f16_tile, true);
         const int i = warp;
@@ -445,14 +472,17 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
           const uint64_t bp = smem_desc(p_s + uint32_t(s) * 32u, 0, 1024);
           umma_f16(tmem + kOCol + uint32_t(16 * i), a, bp, id, (first && s == 0) ? 0u : 1u);
         }
-        umma_commit(mbar);
+        umma_commit(mbar_o);
       }
       first = false;
     }
-    // ---- last tile's MMAs, then O^T out of tensor memory ---------------------------------------------
-    ok = ok && mbar_wait(mbar, phase);
+    // ---- last tile's MMAs, the sums per head, then O^T out of tensor memory -------------------------
+    ok = ok && mbar_wait(mbar_o, ph_o);
     tc_fence_after();
-    __syncthreads();  // l_run of the last tile
+    if ((lane & 3) == 0) ms.red[quarter][8 * half + (lane >> 2)] = l_w;
+    __syncthreads();
+    if (t < CSA2_H) ms.l_fin[t] = (ms.red[0][t] + ms.red[1][t]) + (ms.red[2][t] + ms.red[3][t]);
+    __syncthreads();
     if (inputs_ready) {
       pdl_wait();
       pdl_trigger();
@@ -466,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D + ch;
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
-          const float l = ms.l_run[h];
+          const float l = ms.l_fin[h];
           orow[h * CSA2_D] = uint16_t(f2bf_bits(o[j][h] * (l > 0.0f ? 1.0f / l : 0.0f)));
         }
       } else {
@@ -495,8 +525,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
 
   if (n_split == 1) {
     if (lse && t < CSA2_H) {
-      const float l = ms.l_run[t];
-      lse[int64_t(inst) * CSA2_H + t] = l > 0.0f ? (ms.m_run[t] + log2f(l)) * kLn2 : -INFINITY;
+      const float l = ms.l_fin[t];
+      lse[int64_t(inst) * CSA2_H + t] = l > 0.0f ? (ms.m_run[par][t] + log2f(l)) * kLn2 : -INFINITY;
     }
     return;
   }
@@ -505,8 +535,8 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   float* mlb = ws + instances * n_split * (CSA2_H * CSA2_D);
   if (t < CSA2_H) {
     float* ml = mlb + (ginst * n_split + split) * (2 * CSA2_H);
-    ml[2 * t] = ms.m_run[t];
-    ml[2 * t + 1] = ms.l_run[t];
+    ml[2 * t] = ms.m_run[par][t];
+    ml[2 * t + 1] = ms.l_fin[t];
   }
   __threadfence();
   __syncthreads();

@@ -261,6 +261,8 @@ cudaError_t launch_bitmap_select(const uint16_t* qI, const float* w, int B, int 
                                  const uint32_t* bitmap, int64_t n_words, const uint32_t* ubound,
                                  const int32_t* order, int32_t* idx, int32_t* n_sel, cudaStream_t st);
 int bitmap_list_cap();  // marked keys that one list round of the selection rescores
+// Context split: workspace of csa2_merge_topk_pairs for G shards' k pairs per row (shard.cu).
+size_t merge_pairs_ws_bytes(int rows, int G, int k);
 int attn_auto_split(int64_t instances, int k, int W);
 
 // Library-owned side stream (highest priority) and events of the current device, created on first

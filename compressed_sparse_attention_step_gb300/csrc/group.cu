@@ -127,6 +127,10 @@ extern "C" size_t csa2_workspace_size(int op, const csa2_dims* d) {
     }
     case CSA2_OP_INDEX_SELECT_PREFILL:
       return csa2::prefill_ws_bytes(rows, d->cap, d->B);
+    case CSA2_OP_MERGE_PAIRS:
+      return (d->n >= 1 && d->n <= 64 && d->k >= 1 && d->k <= CSA2_MAX_K)
+                 ? csa2::merge_pairs_ws_bytes(int(rows), int(d->n), d->k)
+                 : 0;
     case CSA2_OP_GROUP_STEP:
       return csa2::group_ws_layout(d->B, d->Nq, d->cap, d->k, d->W, d->hierarchical, d->n_blocks_keep,
                                    d->n_split)
@@ -329,6 +333,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   }
   if (zeroed && !zero_done && !ok(csa2::launch_zero(wsb + zero_lo, zero_hi - zero_lo, st))) return CSA2_ERR_CUDA;
   if (!rec(g->ev_score_begin, st)) return CSA2_ERR_CUDA;
+  bool attn_timed = false;  // the attention event pair brackets the step's first attention launch
 
   for (int c = 0; c < n_chunks; ++c) {
     const int b0 = int(int64_t(g->B) * c / n_chunks), b1 = int(int64_t(g->B) * (c + 1) / n_chunks);
@@ -363,9 +368,13 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
       int ns = csa2::attn_effective_split(
           K, g->W, g->n_split ? g->n_split : std::min(csa2::attn_auto_split(inst, K, g->W), n_chunks > 1 ? 4 : 32));
       while (ns > 1 && csa2::attn_ws_bytes(inst, ns) > attn_cap) --ns;
+      const bool timed = !attn_timed;
+      attn_timed = true;
+      if (timed && !rec(g->ev_attn_begin, aux)) return false;
       const bool r = ok(csa2::launch_sparse_attn_layers(run, run_n, Bc, Nq, codes, scl, g->cap, run_idx, nullptr, K,
                                                          swl, g->W, g->softmax_scale, ns, attn_ws, aux, zeroed,
                                                          false, g->swa_format == CSA2_SWA_E4M3));
+      if (timed && !rec(g->ev_attn_end, aux)) return false;
       run_n = 0;
       return r;
     };

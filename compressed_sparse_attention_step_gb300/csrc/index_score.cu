@@ -7,9 +7,9 @@
 // share one position, each lane owning 16 consecutive channels (32 bytes), so a warp covers four
 // whole 256-byte rows per step.  The indexer query slice (4 heads x 16 channels) stays in
 // registers for the whole CTA.  Contiguous keys (a sequence's cache or its block keys) stream
-// through shared memory by bulk asynchronous copies (index_score_stream_kernel, below); candidate
-// pools, whose positions are gathered, use register loads with four steps in flight per lane
-// (index_score_kernel).
+// through shared memory by bulk asynchronous copies (index_score_stream_kernel, below); so do
+// candidate pools, whose gathered rows arrive as one bulk copy each.  The register-loaded form
+// (index_score_kernel, four steps in flight per lane) serves keys that are not 16-byte aligned.
 //
 // The fp32 result is bit-identical to the canonical order: per head, lane j computes the
 // fused-multiply-add chain p_j over channels 16j..16j+15 from +0; the 8-lane reduction is a
@@ -195,10 +195,14 @@ __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// kCand: the positions are gathered from a candidate pool (ascending cache positions, cand_len[row]
+// valid): each step's 16 key rows arrive as 16 bulk copies of 256 bytes, issued by lanes 0..15.
+template <bool kCand>
 __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
     const uint16_t* __restrict__ qI, const float* __restrict__ w, int Nq,
     const uint16_t* __restrict__ KI, int64_t key_stride_rows, const int32_t* __restrict__ lens,
-    int64_t cap_entries, int block_div, int ratio, const int32_t* __restrict__ q_pos,
+    int64_t cap_entries, int block_div, const int32_t* __restrict__ cand, const int32_t* __restrict__ cand_len,
+    int64_t n_cand, int ratio, const int32_t* __restrict__ q_pos,
     float* __restrict__ scores, int64_t ld, int32_t* __restrict__ n_valid_out, int64_t chunk,
     unsigned int* flags) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -209,13 +213,36 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
   const int64_t T = min(max(int64_t(lens[b]), int64_t(0)), cap_entries);
   const int64_t p = q_pos ? int64_t(q_pos[row]) : int64_t(ratio) * T - Nq + qi;
   const int64_t nvis = (p + 1 < 0) ? 0 : min((p + 1) / ratio, T);
-  const int64_t nv = nvis / block_div;  // scored prefix of this row
+  int64_t nv;  // scored prefix of this row
+  const int32_t* crow = nullptr;
+  if (kCand) {
+    crow = cand + int64_t(row) * n_cand;
+    const int64_t cl = min(max(int64_t(cand_len[row]), int64_t(0)), n_cand);
+    int64_t lo = 0, hi = cl;  // first pool entry not visible (the pool is ascending)
+    if (cl > 0 && int64_t(crow[cl - 1]) < nvis) lo = hi;  // all visible (every decode query): no search
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (int64_t(crow[mid]) < nvis) lo = mid + 1;
+      else hi = mid;
+    }
+    nv = lo;
+  } else {
+    nv = nvis / block_div;
+  }
   if (n_valid_out && blockIdx.x == 0 && threadIdx.x == 0) n_valid_out[row] = int32_t(nv);
 
   const int64_t c0 = int64_t(blockIdx.x) * chunk;
   const int64_t c1 = min(c0 + chunk, ld);
   if (c0 >= c1) return;
-  const int64_t lend = min(min(nv, c1), key_stride_rows);  // positions below this are read
+  // positions below this are read (contiguous keys: also inside the cache)
+  const int64_t lend = kCand ? min(nv, c1) : min(min(nv, c1), key_stride_rows);
+  // a gathered position that can be read
+  auto readable = [&](int64_t t) {
+    if (t >= lend) return false;
+    if (!kCand) return true;
+    const int32_t q = crow[t];
+    return q >= 0 && int64_t(q) < key_stride_rows;
+  };
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane >> 3;
@@ -233,23 +260,48 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
   const uint16_t* kseq = KI + int64_t(b) * key_stride_rows * CSA2_DI;
   const int64_t first = c0 + int64_t(warp) * kPosPerWarpIt;
   const int n_steps = first < c1 ? int((c1 - first + kPosPerCtaIt - 1) / kPosPerCtaIt) : 0;
-  // step i covers positions first + i * kPosPerCtaIt + [0, 16); the keys of those below lend
+  // step i covers positions first + i * kPosPerCtaIt + [0, 16); the keys of those below lend.
+  // Called by the whole warp: contiguous keys are one copy by lane 0; gathered keys one copy per
+  // readable position by lanes 0..15 (row slot = position - base), after lane 0 has announced
+  // their bytes.  An unreadable gathered position below lend is flagged.
   auto issue = [&](int i) {
     const int64_t base = first + int64_t(i) * kPosPerCtaIt;
     const int64_t cnt = min(max(lend - base, int64_t(0)), int64_t(kPosPerWarpIt));
-    const uint32_t bytes = uint32_t(cnt) * CSA2_DI * 2u;
     const uint32_t bar = bars + 8u * uint32_t(i % kStages);
     const uint32_t dst = ring + uint32_t(i % kStages) * kStepBytes;
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
-    if (bytes)
+    if (!kCand) {
+      const uint32_t bytes = uint32_t(cnt) * CSA2_DI * 2u;
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+        if (bytes)
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+              "l"(kseq + base * CSA2_DI), "r"(bytes), "r"(bar)
+              : "memory");
+      }
+      return;
+    }
+    const bool mine = lane < cnt;
+    const int32_t q = mine ? crow[base + lane] : -1;
+    const bool rd = mine && q >= 0 && int64_t(q) < key_stride_rows;
+    if (mine && !rd) atomicOr(flags, CSA2_FLAG_INDEX_OOB);
+    const uint32_t n_rd = __popc(__ballot_sync(0xffffffffu, rd));
+    if (lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar),
+                   "r"(n_rd * uint32_t(CSA2_DI * 2))
+                   : "memory");
+    }
+    __syncwarp();
+    if (rd)
       asm volatile(
-          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-          "l"(kseq + base * CSA2_DI), "r"(bytes), "r"(bar)
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+              dst + uint32_t(lane) * uint32_t(CSA2_DI * 2)),
+          "l"(kseq + int64_t(q) * CSA2_DI), "r"(uint32_t(CSA2_DI * 2)), "r"(bar)
           : "memory");
   };
-  if (lane == 0)
-    for (int i = 0; i < min(n_steps, kStages); ++i) issue(i);
+  for (int i = 0; i < min(n_steps, kStages); ++i) issue(i);
 
   float qf[4][16];
   const uint16_t* qrow = qI + int64_t(row) * (CSA2_HI * CSA2_DI);
@@ -272,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
   int done = n_steps;
   for (int i = 0; i < n_steps; ++i) {
     const int64_t base = first + int64_t(i) * kPosPerCtaIt;
-    if (!stage_wait(bars + 8u * uint32_t(i % kStages), uint32_t(i / kStages) & 1u)) {
+    // the whole warp agrees on the outcome (the copies it issues next are warp-collective)
+    if (!__all_sync(0xffffffffu, stage_wait(bars + 8u * uint32_t(i % kStages), uint32_t(i / kStages) & 1u))) {
       if (lane == 0) atomicOr(flags, CSA2_FLAG_TIMEOUT);
       done = i;
       break;
@@ -281,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
       const int64_t t = base + u * 4 + sub;
-      const bool ok = t < lend;
+      const bool ok = readable(t);
       const uint4* kp = reinterpret_cast<const uint4*>(stg + (u * 4 + sub) * (CSA2_DI * 2) + 32 * j);
       const uint4 k0 = kp[0], k1 = kp[1];
       const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
@@ -311,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
       if (j == 0 && t < c1) srow[t] = ok ? sc : -INFINITY;
     }
     __syncwarp();  // every lane has read the stage before it is refilled
-    if (lane == 0 && i + kStages < n_steps) issue(i + kStages);
+    if (i + kStages < n_steps) issue(i + kStages);
   }
   if (done < n_steps) {
     // gave up waiting: wait (bounded) for the copies still in flight before the CTA leaves
@@ -329,28 +382,36 @@ cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq
                                int64_t ld, int32_t* n_valid, cudaStream_t st) {
   const int64_t rows = int64_t(B) * Nq;
   if (rows == 0 || ld == 0) return cudaSuccess;
-  // chunk: a multiple of the CTA step, sized for at least ~8 CTAs per SM over the grid
-  int64_t chunk = (rows * ld + 152 * 8 - 1) / (152 * 8);
+  // chunk: a multiple of the CTA step.  Contiguous keys: sized for at least ~8 CTAs per SM over the
+  // grid, at most 2048 positions.  Gathered keys (a pool, a few MB in all): one wave of two CTAs per
+  // SM, so that every warp keeps its whole ring of copies in flight.
+  const int64_t per = cand ? 152 * 2 : 152 * 8;
+  int64_t chunk = (rows * ld + per - 1) / per;
   chunk = ((chunk + kPosPerCtaIt - 1) / kPosPerCtaIt) * kPosPerCtaIt;
   chunk = max(int64_t(kPosPerCtaIt), min(chunk, int64_t(2048)));
   const dim3 grid(unsigned((ld + chunk - 1) / chunk), unsigned(rows));
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
-  if (!cand) {
-    // contiguous keys: the bulk-copy streaming kernel
-    static std::atomic<bool> attr_set[64];  // per device; set once, by any host thread
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-      const cudaError_t e = cudaFuncSetAttribute(index_score_stream_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(kStreamSmem));
-      if (e != cudaSuccess) return e;
-      attr_set[dev] = true;
-    }
-    if ((reinterpret_cast<uintptr_t>(KI) & 15u) == 0)
-      return launch_pdl(index_score_stream_kernel, grid, dim3(kThreads), kStreamSmem, st, qI, w, Nq, KI,
-                        key_stride_rows, lens, cap_entries, block_div, ratio, q_pos, scores, ld, n_valid, chunk,
-                        flags);
+  static std::atomic<bool> attr_set[2][64];  // per kernel and device; set once, by any host thread
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int kind = cand ? 1 : 0;
+  if (dev < 64 && !attr_set[kind][dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(cand ? index_score_stream_kernel<true> : index_score_stream_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, int(kStreamSmem));
+    if (e != cudaSuccess) return e;
+    attr_set[kind][dev] = true;
+  }
+  // keys are read by bulk copies, which need 16-byte aligned sources (every 256-byte row of an
+  // aligned KI is)
+  if ((reinterpret_cast<uintptr_t>(KI) & 15u) == 0) {
+    if (cand)
+      return launch_pdl(index_score_stream_kernel<true>, grid, dim3(kThreads), kStreamSmem, st, qI, w, Nq, KI,
+                        key_stride_rows, lens, cap_entries, block_div, cand, cand_len, n_cand, ratio, q_pos, scores,
+                        ld, n_valid, chunk, flags);
+    return launch_pdl(index_score_stream_kernel<false>, grid, dim3(kThreads), kStreamSmem, st, qI, w, Nq, KI,
+                      key_stride_rows, lens, cap_entries, block_div, nullptr, nullptr, int64_t(0), ratio, q_pos,
+                      scores, ld, n_valid, chunk, flags);
   }
   if (cand)
     return launch_pdl(index_score_kernel<true>, grid, dim3(kThreads), 0, st, qI, w, Nq, KI, key_stride_rows, lens,

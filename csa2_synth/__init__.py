@@ -68,9 +68,19 @@ def normal_f32(seed: int, tensor_id: int, index: int, shape) -> np.ndarray:
     return _rng(seed, tensor_id, index).standard_normal(shape, dtype=np.float32)
 
 
-def normal_bf16(seed: int, tensor_id: int, index: int, shape) -> np.ndarray:
-    """N(0, 1) draws rounded to bf16, as uint16 bit patterns."""
-    return f32_to_bf16_bits(normal_f32(seed, tensor_id, index, shape))
+def normal_bf16(seed: int, tensor_id: int, index: int, shape, chunk_elems: int = 1 << 22) -> np.ndarray:
+    """N(0, 1) draws rounded to bf16, as uint16 bit patterns.  The same numbers as rounding
+    normal_f32(...) (successive draws continue one stream), drawn and rounded chunk by chunk so
+    that a large tensor holds only its bf16 result and one small fp32 temporary."""
+    g = _rng(seed, tensor_id, index)
+    out = np.empty(shape, np.uint16)
+    flat = out.reshape(-1)
+    buf = np.empty(min(chunk_elems, max(flat.size, 1)), np.float32)
+    for s in range(0, flat.size, buf.size):
+        n = min(buf.size, flat.size - s)
+        g.standard_normal(out=buf[:n], dtype=np.float32)
+        flat[s:s + n] = f32_to_bf16_bits(buf[:n])
+    return out
 
 
 def outlier_bf16(seed: int, tensor_id: int, index: int, shape,

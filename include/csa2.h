@@ -317,6 +317,9 @@ typedef struct csa2_group_desc {
   float softmax_scale;                /* e.g. 1/sqrt(512)                                */
   csa2_event_t ev_score_begin;        /* optional: recorded on `stream` before the first  */
   csa2_event_t ev_score_end;          /*   indexer scan of the step and after the last   */
+  csa2_event_t ev_attn_begin;         /* optional: recorded on the attention stream right */
+  csa2_event_t ev_attn_end;           /*   before and after the step's first attention
+                                         launch (a run of layers sharing their rows)     */
 } csa2_group_desc;
 
 csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_t ws_bytes,
@@ -336,17 +339,68 @@ csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_t ws_bytes,
 csa2_status csa2_stack_step(const csa2_group_desc* groups, int n_groups, void* ws, size_t ws_bytes,
                             csa2_stream_t stream);
 
+/*
+ * Context split of one sequence's cache over G shards (one per GPU, or G logical shards on one GPU):
+ * shard g holds the cache entries [lo_g, hi_g), lo_0 = 0, hi_g = lo_{g+1}.  A query then selects in
+ * two steps and attends in two (the exchanges between them are the caller's collectives):
+ *   csa2_shard_topk_pairs   each shard: the local Top-k of its own scores as (score, position) pairs;
+ *   csa2_merge_topk_pairs   the G x k pairs -> the exact global Top-k (the union of the local Top-k
+ *                           sets contains the global one);
+ *   csa2_shard_indices      each shard: the selected positions it holds, as local rows;
+ *   csa2_attn_merge_shards  the shards' attention outputs and lse -> attention over the union.
+ * The result equals the unsplit step: the same indices, and attention within the tolerance of the
+ * extra bf16 rounding of each shard's output.  The pages motivate bounded work per query at 1M
+ * context (ai-maestro "Compressed Sparse Attention 2": a pool of up to 16,384 positions); they do
+ * not describe a split, and this one is the plainest exact one.
+ */
+
+/* The local Top-k of one shard as (score, global position) pairs.  scores, rows, n, ld, n_valid, k,
+ * map, map_ld, ws and ws_bytes are as in csa2_topk (the workspace is csa2_workspace_size(
+ * CSA2_OP_TOPK, {B = rows, Nq = 1, n})).  pos_offset is the global position of local column 0 (lo_g);
+ * with a map, the map's entries are the global positions instead.
+ *   pair_score fp32 [rows][k], pair_pos int32 [rows][k]: ascending positions, -1 / -inf padded;
+ *   pair_n int32 [rows] (nullable): the valid pairs, min(k, visible columns). */
+csa2_status csa2_shard_topk_pairs(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
+                                  int k, const int32_t* map, int64_t map_ld, int64_t pos_offset, float* pair_score,
+                                  int32_t* pair_pos, int32_t* pair_n, void* ws, size_t ws_bytes,
+                                  csa2_stream_t stream);
+
+/* The exact Top-k of G shards' pairs (larger score first, equal scores by lower position), as csa2_topk
+ * of the unsplit scores would select.
+ *   pair_score fp32 [G][rows][k], pair_pos int32 [G][rows][k], pair_n int32 [G][rows] (nullable: all k
+ *   valid): shard g's output of csa2_shard_topk_pairs; shards in ascending order of their position
+ *   ranges (the caller's contract: ties are broken by position through that order).  G in 1..64.
+ *   idx int32 [rows][k] ascending global positions, -1 padded; n_sel int32 [rows] (nullable).
+ *   ws csa2_workspace_size(CSA2_OP_MERGE_PAIRS, {B = rows, Nq = 1, n = G, k}) bytes, 16-byte aligned. */
+csa2_status csa2_merge_topk_pairs(const float* pair_score, const int32_t* pair_pos, const int32_t* pair_n, int G,
+                                  int rows, int k, int32_t* idx, int32_t* n_sel, void* ws, size_t ws_bytes,
+                                  csa2_stream_t stream);
+
+/* idx_local[r][j] = idx[r][j] - lo when lo <= idx[r][j] < hi, else -1 (an empty slot for
+ * csa2_sparse_attn_decode): the selected rows a shard holding [lo, hi) attends. */
+csa2_status csa2_shard_indices(const int32_t* idx, int rows, int k, int64_t lo, int64_t hi, int32_t* idx_local,
+                               csa2_stream_t stream);
+
+/* Attention over the union of the shards' rows from each shard's attention over its own rows:
+ * out_g bf16 [G][rows][16][512] and lse_g fp32 [G][rows][16] (csa2_sparse_attn_decode's out and lse)
+ * -> out bf16 [rows][16][512] = sum_g exp(lse_g - L) out_g with L = log sum_g exp(lse_g), combined in
+ * shard order in fp32; lse fp32 [rows][16] (nullable) = L.  A shard with lse = -inf weighs nothing; a
+ * row no shard attended gets out = 0, lse = -inf.  out_g and out 16-byte aligned. */
+csa2_status csa2_attn_merge_shards(const uint16_t* out_g, const float* lse_g, int G, int rows, uint16_t* out,
+                                   float* lse, csa2_stream_t stream);
+
 /* Workspace sizing. */
 #define CSA2_OP_TOPK 1
 #define CSA2_OP_BLOCK_POOL 2
 #define CSA2_OP_SPARSE_ATTN 3
 #define CSA2_OP_GROUP_STEP 4
 #define CSA2_OP_INDEX_SELECT_PREFILL 5
+#define CSA2_OP_MERGE_PAIRS 6
 
 typedef struct csa2_dims {
   int B, Nq;
   int64_t cap;          /* cache capacity per sequence                        */
-  int64_t n;            /* CSA2_OP_TOPK: columns per row                      */
+  int64_t n;            /* CSA2_OP_TOPK: columns per row; CSA2_OP_MERGE_PAIRS: shards */
   int k;                /* Top-K / selected rows                              */
   int W;                /* window                                             */
   int n_split;          /* CSA2_OP_SPARSE_ATTN / GROUP_STEP: 0 = automatic    */

@@ -134,7 +134,7 @@ class GroupCase:
             self.__dict__["_kv"] = share.__dict__.setdefault("_kv", {})
             self.__dict__["_ki"] = share.__dict__.setdefault("_ki", {})
         if share is None and len(self.host_seqs) > 2:   # draw the host sequences' caches in parallel
-            with cf.ThreadPoolExecutor(HOST_THREADS) as ex:
+            with cf.ThreadPoolExecutor(min(HOST_THREADS, 8)) as ex:
                 list(ex.map(lambda b: (self.h_kv(b), self.h_ki(b)), self.host_seqs))
         for b in (range(B) if share is None else ()):
             Tb = self.T[b]
