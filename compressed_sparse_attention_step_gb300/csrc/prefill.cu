@@ -355,18 +355,24 @@ __global__ void __launch_bounds__(256) prefill_key_norm_kernel(const uint16_t* _
   const int64_t T = min(max(int64_t(lens[b]), int64_t(0)), cap);
   const int64_t t0 = int64_t(blockIdx.x) * kNormChunk, t1 = min(t0 + kNormChunk, T);
   float m = 0.0f;
-  // eight threads per entry, 16 channels each
-  for (int64_t t = t0 + (threadIdx.x >> 3); t < t1; t += blockDim.x >> 3) {
-    const uint4* kp = reinterpret_cast<const uint4*>(KI + (int64_t(b) * cap + t) * CSA2_DI) + 2 * (threadIdx.x & 7);
+  // eight threads per entry, 16 channels each; a warp takes four consecutive entries per step.  The
+  // loop runs on the warp's first entry, so every lane of a warp makes the same trips and the
+  // shuffles below always see the full warp (lanes past the chunk's end add nothing).
+  for (int64_t tw = t0 + ((threadIdx.x >> 5) << 2); tw < t1; tw += blockDim.x >> 3) {
+    const int64_t t = tw + ((threadIdx.x & 31) >> 3);
+    const bool valid = t < t1;
     float acc = 0.0f;
+    if (valid) {
+      const uint4* kp = reinterpret_cast<const uint4*>(KI + (int64_t(b) * cap + t) * CSA2_DI) + 2 * (threadIdx.x & 7);
 #pragma unroll
-    for (int v = 0; v < 2; ++v) {
-      const uint4 x = __ldg(kp + v);
-      const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+      for (int v = 0; v < 2; ++v) {
+        const uint4 x = __ldg(kp + v);
+        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(bf16lo(u[e]), bf16lo(u[e]), acc);
-        acc = fmaf(bf16hi(u[e]), bf16hi(u[e]), acc);
+        for (int e = 0; e < 4; ++e) {
+          acc = fmaf(bf16lo(u[e]), bf16lo(u[e]), acc);
+          acc = fmaf(bf16hi(u[e]), bf16hi(u[e]), acc);
+        }
       }
     }
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
