@@ -235,17 +235,6 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
                                       const int32_t* n_valid, int k, const int32_t* swa_len, int W,
                                       float softmax_scale, int n_split, float* ws, cudaStream_t st,
                                       bool tickets_zeroed, bool inputs_ready, bool win_fp8);
-// Runs of 2..4 layers that attend the same selected rows, in one pass over those rows (attn_fused.cu):
-// every FP4 tile is dequantised once for all the layers.  n_split CTAs per query (clamped to the
-// tiles); ws holds the tickets (one per query, zero before the launch unless tickets_zeroed) and
-// the split partials of n_layers * B * Nq instances, as attn_ws_bytes(n_layers * B * Nq, n_split).
-cudaError_t launch_sparse_attn_fused(const AttnLayers& layers, int n_layers, int B, int Nq, const uint8_t* codes,
-                                     const uint8_t* scales, int64_t cap, const int32_t* idx, int k,
-                                     const int32_t* swa_len, int W, float softmax_scale, int n_split, float* ws,
-                                     cudaStream_t st, bool tickets_zeroed, bool win_fp8);
-int attn_fused_split(int64_t instances, int L, int k, int W);  // the automatic split of a fused launch
-int attn_fused_tiles(int L, int k, int W);
-constexpr int kMaxFusedLayers = 4;
 // 8-bit window rows: n bf16 values -> E4M3 bytes (RNE, saturating to +-448).
 cudaError_t launch_fp8_quantize(const uint16_t* x, int64_t n, uint8_t* out, cudaStream_t st);
 cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,

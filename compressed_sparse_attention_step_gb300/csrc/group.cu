@@ -78,10 +78,8 @@ size_t group_attn_ws_bytes(int64_t rows, int K, int W, int n_split) {
   if (n_split) {
     part = partials(rows, attn_effective_split(K, W, n_split));
   } else {
-    part = partials(rows, attn_effective_split(K, W, attn_auto_split(rows, K, W)));
-    // runs of 2 .. 4 layers take the fused kernel at its own split
-    for (int l = 2; l <= kMaxFusedLayers; ++l)
-      part = std::max(part, partials(l * rows, std::min(attn_fused_split(rows, l, K, W), attn_fused_tiles(l, K, W))));
+    for (int l = 1; l <= CSA2_MAX_LAYERS; ++l)
+      part = std::max(part, partials(l * rows, attn_effective_split(K, W, attn_auto_split(l * rows, K, W))));
   }
   return group_attn_ticket_bytes(rows, K, W, n_split) + part;
 }
@@ -369,36 +367,13 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
       const bool timed = !attn_timed;
       attn_timed = true;
       if (timed && !rec(g->ev_attn_begin, aux)) return false;
-      bool r = true;
-      const bool fp8 = g->swa_format == CSA2_SWA_E4M3;
-      if (run_n == 1) {
-        const int64_t inst = rc;
-        int ns = csa2::attn_effective_split(
-            K, g->W, g->n_split ? g->n_split : std::min(csa2::attn_auto_split(inst, K, g->W), n_chunks > 1 ? 4 : 32));
-        while (ns > 1 && csa2::attn_ws_bytes(inst, ns) > attn_cap) --ns;
-        r = ok(csa2::launch_sparse_attn_layers(run, 1, Bc, Nq, codes, scl, g->cap, run_idx, nullptr, K, swl, g->W,
-                                               g->softmax_scale, ns, attn_ws, aux, zeroed, false, fp8));
-      } else {
-        // chunks of at most four layers, as even as possible, each one pass over the shared rows
-        const int n_ch = (run_n + csa2::kMaxFusedLayers - 1) / csa2::kMaxFusedLayers;
-        for (int ci = 0, l0 = 0; ci < n_ch && r; ++ci) {
-          const int nl = (run_n - l0) / (n_ch - ci);
-          csa2::AttnLayers sub{};
-          for (int j = 0; j < nl; ++j) {
-            sub.q[j] = run.q[l0 + j];
-            sub.swa[j] = run.swa[l0 + j];
-            sub.out[j] = run.out[l0 + j];
-            sub.lse[j] = run.lse[l0 + j];
-          }
-          const int64_t inst = int64_t(nl) * rc;
-          int ns = g->n_split ? g->n_split : csa2::attn_fused_split(rc, nl, K, g->W);
-          ns = std::max(1, std::min(ns, csa2::attn_fused_tiles(nl, K, g->W)));
-          while (ns > 1 && csa2::attn_ws_bytes(inst, ns) > attn_cap) --ns;
-          r = ok(csa2::launch_sparse_attn_fused(sub, nl, Bc, Nq, codes, scl, g->cap, run_idx, K, swl, g->W,
-                                                g->softmax_scale, ns, attn_ws, aux, zeroed, fp8));
-          l0 += nl;
-        }
-      }
+      const int64_t inst = int64_t(run_n) * rc;
+      int ns = csa2::attn_effective_split(
+          K, g->W, g->n_split ? g->n_split : std::min(csa2::attn_auto_split(inst, K, g->W), n_chunks > 1 ? 4 : 32));
+      while (ns > 1 && csa2::attn_ws_bytes(inst, ns) > attn_cap) --ns;
+      const bool r = ok(csa2::launch_sparse_attn_layers(run, run_n, Bc, Nq, codes, scl, g->cap, run_idx, nullptr, K,
+                                                         swl, g->W, g->softmax_scale, ns, attn_ws, aux, zeroed,
+                                                         false, g->swa_format == CSA2_SWA_E4M3));
       if (timed && !rec(g->ev_attn_end, aux)) return false;
       run_n = 0;
       return r;
