@@ -7,9 +7,10 @@
 //
 // All kernels here stream: one thread per 16-channel group (32 B of bf16 in, 8 B of codes and
 // 1 B of scale out), so a warp covers one 512-channel row with fully coalesced accesses.
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
-#include "common.cuh"
+#include "attn_common.cuh"
 
 namespace csa2 {
 namespace {
@@ -21,11 +22,6 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
   return (b & 0x80u) ? -v : v;
 }
 
-// E2M1 magnitude code (0..7) -> fp32 bits of {0, .5, 1, 1.5, 2, 3, 4, 6}.
-__device__ __forceinline__ uint32_t e2m1_mag_bits(uint32_t c) {
-  return (c < 2u) ? (c ? 0x3F000000u : 0u) : (((126u + (c >> 1)) << 23) | ((c & 1u) << 22));
-}
-
 // Quantise one 16-channel group held as 8 packed bf16 pairs.
 //
 // The E2M1 code of q = fp32(x / s) under round-to-nearest-even is the number of midpoints
@@ -35,7 +31,10 @@ __device__ __forceinline__ uint32_t e2m1_mag_bits(uint32_t c) {
 // each product has at most 3 + 4 significant bits, so it is exact in fp32, and x (8 significant
 // bits) either equals a product or differs from it by at least 2^-9 of its size, far more than
 // the 2^-24 rounding of the quotient.  Hence |x| > m*s <=> fp32(|x|/s) > m and equality holds
-// exactly when the quotient is the tie, which makes the codes bit-identical to dividing.
+// exactly when the quotient is the tie, which makes the codes bit-identical to dividing.  The
+// midpoints increase, so the count is found by a three-level search: 4 [|x| >= 1.75 s], then
+// 2 [|x| >= 3.5 s or 0.75 s], then [|x| > the lower midpoint of the remaining pair] (the midpoints
+// taken with >= are exactly those whose upper code is even).
 __device__ __forceinline__ void quantize_group(const uint32_t (&wv)[8], uint32_t& lo, uint32_t& hi,
                                                uint32_t& sb) {
   uint32_t amax = 0;
@@ -47,17 +46,28 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&wv)[8], uint32_t
   lo = 0u;
   hi = 0u;
   if (s > 0.0f) {
-    const float t0 = 0.25f * s, t1 = 0.75f * s, t2 = 1.25f * s, t3 = 1.75f * s;
-    const float t4 = 2.5f * s, t5 = 3.5f * s, t6 = 5.0f * s;
+    // the midpoints m s as bf16 pairs: each has at most 3 + 4 significant bits, so it is exact in
+    // bf16, and as |x| is a bf16 value the pairwise bf16 comparisons decide exactly as fp32 ones
+    // (s >= 2^-9 keeps every midpoint normal, so a subnormal |x| compares the same either way)
+    auto pair = [&](float m) {
+      const uint32_t bits = __float_as_uint(m * s) >> 16;
+      return bits | (bits << 16);
+    };
+    auto bf2 = [](uint32_t u) { return *reinterpret_cast<const __nv_bfloat162*>(&u); };
+    const uint32_t T0 = pair(0.25f), T1 = pair(0.75f), T2 = pair(1.25f), T3 = pair(1.75f);
+    const uint32_t T4 = pair(2.5f), T5 = pair(3.5f), T6 = pair(5.0f);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t h = (i & 1) ? (wv[i >> 1] >> 16) : (wv[i >> 1] & 0xFFFFu);
-      const float a = __uint_as_float((h & 0x7FFFu) << 16);
-      uint32_t c = uint32_t(a > t0) + uint32_t(a >= t1) + uint32_t(a > t2) + uint32_t(a >= t3) +
-                   uint32_t(a > t4) + uint32_t(a >= t5) + uint32_t(a > t6);
-      c |= (h >> 12) & 8u;  // sign of x
-      if (i < 8) lo |= c << (4 * i);
-      else hi |= c << (4 * (i - 8));
+    for (int i = 0; i < 8; ++i) {  // channels 2 i (low half) and 2 i + 1 (high half)
+      const uint32_t m2 = wv[i] & 0x7FFF7FFFu;
+      const uint32_t b2 = __hge2_mask(bf2(m2), bf2(T3));
+      const uint32_t b1 = __hge2_mask(bf2(m2), bf2((T5 & b2) | (T1 & ~b2)));
+      const uint32_t tl = (((T6 & b1) | (T4 & ~b1)) & b2) | (((T2 & b1) | (T0 & ~b1)) & ~b2);
+      const uint32_t b0 = __hgt2_mask(bf2(m2), bf2(tl));
+      const uint32_t c = (b2 & 0x00040004u) | (b1 & 0x00020002u) | (b0 & 0x00010001u) |
+                         ((wv[i] >> 12) & 0x00080008u);  // signs of x
+      const uint32_t byte = (c & 0xFu) | ((c >> 12) & 0xF0u);
+      if (i < 4) lo |= byte << (8 * i);
+      else hi |= byte << (8 * (i - 4));
     }
   }
 }
@@ -141,6 +151,11 @@ __global__ void __launch_bounds__(256) zero_kernel(uint4* __restrict__ p, int64_
   if (i < n16) p[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// One 16-channel group per thread.  The codes go through the hardware E2M1 -> f16x2 conversion and
+// one f16x2 multiply by the group's scale (E4M3 -> f16x2, also exact): the product of a code (at
+// most 2 significant bits) and a scale (at most 4) has at most 6 significant bits and lies in f16's
+// normal range (2^-10 .. 2688) or is a signed zero, so the f16 product is exact, and so are its
+// widening to fp32 and its rounding to bf16.  A code of -0 gives -0 (bf16 0x8000).
 __global__ void __launch_bounds__(256) fp4_dequantize_kernel(const uint8_t* __restrict__ codes,
                                                              const uint8_t* __restrict__ scales,
                                                              int64_t n_groups,
@@ -152,22 +167,20 @@ __global__ void __launch_bounds__(256) fp4_dequantize_kernel(const uint8_t* __re
   const int64_t row = gid >> 5;
   const int g = int(gid & 31);
   const uint2 c = __ldcs(reinterpret_cast<const uint2*>(codes + row * CSA2_CODE_BYTES + g * 8));
-  const float s = e4m3_value(scales[row * CSA2_SCALE_BYTES + g]);
+  const uint32_t sb = scales[row * CSA2_SCALE_BYTES + g];
+  const __half2 sc = attn::bits_h2(attn::e4m3x2_to_f16x2(uint16_t(sb | (sb << 8))));
   uint32_t o[8];
+  const uint32_t words[2] = {c.x, c.y};
 #pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    const uint32_t word = (i < 8) ? c.x : c.y;
-    const uint32_t byte = (word >> (4 * (i & 7))) & 0xFFu;
-    uint32_t pair = 0;
+  for (int wi = 0; wi < 2; ++wi) {
+    uint32_t f[4];
+    attn::e2m1x8_to_f16x2x4(words[wi], f[0], f[1], f[2], f[3]);  // channels 8 wi + 2 j (low), + 1 (high)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t nib = (byte >> (4 * h)) & 15u;
-      // the product of a 2-bit and a 4-bit significand is exact in fp32 and in bf16
-      const float v = __uint_as_float(e2m1_mag_bits(nib & 7u)) * s;
-      const uint32_t bits = (__float_as_uint(v) >> 16) | ((nib & 8u) << 12);
-      pair |= bits << (16 * h);
+    for (int j = 0; j < 4; ++j) {
+      const __half2 v = __hmul2(attn::bits_h2(f[j]), sc);
+      const __nv_bfloat162 bv = __floats2bfloat162_rn(__low2float(v), __high2float(v));
+      o[4 * wi + j] = *reinterpret_cast<const uint32_t*>(&bv);
     }
-    o[i >> 1] = pair;
   }
   uint4* dst = reinterpret_cast<uint4*>(out + row * CSA2_D + g * CSA2_GROUP);
   __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
@@ -268,8 +281,8 @@ cudaError_t launch_fp4_quantize(const uint16_t* x, int B, int n_new, uint8_t* co
   if (n_groups == 0) return cudaSuccess;
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
-  return launch_pdl(fp4_quantize_kernel, grid_for(n_groups, 256), dim3(256), 0, st, x, n_groups, n_new, codes, scales, cap,
-                                                               offsets, offset_bias, flags);
+  return launch_pdl(fp4_quantize_kernel, grid_for(n_groups, 256), dim3(256), 0, st, x, n_groups, n_new, codes, scales,
+                    cap, offsets, offset_bias, flags);
 }
 
 cudaError_t launch_fp8_quantize(const uint16_t* x, int64_t n, uint8_t* out, cudaStream_t st) {

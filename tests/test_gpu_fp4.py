@@ -85,6 +85,18 @@ def test_quantize_exhaustive_values_and_scales(orc):
     assert np.array_equal(bf16_host(out), orc.fp4_dequantize(oc, os_))
 
 
+def test_dequantize_every_code_byte_and_scale_byte(orc):
+    """Every packed code byte (both nibbles) under every finite non-negative E4M3 scale byte
+    (0x00 .. 0x7E): one row per scale byte, whose 256 code bytes are 0 .. 255."""
+    scale_bytes = np.arange(0x7F, dtype=np.uint8)
+    codes = np.tile(np.arange(256, dtype=np.uint8), (scale_bytes.size, 1))
+    scales = np.repeat(scale_bytes[:, None], 32, 1)
+    out = torch.empty((scale_bytes.size, 512), dtype=torch.bfloat16, device="cuda")
+    c.csa2_fp4_dequantize(to_dev(codes), to_dev(scales), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_host(out), orc.fp4_dequantize(codes, scales))
+
+
 def test_fp4_roundtrip_full_size_64x8192x512(orc):
     """The FP4 round-trip workload: 64 sequences x 8192 tokens x 512 channels, N(0,1) with 1% of
     entries x20, quantised then dequantised in one launch each."""

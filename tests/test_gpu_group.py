@@ -50,7 +50,7 @@ def test_decode_group_pipelined_sequence_chunks(orc):
 
 
 def test_decode_group_long_rows_ragged(orc):
-    """Contexts above 8192 entries (the score scan also writes the Top-K's group keys), ragged,
+    """A cache of 20000 entries (rows longer than 8192 select in three launches), ragged contexts,
     some below k groups of 16, with a Reindex layer; unchunked and in three sequence chunks (each
     chunk's rows of the group keys are its own)."""
     gc = GroupCase(58, [20000, 9000, 8193, 3000, 12345], [F, R, RX, R])

@@ -124,7 +124,8 @@ def _topk_rows(n):
     return s
 
 
-@pytest.mark.parametrize("n,k", [(1000, 512), (131072, 512), (131072, 2048), (4096, 1), (600, 512)])
+@pytest.mark.parametrize("n,k", [(1000, 512), (131072, 512), (131072, 2048), (4096, 1), (600, 512), (16384, 512),
+                                 (16384, 2048), (12000, 512), (16385, 512)])
 def test_topk_matches_oracle(orc, n, k):
     s = _topk_rows(n)
     rows = s.shape[0]
