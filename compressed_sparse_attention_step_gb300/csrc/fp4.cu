@@ -79,7 +79,9 @@ __device__ __forceinline__ void quantize_append_group(const uint16_t* __restrict
                                                       int offset_bias, unsigned int* flags) {
   const int64_t row = gid >> 5;
   const int g = int(gid & 31);
-  const int64_t b = row / n_new, r = row - b * n_new;
+  // rows fit in 32 bits (2^32 rows of 1 KiB would be 4 TiB of input): a 32-bit division
+  const uint32_t b32 = uint32_t(row) / uint32_t(n_new);
+  const int64_t b = b32, r = int64_t(uint32_t(row) - b32 * uint32_t(n_new));
   const int64_t pos = (offsets ? int64_t(offsets[b]) + offset_bias : 0) + r;
   if (pos < 0 || pos >= cap) {
     if (g == 0) atomicOr(flags, CSA2_FLAG_APPEND_OOB);
