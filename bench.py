@@ -626,7 +626,7 @@ def run_full_layer(args, torch, c, syn, dev, sampler):
         rl = roofline("index_score_stream_kernel", "full_layer_decode_b1_t4096", "hbm", T * 256, score_ms, K, peak,
                       f"{kind} (hbm copy)")
     else:
-        rl = roofline("sparse_attn_kernel", "full_layer_decode_b1_t4096", "hbm", BYTES_ATTN_PER_SEQ_LAYER, attn_ms, K,
+        rl = roofline("sparse_attn_ws_kernel", "full_layer_decode_b1_t4096", "hbm", BYTES_ATTN_PER_SEQ_LAYER, attn_ms, K,
                       peak, f"{kind} (hbm copy)")
     cpu = None
     if not args.no_cpu_baseline:
@@ -643,7 +643,7 @@ def run_full_layer(args, torch, c, syn, dev, sampler):
                        "l2": "flushed (256 MiB written) before every step; each step timed by its own events"},
             "tokens_per_s": B / (ms / 1e3), "kv_gbs": bytes_step / (ms / 1e3) / 1e9, "bytes_per_step": bytes_step,
             "hbm_frac_step": bytes_step / (ms / 1e3) / 1e9 / peak,
-            "kernel_ms": {"index_score_stream_kernel": score_ms, "sparse_attn_kernel": attn_ms},
+            "kernel_ms": {"index_score_stream_kernel": score_ms, "sparse_attn_ws_kernel": attn_ms},
             # the append, the score scan, Top-K (one launch for rows of at most 8192 entries), attention
             "roofline": rl, "cpu_baseline": cpu, "gpu_launches": 4 * K,
             "clocks": sampler.summary(t0, t1) if sampler else None}

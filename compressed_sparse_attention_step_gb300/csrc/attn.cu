@@ -27,6 +27,10 @@
 // Splits of a query are merged by the last CTA to finish (an atomic ticket), in split order, so
 // the result does not depend on which CTA finishes last.
 //
+// This kernel runs the launches of many queries (prefill chunks), where the second CTA on an SM
+// hides each CTA's setup and tail; launches of at most a few CTAs per SM (decode) go to the
+// warp-specialised kernel of attn_ws.cu, whose pipeline overlaps the tiles of one query.
+//
 // Operand types: a tile's MMA operands share one type.  FP4 tiles run in f16: the dequantised row
 // is exact in f16 (at most 6 significant bits, magnitudes in [2^-10, 2688]), Q is converted from
 // bf16 (exact for magnitudes in [2^-14, 65504]) and P is rounded to f16.  Window tiles run in bf16
@@ -81,16 +85,11 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     const __grid_constant__ AttnLayers layers, int Nq, const uint8_t* __restrict__ codes,
     const uint8_t* __restrict__ scales, int64_t cap, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ n_valid, int k, const int32_t* __restrict__ swa_len, int W, float scale_log2,
-    int n_split, float* __restrict__ ws, unsigned int* __restrict__ tickets, unsigned int* flags, int inputs_ready,
-    int win_fp8) {
+    int n_split, float* __restrict__ ws, unsigned int* __restrict__ tickets, unsigned int* flags, int win_fp8) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // Inputs not yet known to be complete (the selected positions may come from the kernel right
-  // before this one): wait first.  Otherwise (a layer that reuses earlier positions) wait only
-  // before the first write to the split workspace, which the kernel before this one may still read.
-  if (!inputs_ready) {
-    pdl_wait();
-    pdl_trigger();
-  }
+  // the selected positions may come from the kernel right before this one
+  pdl_wait();
+  pdl_trigger();
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
   unsigned char* base = smem_raw + (base_s - raw_s);
@@ -483,10 +482,6 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     __syncthreads();
     if (t < CSA2_H) ms.l_fin[t] = (ms.red[0][t] + ms.red[1][t]) + (ms.red[2][t] + ms.red[3][t]);
     __syncthreads();
-    if (inputs_ready) {
-      pdl_wait();
-      pdl_trigger();
-    }
     float o[2][16];
     tmem_ld16x2(t_lane + kOCol + uint32_t(32 * half), o);
 #pragma unroll
@@ -513,10 +508,6 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     }
     if (!ok && t == 0) atomicOr(flags, CSA2_FLAG_TIMEOUT);
   } else {
-    if (inputs_ready) {
-      pdl_wait();
-      pdl_trigger();
-    }
     if (n_split == 1) {
       uint16_t* orow = out + int64_t(inst) * CSA2_H * CSA2_D;
       for (int e = t; e < CSA2_H * CSA2_D; e += kThreads) orow[e] = 0;
@@ -636,10 +627,26 @@ size_t attn_ws_bytes(int64_t instances, int n_split) {
          size_t(instances) * size_t(n_split) * (CSA2_H * CSA2_D + 2 * CSA2_H) * sizeof(float);
 }
 
+// SMs of the current device, looked up once per device.
+int sm_count() {
+  static std::atomic<int> count[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int c = count[dev].load();
+  if (c <= 0) {
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 152;
+    count[dev] = c;
+  }
+  return c;
+}
+
+// Launches of at most this many CTAs per SM run the warp-specialised kernel (one CTA per SM).
+constexpr int kWsMaxCtasPerSm = 4;
+
 int attn_auto_split(int64_t instances, int k, int W) {
   const int nt = attn_tiles(k, W);
   if (instances <= 0 || nt <= 0) return 1;
-  const int64_t slots = 2 * 152;  // two resident CTAs per SM
+  const int64_t slots = sm_count();  // one CTA per SM for the launches that split
   int64_t s = std::max<int64_t>(slots / instances, 1);
   s = std::min<int64_t>(s, std::min(nt, kMaxSplit));
   return int(std::max<int64_t>(s, 1));
@@ -649,7 +656,7 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
                                       const uint8_t* scales, int64_t cap, const int32_t* idx,
                                       const int32_t* n_valid, int k, const int32_t* swa_len, int W,
                                       float softmax_scale, int n_split, float* ws, cudaStream_t st,
-                                      bool tickets_zeroed, bool inputs_ready, bool win_fp8) {
+                                      bool tickets_zeroed, bool win_fp8) {
   const int64_t per_layer = int64_t(B) * Nq, instances = per_layer * n_layers;
   if (instances == 0) return cudaSuccess;
   if (n_layers < 1 || n_layers > CSA2_MAX_LAYERS || per_layer > 65535) return cudaErrorInvalidValue;
@@ -657,15 +664,6 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
   n_split = attn_effective_split(k, W, n_split);
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
-  static std::atomic<bool> attr_set[64];  // per device; set once, by any host thread
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   unsigned int* tickets = nullptr;
   float* partials = nullptr;
@@ -677,25 +675,35 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
       if (e != cudaSuccess) return e;
     }
   }
+  if (instances * n_split <= int64_t(kWsMaxCtasPerSm) * sm_count())
+    return launch_sparse_attn_ws(layers, n_layers, int(per_layer), Nq, codes, scales, cap, idx, n_valid, k, swa_len,
+                                 W, scale_log2, n_split, partials, tickets, flags, win_fp8, st);
+  static std::atomic<bool> attr_set[64];  // per device; set once, by any host thread
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
   const dim3 grid{unsigned(n_split), unsigned(per_layer), unsigned(n_layers)};
   return launch_pdl(sparse_attn_kernel, grid, dim3(kThreads), kSmemBytes, st, layers, Nq, codes, scales, cap, idx,
-                    n_valid, k, swa_len, W, scale_log2, n_split, partials, tickets, flags, int(inputs_ready),
-                    int(win_fp8));
+                    n_valid, k, swa_len, W, scale_log2, n_split, partials, tickets, flags, int(win_fp8));
 }
 
 cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
                                const uint8_t* scales, int64_t cap, const int32_t* idx,
                                const int32_t* n_valid, int k, const uint16_t* swa,
                                const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
-                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed,
-                               bool inputs_ready) {
+                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed) {
   AttnLayers layers{};
   layers.q[0] = q;
   layers.swa[0] = swa;
   layers.out[0] = out;
   layers.lse[0] = lse;
   return launch_sparse_attn_layers(layers, 1, B, Nq, codes, scales, cap, idx, n_valid, k, swa_len, W, softmax_scale,
-                                   n_split, ws, st, tickets_zeroed, inputs_ready, false);
+                                   n_split, ws, st, tickets_zeroed, false);
 }
 
 }  // namespace csa2

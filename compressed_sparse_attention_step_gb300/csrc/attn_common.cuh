@@ -85,17 +85,19 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Waits for phase `parity` of the mbarrier, for at most about one second.
+// Waits for phase `parity` of the mbarrier, for at most about one second.  Each test suspends the
+// thread until the phase completes or 20 us pass, so waiting warps take no issue slots from the
+// working ones.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     uint32_t done;
     asm volatile(
         "{ .reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p; }\n"
         : "=r"(done)
-        : "r"(mbar), "r"(parity)
+        : "r"(mbar), "r"(parity), "n"(20000)
         : "memory");
     if (done) return true;
     if ((it & 63u) == 0u) {

@@ -234,15 +234,21 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
                                       const uint8_t* scales, int64_t cap, const int32_t* idx,
                                       const int32_t* n_valid, int k, const int32_t* swa_len, int W,
                                       float softmax_scale, int n_split, float* ws, cudaStream_t st,
-                                      bool tickets_zeroed, bool inputs_ready, bool win_fp8);
+                                      bool tickets_zeroed, bool win_fp8);
+// The warp-specialised attention kernel (attn_ws.cu), for launches of a few CTAs per SM: the split
+// is effective, partials and tickets as in launch_sparse_attn_layers (tickets zero).
+cudaError_t launch_sparse_attn_ws(const AttnLayers& layers, int n_layers, int per_layer, int Nq,
+                                  const uint8_t* codes, const uint8_t* scales, int64_t cap, const int32_t* idx,
+                                  const int32_t* n_valid, int k, const int32_t* swa_len, int W, float scale_log2,
+                                  int n_split, float* partials, unsigned int* tickets, unsigned int* flags,
+                                  bool win_fp8, cudaStream_t st);
 // 8-bit window rows: n bf16 values -> E4M3 bytes (RNE, saturating to +-448).
 cudaError_t launch_fp8_quantize(const uint16_t* x, int64_t n, uint8_t* out, cudaStream_t st);
 cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* codes,
                                const uint8_t* scales, int64_t cap, const int32_t* idx,
                                const int32_t* n_valid, int k, const uint16_t* swa,
                                const int32_t* swa_len, int W, float softmax_scale, uint16_t* out,
-                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed,
-                               bool inputs_ready = false);
+                               float* lse, int n_split, float* ws, cudaStream_t st, bool tickets_zeroed);
 // Attention splits: at most one per 128-row tile; attn_ws_bytes with the effective split.
 int attn_effective_split(int k, int W, int n_split);
 size_t attn_ws_bytes(int64_t instances, int n_split);

@@ -65,7 +65,7 @@ inline bool prefill_path(int B, int Nq, int hierarchical, int64_t cap) {
 // Attention workspace of a group step.  One launch serves a run of L' layers that share their
 // selected rows, L' * rows instances at a split.  Tickets: for rows * max(ns, CSA2_MAX_LAYERS)
 // instances (ns: one layer's split).  Partials: with the automatic split, enough for a run of any
-// length L' <= CSA2_MAX_LAYERS at its own automatic split (about max(304, L' rows) instance-splits,
+// length L' <= CSA2_MAX_LAYERS at its own automatic split (about max(152, L' rows) instance-splits,
 // a few MB); with a forced split, for one layer's rows at that split (a longer run takes the
 // largest split that fits).
 size_t group_attn_ticket_bytes(int64_t rows, int K, int W, int n_split) {
@@ -373,7 +373,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
       while (ns > 1 && csa2::attn_ws_bytes(inst, ns) > attn_cap) --ns;
       const bool r = ok(csa2::launch_sparse_attn_layers(run, run_n, Bc, Nq, codes, scl, g->cap, run_idx, nullptr, K,
                                                          swl, g->W, g->softmax_scale, ns, attn_ws, aux, zeroed,
-                                                         false, g->swa_format == CSA2_SWA_E4M3));
+                                                         g->swa_format == CSA2_SWA_E4M3));
       if (timed && !rec(g->ev_attn_end, aux)) return false;
       run_n = 0;
       return r;

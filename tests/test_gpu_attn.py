@@ -140,3 +140,20 @@ def test_split_partials_of_empty_splits_are_never_read(orc, n_split):
     torch.cuda.synchronize()
     ref, rlse = _oracle(orc, kv, q, swa, idx, nvalid, swa_len, W)
     _cmp(bf16_host(out), lse.cpu().numpy(), ref, rlse)
+
+
+@pytest.mark.parametrize("n_split", [0, 2])
+def test_many_queries_ragged(orc, n_split):
+    """640 queries (more than four CTAs per SM): the launch runs the kernel with two CTAs per SM
+    instead of the warp-specialised one.  Ragged selections, empty slots and partial windows; with
+    a forced split of 2 its partials are merged too."""
+    B, Nq, cap, k, W = 4, 160, 2000, 512, 128
+    kv, q, swa, idx = _case(45, B, Nq, cap, k, W)
+    g = np.random.default_rng(45)
+    nvalid = g.integers(0, k + 1, size=B * Nq).astype(np.int32)
+    nvalid[:3] = [k, 0, 1]
+    idx[g.random(idx.shape) < 0.02] = -1
+    swa_len = np.array([W - 1 + Nq, 100, 0, 60], np.int32)
+    got, glse = _run(kv, q, swa, idx, nvalid, swa_len, W, n_split)
+    ref, rlse = _oracle(orc, kv, q, swa, idx, nvalid, swa_len, W)
+    _cmp(got, glse, ref, rlse)

@@ -52,6 +52,16 @@ def test_prefill_chunk_fp8_window_tensor_core_path(orc):
     gc.check(orc)
 
 
+def test_prefill_chunk_fp8_window_many_queries(orc):
+    """256 queries x 3 layers sharing their selection: one attention launch of 768 queries, which
+    runs the kernel with two CTAs per SM."""
+    Nq, T = 256, 6000
+    q_pos = np.arange(2 * T - Nq, 2 * T, dtype=np.int32)[None]
+    gc = GroupCase(84, [T], [F, R, R], Nq=Nq, ratio=2, K=256, W=64, append=False, q_pos=q_pos, swa_fp8=True)
+    gc.run()
+    gc.check(orc)
+
+
 def test_decode_group_fp8_window_full_size_b64_t131072(orc):
     """The decode workload with 8-bit windows: batch 64, 128K context, 1 Full + 3 Reuse, sampled
     sequences."""
