@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) sparse_attn_ws_kernel(
   const int nf = max(fb - fa, 0), n_live = nf + max(wb - wa, 0);
   auto tile_of = [&](int n) { return n < nf ? fa + n : wa + (n - nf); };
 
-  const int32_t* irow = idx + int64_t(inst) * k;
+  const int32_t* irow = (layers.idx[blockIdx.z] ? layers.idx[blockIdx.z] : idx) + int64_t(inst) * k;
   const uint8_t* cbase = codes + int64_t(b) * cap * CSA2_CODE_BYTES;
   const uint8_t* sbase = scales + int64_t(b) * cap * CSA2_SCALE_BYTES;
   const uint16_t* swbase = swa ? swa + int64_t(b) * SW * CSA2_D : nullptr;

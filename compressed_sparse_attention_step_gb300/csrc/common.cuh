@@ -219,13 +219,15 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
 // topk_ws_bytes); a launch leaves them zero.
 size_t topk_counters_offset(int rows);
 size_t attn_ticket_bytes(int64_t instances);
-// Per-layer operands of one attention launch over layers that attend the same selected rows (a
-// Full or Reindex layer and the Reuse layers after it): query, window buffer, output, lse.
+// Per-layer operands of one attention launch over layers of one group: query, window buffer,
+// output, lse, and the selected rows (null: the launch's shared `idx`, as for a Full or Reindex
+// layer and the Reuse layers after it).
 struct AttnLayers {
   const uint16_t* q[CSA2_MAX_LAYERS];
   const uint16_t* swa[CSA2_MAX_LAYERS];
   uint16_t* out[CSA2_MAX_LAYERS];
   float* lse[CSA2_MAX_LAYERS];
+  const int32_t* idx[CSA2_MAX_LAYERS];
 };
 // n_layers layers of B*Nq queries each in one launch; the split workspace holds
 // n_layers * B * Nq instances (attn_ws_bytes), tickets first.  win_fp8: the window buffers hold
@@ -279,6 +281,9 @@ struct DeviceStreams {
   cudaStream_t aux = nullptr;
   cudaEvent_t fork[kMaxSeqChunks] = {};
   cudaEvent_t join = nullptr;
+  // a second side stream: a hierarchical group's Reindex selection beside its Full layer's
+  cudaStream_t aux2 = nullptr;
+  cudaEvent_t pool_ready = nullptr, sel_done = nullptr;
   std::mutex mu;
 };
 DeviceStreams* device_streams();

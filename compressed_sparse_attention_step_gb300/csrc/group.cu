@@ -43,6 +43,9 @@ DeviceStreams* device_streams() {
     for (auto& e : r.fork)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
     if (cudaEventCreateWithFlags(&r.join, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithPriority(&r.aux2, cudaStreamNonBlocking, greatest) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&r.pool_ready, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&r.sel_done, cudaEventDisableTiming) != cudaSuccess) return nullptr;
     r.ready = true;
   }
   return &r;
@@ -85,7 +88,7 @@ size_t group_attn_ws_bytes(int64_t rows, int K, int W, int n_split) {
 }
 
 struct GroupWs {
-  size_t scores_off, nv_off, topk_off, attn_off, pf_off, total;
+  size_t scores_off, nv_off, topk_off, attn_off, pf_off, topk2_off, nv2_off, total;
   int64_t score_ld;
 };
 
@@ -102,6 +105,15 @@ GroupWs group_ws_layout(int B, int Nq, int64_t cap, int K, int W, int hierarchic
   L.attn_off = L.topk_off + align256(topk_ws_bytes(int(rows), ld));
   L.pf_off = L.attn_off + align256(group_attn_ws_bytes(rows, K, W, n_split));
   L.total = L.pf_off + (pf ? align256(prefill_ws_bytes(rows, cap, B)) : 0);
+  // hierarchical: the Top-K workspace and valid counts of a Reindex selection that runs beside the
+  // Full layer's (its pool scores take the second pool-sized region of the score buffer)
+  L.topk2_off = L.nv2_off = L.total;
+  if (hierarchical) {
+    const int64_t pool_w = int64_t(keep) * CSA2_BLOCK;
+    L.topk2_off = L.total;
+    L.nv2_off = L.topk2_off + align256(topk_ws_bytes(int(rows), pool_w));
+    L.total = L.nv2_off + align256(size_t(rows) * sizeof(int32_t));
+  }
   return L;
 }
 
@@ -291,14 +303,24 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   // (selection, pool work, attention of every layer) runs on the side stream.
   int n_chunks = g->seq_chunks > 0 ? g->seq_chunks : 1;
   n_chunks = std::max(1, std::min({n_chunks, g->B, csa2::kMaxSeqChunks}));
+  // A hierarchical group in one chunk whose Full layer 0 is followed by a Reindex layer l_rx: once
+  // the pool is selected, l_rx's pool scan and selection run on a second side stream beside the
+  // Full layer's pool scan, selection and attention (they share only the pool)
+  int l_rx = -1;
+  if (g->hierarchical && n_chunks == 1 && g->modes[0] == CSA2_MODE_FULL && nb > 0 && 2 * pool_w <= sld)
+    for (int l = 1; l < g->n_layers; ++l)
+      if (g->modes[l] != CSA2_MODE_REUSE) {
+        if (g->modes[l] == CSA2_MODE_REINDEX) l_rx = l;
+        break;
+      }
   csa2::DeviceStreams* ds = nullptr;
-  if (n_chunks > 1) {
+  if (n_chunks > 1 || l_rx > 0) {
     ds = csa2::device_streams();
     if (!ds) return CSA2_ERR_CUDA;
   }
   std::unique_lock<std::mutex> lock;
   if (ds) lock = std::unique_lock<std::mutex>(ds->mu);
-  cudaStream_t aux = ds ? ds->aux : st;
+  cudaStream_t aux = ds && n_chunks > 1 ? ds->aux : st;
 
   // Top-K counters and attention tickets sit back to back in the workspace; every launch leaves them
   // zero, so clearing them once per step serves all layers of an unchunked step (by the append's
@@ -354,10 +376,10 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
     auto qI_of = [&](int l) { return g->qI[l] + r0 * (CSA2_HI * CSA2_DI); };
     auto w_of = [&](int l) { return g->w[l] + r0 * CSA2_HI; };
     auto idx_of = [&](int l) { return g->idx[l] + r0 * K; };
-    // One attention launch per run of layers that attend the same selected rows (a Full or Reindex
-    // layer and the Reuse layers after it), issued before the next layer's selection.  Its split:
-    // the forced one, else the automatic one for all the run's queries (at most 4 when chunks
-    // overlap), within the sized workspace.
+    // One attention launch for all the chunk's layers, each with its own selected rows (a Full or
+    // Reindex layer's, which the Reuse layers after it share), after the last selection.  Its split:
+    // the forced one, else the automatic one for all its queries (at most 4 when chunks overlap),
+    // within the sized workspace.
     const size_t attn_cap = csa2::group_attn_ws_bytes(rows, K, g->W, g->n_split);
     csa2::AttnLayers run{};
     int run_n = 0;
@@ -401,8 +423,10 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
     for (int l = 0; l < L; ++l) {
       const int mode = g->modes[l];
       if (mode != CSA2_MODE_REUSE) {
-        if (!flush_run()) return CSA2_ERR_CUDA;
-        if (g->hierarchical) {
+        if (l == l_rx) {
+          // its selection ran on the second side stream
+          if (!ok(cudaStreamWaitEvent(aux, ds->sel_done, 0))) return CSA2_ERR_CUDA;
+        } else if (g->hierarchical) {
           if (mode == CSA2_MODE_FULL) {
             if (nb > 0 && l != 0 &&
                 !ok(csa2::launch_index_score(qI_of(l), w_of(l), Bc, Nq, bkeys, nb, lens, g->cap, CSA2_BLOCK, nullptr,
@@ -412,6 +436,19 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
               if (!ok(csa2::launch_topk(sc, int(rc), nb, nb, pool_len, g->n_blocks_keep, nullptr, 0, pool, nullptr, 1,
                                         pool_len, tws, aux, zeroed)))
                 return CSA2_ERR_CUDA;
+              if (l == 0 && l_rx > 0) {
+                // the Reindex layer's pool scores in the score buffer's second pool-sized region, its
+                // own Top-K workspace and valid counts, on the second side stream
+                float* sc2 = sc + rc * pool_w;
+                int32_t* nv2 = reinterpret_cast<int32_t*>(wsb + lay.nv2_off) + r0;
+                if (!ok(cudaEventRecord(ds->pool_ready, aux)) || !ok(cudaStreamWaitEvent(ds->aux2, ds->pool_ready, 0)) ||
+                    !ok(csa2::launch_index_score(qI_of(l_rx), w_of(l_rx), Bc, Nq, KI, g->cap, lens, g->cap, 1, pool,
+                                                 pool_len, pool_w, g->ratio, qpos, sc2, pool_w, nv2, ds->aux2)) ||
+                    !ok(csa2::launch_topk(sc2, int(rc), pool_w, pool_w, nv2, K, pool, pool_w, idx_of(l_rx), nullptr, 0,
+                                          nullptr, wsb + lay.topk2_off, ds->aux2, false)) ||
+                    !ok(cudaEventRecord(ds->sel_done, ds->aux2)))
+                  return CSA2_ERR_CUDA;
+              }
             } else if (!ok(cudaMemsetAsync(pool_len, 0, size_t(rc) * sizeof(int32_t), aux))) {
               return CSA2_ERR_CUDA;
             }
@@ -449,6 +486,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
                            : g->swa[l] + win_off;
       run.out[run_n] = g->out[l] + r0 * (CSA2_H * CSA2_D);
       run.lse[run_n] = g->lse[l] ? g->lse[l] + r0 * CSA2_H : nullptr;
+      run.idx[run_n] = latest;
       run_idx = latest;
       ++run_n;
     }
