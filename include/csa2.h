@@ -241,8 +241,9 @@ csa2_status csa2_sparse_attn_decode(const uint16_t* q, int B, int Nq, const uint
  * partials and one ticket per query) is a fixed array of csa2_sparse_attn_static_scratch_bytes()
  * (16 MiB) inside the library, which every GPU that loads the library reserves until the process
  * exits; a call whose split needs more returns CSA2_ERR_TOO_LARGE.  A split needs 32,896 B per
- * query and split plus 4 B per query: a decode batch of 64 queries at its automatic split of 4
- * needs about 8.4 MB and fits, 128 queries forced to a split of 5 need about 21 MB and are refused
+ * query and split plus 4 B per query: a decode batch of 64 queries at its automatic split of 2
+ * (one CTA per SM on a 152-SM GB300) needs about 4.2 MB and fits, 128 queries forced to a split
+ * of 5 need about 21 MB and are refused
  * (csa2_attn_auto_split gives the automatic split).  The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) and keeps it for the life of the process (a device
  * reset while the library is loaded is not supported), so make that first call before any stream
