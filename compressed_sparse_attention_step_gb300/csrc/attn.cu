@@ -15,15 +15,16 @@
 //   - per tile, the rows are written to shared memory as a 64 x 512 operand in the 128-byte-swizzled
 //     layout the tensor core reads (FP4 rows dequantised to f16 with the E2M1 -> f16x2 and
 //     E4M3 -> f16x2 hardware conversions and one exact f16 multiply; window rows as bf16);
-//   - four warps each issue a quarter of S^T = K Q^T on the 5th-generation tensor core
-//     (tcgen05.mma, M = 64 rows, N = 16 heads, 128 of the 512 channels each) into their own
+//   - eight warps each issue an eighth of S^T = K Q^T on the 5th-generation tensor core
+//     (tcgen05.mma, M = 64 rows, N = 16 heads, 64 of the 512 channels each) into their own
 //     tensor-memory accumulator; a chain of N = 16 MMAs is bound by per-instruction latency, so
 //     independent chains from several warps run side by side;
-//   - the warps read the four partial S^T back (one row per lane), add them, run the online
-//     softmax and write P^T;
+//   - the warps read the eight partial S^T back (one row per lane), add them, run the online
+//     softmax and write P^T.  A running offset moves only when a score passes it by more than 2^12
+//     (one block barrier with an OR tells every warp whether any did; only then the tile's maxima);
 //   - four warps each issue one 128-channel block of O^T += V^T P^T (M = 128 channels, N = 16
 //     heads, K = 64 rows), V^T being the same shared-memory tile read channel-major; O^T stays in
-//     tensor memory across the CTA's tiles and is rescaled there when the running maximum moves.
+//     tensor memory across the CTA's tiles and is rescaled there when an offset moves.
 // Splits of a query are merged by the last CTA to finish (an atomic ticket), in split order, so
 // the result does not depend on which CTA finishes last.
 //
@@ -54,9 +55,9 @@ constexpr int kOIssuers = 4;         // warps whose lane 0 issues a 128-channel 
 constexpr uint32_t kOCol = 16 * kSIssuers;  // S^T partial i in columns [16 i, 16 i + 16); O^T block i at kOCol + 16 i
 constexpr uint32_t kTmemCols = 256;
 // Lazy rescaling: a head's running offset moves only when a tile's maximum exceeds it by more than
-// this many (log2 units), so P = 2^(x - m) stays below 2^8 and the accumulated O^T and sums are
-// rescaled only on such a jump.
-constexpr float kLazy = 8.0f;
+// this many (log2 units), so P = 2^(x - m) stays below 2^12 (f16 P stays far from its 65504 limit)
+// and the accumulated O^T and sums are rescaled only on such a jump.
+constexpr float kLazy = 12.0f;
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr uint32_t kTileGroup = kRows * 128;                 // 8 KiB per 64-channel group
@@ -75,8 +76,7 @@ struct Misc {
   int is_last;
   int32_t pos[kMaxTiles][kRows];  // source row of each row of the CTA's tiles, -1 if empty
   float red[4][CSA2_H];           // per-quarter tile maximum, then (at the end) partial sums
-  float m_run[2][CSA2_H];         // running offset (log2 units) per head, by tile parity
-  float corr[CSA2_H];             // rescale factor of a tile that moved an offset, per head
+  float m_fin[CSA2_H];            // final offset per head (log2 units)
   float l_fin[CSA2_H];            // final sum per head
 };
 constexpr size_t kSmemBytes = 1024 + kMiscOff + sizeof(Misc);
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   };
 
   if (t < CSA2_H) {
-    ms.m_run[0][t] = -INFINITY;
+    ms.m_fin[t] = -INFINITY;
     ms.l_fin[t] = 0.0f;
   }
   if (first_live >= 0) {
@@ -235,7 +235,6 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   };
 
   bool ok = true;
-  int par = 0;  // parity of the running offsets in use
   if (first_live >= 0) {
     tc_fence_after();
     const uint32_t tmem = ms.tmem_base;
@@ -245,8 +244,14 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     uint32_t ph_s = 0, ph_o = 0;
     int q_kind = -1;  // 0: Q staged as f16, 1: as bf16
     bool first = true;
-    // running sum of this lane's head (8 half + lane / 4) over this warp's rows
-    float l_w = 0.0f;
+    // mj[j]: the running offset of head 8 half + j (the same in every thread of the half); ls[j]: this
+    // lane's row's running sum for that head; lanes 0..15 also keep the offset of head `lane` in m_h
+    float mj[8], ls[8], m_h = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      mj[j] = -INFINITY;
+      ls[j] = 0.0f;
+    }
 
     for (int tile = first_live; tile <= last_live; ++tile) {
       if (!live(tile)) continue;
@@ -393,32 +398,55 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         for (int j = 0; j < 8; ++j)
           x[j] = row_ok ? (lo4[j] + ((sp[0][j] + sp[1][j]) + (sp[2][j] + sp[3][j]))) * scale_log2 : -INFINITY;
       }
-      {
+      // Does any score pass its head's offset by more than kLazy?  Usually not, and then the offsets
+      // stay and no maximum is needed (one block barrier with an OR); otherwise the tile's maxima set
+      // the offsets that move, and the O^T accumulated so far (complete: its MMAs were waited for
+      // above) and the sums are rescaled.
+      bool jump = false;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) jump |= x[j] > mj[j] + kLazy;
+      tc_fence_before();
+      if (__syncthreads_or(jump)) {
         const float mx = reduce_scatter8<true>(x, lane);
         if ((lane & 3) == 0) ms.red[quarter][8 * half + (lane >> 2)] = mx;
-      }
-      tc_fence_before();
-      __syncthreads();
-      // every thread derives the new offsets of its half's heads itself from the four quarters'
-      // maxima; threads t < 16 publish head t's offset and correction factor
-      const float* m_old = ms.m_run[par];
-      float* m_new = ms.m_run[par ^ 1];
-      float mj[8];
+        __syncthreads();
+        // lanes 0..15: head `lane`'s new offset and the factor that rescales what came before
+        float mn = m_h, corr = 1.0f;
+        if (lane < 16) {
+          const float mt = fmaxf(fmaxf(ms.red[0][lane], ms.red[1][lane]), fmaxf(ms.red[2][lane], ms.red[3][lane]));
+          mn = mt > m_h + kLazy ? mt : m_h;
+          corr = (mn != m_h && m_h != -INFINITY) ? ex2(m_h - mn) : 1.0f;
+          m_h = mn;
+        }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int h = 8 * half + j;
-        const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
-        mj[j] = mt > m_old[h] + kLazy ? mt : m_old[h];
-      }
-      if (t < CSA2_H) {
-        const float mt = fmaxf(fmaxf(ms.red[0][t], ms.red[1][t]), fmaxf(ms.red[2][t], ms.red[3][t]));
-        const float mo = m_old[t], mn = mt > mo + kLazy ? mt : mo;
-        m_new[t] = mn;
-        ms.corr[t] = (mn != mo && mo != -INFINITY) ? exp2f(mo - mn) : 1.0f;
+        for (int j = 0; j < 8; ++j) {
+          mj[j] = __shfl_sync(0xffffffffu, mn, 8 * half + j);
+          ls[j] *= __shfl_sync(0xffffffffu, corr, 8 * half + j);
+        }
+        if (__any_sync(0xffffffffu, corr != 1.0f)) {
+          // channel blocks 2 half, 2 half + 1 of this lane quarter
+          tc_fence_after();
+          float cr[16];
+#pragma unroll
+          for (int h = 0; h < 16; ++h) cr[h] = __shfl_sync(0xffffffffu, corr, h);
+          const uint32_t ta = t_lane + kOCol + uint32_t(32 * half);
+          float o[2][16];
+          tmem_ld16x2(ta, o);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int h = 0; h < 16; ++h) o[j][h] *= cr[h];
+          tmem_st16x2(ta, o);
+        }
       }
       float pr[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) pr[j] = mj[j] == -INFINITY ? 0.0f : exp2f(x[j] - mj[j]);
+      for (int j = 0; j < 8; ++j) {
+        // an empty row (x = -inf) gives 0; a finite x has a finite offset (the tile that first held a
+        // finite score for the head took the slow path)
+        pr[j] = x[j] == -INFINITY ? 0.0f : ex2(x[j] - mj[j]);
+        ls[j] += pr[j];
+      }
       // P^T (heads x rows, K-major, 128-byte swizzle): element (h, row)
       if (lane < 16) {
 #pragma unroll
@@ -429,36 +457,9 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
           *reinterpret_cast<uint16_t*>(base + kPOff + off) = bits;
         }
       }
-      const float sum = reduce_scatter8<false>(pr, lane);  // this warp's rows, head 8 half + lane / 4
-      {
-        const int h = 8 * half + (lane >> 2);
-        const float mo = m_old[h];
-        const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
-        const float mn = mt > mo + kLazy ? mt : mo;
-        const float cr = (mn != mo && mo != -INFINITY) ? exp2f(mo - mn) : 1.0f;
-        l_w = l_w * cr + sum;
-      }
       fence_async_smem();
       tc_fence_before();
       __syncthreads();
-      par ^= 1;
-      bool moved = false;  // an offset moved: the accumulated O^T is rescaled (the same on every thread)
-#pragma unroll
-      for (int h = 0; h < CSA2_H; ++h) moved |= ms.corr[h] != 1.0f;
-      if (moved) {
-        // rescale the O^T accumulated so far (channel blocks 2 half, 2 half + 1 of this lane quarter)
-        tc_fence_after();
-        const uint32_t ta = t_lane + kOCol + uint32_t(32 * half);
-        float o[2][16];
-        tmem_ld16x2(ta, o);
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-          for (int h = 0; h < 16; ++h) o[j][h] *= ms.corr[h];
-        tmem_st16x2(ta, o);
-        tc_fence_before();
-        __syncthreads();
-      }
 
       // -- O^T += V^T P^T (tensor core): warp i < 4 issues channel block i in 4 steps of 16 rows
       if (lane == 0 && warp < kOIssuers) {
@@ -478,9 +479,13 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
     // ---- last tile's MMAs, the sums per head, then O^T out of tensor memory -------------------------
     ok = ok && mbar_wait(mbar_o, ph_o);
     tc_fence_after();
+    const float l_w = reduce_scatter8<false>(ls, lane);  // this warp's rows, head 8 half + lane / 4
     if ((lane & 3) == 0) ms.red[quarter][8 * half + (lane >> 2)] = l_w;
     __syncthreads();
-    if (t < CSA2_H) ms.l_fin[t] = (ms.red[0][t] + ms.red[1][t]) + (ms.red[2][t] + ms.red[3][t]);
+    if (t < CSA2_H) {
+      ms.l_fin[t] = (ms.red[0][t] + ms.red[1][t]) + (ms.red[2][t] + ms.red[3][t]);
+      ms.m_fin[t] = m_h;
+    }
     __syncthreads();
     float o[2][16];
     tmem_ld16x2(t_lane + kOCol + uint32_t(32 * half), o);
@@ -517,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   if (n_split == 1) {
     if (lse && t < CSA2_H) {
       const float l = ms.l_fin[t];
-      lse[int64_t(inst) * CSA2_H + t] = l > 0.0f ? (ms.m_run[par][t] + log2f(l)) * kLn2 : -INFINITY;
+      lse[int64_t(inst) * CSA2_H + t] = l > 0.0f ? (ms.m_fin[t] + log2f(l)) * kLn2 : -INFINITY;
     }
     return;
   }
@@ -526,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
   float* mlb = ws + instances * n_split * (CSA2_H * CSA2_D);
   if (t < CSA2_H) {
     float* ml = mlb + (ginst * n_split + split) * (2 * CSA2_H);
-    ml[2 * t] = ms.m_run[par][t];
+    ml[2 * t] = ms.m_fin[t];
     ml[2 * t + 1] = ms.l_fin[t];
   }
   __threadfence();

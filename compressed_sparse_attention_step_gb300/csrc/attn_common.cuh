@@ -51,6 +51,13 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
   return h2_bits(__floats2half2_rn(bf16lo(u), bf16hi(u)));
 }
 
+// 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---- tcgen05 / mbarrier wrappers -----------------------------------------------------------------
 // Shared-memory matrix descriptor: start address, leading / stride byte offsets, descriptor
 // version 1, 128-byte swizzle.

@@ -118,12 +118,6 @@ __device__ __forceinline__ bool softmax_any(bool v) {
       : "memory");
   return r != 0;
 }
-// 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 // Waits for the completion of use n / 3 of barrier bars[n % 3].
 __device__ __forceinline__ bool wait_use(const unsigned long long* bars, int n) {
   return mbar_wait(smem_u32(&bars[n % kNBuf]), uint32_t(n / kNBuf) & 1u);
