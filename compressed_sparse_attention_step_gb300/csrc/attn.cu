@@ -28,9 +28,10 @@
 // Splits of a query are merged by the last CTA to finish (an atomic ticket), in split order, so
 // the result does not depend on which CTA finishes last.
 //
-// This kernel runs the launches of many queries (prefill chunks), where the second CTA on an SM
-// hides each CTA's setup and tail; launches of at most a few CTAs per SM (decode) go to the
-// warp-specialised kernel of attn_ws.cu, whose pipeline overlaps the tiles of one query.
+// This kernel runs every launch of more than one CTA per SM (the decode group's 256 queries, prefill
+// chunks), where the second CTA on an SM hides each CTA's setup and tail; launches that fit in one
+// wave (a Full layer's split query, the hierarchical step's 40 queries) go to the warp-specialised
+// kernel of attn_ws.cu, whose pipeline overlaps the tiles of one query.
 //
 // Operand types: a tile's MMA operands share one type.  FP4 tiles run in f16: the dequantised row
 // is exact in f16 (at most 6 significant bits, magnitudes in [2^-10, 2688]), Q is converted from
@@ -645,8 +646,9 @@ int sm_count() {
   return c;
 }
 
-// Launches of at most this many CTAs per SM run the warp-specialised kernel (one CTA per SM).
-constexpr int kWsMaxCtasPerSm = 4;
+// Launches of at most this many CTAs per SM run the warp-specialised kernel (one CTA per SM, so one
+// wave); larger ones this kernel, whose second CTA per SM hides each CTA's setup.
+constexpr int kWsMaxCtasPerSm = 1;
 
 int attn_auto_split(int64_t instances, int k, int W) {
   const int nt = attn_tiles(k, W);

@@ -5,8 +5,8 @@
 // architecture"; E2M1 codes with an E4M3 scale per 16 channels: section "FP4 KV, Bounded Replay,
 // and other extensions").  K = V = the dequantised row.
 //
-// The warp-specialised kernel, for launches of at most a few CTAs per SM (decode steps; launches of
-// many queries run the kernel of attn.cu, whose two CTAs per SM hide each other's setup).  A
+// The warp-specialised kernel, for launches of at most one CTA per SM (one wave; larger launches run
+// the kernel of attn.cu, whose two CTAs per SM hide each other's setup).  A
 // query's rows form 64-row tiles: the selected FP4 rows (ceil(k/64) tiles), then the window rows
 // (ceil(W/64) tiles).  A CTA takes a contiguous range of one query's tiles (the split) and runs its
 // live tiles through a pipeline of warp roles, one CTA per SM:
@@ -641,8 +641,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) sparse_attn_ws_kernel(
 
 }  // namespace
 
-// The warp-specialised kernel for launches of at most a few CTAs per SM (decode shapes).  The split
-// is already effective (attn_effective_split) and the tickets are zero.
+// The warp-specialised kernel for launches of at most one CTA per SM.  The split is already
+// effective (attn_effective_split) and the tickets are zero.
 cudaError_t launch_sparse_attn_ws(const AttnLayers& layers, int n_layers, int per_layer, int Nq,
                                   const uint8_t* codes, const uint8_t* scales, int64_t cap, const int32_t* idx,
                                   const int32_t* n_valid, int k, const int32_t* swa_len, int W, float scale_log2,

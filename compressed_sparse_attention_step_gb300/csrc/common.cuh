@@ -237,7 +237,7 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
                                       const int32_t* n_valid, int k, const int32_t* swa_len, int W,
                                       float softmax_scale, int n_split, float* ws, cudaStream_t st,
                                       bool tickets_zeroed, bool win_fp8);
-// The warp-specialised attention kernel (attn_ws.cu), for launches of a few CTAs per SM: the split
+// The warp-specialised attention kernel (attn_ws.cu), for launches of one CTA per SM: the split
 // is effective, partials and tickets as in launch_sparse_attn_layers (tickets zero).
 cudaError_t launch_sparse_attn_ws(const AttnLayers& layers, int n_layers, int per_layer, int Nq,
                                   const uint8_t* codes, const uint8_t* scales, int64_t cap, const int32_t* idx,

@@ -144,7 +144,7 @@ def test_split_partials_of_empty_splits_are_never_read(orc, n_split):
 
 @pytest.mark.parametrize("n_split", [0, 2])
 def test_many_queries_ragged(orc, n_split):
-    """640 queries (more than four CTAs per SM): the launch runs the kernel with two CTAs per SM
+    """640 queries (more than one CTA per SM): the launch runs the kernel with two CTAs per SM
     instead of the warp-specialised one.  Ragged selections, empty slots and partial windows; with
     a forced split of 2 its partials are merged too."""
     B, Nq, cap, k, W = 4, 160, 2000, 512, 128
