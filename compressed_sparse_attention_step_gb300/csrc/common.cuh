@@ -211,6 +211,7 @@ cudaError_t launch_index_score(const uint16_t* qI, const float* w, int B, int Nq
                                int64_t ld, int32_t* n_valid, cudaStream_t st);
 // Exact Top-K of `rows` score rows.  Rows longer than one slice are spread over several CTAs and
 // need workspace (topk_ws_bytes); ws may be NULL when topk_ws_bytes(...) == 0.
+int sm_count();  // SMs of the current device
 size_t topk_ws_bytes(int rows, int64_t n);
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
                         int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,

@@ -6,8 +6,13 @@
 // Radix select on ordered 32-bit score keys (-0 and +0 share a key):
 //  * rows up to 8192 columns (topk_kernel): one CTA per row histograms the top 12 key bits, lists
 //    the keys in and above the bin of the k-th largest key, and selects among them;
-//  * longer rows, three launches over (slices x rows) CTAs and then one CTA per row:
-//    topk_hist_kernel histograms the rows' 16-key group maxima and keeps every group's key;
+//  * rows of 8193 to 131072 columns (topk_cluster_kernel): one thread-block cluster of four or eight
+//    CTAs per row, in one launch.  The CTAs histogram the maxima of their 16-key groups, sum the
+//    histograms through distributed shared memory, take the bin of the k-th largest group maximum
+//    as a lower bound on the k-th largest key (those k maxima are k distinct keys) and append the
+//    keys at or above it to the first CTA's list, which selects among them;
+//  * longer rows, the same bound over three launches of (slices x rows) CTAs and then one CTA per
+//    row: topk_hist_kernel histograms the rows' 16-key group maxima and keeps every group's key;
 //    topk_filter_kernel takes the bin of the k-th largest group maximum as a lower bound on the
 //    k-th largest key (those k maxima are k distinct keys) and lists the keys at or above it,
 //    reading only the groups whose key reaches it; topk_select_kernel selects among the list.
@@ -33,6 +38,8 @@ constexpr int64_t kBitmapCols = 262144;   // rows up to this long are ordered th
 
 struct SelSmem {
   static constexpr int kNT = kThreads;
+  static constexpr int kCap = kCandCap;
+  static constexpr int kHistBins = kBins;
   uint32_t hist[kBins];
   uint32_t cand_key[kCandCap];
   int32_t cand_col[kCandCap];
@@ -45,6 +52,7 @@ struct SelSmem {
   uint32_t res_bin, res_before;
   uint32_t run_g, run_e;
   int is_last;
+  __device__ __forceinline__ int phys(int c) const { return c; }
 };
 
 // The prefill rows' selection (bitmap_select_kernel): a shorter candidate list (marked keys beyond
@@ -53,6 +61,7 @@ constexpr int kBmThreads = 256;
 constexpr int kBmCap = 4096;  // > CSA2_MAX_K
 struct BmSmem {
   static constexpr int kNT = kBmThreads;
+  static constexpr int kHistBins = 2048;
   uint32_t hist[2048];
   uint32_t cand_key[kBmCap];
   int32_t cand_col[kBmCap];  // always in column order
@@ -60,6 +69,7 @@ struct BmSmem {
   uint32_t nsel, ncand, base;
   uint32_t res_bin, res_before;
   uint32_t run_g, run_e;
+  __device__ __forceinline__ int phys(int c) const { return c; }
 };
 
 // Visit keys [lo, hi) of a row in tiles of 4 * U * blockDim.x (each thread takes U groups of 4
@@ -186,28 +196,36 @@ __device__ void finish_row(const RowOut& o, int64_t cnt, int row, int32_t* n_sel
 
 // The cut of the k largest of the nc candidates in shared memory (nc >= k) by (key desc, column
 // asc): a candidate is among them iff key > tau, or key == tau and column <= col_cut.
+// kmin / kmax: bounds of the candidates' keys (the bits they share need no round).
 template <class S>
-__device__ __forceinline__ void candidate_cut(S& sm, int nc, int k, uint32_t& tau_out, int32_t& cut_out) {
+__device__ __forceinline__ void candidate_cut(S& sm, int nc, int k, uint32_t& tau_out, int32_t& cut_out,
+                                              uint32_t kmin = 0u, uint32_t kmax = 0xFFFFFFFFu) {
   const int t = threadIdx.x;
-  uint32_t need = uint32_t(k), prefix = 0, mask = 0;
-  const int kshift[3] = {21, 10, 0}, kwidth[3] = {11, 11, 10};
-  for (int r = 0; r < 3; ++r) {
-    const int nb = 1 << kwidth[r];
+  const uint32_t diff = kmin ^ kmax;
+  int top = diff ? 32 - __clz(diff) : 0;  // key bits [0, top) differ among the candidates
+  uint32_t need = uint32_t(k);
+  uint32_t mask = top >= 32 ? 0u : 0xFFFFFFFFu << top;
+  uint32_t prefix = kmin & mask;
+  uint32_t nties = uint32_t(nc);  // candidates equal to tau (all of them when no round runs)
+  while (top > 0) {  // rounds of up to 12 bits (11 with a 2048-bin histogram), from the highest differing bit down
+    const int w = min(S::kHistBins >= 4096 ? 12 : 11, top), sh = top - w;
+    const uint32_t wmask = (1u << w) - 1u;
+    const int nb = max(1 << w, 1024);  // find_bin's smallest width
     zero(sm.hist, nb);
     for (int c = t; c < nc; c += blockDim.x) {
-      const uint32_t key = sm.cand_key[c];
-      if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> kshift[r]) & uint32_t(nb - 1)], 1u);
+      const uint32_t key = sm.cand_key[sm.phys(c)];
+      if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> sh) & wmask], 1u);
     }
     __syncthreads();
     find_bin<S::kNT>(sm.hist, nb, need, true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
-    prefix |= sm.res_bin << kshift[r];
-    mask |= uint32_t(nb - 1) << kshift[r];
+    prefix |= sm.res_bin << sh;
+    mask |= wmask << sh;
     need -= sm.res_before;
+    nties = sm.hist[sm.res_bin];
     __syncthreads();
+    top = sh;
   }
   const uint32_t tau = prefix;                       // the k-th largest key
-  const uint32_t nties = sm.hist[sm.res_bin];         // candidates equal to tau
-  __syncthreads();
   int32_t col_cut = 0x7FFFFFFF;                       // take ties at tau with column <= col_cut
   if (need < nties) {
     uint32_t cpre = 0;
@@ -217,8 +235,8 @@ __device__ __forceinline__ void candidate_cut(S& sm, int nc, int k, uint32_t& ta
       zero(sm.hist, nb);
       const uint32_t hi_mask = (r == 0) ? 0u : (0xFFFFFFFFu << (cshift[r] + cwidth[r]));
       for (int c = t; c < nc; c += blockDim.x) {
-        const uint32_t col = uint32_t(sm.cand_col[c]);
-        if (sm.cand_key[c] == tau && (col & hi_mask) == cpre)
+        const uint32_t col = uint32_t(sm.cand_col[sm.phys(c)]);
+        if (sm.cand_key[sm.phys(c)] == tau && (col & hi_mask) == cpre)
           atomicAdd(&sm.hist[(col >> cshift[r]) & uint32_t(nb - 1)], 1u);
       }
       __syncthreads();
@@ -233,30 +251,14 @@ __device__ __forceinline__ void candidate_cut(S& sm, int nc, int k, uint32_t& ta
   cut_out = col_cut;
 }
 
-// Position of the n-th set bit (from 0) of m (n < popcount(m)), by halving.
-__device__ __forceinline__ int nth_set_bit(uint32_t m, int n) {
-  int pos = 0;
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) {
-    const uint32_t low = (1u << s) - 1u;
-    const int c = __popc(m & low);
-    if (n >= c) {
-      n -= c;
-      m >>= s;
-      pos += s;
-    } else {
-      m &= low;
-    }
-  }
-  return pos;
-}
-
-// Emits the first cnt set columns of the bitmap sm.bits (nwords words, zero up to per * NT words,
-// per a power of two <= 8) in column order: out slot r gets the column of rank r.  Each thread
-// owns a run of per words; the words' exclusive prefix counts go to sm.hist, and every rank is
-// placed by a binary search over them, so the work does not depend on where the columns lie.
+// Writes each winner (key > tau, or key == tau and column <= col_cut) of the nc candidates whose
+// rank among the set bits of the bitmap sm.bits (the winners' columns; nwords words, zero up to
+// per * NT words, per a power of two <= 8) is below cnt to out slot = that rank.  Each thread owns
+// a run of per words; the words' exclusive prefix counts go to sm.hist, and a winner's rank is its
+// word's prefix plus the set bits below it in the word.
 template <class S>
-__device__ __forceinline__ void emit_by_rank(S& sm, int nwords, int per, int cnt, const RowOut& o) {
+__device__ __forceinline__ void emit_by_column(S& sm, int nc, int per, int cnt, uint32_t tau, int32_t col_cut,
+                                               const RowOut& o) {
   const int t = threadIdx.x;
   uint32_t wv[8];
   const uint32_t* run = sm.bits + t * per;
@@ -285,14 +287,14 @@ __device__ __forceinline__ void emit_by_rank(S& sm, int nwords, int per, int cnt
       pre += __popc(wv[e]);
     }
   __syncthreads();
-  for (int r = t; r < cnt; r += blockDim.x) {
-    int lo = 0, hi = nwords - 1;  // the last word whose prefix is <= r holds rank r
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pw[mid] <= uint32_t(r)) lo = mid;
-      else hi = mid - 1;
+  for (int c = t; c < nc; c += blockDim.x) {
+    const uint32_t key = sm.cand_key[sm.phys(c)];
+    const int32_t col = sm.cand_col[sm.phys(c)];
+    if (key > tau || (key == tau && col <= col_cut)) {
+      const int w = col >> 5;
+      const uint32_t r = pw[w] + __popc(sm.bits[w] & ((1u << (col & 31)) - 1u));
+      if (r < uint32_t(cnt)) o.emit(int(r), col);
     }
-    o.emit(r, int32_t(lo * 32 + nth_set_bit(sm.bits[lo], r - int(pw[lo]))));
   }
 }
 
@@ -305,7 +307,7 @@ __device__ __noinline__ void select_candidates(S& sm, int nc, int k, int64_t nco
   // negative do): the k lowest columns win, with no radix rounds.
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   for (int c = t; c < nc; c += blockDim.x) {
-    const uint32_t key = sm.cand_key[c];
+    const uint32_t key = sm.cand_key[sm.phys(c)];
     kmin = min(kmin, key);
     kmax = max(kmax, key);
   }
@@ -321,26 +323,28 @@ __device__ __noinline__ void select_candidates(S& sm, int nc, int k, int64_t nco
     atomicMax(&sm.run_e, kmax);
   }
   __syncthreads();
-  const bool one_key = sm.run_g == sm.run_e;
-  uint32_t tau = sm.run_g;
+  const uint32_t kmin_all = sm.run_g, kmax_all = sm.run_e;
+  const bool one_key = kmin_all == kmax_all;
+  uint32_t tau = kmin_all;
   int32_t col_cut = 0x7FFFFFFF;
   __syncthreads();
   const int nwords = int((ncols + 31) / 32);
   int per = 1;
   while (per * int(blockDim.x) < nwords) per <<= 1;
   const bool rank_emit = per <= 8 && per * int(blockDim.x) <= kBins;
-  if (!(one_key && rank_emit)) candidate_cut(sm, nc, k, tau, col_cut);
+  if (!(one_key && rank_emit)) candidate_cut(sm, nc, k, tau, col_cut, kmin_all, kmax_all);
   if (rank_emit) {
-    // bitmap of the winners (of every candidate for one key), then the first k ranks
+    // bitmap of the winners (of every candidate for one key); each winner of column rank below k
+    // goes to that slot
     for (int i = t; i < per * int(blockDim.x); i += blockDim.x) sm.bits[i] = 0u;
     __syncthreads();
     for (int c = t; c < nc; c += blockDim.x) {
-      const uint32_t key = sm.cand_key[c];
-      const int32_t col = sm.cand_col[c];
+      const uint32_t key = sm.cand_key[sm.phys(c)];
+      const int32_t col = sm.cand_col[sm.phys(c)];
       if (key > tau || (key == tau && col <= col_cut)) atomicOr(&sm.bits[col >> 5], 1u << (col & 31));
     }
     __syncthreads();
-    emit_by_rank(sm, nwords, per, k, o);
+    emit_by_column(sm, nc, per, k, tau, col_cut, o);
     return;
   }
   if (ncols <= kBitmapCols) {
@@ -348,8 +352,8 @@ __device__ __noinline__ void select_candidates(S& sm, int nc, int k, int64_t nco
     for (int i = t; i < nwords; i += blockDim.x) sm.bits[i] = 0u;
     __syncthreads();
     for (int c = t; c < nc; c += blockDim.x) {
-      const uint32_t key = sm.cand_key[c];
-      const int32_t col = sm.cand_col[c];
+      const uint32_t key = sm.cand_key[sm.phys(c)];
+      const int32_t col = sm.cand_col[sm.phys(c)];
       if (key > tau || (key == tau && col <= col_cut)) atomicOr(&sm.bits[col >> 5], 1u << (col & 31));
     }
     __syncthreads();
@@ -375,8 +379,8 @@ __device__ __noinline__ void select_candidates(S& sm, int nc, int k, int64_t nco
   if (t == 0) sm.nsel = 0;
   __syncthreads();
   for (int c = t; c < nc; c += blockDim.x) {
-    const uint32_t key = sm.cand_key[c];
-    if (key > tau || (key == tau && sm.cand_col[c] <= col_cut)) sm.sel[atomicAdd(&sm.nsel, 1u)] = sm.cand_col[c];
+    const uint32_t key = sm.cand_key[sm.phys(c)];
+    if (key > tau || (key == tau && sm.cand_col[sm.phys(c)] <= col_cut)) sm.sel[atomicAdd(&sm.nsel, 1u)] = sm.cand_col[sm.phys(c)];
   }
   __syncthreads();
   int P = 1;
@@ -449,7 +453,8 @@ __device__ __noinline__ void select_listed(S& sm, int nc, int k, const RowOut o)
 }
 
 // Whole-row selection by one CTA (short rows, and rows whose candidates overflow).
-__device__ __noinline__ void select_row(SelSmem& sm, const float* s, int64_t nv, int k, const RowOut o) {
+template <class S>
+__device__ __noinline__ void select_row(S& sm, const float* s, int64_t nv, int k, const RowOut o) {
   const int t = threadIdx.x, lane = t & 31;
   const unsigned lanes_below = (1u << lane) - 1u;
   zero(sm.hist, kBins);
@@ -460,7 +465,7 @@ __device__ __noinline__ void select_row(SelSmem& sm, const float* s, int64_t nv,
   const uint32_t ncand = sm.res_before + sm.hist[b1];   // keys in bins >= b1
   uint32_t need = uint32_t(k) - sm.res_before;
   __syncthreads();
-  if (ncand <= uint32_t(kCandCap)) {
+  if (ncand <= uint32_t(S::kCap)) {
     if (t == 0) sm.ncand = 0;
     __syncthreads();
     for_each_key<8>(s, 0, nv, [&](int64_t i, uint32_t key, bool valid) {
@@ -805,6 +810,338 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(
   }
 }
 
+// ---- rows of 8193 to 131072 columns: one thread-block cluster per row, one launch ------------------
+// The C CTAs of a cluster (C = 4 or 8) split the row into C runs of whole sweeps (8192 columns).  In a
+// sweep, thread t's group is the 16 keys at columns 4 (u kThreads + t) + e (u, e < 4), so that a warp's
+// loads are contiguous.  Each CTA keeps its groups' largest keys (and how many keys equal them) in
+// shared memory and histograms them by the top 12 key bits; the C histograms are summed through
+// distributed shared memory (each CTA sums a C-th of the bins and writes the sums into every CTA).
+// Then the bin of the k-th largest group maximum bounds the k-th largest key from below (those k
+// maxima are k distinct keys), and every CTA lists its keys at or above the bound, read again from
+// only its groups that reach it: the first CTA at the front of its list, the others in their own
+// shared memory and then, behind one reservation each, at the back of the first CTA's list, which
+// selects among the whole list.  When at least k keys equal the row's largest key, those k with the
+// lowest columns are the answer, and every CTA writes its share in column order without a list.
+constexpr int kClCap = 8192;        // candidates the first CTA of a cluster holds
+constexpr int kClSweep = 16 * kThreads;
+constexpr int kClGroups = 2048;     // groups per CTA: four sweeps
+constexpr int64_t kClMaxCols = 131072;
+
+struct ClSmem {
+  static constexpr int kNT = kThreads;
+  static constexpr int kCap = kClCap;
+  static constexpr int kHistBins = kBins;
+  uint32_t hist[kBins];          // this CTA's histogram of its group maxima; later the selection's
+  union {
+    uint32_t hsum[kBins];        // the row's histogram (every CTA holds all of it)
+    uint32_t bits[kBins];        // the first CTA's winner bitmap (columns < 131072)
+    int32_t sel[CSA2_MAX_K];
+  };
+  uint32_t gmax[kClGroups];      // largest key of each of this CTA's groups
+  uint8_t gcnt[kClGroups];       // how many of the group's keys equal it (0: an empty group)
+  uint32_t cand_key[kClCap];     // the list: the first CTA's keys at the front, the others' at the back
+  int32_t cand_col[kClCap];
+  uint32_t scan_tmp[32];
+  uint32_t peer_max[8], peer_cnt[8], peer_ng[8];  // every CTA's largest key, its count, its groups
+  uint32_t nsel, ncand, base, tail, ngrp;
+  uint32_t res_bin, res_before;
+  uint32_t run_g, run_e;
+  int n0, gap;                   // list entry c lies at c (c < n0) or c + gap
+  __device__ __forceinline__ int phys(int c) const { return c < n0 ? c : c + gap; }
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// The address of the same shared-memory word in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t dsmem_ld(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void dsmem_st(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_add(uint32_t a, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(a), "r"(v) : "memory");
+  return old;
+}
+// Every thread of every CTA of the cluster; what any of them wrote before it is visible after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Group t of the sweep at column c0: key[4 u + e] = column c0 + 4 (u kThreads + t) + e, below hi;
+// bit 4 u + e of the returned mask: that key exists.
+__device__ __forceinline__ uint32_t load_sweep_group(const float* s, int64_t c0, int64_t hi, int t,
+                                                     uint32_t (&key)[16]) {
+  const bool full = c0 + kClSweep <= hi && ((reinterpret_cast<uintptr_t>(s + c0) & 15u) == 0);
+  uint32_t m = 0u;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int64_t i0 = c0 + 4 * (int64_t(u) * kThreads + t);
+    if (full) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(s + i0));
+      key[4 * u] = score_key(x.x); key[4 * u + 1] = score_key(x.y);
+      key[4 * u + 2] = score_key(x.z); key[4 * u + 3] = score_key(x.w);
+      m |= 0xFu << (4 * u);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool in = i0 + e < hi;
+        key[4 * u + e] = in ? score_key(__ldg(s + i0 + e)) : 0u;
+        m |= in ? 1u << (4 * u + e) : 0u;
+      }
+    }
+  }
+  return m;
+}
+
+template <int C>
+__global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(
+    const float* __restrict__ scores, int64_t n, int64_t ld, const int32_t* __restrict__ n_valid, int k,
+    const int32_t* __restrict__ map, int64_t map_ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
+    int expand8, int32_t* __restrict__ pool_len) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  ClSmem& sm = *reinterpret_cast<ClSmem*>(smem_raw);
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.y, t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const uint32_t rank = cluster_rank();
+  const float* s = scores + int64_t(row) * ld;
+  const int64_t nv = row_valid(n_valid, row, n);  // read by every CTA before the first CTA writes pool_len
+  const RowOut o{map ? map + int64_t(row) * map_ld : nullptr, idx + int64_t(row) * (expand8 ? k * CSA2_BLOCK : k),
+                 expand8 ? k * CSA2_BLOCK : k, expand8};
+  const bool all = nv <= k;  // the same in every CTA of the cluster
+  // this CTA's sweeps [q0, q0 + nq) of the row's ceil(nv / kClSweep)
+  const int64_t sweeps = (nv + kClSweep - 1) / kClSweep, spc = (sweeps + C - 1) / C;
+  const int64_t q0 = int64_t(rank) * spc;
+  const int nq = all ? 0 : int(max(min(spc, sweeps - q0), int64_t(0)));
+  const int ng = nq * kThreads;  // group q kThreads + t: thread t's group of sweep q0 + q
+  auto sweep_col = [&](int q) { return (q0 + q) * int64_t(kClSweep); };
+
+  // ---- 1. group maxima, their histogram, this CTA's largest key and its count ---------------------
+  for (int i = t; i < kBins; i += kThreads) sm.hist[i] = 0u;
+  if (t == 0) {
+    sm.nsel = 0u;
+    sm.base = 0u;
+    sm.tail = 0u;
+    sm.ngrp = 0u;
+  }
+  __syncthreads();
+  uint32_t lmax = 0u, lng = 0u;
+  for (int q = 0; q < nq; q += 2) {  // two sweeps' loads in flight
+    uint32_t key[2][16], m[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      m[u] = 0u;
+      if (q + u < nq) m[u] = load_sweep_group(s, sweep_col(q + u), nv, t, key[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (q + u >= nq) break;
+      uint32_t gm = 0u, gc = 0u;
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if ((m[u] >> e) & 1u) gm = max(gm, key[u][e]);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) gc += ((m[u] >> e) & 1u) && key[u][e] == gm;
+      const bool has = m[u] != 0u;
+      const int gi = (q + u) * kThreads + t;
+      sm.gmax[gi] = gm;
+      sm.gcnt[gi] = uint8_t(gc);
+      lmax = max(lmax, gm);
+      lng += has;
+      const uint32_t bin = has ? gm >> 20 : 0xFFFFFFFFu;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (has && (__ffs(peers) - 1) == lane) atomicAdd(&sm.hist[bin], uint32_t(__popc(peers)));
+    }
+  }
+  lmax = __reduce_max_sync(0xffffffffu, lmax);
+  lng = __reduce_add_sync(0xffffffffu, lng);
+  if (lane == 0) {
+    sm.scan_tmp[wid] = lmax;
+    if (lng) atomicAdd(&sm.ngrp, lng);
+  }
+  __syncthreads();
+  lmax = 0u;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) lmax = max(lmax, sm.scan_tmp[w]);
+  uint32_t lcnt = 0u;
+  for (int gi = t; gi < ng; gi += kThreads)
+    if (sm.gmax[gi] == lmax) lcnt += sm.gcnt[gi];
+  lcnt = __reduce_add_sync(0xffffffffu, lcnt);
+  if (lane == 0 && lcnt) atomicAdd(&sm.base, lcnt);
+  cluster_sync_all();  // 1: every CTA has started, and its histogram and counts are complete
+
+  if (all) {  // everything valid is selected, already ascending
+    if (rank == 0) {
+      for (int i = t; i < nv; i += kThreads) o.emit(i, i);
+      finish_row(o, nv, row, n_sel, pool_len);
+    }
+    return;
+  }
+  // ---- 2. the row's histogram in every CTA; every CTA's largest key, its count, its groups --------
+  constexpr int kPer = kBins / C;
+  for (int b = t; b < kPer; b += kThreads) {
+    const int bin = int(rank) * kPer + b;
+    uint32_t sum = 0u;
+#pragma unroll
+    for (int r = 0; r < C; ++r) sum += dsmem_ld(dsmem_addr(&sm.hist[bin], uint32_t(r)));
+#pragma unroll
+    for (int r = 0; r < C; ++r) dsmem_st(dsmem_addr(&sm.hsum[bin], uint32_t(r)), sum);
+  }
+  if (t < C) {
+    dsmem_st(dsmem_addr(&sm.peer_max[rank], uint32_t(t)), lmax);
+    dsmem_st(dsmem_addr(&sm.peer_cnt[rank], uint32_t(t)), sm.base);
+    dsmem_st(dsmem_addr(&sm.peer_ng[rank], uint32_t(t)), sm.ngrp);
+  }
+  cluster_sync_all();  // 2
+
+  uint32_t M = 0u, cnt_m = 0u, before_m = 0u, groups = 0u;  // the row's largest key, its count, its
+#pragma unroll                                               // count in lower CTAs; non-empty groups
+  for (int r = 0; r < C; ++r) {
+    M = max(M, sm.peer_max[r]);
+    groups += sm.peer_ng[r];
+  }
+#pragma unroll
+  for (int r = 0; r < C; ++r)
+    if (sm.peer_max[r] == M) {
+      cnt_m += sm.peer_cnt[r];
+      before_m += r < int(rank) ? sm.peer_cnt[r] : 0u;
+    }
+  if (cnt_m >= uint32_t(k)) {
+    // ---- at least k keys equal the largest: the k lowest columns holding it, in column order ------
+    if (lmax == M && before_m < uint32_t(k)) {
+      uint32_t done = before_m;
+      for (int q = 0; q < nq && done < uint32_t(k); ++q) {
+        const int gi = q * kThreads + t;
+        uint32_t key[16], m = 0u;
+        if (sm.gmax[gi] == M) m = load_sweep_group(s, sweep_col(q), nv, t, key);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {  // the sweep's columns in order: by u, then thread, then e
+          uint32_t c = 0u;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) c += ((m >> (4 * u + e)) & 1u) && key[4 * u + e] == M;
+          uint32_t tot;
+          uint32_t slot = done + block_exclusive_scan(c, sm.scan_tmp, &tot);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (((m >> (4 * u + e)) & 1u) && key[4 * u + e] == M) {
+              if (slot < uint32_t(k)) o.emit(int(slot), int32_t(sweep_col(q) + 4 * (u * kThreads + t) + e));
+              ++slot;
+            }
+          done += tot;
+        }
+      }
+    }
+    if (rank == 0) finish_row(o, k, row, n_sel, pool_len);
+    return;
+  }
+  // ---- 3. the bound; this CTA's keys at or above it listed -----------------------------------------
+  uint32_t bound = 0u;  // keys >= bound: a superset of the row's Top-k
+  if (groups >= uint32_t(k)) {
+    find_bin<kThreads>(sm.hsum, kBins, uint32_t(k), true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+    bound = sm.res_bin << 20;
+  }
+  // the groups that reach the bound, listed (the row histogram's space is free now), so that each
+  // thread loads at most one group per round and all of a round's loads are in flight together
+  uint32_t* glist = sm.hsum;
+  if (t == 0) sm.ncand = 0u;
+  __syncthreads();
+  {
+    uint32_t hits = 0u;  // bit q: this thread's group of sweep q0 + q reaches the bound
+    for (int q = 0; q < nq; ++q) {
+      const int gi = q * kThreads + t;
+      if (sm.gcnt[gi] && sm.gmax[gi] >= bound) hits |= 1u << q;
+    }
+    const uint32_t hc = __popc(hits);
+    uint32_t incl = hc;  // the warp's inclusive prefix of the counts, one reservation per warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t wb = 0u;
+    if (lane == 31 && wtot) wb = atomicAdd(&sm.ncand, wtot);
+    uint32_t slot = __shfl_sync(0xffffffffu, wb, 31) + incl - hc;
+    for (int q = 0; q < nq; ++q)
+      if ((hits >> q) & 1u) glist[slot++] = uint32_t(q * kThreads + t);
+  }
+  __syncthreads();
+  const int nlist = int(sm.ncand);
+  for (int i0 = 0; i0 < nlist; i0 += kThreads) {  // the same trip count for every thread of the CTA
+    const int i = i0 + t;
+    const int gi = i < nlist ? int(glist[i]) : 0, q = gi / kThreads, gt = gi % kThreads;
+    uint32_t key[16], m = 0u;
+    if (i < nlist) m = load_sweep_group(s, sweep_col(q), nv, gt, key);
+    uint32_t take = 0u;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) take |= (((m >> e) & 1u) && key[e] >= bound) ? 1u << e : 0u;
+    const uint32_t cnt = __popc(take);
+    uint32_t incl = cnt;  // the warp's inclusive prefix of the counts
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t wbase = 0u;
+    if (lane == 31 && wtot) wbase = atomicAdd(&sm.nsel, wtot);
+    wbase = __shfl_sync(0xffffffffu, wbase, 31);
+    uint32_t slot = wbase + incl - cnt;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if ((take >> e) & 1u) {
+        if (slot < uint32_t(kClCap)) {
+          sm.cand_key[slot] = key[e];
+          sm.cand_col[slot] = int32_t(sweep_col(q) + 4 * ((e >> 2) * kThreads + gt) + (e & 3));
+        }
+        ++slot;
+      }
+  }
+  __syncthreads();
+  const uint32_t mine = sm.nsel;  // may exceed kClCap: then the row falls back to the whole-row path
+  if (rank != 0 && mine) {
+    // behind one reservation, at the back of the first CTA's list
+    if (t == 0) sm.base = dsmem_add(dsmem_addr(&sm.tail, 0u), mine > uint32_t(kClCap) ? uint32_t(kClCap) + 1u : mine);
+    __syncthreads();
+    const uint32_t end = uint32_t(kClCap) - sm.base;  // this CTA's entries end here
+    if (sm.base + mine <= uint32_t(kClCap)) {
+      const uint32_t key_at = dsmem_addr(sm.cand_key, 0u), col_at = dsmem_addr(sm.cand_col, 0u);
+      for (uint32_t i = t; i < mine; i += kThreads) {
+        const uint32_t d = end - mine + i;
+        dsmem_st(key_at + 4u * d, sm.cand_key[i]);
+        dsmem_st(col_at + 4u * d, uint32_t(sm.cand_col[i]));
+      }
+    }
+  }
+  cluster_sync_all();  // 3: the list is complete; no CTA touches another's shared memory after this
+  if (rank != 0) return;
+  // ---- 4. the first CTA selects among the list (the whole row should it have overflowed) -----------
+  const uint32_t back = sm.tail;  // the other CTAs' entries, [kClCap - back, kClCap)
+  const uint32_t nc = mine + back;
+  if (nc <= uint32_t(kClCap)) {
+    sm.n0 = int(mine);
+    sm.gap = kClCap - int(back) - int(mine);
+    select_candidates(sm, int(nc), k, nv, o);
+  } else {
+    sm.n0 = kClCap;
+    sm.gap = 0;
+    select_row(sm, s, nv, k, o);
+  }
+  finish_row(o, k, row, n_sel, pool_len);
+}
+
 // Prefill rows: the keys marked in the tensor-core filter's bitmap are rescored in the canonical
 // order (eight lanes per key, the query slice in registers) and the exact Top-k is selected among
 // them.  One CTA per query row.
@@ -951,6 +1288,38 @@ size_t topk_ws_bytes(int rows, int64_t n) {
          topk_ctl_words(rows) * sizeof(uint32_t) + size_t(rows) * size_t(topk_group_ld(n)) * sizeof(uint32_t);
 }
 
+// One cluster of C CTAs per row (rows of kSmallRow + 1 to kClMaxCols columns).
+template <int C>
+cudaError_t launch_topk_cluster(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid, int k,
+                                const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel, int expand8,
+                                int32_t* pool_len, cudaStream_t st) {
+  const size_t smem = sizeof(ClSmem);
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(C), unsigned(rows), 1u);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = unsigned(C);
+  attr[1].val.clusterDim.y = 1u;
+  attr[1].val.clusterDim.z = 1u;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<C>, scores, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8,
+                            pool_len);
+}
+
 cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
                         int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,
                         int expand8, int32_t* pool_len, void* ws, cudaStream_t st, bool counters_zeroed) {
@@ -967,6 +1336,13 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
   if (topk_ws_bytes(rows, n) == 0)  // one CTA per row over the whole row
     return launch_pdl(topk_kernel, dim3(1u, unsigned(rows), 1u), dim3(kThreads), smem, st, scores, n, ld, n_valid, k,
                       map, map_ld, idx, n_sel, expand8, pool_len);
+  if (n <= kClMaxCols) {
+    // one cluster per row: eight CTAs when every row's cluster fits in one wave of two CTAs per SM
+    // and each CTA keeps at least 8192 columns, else four
+    if (int64_t(rows) * 8 <= 2 * int64_t(sm_count()) && n >= 8 * 8192)
+      return launch_topk_cluster<8>(scores, rows, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len, st);
+    return launch_topk_cluster<4>(scores, rows, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len, st);
+  }
   if (!ws) return cudaErrorInvalidValue;
   uint32_t* ckey = static_cast<uint32_t*>(ws);
   int32_t* ccol = reinterpret_cast<int32_t*>(ckey + size_t(rows) * kCandCap);

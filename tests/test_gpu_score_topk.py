@@ -160,6 +160,52 @@ def test_topk_long_rows_bound_and_overflow(orc):
         assert np.array_equal(idx[r], exp), r
 
 
+def _cluster_rows(n, k, g):
+    """Rows for the one-cluster-per-row selection (8193 to 131072 columns)."""
+    rows = []
+    r = g.standard_normal(n).astype(np.float32)
+    r[g.choice(n, k + 700, replace=False)] = 5.0       # the largest key k + 700 times: its k lowest columns
+    rows.append(r)
+    r = g.standard_normal(n).astype(np.float32)
+    r[g.choice(n, k, replace=False)] = 5.0             # exactly k times
+    rows.append(r)
+    r = g.standard_normal(n).astype(np.float32)
+    pos = g.choice(n, k + 9, replace=False)
+    r[pos[:k - 1]] = 5.0                               # k - 1 times, then ten ties one key lower
+    r[pos[k - 1:]] = 4.0
+    rows.append(r)
+    rows.append(np.where(g.random(n) < 0.5, 0.0, -0.0).astype(np.float32))  # +0 and -0 only: one key
+    r = (g.standard_normal(n) * 1e-4).astype(np.float32)
+    r[n // 4 - 3:n // 4 + 3] = 1.0                     # ties across the boundary of the first CTA's run
+    r[n // 2 - 8:n // 2 + 8] = 1.0
+    rows.append(r)
+    rows.append(np.round(g.standard_normal(n) * 8).astype(np.float32))  # wide bins, many ties at the cut
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("k", [512, 2048])
+@pytest.mark.parametrize("reps", [1, 8])
+def test_topk_cluster_rows(orc, k, reps):
+    """One thread-block cluster per row (eight CTAs for the 6 rows, four for 48): the largest key held
+    by at least k columns (each CTA writes its share of the k lowest in column order), by exactly k
+    and by k - 1 (then the list), signed zeros only, ties across the CTAs' runs, and valid prefixes
+    whose every key is listed (8000: the list holds them; 8193 and 9000: the whole-row fallback)."""
+    g = np.random.default_rng(31 + k)
+    n = 131072
+    s = np.concatenate([_cluster_rows(n, k, g) for _ in range(reps)])
+    rows = s.shape[0]
+    nvalid = np.full(rows, n, np.int32)
+    nvalid[5::6] = [8000, 8193, 9000, n - 5, 40000, 131071, 70000, 16 * k + 1][:len(nvalid[5::6])]
+    idx = torch.full((rows, k), -5, dtype=torch.int32, device="cuda")
+    nsel = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    c.csa2_topk(to_dev(s), k, idx, n_valid=to_dev(nvalid), n_sel=nsel)
+    idx, nsel = idx.cpu().numpy(), nsel.cpu().numpy()
+    for r in range(rows):
+        exp, cnt = orc.topk(s[r, :nvalid[r]], k)
+        assert nsel[r] == cnt
+        assert np.array_equal(idx[r], exp), r
+
+
 def test_topk_with_map(orc):
     g = np.random.default_rng(5)
     n, k = 16384, 512
