@@ -281,9 +281,9 @@ def make_desc(c, wl, events=None, q=None, qI=None, w=None, kv_new=None, ki_new=N
 
 def launches_per_step(c):
     # the append (quantise the new KV row, copy the new indexer-K row: one launch) + score + Top-K
-    # (row histogram, filter, select) + one attention launch for the four layers (they attend the
-    # same selected rows; split partials are merged inside that launch)
-    return 6
+    # (one cluster launch for rows of up to 131072 entries) + one attention launch for the four layers
+    # (they attend the same selected rows; split partials are merged inside that launch)
+    return 4
 
 
 def max_over_ranks(torch, dist, value, world, device):
@@ -743,8 +743,8 @@ def run_stack20(args, torch, c, syn, dev, sampler):
             "roofline": roofline("index_score_stream_kernel", f"decode_group_b{B}_t{T}", "hbm", B * BYTES_KI_PER_SEQ,
                                  statistics.mean(sc.ms()), K, peak, f"{kind} (hbm copy)"),
             "cpu_baseline": cpu,
-            # group 1: append + score + Top-K (3) + attention; groups 2-5: score + Top-K (3) + attention
-            "gpu_launches": (6 + 4 * 5) * K, "clocks": sampler.summary(t0, t1) if sampler else None}
+            # group 1: append + score + Top-K + attention; groups 2-5: score + Top-K + attention
+            "gpu_launches": (4 + 3 * 4) * K, "clocks": sampler.summary(t0, t1) if sampler else None}
 
 
 def run_prefill(args, torch, c, syn, dev, sampler):
@@ -922,10 +922,9 @@ def run_hier1m(args, torch, c, syn, dev, sampler):
             "roofline": roofline("index_score_stream_kernel", f"hier_decode_b{B}_t1m", "hbm", B * (T // 8) * 256,
                                  statistics.mean(sc.ms()), K, peak, f"{kind} (hbm copy)"),
             "cpu_baseline": cpu,
-            # the append, the block-key refresh, the block scan, Top-2048 (3 launches), then for Full and
-            # Reindex each a pool scan and Top-512 (3 launches), and one attention launch per run of layers
-            # (Full; Reindex + 3 Reuse)
-            "gpu_launches": 16 * K, "clocks": sampler.summary(t0, t1) if sampler else None}
+            # the append, the block-key refresh, the block scan, Top-2048, then for Full and Reindex each
+            # a pool scan and Top-512, and one attention launch for the five layers
+            "gpu_launches": 9 * K, "clocks": sampler.summary(t0, t1) if sampler else None}
 
 
 EXTRA = {"full_layer_decode": run_full_layer, "fp4_roundtrip": run_fp4_roundtrip, "prefill_chunk": run_prefill,

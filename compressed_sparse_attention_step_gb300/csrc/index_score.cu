@@ -258,6 +258,8 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
   __syncwarp();
 
   const uint16_t* kseq = KI + int64_t(b) * key_stride_rows * CSA2_DI;
+  uint64_t stream_policy = 0;
+  if (!kCand) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(stream_policy));
   const int64_t first = c0 + int64_t(warp) * kPosPerWarpIt;
   const int n_steps = first < c1 ? int((c1 - first + kPosPerCtaIt - 1) / kPosPerCtaIt) : 0;
   // step i covers positions first + i * kPosPerCtaIt + [0, 16); the keys of those below lend.
@@ -274,10 +276,13 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
       if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+        // the keys are read once: first out of L2, so that the scores written beside them stay
+        // there for the selection that reads them next
         if (bytes)
           asm volatile(
-              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-              "l"(kseq + base * CSA2_DI), "r"(bytes), "r"(bar)
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+              "%4;\n" ::"r"(dst),
+              "l"(kseq + base * CSA2_DI), "r"(bytes), "r"(bar), "l"(stream_policy)
               : "memory");
       }
       return;

@@ -47,12 +47,14 @@ struct SelSmem {
     int32_t sel[CSA2_MAX_K];
     uint32_t bits[kBitmapCols / 32];
   };
+  int32_t stage[CSA2_MAX_K];  // the winners' columns by output slot
   uint32_t scan_tmp[32];
   uint32_t nsel, ncand, base;
   uint32_t res_bin, res_before;
   uint32_t run_g, run_e;
   int is_last;
   __device__ __forceinline__ int phys(int c) const { return c; }
+  __device__ __forceinline__ int32_t* out_stage() { return stage; }
 };
 
 // The prefill rows' selection (bitmap_select_kernel): a shorter candidate list (marked keys beyond
@@ -171,6 +173,7 @@ __device__ __forceinline__ void hist12(const float* s, int64_t lo, int64_t hi, u
 
 // Output of one row (optionally through a column -> position map, optionally expanded to the
 // eight positions of each selected block).
+static_assert(CSA2_BLOCK == 8, "a block's positions are written as two 16-byte stores");
 struct RowOut {
   const int32_t* mrow;
   int32_t* out;
@@ -182,6 +185,28 @@ struct RowOut {
       for (int r = 0; r < CSA2_BLOCK; ++r) out[slot * CSA2_BLOCK + r] = v * CSA2_BLOCK + r;
     } else {
       out[slot] = v;
+    }
+  }
+  // Slots [0, cnt) from stage[slot] = column, consecutive threads writing consecutive outputs.
+  __device__ __forceinline__ void emit_staged(const int32_t* stage, int cnt) const {
+    if (expand8 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {  // a slot's eight positions: two 16-byte stores
+      for (int sl = threadIdx.x; sl < cnt; sl += blockDim.x) {
+        const int32_t col = stage[sl];
+        const int32_t v = (mrow ? __ldg(mrow + col) : col) * CSA2_BLOCK;
+        int4* o4 = reinterpret_cast<int4*>(out + int64_t(sl) * CSA2_BLOCK);
+        o4[0] = make_int4(v, v + 1, v + 2, v + 3);
+        o4[1] = make_int4(v + 4, v + 5, v + 6, v + 7);
+      }
+    } else if (expand8) {
+      for (int i = threadIdx.x; i < cnt * CSA2_BLOCK; i += blockDim.x) {
+        const int32_t col = stage[i / CSA2_BLOCK];
+        out[i] = (mrow ? __ldg(mrow + col) : col) * CSA2_BLOCK + i % CSA2_BLOCK;
+      }
+    } else {
+      for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+        const int32_t col = stage[i];
+        out[i] = mrow ? __ldg(mrow + col) : col;
+      }
     }
   }
 };
@@ -255,7 +280,8 @@ __device__ __forceinline__ void candidate_cut(S& sm, int nc, int k, uint32_t& ta
 // rank among the set bits of the bitmap sm.bits (the winners' columns; nwords words, zero up to
 // per * NT words, per a power of two <= 8) is below cnt to out slot = that rank.  Each thread owns
 // a run of per words; the words' exclusive prefix counts go to sm.hist, and a winner's rank is its
-// word's prefix plus the set bits below it in the word.
+// word's prefix plus the set bits below it in the word.  The columns are placed by rank in shared
+// memory first (sm.out_stage()), so that the output is written in order.
 template <class S>
 __device__ __forceinline__ void emit_by_column(S& sm, int nc, int per, int cnt, uint32_t tau, int32_t col_cut,
                                                const RowOut& o) {
@@ -287,15 +313,18 @@ __device__ __forceinline__ void emit_by_column(S& sm, int nc, int per, int cnt, 
       pre += __popc(wv[e]);
     }
   __syncthreads();
+  int32_t* stage = sm.out_stage();
   for (int c = t; c < nc; c += blockDim.x) {
     const uint32_t key = sm.cand_key[sm.phys(c)];
     const int32_t col = sm.cand_col[sm.phys(c)];
     if (key > tau || (key == tau && col <= col_cut)) {
       const int w = col >> 5;
       const uint32_t r = pw[w] + __popc(sm.bits[w] & ((1u << (col & 31)) - 1u));
-      if (r < uint32_t(cnt)) o.emit(int(r), col);
+      if (r < uint32_t(cnt)) stage[r] = col;
     }
   }
+  __syncthreads();
+  o.emit_staged(stage, cnt);
 }
 
 // The k largest of the nc candidates in shared memory (nc >= k) by (key desc, column asc), emitted
@@ -825,6 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(
 constexpr int kClCap = 8192;        // candidates the first CTA of a cluster holds
 constexpr int kClSweep = 16 * kThreads;
 constexpr int kClGroups = 2048;     // groups per CTA: four sweeps
+static_assert(kClGroups >= CSA2_MAX_K, "the group maxima's space stages the output");
 constexpr int64_t kClMaxCols = 131072;
 
 struct ClSmem {
@@ -848,6 +878,8 @@ struct ClSmem {
   uint32_t run_g, run_e;
   int n0, gap;                   // list entry c lies at c (c < n0) or c + gap
   __device__ __forceinline__ int phys(int c) const { return c < n0 ? c : c + gap; }
+  // the winners' columns by output slot (the group maxima are no longer needed then)
+  __device__ __forceinline__ int32_t* out_stage() { return reinterpret_cast<int32_t*>(gmax); }
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
