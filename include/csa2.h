@@ -155,7 +155,9 @@ csa2_status csa2_index_score(const uint16_t* qI, const float* w, int B, int Nq, 
  *   ws      workspace of csa2_workspace_size(CSA2_OP_TOPK, ...) bytes, 16-byte aligned: for rows
  *           longer than 8192 columns the candidate lists, per-row counters, histograms and
  *           16-column group keys of the multi-CTA selection (the call clears what must start at
- *           zero); 0 bytes, and ws may be NULL, otherwise.
+ *           zero); 0 bytes, and ws may be NULL, otherwise.  Rows of 8193 to 131072 columns select
+ *           in one launch of a thread-block cluster per row that keeps all of this in shared
+ *           memory, so only longer rows touch ws; the size asked for stays the same.
  */
 csa2_status csa2_topk(const float* scores, int rows, int64_t n, int64_t ld, const int32_t* n_valid,
                       int k, const int32_t* map, int64_t map_ld, int32_t* idx, int32_t* n_sel,
