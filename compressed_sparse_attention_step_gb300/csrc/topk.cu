@@ -102,6 +102,26 @@ __device__ __forceinline__ void for_each_key(const float* s, int64_t lo, int64_t
   }
 }
 
+// The 16 scores thread t reads in one sweep step starting at b0: float4 number u * kThreads + t
+// (u < 4) of the step, i.e. v[4 u + e] = s[b0 + 4 (u kThreads + t) + e]; past hi they are NaN,
+// which every comparison rejects and fmaxf ignores.
+template <int NT = kThreads>
+__device__ __forceinline__ void load16(const float* s, int64_t b0, int64_t hi, float (&v)[16]) {
+  const int t = threadIdx.x;
+  const bool full = b0 + int64_t(16) * NT <= hi && ((reinterpret_cast<uintptr_t>(s + b0) & 15u) == 0);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int64_t i0 = b0 + (int64_t(u) * NT + t) * 4;
+    if (full) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(s + i0));
+      v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[4 * u + e] = (i0 + e < hi) ? __ldg(s + i0 + e) : __int_as_float(0x7FC00000);
+    }
+  }
+}
+
 template <int NB, int NT>
 __device__ void find_bin_n(const uint32_t* hist, uint32_t need, bool from_top, uint32_t* scan_tmp,
                            uint32_t* res_bin, uint32_t* res_before) {
@@ -484,8 +504,35 @@ __device__ __noinline__ void select_listed(S& sm, int nc, int k, const RowOut o)
 // Whole-row selection by one CTA (short rows, and rows whose candidates overflow).
 template <class S>
 __device__ __noinline__ void select_row(S& sm, const float* s, int64_t nv, int k, const RowOut o) {
-  const int t = threadIdx.x, lane = t & 31;
-  const unsigned lanes_below = (1u << lane) - 1u;
+  const int t = threadIdx.x;
+  if (nv <= int64_t(16) * S::kNT) {
+    // the whole row in registers, 16 keys per thread: one read serves the histogram and the list
+    float v[16];
+    load16<S::kNT>(s, 0, nv, v);  // NaN past nv: neither counted nor listed
+    zero(sm.hist, kBins);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (v[e] == v[e]) atomicAdd(&sm.hist[score_key(v[e]) >> 20], 1u);
+    __syncthreads();
+    find_bin(sm.hist, kBins, uint32_t(k), true, sm.scan_tmp, &sm.res_bin, &sm.res_before);
+    const uint32_t b1 = sm.res_bin;  // the list (keys in bins >= b1) holds at most nv <= S::kCap keys
+    __syncthreads();
+    uint32_t take = 0;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) take |= (v[e] == v[e] && (score_key(v[e]) >> 20) >= b1) ? 1u << e : 0u;
+    uint32_t listed;
+    uint32_t slot = block_exclusive_scan(uint32_t(__popc(take)), sm.scan_tmp, &listed);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if ((take >> e) & 1u) {
+        sm.cand_key[slot] = score_key(v[e]);
+        sm.cand_col[slot] = int32_t(4 * ((e >> 2) * S::kNT + t) + (e & 3));
+        ++slot;
+      }
+    __syncthreads();
+    select_candidates(sm, int(listed), k, nv, o);
+    return;
+  }
   zero(sm.hist, kBins);
   hist12(s, 0, nv, sm.hist);
   __syncthreads();
@@ -495,23 +542,28 @@ __device__ __noinline__ void select_row(S& sm, const float* s, int64_t nv, int k
   uint32_t need = uint32_t(k) - sm.res_before;
   __syncthreads();
   if (ncand <= uint32_t(S::kCap)) {
-    if (t == 0) sm.ncand = 0;
+    // the keys in bins >= b1, listed one tile of 16 keys per thread at a time: one block scan of the
+    // threads' counts per tile places them (one counter shared by every warp would serialise)
+    uint32_t listed = 0;
+    for (int64_t b0 = 0; b0 < nv; b0 += int64_t(16) * blockDim.x) {  // the same trip count for every thread
+      float v[16];
+      load16<S::kNT>(s, b0, nv, v);  // NaN past nv: never listed
+      uint32_t take = 0;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) take |= (v[e] == v[e] && (score_key(v[e]) >> 20) >= b1) ? 1u << e : 0u;
+      uint32_t tot;
+      uint32_t slot = listed + block_exclusive_scan(uint32_t(__popc(take)), sm.scan_tmp, &tot);
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if ((take >> e) & 1u) {
+          sm.cand_key[slot] = score_key(v[e]);
+          sm.cand_col[slot] = int32_t(b0 + 4 * ((e >> 2) * int64_t(S::kNT) + t) + (e & 3));
+          ++slot;
+        }
+      listed += tot;
+    }
     __syncthreads();
-    for_each_key<8>(s, 0, nv, [&](int64_t i, uint32_t key, bool valid) {
-      const bool take = valid && (key >> 20) >= b1;
-      const unsigned m = __ballot_sync(0xffffffffu, take);
-      if (!m) return;
-      uint32_t base = 0;
-      if (lane == 0) base = atomicAdd(&sm.ncand, uint32_t(__popc(m)));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (take) {
-        const uint32_t c = base + __popc(m & lanes_below);
-        sm.cand_key[c] = key;
-        sm.cand_col[c] = int32_t(i);
-      }
-    });
-    __syncthreads();
-    select_candidates(sm, int(sm.ncand), k, nv, o);
+    select_candidates(sm, int(listed), k, nv, o);
     return;
   }
   // rounds on key bits [19:10] and [9:0] over the row, then an ordered pass
@@ -563,26 +615,6 @@ __device__ __noinline__ void select_row(S& sm, const float* s, int64_t nv, int k
     __syncthreads();
     if (t == 0) { sm.run_g += tot >> 16; sm.run_e += tot & 0xFFFFu; }
     __syncthreads();
-  }
-}
-
-// The 16 scores thread t reads in one sweep step starting at b0: float4 number u * kThreads + t
-// (u < 4) of the step, i.e. v[4 u + e] = s[b0 + 4 (u kThreads + t) + e]; past hi they are NaN,
-// which every comparison rejects and fmaxf ignores.
-template <int NT = kThreads>
-__device__ __forceinline__ void load16(const float* s, int64_t b0, int64_t hi, float (&v)[16]) {
-  const int t = threadIdx.x;
-  const bool full = b0 + int64_t(16) * NT <= hi && ((reinterpret_cast<uintptr_t>(s + b0) & 15u) == 0);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int64_t i0 = b0 + (int64_t(u) * NT + t) * 4;
-    if (full) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(s + i0));
-      v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[4 * u + e] = (i0 + e < hi) ? __ldg(s + i0 + e) : __int_as_float(0x7FC00000);
-    }
   }
 }
 
