@@ -196,7 +196,8 @@ __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity) {
 }
 
 // kCand: the positions are gathered from a candidate pool (ascending cache positions, cand_len[row]
-// valid): each step's 16 key rows arrive as 16 bulk copies of 256 bytes, issued by lanes 0..15.
+// valid): each step's 16 key rows arrive by bulk copies issued by lanes 0..15, one per run of
+// consecutive positions (a pool expanded from blocks of 8 holds such runs).
 template <bool kCand>
 __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
     const uint16_t* __restrict__ qI, const float* __restrict__ w, int Nq,
@@ -292,6 +293,12 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
     const bool rd = mine && q >= 0 && int64_t(q) < key_stride_rows;
     if (mine && !rd) atomicOr(flags, CSA2_FLAG_INDEX_OOB);
     const uint32_t n_rd = __popc(__ballot_sync(0xffffffffu, rd));
+    // runs of consecutive readable positions (a pool expanded from blocks holds runs of 8): the
+    // lane that starts a run copies the whole run's rows in one bulk copy
+    const int32_t q_prev = __shfl_up_sync(0xffffffffu, q, 1);
+    const bool rd_prev = __shfl_up_sync(0xffffffffu, rd, 1);
+    const bool cont = rd && lane > 0 && rd_prev && q_prev + 1 == q;  // continues lane - 1's run
+    const uint32_t cont_mask = __ballot_sync(0xffffffffu, cont);
     if (lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar),
@@ -299,12 +306,15 @@ __global__ void __launch_bounds__(kThreads, 2) index_score_stream_kernel(
                    : "memory");
     }
     __syncwarp();
-    if (rd)
+    if (rd && !cont) {
+      // lanes lane + 1 .. continue the run while their bits of cont_mask are set (lanes < 16 only)
+      const uint32_t run = uint32_t(__ffs(~(cont_mask >> (lane + 1))));
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
               dst + uint32_t(lane) * uint32_t(CSA2_DI * 2)),
-          "l"(kseq + int64_t(q) * CSA2_DI), "r"(uint32_t(CSA2_DI * 2)), "r"(bar)
+          "l"(kseq + int64_t(q) * CSA2_DI), "r"(run * uint32_t(CSA2_DI * 2)), "r"(bar)
           : "memory");
+    }
   };
   for (int i = 0; i < min(n_steps, kStages); ++i) issue(i);
 
