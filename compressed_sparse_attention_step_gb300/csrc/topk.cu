@@ -6,8 +6,8 @@
 // Radix select on ordered 32-bit score keys (-0 and +0 share a key):
 //  * rows up to 8192 columns (topk_kernel): one CTA per row histograms the top 12 key bits, lists
 //    the keys in and above the bin of the k-th largest key, and selects among them;
-//  * rows of 8193 to 131072 columns (topk_cluster_kernel): one thread-block cluster of four or eight
-//    CTAs per row, in one launch.  The CTAs histogram the maxima of their 16-key groups, sum the
+//  * rows of 8193 to 131072 columns (topk_cluster_kernel): one thread-block cluster of two, four or
+//    eight CTAs per row, in one launch.  The CTAs histogram the maxima of their 16-key groups, sum the
 //    histograms through distributed shared memory, take the bin of the k-th largest group maximum
 //    as a lower bound on the k-th largest key (those k maxima are k distinct keys) and append the
 //    keys at or above it to the first CTA's list, which selects among them;
@@ -872,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_select_kernel(
 }
 
 // ---- rows of 8193 to 131072 columns: one thread-block cluster per row, one launch ------------------
-// The C CTAs of a cluster (C = 4 or 8) split the row into C runs of whole sweeps (8192 columns).  In a
+// The C CTAs of a cluster (C = 2, 4 or 8) split the row into C runs of whole sweeps (8192 columns).  In a
 // sweep, thread t's group is the 16 keys at columns 4 (u kThreads + t) + e (u, e < 4), so that a warp's
 // loads are contiguous.  Each CTA keeps its groups' largest keys (and how many keys equal them) in
 // shared memory and histograms them by the top 12 key bits; the C histograms are summed through
@@ -1402,9 +1402,11 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
                       map, map_ld, idx, n_sel, expand8, pool_len);
   if (n <= kClMaxCols) {
     // one cluster per row: eight CTAs when every row's cluster fits in one wave of two CTAs per SM
-    // and each CTA keeps at least 8192 columns, else four
+    // and each CTA keeps at least 8192 columns; two for rows of at most two sweeps; else four
     if (int64_t(rows) * 8 <= 2 * int64_t(sm_count()) && n >= 8 * 8192)
       return launch_topk_cluster<8>(scores, rows, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len, st);
+    if (n <= 2 * kClSweep)
+      return launch_topk_cluster<2>(scores, rows, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len, st);
     return launch_topk_cluster<4>(scores, rows, n, ld, n_valid, k, map, map_ld, idx, n_sel, expand8, pool_len, st);
   }
   if (!ws) return cudaErrorInvalidValue;
