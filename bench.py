@@ -801,11 +801,12 @@ def run_prefill(args, torch, c, syn, dev, sampler):
                              "gathered rows; steps run back to back"},
             "dense_gflop_per_step": gflop, "tflops_step": tflops, "bf16_peak_tflops": peak,
             "frac_of_bf16_peak": tflops / peak, "peak_kind": kind,
-            "roofline": roofline("sparse_attn_kernel", "prefill_chunk_q2048_t131072", "tensor", attn_flop,
+            "roofline": roofline("sparse_attn_pair_kernel", "prefill_chunk_q2048_t131072", "tensor", attn_flop,
                                  statistics.mean(at.ms()), K, peak, f"{kind} (bf16 dense, burst)"),
             "cpu_baseline": cpu,
-            # key norms, two tensor-core passes, threshold, count, order, rescore/select, attention
-            "gpu_launches": 8 * K, "clocks": sampler.summary(t0, t1) if sampler else None}
+            # counters cleared, key norms, two tensor-core passes, threshold, count, order,
+            # rescore/select, attention
+            "gpu_launches": 9 * K, "clocks": sampler.summary(t0, t1) if sampler else None}
 
 
 def run_fp8win(args, torch, c, syn, dev, sampler):

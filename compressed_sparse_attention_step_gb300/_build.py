@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libcsa2.so")
-SOURCES = ["fp4.cu", "index_score.cu", "topk.cu", "attn.cu", "attn_ws.cu", "attn_static.cu", "prefill.cu", "group.cu", "shard.cu"]
+SOURCES = ["fp4.cu", "index_score.cu", "topk.cu", "attn.cu", "attn_ws.cu", "attn_pair.cu", "attn_static.cu", "prefill.cu", "group.cu", "shard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

@@ -659,11 +659,19 @@ int attn_auto_split(int64_t instances, int k, int W) {
   return int(std::max<int64_t>(s, 1));
 }
 
+// The pair path (attn_pair.cu) for a run of layers that attend the same selected rows: two layers per
+// CTA, one CTA per (query, pair), two CTAs per SM.  Taken when those CTAs fill at least one wave;
+// smaller runs keep the per-layer kernels, which split a query over CTAs.
+bool attn_pair_path(int64_t per_layer, int n_layers) {
+  if (n_layers < 2 || per_layer <= 0) return false;
+  return per_layer * ((n_layers + 1) / 2) >= 2 * int64_t(sm_count());
+}
+
 cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, int B, int Nq, const uint8_t* codes,
                                       const uint8_t* scales, int64_t cap, const int32_t* idx,
                                       const int32_t* n_valid, int k, const int32_t* swa_len, int W,
                                       float softmax_scale, int n_split, float* ws, cudaStream_t st,
-                                      bool tickets_zeroed, bool win_fp8) {
+                                      bool tickets_zeroed, bool win_fp8, bool allow_pairs) {
   const int64_t per_layer = int64_t(B) * Nq, instances = per_layer * n_layers;
   if (instances == 0) return cudaSuccess;
   if (n_layers < 1 || n_layers > CSA2_MAX_LAYERS || per_layer > 65535) return cudaErrorInvalidValue;
@@ -674,6 +682,12 @@ cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, in
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   unsigned int* tickets = nullptr;
   float* partials = nullptr;
+  // the pair path, when every layer of the run attends the same rows
+  bool shared_rows = true;
+  for (int l = 1; l < n_layers; ++l) shared_rows = shared_rows && layers.idx[l] == layers.idx[0];
+  if (allow_pairs && shared_rows && attn_pair_path(per_layer, n_layers))
+    return launch_sparse_attn_pairs(layers, n_layers, int(per_layer), Nq, codes, scales, cap, idx, n_valid, k, swa_len,
+                                    W, scale_log2, win_fp8, flags, st);
   if (n_split > 1) {
     tickets = reinterpret_cast<unsigned int*>(ws);
     partials = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + attn_ticket_bytes(instances));
@@ -710,7 +724,7 @@ cudaError_t launch_sparse_attn(const uint16_t* q, int B, int Nq, const uint8_t* 
   layers.out[0] = out;
   layers.lse[0] = lse;
   return launch_sparse_attn_layers(layers, 1, B, Nq, codes, scales, cap, idx, n_valid, k, swa_len, W, softmax_scale,
-                                   n_split, ws, st, tickets_zeroed, false);
+                                   n_split, ws, st, tickets_zeroed, false, false);
 }
 
 }  // namespace csa2

@@ -232,12 +232,20 @@ struct AttnLayers {
 };
 // n_layers layers of B*Nq queries each in one launch; the split workspace holds
 // n_layers * B * Nq instances (attn_ws_bytes), tickets first.  win_fp8: the window buffers hold
-// E4M3 bytes (rows of 512 B) instead of bf16.
+// E4M3 bytes (rows of 512 B) instead of bf16.  allow_pairs: a run of layers that share their
+// selected rows may take the pair path (attn_pair_path), which needs no workspace.
 cudaError_t launch_sparse_attn_layers(const AttnLayers& layers, int n_layers, int B, int Nq, const uint8_t* codes,
                                       const uint8_t* scales, int64_t cap, const int32_t* idx,
                                       const int32_t* n_valid, int k, const int32_t* swa_len, int W,
                                       float softmax_scale, int n_split, float* ws, cudaStream_t st,
-                                      bool tickets_zeroed, bool win_fp8);
+                                      bool tickets_zeroed, bool win_fp8, bool allow_pairs);
+// The pair path of a run of n_layers layers that attend the same selected rows: two layers per CTA,
+// one CTA per (query, pair), outputs written directly.  attn_pair_path: whether a run takes it.
+bool attn_pair_path(int64_t per_layer, int n_layers);
+cudaError_t launch_sparse_attn_pairs(const AttnLayers& layers, int n_layers, int per_layer, int Nq,
+                                     const uint8_t* codes, const uint8_t* scales, int64_t cap, const int32_t* idx,
+                                     const int32_t* n_valid, int k, const int32_t* swa_len, int W, float scale_log2,
+                                     bool win_fp8, unsigned int* flags, cudaStream_t st);
 // The warp-specialised attention kernel (attn_ws.cu), for launches of one CTA per SM: the split
 // is effective, partials and tickets as in launch_sparse_attn_layers (tickets zero).
 cudaError_t launch_sparse_attn_ws(const AttnLayers& layers, int n_layers, int per_layer, int Nq,

@@ -395,7 +395,8 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
       while (ns > 1 && csa2::attn_ws_bytes(inst, ns) > attn_cap) --ns;
       const bool r = ok(csa2::launch_sparse_attn_layers(run, run_n, Bc, Nq, codes, scl, g->cap, run_idx, nullptr, K,
                                                          swl, g->W, g->softmax_scale, ns, attn_ws, aux, zeroed,
-                                                         g->swa_format == CSA2_SWA_E4M3));
+                                                         g->swa_format == CSA2_SWA_E4M3,
+                                                         g->n_split == 0));
       if (timed && !rec(g->ev_attn_end, aux)) return false;
       run_n = 0;
       return r;

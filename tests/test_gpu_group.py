@@ -96,6 +96,21 @@ def test_group_starting_with_reindex_reuses_pool(orc):
     assert np.array_equal(gc2.idx[0].cpu().numpy()[0], exp)
 
 
+@pytest.mark.parametrize("swa_fp8", [False, True])
+def test_decode_group_pair_path_odd_layer_count(orc, swa_fp8):
+    """160 ragged sequences (contexts from 1 entry to 3100, some below k and below the window) and
+    1 Full + 4 Reuse layers: enough (query, layer pair) CTAs to fill a wave, so the five layers that
+    share the Full layer's rows run two per CTA, the last pair holding one layer; bf16 and 8-bit
+    window rows."""
+    T = [1, 2, 9, 16, 17, 127, 128, 129, 511, 512, 513, 640] + \
+        [(37 * i * i + 11 * i) % 3100 + 1 for i in range(148)]
+    gc = GroupCase(59, T, [F, R, R, R, R], swa_fp8=swa_fp8)
+    gc.run()
+    ref = gc.check(orc)
+    for l in range(1, 5):
+        assert np.array_equal(ref["idx"][l], ref["idx"][0])
+
+
 def test_prefill_chunk_ratio2_causal(orc):
     Nq, T = 24, 300
     q_pos = np.arange(2 * T - Nq, 2 * T, dtype=np.int32)[None]      # the last 24 of 600 tokens
