@@ -271,12 +271,24 @@ float prefill_delta_coef();
 cudaError_t launch_prefill_select(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
                                   int64_t cap, const int32_t* lens, int ratio, const int32_t* q_pos, int k,
                                   int32_t* idx, int32_t* n_sel, void* ws, cudaStream_t st);
+// The rows of the selection that several CTAs share: the first n_rows rows of the order take
+// n_slices CTAs each; per (row, slice) up to k candidate keys and columns and their count, and one
+// ticket per row (zero before the launch; the launch leaves it zero).
+struct BmSlices {
+  int n_rows, n_slices;
+  uint32_t* key;
+  int32_t* col;
+  uint32_t* cnt;
+  unsigned int* tickets;
+};
 // bitmap: [rows][n_words] marked keys; ubound: per row, the score key of an upper bound on every
-// canonical score of the row (or null: no bound); order: the rows in processing order (or null).
+// canonical score of the row (or null: no bound); order: the rows in processing order (or null:
+// then no row is sliced).
 cudaError_t launch_bitmap_select(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
                                  int64_t cap, const int32_t* lens, int ratio, const int32_t* q_pos, int k,
                                  const uint32_t* bitmap, int64_t n_words, const uint32_t* ubound,
-                                 const int32_t* order, int32_t* idx, int32_t* n_sel, cudaStream_t st);
+                                 const int32_t* order, const BmSlices& sl, int32_t* idx, int32_t* n_sel,
+                                 cudaStream_t st);
 int bitmap_list_cap();  // marked keys that one list round of the selection rescores
 // Context split: workspace of csa2_merge_topk_pairs for G shards' k pairs per row (shard.cu).
 size_t merge_pairs_ws_bytes(int rows, int G, int k);

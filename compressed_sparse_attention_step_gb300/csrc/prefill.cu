@@ -534,31 +534,70 @@ __global__ void __launch_bounds__(256) prefill_count_kernel(const uint32_t* __re
   }
 }
 
-// The rows in selection order: rows with more than `heavy` marked keys first (they take several
-// list rounds and would otherwise finish last), each class in row order.  One CTA.
+// The rows in selection order: first the n_top rows with the most rescoring work (the selection
+// splits each of them over several CTAs), then the rows with more than `heavy` marked keys (they
+// take several list rounds and would otherwise finish last), then the rest, each class in row
+// order.  A row's work is its marked keys, or only the first chunk of `lim` when the list
+// overflows and its bound is <= 0 (it stops after that chunk).  Zeroes the sliced rows' tickets.
+// One CTA.
 constexpr int kOrdThreads = 1024;
 constexpr int64_t kOrderMaxRows = 16384;  // longer launches keep the natural order
-__global__ void __launch_bounds__(kOrdThreads) prefill_order_kernel(const uint32_t* __restrict__ counts, int rows,
-                                                                    uint32_t heavy, int32_t* __restrict__ order) {
+constexpr int kSliceRows = 4;             // rows split over several CTAs
+constexpr int kSlices = 8;                // CTAs per split row
+__global__ void __launch_bounds__(kOrdThreads) prefill_order_kernel(const uint32_t* __restrict__ counts,
+                                                                    const uint32_t* __restrict__ ubound, int rows,
+                                                                    uint32_t heavy, uint32_t lim, int n_top,
+                                                                    int32_t* __restrict__ order,
+                                                                    unsigned int* __restrict__ tickets) {
   pdl_wait();
   pdl_trigger();
   __shared__ uint32_t scan_tmp[32];
   __shared__ uint32_t run_h, run_l, n_heavy;
+  __shared__ unsigned long long wmax[kOrdThreads / 32];
+  __shared__ int top[kSliceRows];
   const int t = threadIdx.x;
+  auto work = [&](int r) -> uint32_t {
+    const uint32_t c = counts[r];
+    return (c > heavy && ubound[r] <= score_key(0.0f)) ? min(c, lim) : c;
+  };
+  auto picked = [&](int r, int n) {
+    bool p = false;
+    for (int i = 0; i < n; ++i) p = p || top[i] == r;
+    return p;
+  };
+  // the n_top rows of most work (ties: the lower row), one block maximum each
+  for (int i = 0; i < n_top; ++i) {
+    unsigned long long best = 0;
+    for (int r = t; r < rows; r += kOrdThreads)
+      if (!picked(r, i)) best = max(best, (static_cast<unsigned long long>(work(r)) << 32) | (0xFFFFFFFFu - uint32_t(r)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+    if ((t & 31) == 0) wmax[t >> 5] = best;
+    __syncthreads();
+    if (t == 0) {
+      unsigned long long m = 0;
+      for (int j = 0; j < kOrdThreads / 32; ++j) m = max(m, wmax[j]);
+      top[i] = int(0xFFFFFFFFu - uint32_t(m & 0xFFFFFFFFull));
+      order[i] = top[i];
+      tickets[i] = 0u;
+    }
+    __syncthreads();
+  }
   uint32_t h = 0;
-  for (int r = t; r < rows; r += kOrdThreads) h += counts[r] > heavy ? 1u : 0u;
+  for (int r = t; r < rows; r += kOrdThreads) h += (counts[r] > heavy && !picked(r, n_top)) ? 1u : 0u;
   uint32_t tot;
   block_exclusive_scan(h, scan_tmp, &tot);
   if (t == 0) {
-    n_heavy = tot;
-    run_h = 0;
+    n_heavy = uint32_t(n_top) + tot;
+    run_h = uint32_t(n_top);
     run_l = 0;
   }
   __syncthreads();
   for (int base = 0; base < rows; base += kOrdThreads) {
     const int r = base + t;
-    const bool hv = r < rows && counts[r] > heavy;
-    const bool lt = r < rows && !hv;
+    const bool pk = r < rows && picked(r, n_top);
+    const bool hv = r < rows && !pk && counts[r] > heavy;
+    const bool lt = r < rows && !pk && !hv;
     uint32_t th;
     const uint32_t ph = block_exclusive_scan((hv ? 1u : 0u) | ((lt ? 1u : 0u) << 16), scan_tmp, &th);
     if (hv) order[run_h + (ph & 0xFFFFu)] = r;
@@ -618,11 +657,19 @@ float prefill_delta_coef() {
   return float(8.0 * c * (1.0 + 1e-3));
 }
 
+// The split rows' candidates (keys, columns, counts) and tickets, at the end of the workspace.
+constexpr size_t kSliceCand = size_t(kSliceRows) * kSlices * CSA2_MAX_K;
+size_t slice_ws_bytes() {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return 2 * al(kSliceCand * 4) + al(size_t(kSliceRows) * kSlices * 4) + al(size_t(kSliceRows) * 4);
+}
+
 size_t prefill_ws_bytes(int64_t rows, int64_t cap, int B) {
   const int64_t ng = (cap + 31) / 32;
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   const int64_t nch = (cap + kNormChunk - 1) / kNormChunk;
-  return 2 * al(size_t(rows) * size_t(ng) * 4) + 4 * al(size_t(rows) * 4) + al(size_t(B) * size_t(nch) * 4);
+  return 2 * al(size_t(rows) * size_t(ng) * 4) + 4 * al(size_t(rows) * 4) + al(size_t(B) * size_t(nch) * 4) +
+         slice_ws_bytes();
 }
 
 int64_t prefill_max_groups() { return kMaxGroups; }
@@ -645,6 +692,14 @@ cudaError_t launch_prefill_select(const uint16_t* qI, const float* w, int B, int
   uint32_t* counts = reinterpret_cast<uint32_t*>(p + 2 * al(size_t(rows) * ng * 4) + 2 * al(size_t(rows) * 4));
   int32_t* order = reinterpret_cast<int32_t*>(p + 2 * al(size_t(rows) * ng * 4) + 3 * al(size_t(rows) * 4));
   float* kmax = reinterpret_cast<float*>(p + 2 * al(size_t(rows) * ng * 4) + 4 * al(size_t(rows) * 4));
+  char* ps = p + 2 * al(size_t(rows) * ng * 4) + 4 * al(size_t(rows) * 4) +
+             al(size_t(B) * size_t((cap + kNormChunk - 1) / kNormChunk) * 4);
+  BmSlices sl;
+  sl.n_slices = kSlices;
+  sl.key = reinterpret_cast<uint32_t*>(ps);
+  sl.col = reinterpret_cast<int32_t*>(ps + al(kSliceCand * 4));
+  sl.cnt = reinterpret_cast<uint32_t*>(ps + 2 * al(kSliceCand * 4));
+  sl.tickets = reinterpret_cast<unsigned int*>(ps + 2 * al(kSliceCand * 4) + al(size_t(kSliceRows) * kSlices * 4));
 
   CUtensorMap map_k, map_q;
   if (!make_map(&map_k, KI, int64_t(B) * cap, kKeyTile) || !make_map(&map_q, qI, rows * 4, 4 * kQPerTile))
@@ -688,16 +743,18 @@ cudaError_t launch_prefill_select(const uint16_t* qI, const float* w, int B, int
                  ratio, q_pos, items, ng, bitmap, static_cast<const float*>(thr), flags);
   if (e != cudaSuccess) return e;
   const bool ordered = rows <= kOrderMaxRows;
+  sl.n_rows = ordered ? int(std::min<int64_t>(rows, kSliceRows)) : 0;
   if (ordered) {
     e = launch_pdl(prefill_count_kernel, dim3(unsigned(rows)), dim3(256), 0, st, static_cast<const uint32_t*>(bitmap),
                    ng, lens, cap, Nq, ratio, q_pos, counts);
     if (e != cudaSuccess) return e;
     e = launch_pdl(prefill_order_kernel, dim3(1), dim3(kOrdThreads), 0, st, static_cast<const uint32_t*>(counts),
-                   int(rows), uint32_t(bitmap_list_cap()), order);
+                   static_cast<const uint32_t*>(ubound), int(rows), uint32_t(bitmap_list_cap()),
+                   uint32_t(std::max(2 * k, 1024)), sl.n_rows, order, sl.tickets);
     if (e != cudaSuccess) return e;
   }
   return launch_bitmap_select(qI, w, B, Nq, KI, cap, lens, ratio, q_pos, k, bitmap, ng,
-                              static_cast<const uint32_t*>(ubound), ordered ? order : nullptr, idx, n_sel, st);
+                              static_cast<const uint32_t*>(ubound), ordered ? order : nullptr, sl, idx, n_sel, st);
 }
 
 }  // namespace csa2

@@ -71,6 +71,7 @@ struct BmSmem {
   uint32_t nsel, ncand, base;
   uint32_t res_bin, res_before;
   uint32_t run_g, run_e;
+  uint32_t is_last;
   __device__ __forceinline__ int phys(int c) const { return c; }
 };
 
@@ -1208,23 +1209,39 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(
 
 // Prefill rows: the keys marked in the tensor-core filter's bitmap are rescored in the canonical
 // order (eight lanes per key, the query slice in registers) and the exact Top-k is selected among
-// them.  One CTA per query row.
+// them.  One CTA per query row, except that the first n_sliced rows of the order (those with the
+// most marked keys) take n_slices CTAs each: CTA s rescores the marked keys of ranks
+// [s total / n_slices, (s + 1) total / n_slices), keeps its k best (in column order) in the
+// workspace, and the last of them to finish (an atomic ticket) merges the slices in order and
+// selects among them.  The k best of the row are among the slices' k best, so this is exact.
 __global__ void __launch_bounds__(kBmThreads, 2) bitmap_select_kernel(
     const uint16_t* __restrict__ qI, const float* __restrict__ w, int Nq, const uint16_t* __restrict__ KI,
     int64_t cap, const int32_t* __restrict__ lens, int ratio, const int32_t* __restrict__ q_pos, int k,
     const uint32_t* __restrict__ bitmap, int64_t n_words, const uint32_t* __restrict__ ubound,
-    const int32_t* __restrict__ order, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel) {
+    const int32_t* __restrict__ order, int n_sliced, int n_slices, uint32_t* __restrict__ sl_key,
+    int32_t* __restrict__ sl_col, uint32_t* __restrict__ sl_cnt, unsigned int* __restrict__ tickets,
+    int32_t* __restrict__ idx, int32_t* __restrict__ n_sel) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BmSmem& sm = *reinterpret_cast<BmSmem*>(smem_raw);
   pdl_wait();
   pdl_trigger();
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int64_t row = order ? int64_t(__ldg(order + blockIdx.x)) : int64_t(blockIdx.x), b = row / Nq, qi = row - b * Nq;
+  // this CTA's place in the order, and its slice (-1: the whole row)
+  const int n_sl_ctas = n_sliced * n_slices;
+  int pos = int(blockIdx.x), slice = -1;
+  if (pos < n_sl_ctas) {
+    slice = pos % n_slices;
+    pos /= n_slices;
+  } else {
+    pos -= n_sl_ctas - n_sliced;
+  }
+  const int64_t row = order ? int64_t(__ldg(order + pos)) : int64_t(pos), b = row / Nq, qi = row - b * Nq;
   const int64_t T = min(max(int64_t(lens[b]), int64_t(0)), cap);
   const int64_t p = q_pos ? int64_t(q_pos[row]) : int64_t(ratio) * T - Nq + qi;
   const int64_t vis = (p + 1 < 0) ? 0 : min((p + 1) / ratio, T);
   RowOut o{nullptr, idx + row * k, k, 0};
   if (vis <= k) {
+    if (slice > 0) return;
     for (int64_t i = t; i < vis; i += kBmThreads) o.emit(int(i), int32_t(i));
     finish_row(o, vis, int(row), n_sel, nullptr);
     return;
@@ -1271,9 +1288,12 @@ __global__ void __launch_bounds__(kBmThreads, 2) bitmap_select_kernel(
   const uint32_t ub = ubound ? __ldg(ubound + row) : 0xFFFFFFFFu;
   const uint32_t lim = (total > uint32_t(kBmCap) && ub <= score_key(0.0f)) ? uint32_t(max(2 * k, 1024))
                                                                           : uint32_t(kBmCap);
+  // the ranks this CTA rescores
+  const uint32_t r_lo = slice < 0 ? 0u : uint32_t(uint64_t(total) * uint32_t(slice) / uint32_t(n_slices));
+  const uint32_t r_hi = slice < 0 ? total : uint32_t(uint64_t(total) * uint32_t(slice + 1) / uint32_t(n_slices));
   uint32_t n = 0;
-  for (uint32_t lo = 0; lo < total;) {
-    const uint32_t hi = min(total, lo + min(uint32_t(kBmCap) - n, lim));
+  for (uint32_t lo = r_lo; lo < r_hi;) {
+    const uint32_t hi = min(r_hi, lo + min(uint32_t(kBmCap) - n, lim));
     uint32_t slot = first;
     for (int e = 0; e < per && slot < hi; ++e) {
       const int64_t wi = int64_t(t) * per + e;
@@ -1318,11 +1338,46 @@ __global__ void __launch_bounds__(kBmThreads, 2) bitmap_select_kernel(
     __syncthreads();
     n = n_end;
     lo = hi;
-    if (lo < total) {
+    if (lo < r_hi) {
       const uint32_t tau = keep_top(sm, int(n), k);
       n = uint32_t(k);
       if (tau >= ub) break;
     }
+  }
+  if (slice >= 0) {
+    // this slice's k best into the workspace; the last slice of the row merges them in order
+    if (n > uint32_t(k)) {
+      keep_top(sm, int(n), k);
+      n = uint32_t(k);
+    }
+    const int64_t sbase = (int64_t(pos) * n_slices + slice) * k;
+    for (uint32_t i = t; i < n; i += kBmThreads) {
+      sl_key[sbase + i] = sm.cand_key[i];
+      sl_col[sbase + i] = sm.cand_col[i];
+    }
+    if (t == 0) sl_cnt[pos * n_slices + slice] = n;
+    __threadfence();
+    __syncthreads();
+    if (t == 0) sm.is_last = atomicAdd(tickets + pos, 1u) == unsigned(n_slices - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!sm.is_last) return;
+    __threadfence();
+    n = 0;
+    for (int s2 = 0; s2 < n_slices; ++s2) {
+      const uint32_t c = __ldcg(sl_cnt + pos * n_slices + s2);
+      if (n + c > uint32_t(kBmCap)) {  // then n > kBmCap - k >= k
+        keep_top(sm, int(n), k);
+        n = uint32_t(k);
+      }
+      const int64_t b2 = (int64_t(pos) * n_slices + s2) * k;
+      for (uint32_t i = t; i < c; i += kBmThreads) {
+        sm.cand_key[n + i] = __ldcg(sl_key + b2 + i);
+        sm.cand_col[n + i] = __ldcg(sl_col + b2 + i);
+      }
+      __syncthreads();
+      n += c;
+    }
+    if (t == 0) tickets[pos] = 0u;  // ready for the next launch
   }
   if (n < uint32_t(k)) {  // not reached: at least k groups hold a key at or above the threshold
     for (uint32_t i = t; i < n; i += kBmThreads) o.emit(int(i), sm.cand_col[i]);
@@ -1446,9 +1501,14 @@ cudaError_t launch_topk(const float* scores, int rows, int64_t n, int64_t ld, co
 cudaError_t launch_bitmap_select(const uint16_t* qI, const float* w, int B, int Nq, const uint16_t* KI,
                                  int64_t cap, const int32_t* lens, int ratio, const int32_t* q_pos, int k,
                                  const uint32_t* bitmap, int64_t n_words, const uint32_t* ubound,
-                                 const int32_t* order, int32_t* idx, int32_t* n_sel, cudaStream_t st) {
+                                 const int32_t* order, const BmSlices& sl, int32_t* idx, int32_t* n_sel,
+                                 cudaStream_t st) {
   const int64_t rows = int64_t(B) * Nq;
   if (rows == 0) return cudaSuccess;
+  const int n_sliced = order ? sl.n_rows : 0;
+  if (n_sliced < 0 || n_sliced > rows || (n_sliced > 0 && (sl.n_slices < 1 || !sl.key || !sl.col || !sl.cnt ||
+                                                          !sl.tickets)))
+    return cudaErrorInvalidValue;
   const size_t smem = sizeof(BmSmem);
   static std::atomic<bool> attr_set[64];  // per device; set once, by any host thread
   int dev = 0;
@@ -1458,8 +1518,10 @@ cudaError_t launch_bitmap_select(const uint16_t* qI, const float* w, int B, int 
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  return launch_pdl(bitmap_select_kernel, dim3(unsigned(rows)), dim3(kBmThreads), smem, st, qI, w, Nq, KI, cap, lens,
-                    ratio, q_pos, k, bitmap, n_words, ubound, order, idx, n_sel);
+  const int64_t grid = rows + int64_t(n_sliced) * (sl.n_slices - 1);
+  return launch_pdl(bitmap_select_kernel, dim3(unsigned(grid)), dim3(kBmThreads), smem, st, qI, w, Nq, KI, cap,
+                    lens, ratio, q_pos, k, bitmap, n_words, ubound, order, n_sliced, sl.n_slices, sl.key, sl.col,
+                    sl.cnt, sl.tickets, idx, n_sel);
 }
 
 int bitmap_list_cap() { return kBmCap; }
