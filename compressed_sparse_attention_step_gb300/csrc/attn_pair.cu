@@ -222,22 +222,20 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_pair_kernel(
 
   // an FP4 tile's bytes into registers: thread t takes 16-byte piece (t >> 3) & 15 of rows
   // (t & 7) + 8 ((t >> 7) + 2 i), i < 4, and the two scale bytes of each piece (empty rows: zeros)
+  // (the loads are not used until the tile is converted, so the thread does not wait for them)
   uint4 cw[4];
-  uint32_t sw[2];  // scale byte pairs of rows i = 0, 1 (low, high half) and 2, 3
+  uint32_t sw[4];  // the two scale bytes of each row's piece
   auto load_fp4 = [&](int tile) {
     const int32_t* pos = ms.pos[tile];
-    uint32_t s16[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = (t & 7) + 8 * ((t >> 7) + 2 * i), piece = (t >> 3) & 15;
       const int32_t p = pos[r];
       cw[i] = p >= 0 ? __ldg(reinterpret_cast<const uint4*>(cbase + int64_t(p) * CSA2_CODE_BYTES) + piece)
                      : make_uint4(0, 0, 0, 0);
-      s16[i] = p >= 0 ? uint32_t(__ldg(reinterpret_cast<const unsigned short*>(sbase + int64_t(p) * CSA2_SCALE_BYTES) + piece))
-                      : 0u;
+      sw[i] = p >= 0 ? uint32_t(__ldg(reinterpret_cast<const unsigned short*>(sbase + int64_t(p) * CSA2_SCALE_BYTES) + piece))
+                     : 0u;
     }
-    sw[0] = s16[0] | (s16[1] << 16);
-    sw[1] = s16[2] | (s16[3] << 16);
   };
 
   // ls[c]: this lane's row's running sum for column half NC + c (the columns' running offsets are
@@ -299,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_pair_kernel(
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = (t & 7) + 8 * ((t >> 7) + 2 * i), piece = (t >> 3) & 15;
-          const __half2 sab = bits_h2(e4m3x2_to_f16x2(uint16_t(sw[i >> 1] >> (16 * (i & 1)))));
+          const __half2 sab = bits_h2(e4m3x2_to_f16x2(uint16_t(sw[i])));
           const __half2 sA = __low2half2(sab), sB = __high2half2(sab);
           const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
 #pragma unroll
@@ -330,27 +328,35 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_pair_kernel(
           *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, cc + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
         }
       } else {
+        // the second half of the rows' channels straight into the tile (cp.async; empty rows are
+        // zero-filled), and at the first bf16 window tile the pair's Q as bf16 (the previous tile's
+        // S^T products are complete); the first half, already in registers, is stored meanwhile
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = (t & 7) + 8 * j, cc = (t >> 3) + 32;
+          const int br = win_row(wt, r);
+          cp_async16(tile_s + sw128(kTileGroup, r, cc), swbase + (br >= 0 ? int64_t(br) * CSA2_D + 8 * cc : 0),
+                     br >= 0 ? 16 : 0);
+        }
+        if (q_f16) {
+#pragma unroll
+          for (int l = 0; l < 2; ++l)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int e = u * kThreads + t, row = 16 * l + (e >> 6), cc = e & 63;
+              const uint16_t* src = layers.q[l0] + int64_t(inst) * CSA2_H * CSA2_D;
+              if (l < gv) src = layers.q[l0 + l] + int64_t(inst) * CSA2_H * CSA2_D + 8 * e;
+              cp_async16(q_s + sw128(kQGroup, row, cc), src, l < gv ? 16 : 0);
+            }
+          q_f16 = false;
+        }
+        cp_async_commit();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int r = (t & 7) + 8 * j, cc = t >> 3;
           *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, cc)) = wv[j];
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int br = win_row(wt, (t & 7) + 8 * j), cc = (t >> 3) + 32;
-          wv[j] = br >= 0 ? __ldg(reinterpret_cast<const uint4*>(swbase + int64_t(br) * CSA2_D + 8 * cc))
-                          : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = (t & 7) + 8 * j, cc = (t >> 3) + 32;
-          *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, cc)) = wv[j];
-        }
-        // the pair's Q as bf16 for the window tiles (the previous tile's S^T products are complete)
-        if (q_f16) {
-          load_q(false);
-          q_f16 = false;
-        }
+        cp_async_wait<0>();
       }
       fence_async_smem();
       __syncthreads();
@@ -386,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_pair_kernel(
       const bool row_ok = lane < 16 && (is_fp4 ? ms.pos[tile][row] >= 0 : win_row(wt, row) >= 0);
       const bool cols_in = half * NC >= c0 && half * NC < c0 + nc;  // a half's columns are all in or all out
       float x[NC];
-      {
+      if (cols_in) {  // (warp-uniform; the warps of the other layer's columns skip a window tile)
         tmem_ld16c(t_lane + kSCol + uint32_t(half * NC), x);
 #pragma unroll
         for (int p = 1; p < P; ++p)
@@ -398,7 +404,10 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_pair_kernel(
             for (int c = 0; c < 8; ++c) x[8 * h8 + c] += part[c];
           }
 #pragma unroll
-        for (int c = 0; c < NC; ++c) x[c] = (row_ok && cols_in) ? x[c] * scale_log2 : -INFINITY;
+        for (int c = 0; c < NC; ++c) x[c] = row_ok ? x[c] * scale_log2 : -INFINITY;
+      } else {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) x[c] = -INFINITY;
       }
       const float* mjh = ms.mj + half * NC;  // this half's offsets (the same for every lane: a broadcast)
       const float* crh = ms.corr + half * NC;
@@ -436,9 +445,10 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_pair_kernel(
         rescale = __any_sync(0xffffffffu, moved);
       }
       // P^T (columns x rows, K-major, 128-byte swizzle): element (col, row); columns outside the
-      // tile's range get zeros, which its O^T products do not read
+      // tile's range are not written (its O^T products do not read them)
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
+        if (!cols_in) break;
         // an empty row (x = -inf) gives 0; a finite x has a finite offset
         const float pr = x[c] == -INFINITY ? 0.0f : ex2(x[c] - mjh[c]);
         ls[c] += pr;
