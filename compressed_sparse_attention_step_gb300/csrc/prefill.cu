@@ -185,10 +185,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_score_kernel(
     qt = int(r / it.chunks);
     const int ch = int(r - int64_t(qt) * it.chunks);
     const int q1 = min((qt + 1) * kQPerTile, Nq);
-    int64_t vis = 0;  // the largest visible prefix of the tile's queries
-    if (!q_pos) vis = pf_visible(int64_t(b) * Nq + q1 - 1, Nq, lens, cap, ratio, q_pos);
-    else
-      for (int qq = qt * kQPerTile; qq < q1; ++qq) vis = max(vis, pf_visible(int64_t(b) * Nq + qq, Nq, lens, cap, ratio, q_pos));
+    // the largest visible prefix of the tile's queries: a query's prefix does not shrink as its
+    // position grows, so it is the prefix of the tile's last (or largest explicit) position
+    int64_t vis = 0;
+    if (!q_pos) {
+      vis = pf_visible(int64_t(b) * Nq + q1 - 1, Nq, lens, cap, ratio, q_pos);
+    } else {
+      const int32_t* qp = q_pos + int64_t(b) * Nq;
+      int32_t pm = qp[qt * kQPerTile];
+#pragma unroll 8
+      for (int qq = qt * kQPerTile + 1; qq < q1; ++qq) pm = max(pm, __ldg(qp + qq));
+      const int64_t T = min(max(int64_t(lens[b]), int64_t(0)), cap);
+      vis = (int64_t(pm) + 1 < 0) ? 0 : min((int64_t(pm) + 1) / ratio, T);
+    }
     const int n_kt = int((vis + kKeyTile - 1) / kKeyTile);
     kt0 = min(ch * kTilesPerItem, n_kt);
     kt1 = min(kt0 + kTilesPerItem, n_kt);
