@@ -347,12 +347,19 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
           *reinterpret_cast<uint4*>(base + kTileOff + sw128(kTileGroup, r, cc + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
         }
       } else if (win_regs) {
+        // the second half of the rows' channels by cp.async (empty rows zero-filled) while the first
+        // half, already in registers, is stored; the FP4 tile staged before it is older and done
+#pragma unroll
+        for (int j = 8; j < 16; ++j) {
+          const int r = (t & 7) + 8 * (j & 7), cc = (t >> 3) + 32 * (j >> 3);
+          const int32_t br = pos[r];
+          cp_async16(tile_s + sw128(kTileGroup, r, cc), br >= 0 ? swbase + int64_t(br) * CSA2_D + 8 * cc : swa,
+                     br >= 0 ? 16 : 0);
+        }
+        cp_async_commit();
 #pragma unroll
         for (int j = 0; j < 8; ++j) win_store(j, wv[j]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) wv[j] = win_load(8 + j);  // hits L2 (prefetched)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) win_store(8 + j, wv[j]);
+        cp_async_wait<0>();
       } else if (first_fp4 <= last_live) {
         cp_async_wait<1>();  // the window copy; the staged FP4 tile may still be in flight
       } else {
