@@ -381,14 +381,14 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_attn_kernel(
         }
         umma_commit(mbar_s);
       }
+      ok = ok && mbar_wait(mbar_s, ph_s);
+      ph_s ^= 1u;
+      tc_fence_after();
       // -- the staging buffer is free again: copy the next FP4 tile while this one is computed
       if (is_fp4) {
         const int nxt = next_live(tile + 1);
         if (nxt <= last_live) stage_fp4(nxt);
       }
-      ok = ok && mbar_wait(mbar_s, ph_s);
-      ph_s ^= 1u;
-      tc_fence_after();
 
       // -- online softmax: warp (quarter, half) holds rows 16 quarter + lane (lanes < 16) and
       //    heads 8 half .. 8 half + 7; S^T is the sum of the eight channel-eighth partials
