@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_score_kernel(
 
 // Per sequence and chunk of kNormChunk entries: the largest sum of squares of KI_t over the visible
 // part of the chunk (kmax_part[b][chunk]; the threshold kernel takes the maximum over chunks).
-constexpr int kNormChunk = 1024;
+constexpr int kNormChunk = 256;  // entries per CTA: about three CTAs per SM at 131072 entries
 __global__ void __launch_bounds__(256) prefill_key_norm_kernel(const uint16_t* __restrict__ KI,
                                                                const int32_t* __restrict__ lens, int64_t cap,
                                                                float* __restrict__ kmax_part) {
@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(256) prefill_key_norm_kernel(const uint16_t* _
   // eight threads per entry, 16 channels each; a warp takes four consecutive entries per step.  The
   // loop runs on the warp's first entry, so every lane of a warp makes the same trips and the
   // shuffles below always see the full warp (lanes past the chunk's end add nothing).
+#pragma unroll 4
   for (int64_t tw = t0 + ((threadIdx.x >> 5) << 2); tw < t1; tw += blockDim.x >> 3) {
     const int64_t t = tw + ((threadIdx.x & 31) >> 3);
     const bool valid = t < t1;
