@@ -195,10 +195,11 @@ cudaError_t launch_copy_rows_append(const uint16_t* src, int B, int n_new, int r
                                     uint16_t* dst, int64_t cap, const int32_t* lens, cudaStream_t st);
 // The decode append (new main-KV rows quantised to FP4, new indexer-K rows copied) in one launch;
 // rows land at lens[b] - n_new + r.  The same launch clears zero_bytes at `zero` (nullable; both
-// multiples of 16).
+// multiples of 16) and, when block_keys is not null, refreshes the keys of the blocks the append
+// completes (as launch_block_keys with only_new).
 cudaError_t launch_append(const uint16_t* kv_new, const uint16_t* ki_new, int B, int n_new, uint8_t* codes,
                           uint8_t* scales, uint16_t* KI, int64_t cap, const int32_t* lens, void* zero,
-                          size_t zero_bytes, cudaStream_t st);
+                          size_t zero_bytes, uint16_t* block_keys, cudaStream_t st);
 // Clears `bytes` at p with a kernel launched like every other (a memset when p or bytes is not a
 // multiple of 16).
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st);

@@ -124,15 +124,20 @@ __global__ void __launch_bounds__(256) fp4_quantize_kernel(
 }
 
 // The decode append in one launch: threads [0, n_groups) quantise the new main-KV rows, the next
-// n_vecs copy the new indexer-K rows (16 bytes each), and the last n_zero clear 16 bytes each of
-// `zero` (a step's counters, which must start at zero).
+// n_vecs copy the new indexer-K rows (16 bytes each), the next n_zero clear 16 bytes each of
+// `zero` (a step's counters, which must start at zero), and the last n_bk refresh the keys of the
+// blocks the append completes (as block_keys_kernel with only_new, bps blocks per sequence, 16
+// threads of 8 channels per block): a block's rows from before this step are read from the cache,
+// its new rows from ki_new itself, so nothing this launch writes is read, and the sum runs in the
+// same row order.
 __global__ void __launch_bounds__(256) append_kernel(const uint16_t* __restrict__ kv_new,
                                                      const uint16_t* __restrict__ ki_new, int64_t n_groups,
                                                      int64_t n_vecs, int n_new, int ki_vecs,
                                                      uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                      uint16_t* __restrict__ KI, int64_t cap,
                                                      const int32_t* __restrict__ lens, uint4* __restrict__ zero,
-                                                     int64_t n_zero, unsigned int* flags) {
+                                                     int64_t n_zero, uint16_t* __restrict__ bkeys, int64_t bps,
+                                                     int64_t n_bk, unsigned int* flags) {
   pdl_wait();
   pdl_trigger();
   const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -143,6 +148,35 @@ __global__ void __launch_bounds__(256) append_kernel(const uint16_t* __restrict_
     copy_append_vec(ki_new, row, int(q - row * ki_vecs), n_new, ki_vecs, KI, cap, lens, flags);
   } else if (gid - n_groups - n_vecs < n_zero) {
     zero[gid - n_groups - n_vecs] = make_uint4(0u, 0u, 0u, 0u);
+  } else if (gid - n_groups - n_vecs - n_zero < n_bk) {
+    const int64_t q = gid - n_groups - n_vecs - n_zero;
+    const int sl = int(q & 15);
+    const int64_t tb = q >> 4, b = tb / bps;
+    const int64_t lb = lens[b], T = min(lb, cap), first_new = lb - n_new;
+    const int64_t j = tb - b * bps + max(int64_t(0), (T - n_new) / CSA2_BLOCK);
+    if (j >= T / CSA2_BLOCK) return;
+    float acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < CSA2_BLOCK; ++i) {
+      const int64_t p = j * CSA2_BLOCK + i;
+      const uint16_t* src = p >= first_new ? ki_new + ((b * n_new + (p - first_new)) * CSA2_DI + sl * 8)
+                                           : KI + ((b * cap + p) * CSA2_DI + sl * 8);
+      const uint4 v = *reinterpret_cast<const uint4*>(src);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        acc[2 * c] = __fadd_rn(acc[2 * c], bf16lo(wv[c]));
+        acc[2 * c + 1] = __fadd_rn(acc[2 * c + 1], bf16hi(wv[c]));
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      o[c] = pack_bf16x2(__fmul_rn(acc[2 * c], 0.125f), __fmul_rn(acc[2 * c + 1], 0.125f));
+    *reinterpret_cast<uint4*>(bkeys + ((b * (cap / CSA2_BLOCK) + j) * CSA2_DI + sl * 8)) =
+        make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -305,18 +339,20 @@ cudaError_t launch_copy_rows_append(const uint16_t* src, int B, int n_new, int r
 
 cudaError_t launch_append(const uint16_t* kv_new, const uint16_t* ki_new, int B, int n_new, uint8_t* codes,
                           uint8_t* scales, uint16_t* KI, int64_t cap, const int32_t* lens, void* zero,
-                          size_t zero_bytes, cudaStream_t st) {
+                          size_t zero_bytes, uint16_t* block_keys, cudaStream_t st) {
   const int64_t n_groups = int64_t(B) * n_new * (CSA2_D / CSA2_GROUP);
   const int ki_vecs = CSA2_DI / 8;
   const int64_t n_vecs = int64_t(B) * n_new * ki_vecs;
   if ((reinterpret_cast<uintptr_t>(zero) | zero_bytes) & 15u) return cudaErrorInvalidValue;
   const int64_t n_zero = zero ? int64_t(zero_bytes / 16) : 0;
-  if (n_groups + n_vecs + n_zero == 0) return cudaSuccess;
+  const int64_t bps = int64_t(n_new / CSA2_BLOCK + 1);  // blocks the append may complete, per sequence
+  const int64_t n_bk = block_keys ? int64_t(B) * bps * 16 : 0;
+  if (n_groups + n_vecs + n_zero + n_bk == 0) return cudaSuccess;
   unsigned int* flags = device_flags_ptr();
   if (!flags) return cudaErrorUnknown;
-  return launch_pdl(append_kernel, grid_for(n_groups + n_vecs + n_zero, 256), dim3(256), 0, st, kv_new, ki_new,
+  return launch_pdl(append_kernel, grid_for(n_groups + n_vecs + n_zero + n_bk, 256), dim3(256), 0, st, kv_new, ki_new,
                     n_groups, n_vecs, n_new, ki_vecs, codes, scales, KI, cap, lens, static_cast<uint4*>(zero), n_zero,
-                    flags);
+                    block_keys, bps, n_bk, flags);
 }
 
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st) {

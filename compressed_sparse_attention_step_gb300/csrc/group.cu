@@ -335,8 +335,10 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
   // ---- append (Full layer of a decode step), before any scoring --------------------------------
   if (g->n_new > 0) {
     if (g->kv_new && g->ki_new) {
+      // (the hierarchical step's completed block keys in the same launch)
       if (!ok(csa2::launch_append(g->kv_new, g->ki_new, g->B, g->n_new, g->codes, g->scales, g->KI, g->cap, g->lens,
-                                  zeroed ? wsb + zero_lo : nullptr, zeroed ? zero_hi - zero_lo : 0, st)))
+                                  zeroed ? wsb + zero_lo : nullptr, zeroed ? zero_hi - zero_lo : 0,
+                                  g->hierarchical ? g->block_keys : nullptr, st)))
         return CSA2_ERR_CUDA;
       zero_done = zeroed;
     } else if (g->kv_new &&
@@ -348,7 +350,7 @@ extern "C" csa2_status csa2_group_step(const csa2_group_desc* g, void* ws, size_
       if (!g->kv_new &&
           !ok(csa2::launch_copy_rows_append(g->ki_new, g->B, g->n_new, CSA2_DI, g->KI, g->cap, g->lens, st)))
         return CSA2_ERR_CUDA;
-      if (g->hierarchical &&
+      if (g->hierarchical && !g->kv_new &&
           !ok(csa2::launch_block_keys(g->KI, g->B, g->cap, g->lens, g->block_keys, 1, g->n_new, st)))
         return CSA2_ERR_CUDA;
     }
