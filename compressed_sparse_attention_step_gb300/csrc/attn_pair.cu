@@ -12,8 +12,12 @@
 // 32 columns each) and about 104 KB of shared memory keep two CTAs on an SM, so one CTA's loads and
 // conversions overlap the other's tensor-core work, as in the per-layer kernel:
 //   - the next FP4 tile's code and scale bytes are loaded into registers while the current tile is
-//     computed, and dequantised (E2M1 -> f16x2 and E4M3 -> f16x2 conversions, one exact f16
-//     multiply) into a 64 x 512 operand tile in the 128-byte-swizzled layout;
+//     computed (kept as loaded: a thread that combined them at once would wait for the loads), and
+//     dequantised (E2M1 -> f16x2 and E4M3 -> f16x2 conversions, one exact f16 multiply) into a
+//     64 x 512 operand tile in the 128-byte-swizzled layout;
+//   - a window tile's first 256 channels per row are loaded into registers before the previous
+//     tile's O^T products release the operand tile, the other 256 go there by cp.async while the
+//     first half is stored; the warps of the other layer's columns skip the tile's softmax;
 //   - four warps issue a 128-channel quarter each of S^T into their own partial; the softmax warps
 //     add the four partials, run the online softmax per column (two warps per tensor-memory lane
 //     quarter, 16 columns each) with lazy offsets (an offset moves only when a score passes it by
