@@ -401,12 +401,12 @@ __global__ void __launch_bounds__(256) prefill_key_norm_kernel(const uint16_t* _
   }
 }
 
-// Per query row: thr = (k-th largest group maximum of the tensor-core scores) - 2 delta, rounded
-// down; -inf when fewer than k groups are visible (every visible key is then kept).  Also the row's
+// Per query row: thr = L - 2 delta, rounded down, with L at most the k-th largest group maximum of
+// the tensor-core scores; -inf when fewer than k groups are visible (every visible key is then kept).  Also the row's
 // score bound ub (as a score key): every canonical score is <= (largest tensor-core score) + 2 delta,
 // and <= -0 when all four head weights are negative (each product w_h relu(.) is then <= -0).  One
-// CTA of 256 threads per row: the row's group maxima (keys) go to shared memory, and three radix
-// rounds of 11/11/10 bits find the k-th largest.
+// CTA of 256 threads per row: the row's group maxima (keys) go to shared memory, and two radix
+// rounds of 11 bits bound the k-th largest from below (its top 22 bits, the rest zero).
 constexpr int kThThreads = 256;
 constexpr int64_t kMaxGroups = 49152;  // group maxima of one row held in shared memory (cap <= 1.5 Mi)
 constexpr int kThBins = 2048;
@@ -461,9 +461,12 @@ __global__ void __launch_bounds__(kThThreads) prefill_threshold_kernel(
     if (t < 4) part[t] = __uint_as_float(scan_tmp[2 * t]) + __uint_as_float(scan_tmp[2 * t + 1]);
     __syncthreads();
   }
+  // two radix rounds resolve the top 22 key bits of the k-th largest group maximum; the key with the
+  // low 10 bits zero is at most that maximum, so L below stays a lower bound on the k-th largest
+  // filter score (about 2^-13 lower, relative, than the exact value)
   uint32_t prefix = 0, mask = 0, need = uint32_t(k);
-  const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
-  for (int r = 0; r < 3; ++r) {
+  const int shifts[2] = {21, 10}, widths[2] = {11, 11};
+  for (int r = 0; r < 2; ++r) {
     const int nb = 1 << widths[r];
     for (int i = t; i < nb; i += kThThreads) hist[i] = 0u;
     __syncthreads();
