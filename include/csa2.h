@@ -220,8 +220,8 @@ csa2_status csa2_index_select_prefill(const uint16_t* qI, const float* w, int B,
  *   out    bf16 [B][Nq][16][512];  lse fp32 [B][Nq][16] (nullable), natural log; a query with
  *          no rows gets out = 0 and lse = -inf.
  *   n_split  CTAs per query (0..32, 0 = chosen from the problem size).  A query's rows form
- *          128-row tiles (ceil(k/128) of selected rows, one of window rows); larger splits than
- *          tiles are clamped to the tile count.  Entries of the same query are combined in split
+ *          64-row tiles (ceil(k/64) of selected rows, ceil(W/64) of window rows); larger splits
+ *          than tiles are clamped to the tile count.  Entries of the same query are combined in split
  *          order, so results do not depend on scheduling.
  *   ws     csa2_workspace_size(CSA2_OP_SPARSE_ATTN, ...) bytes for the chosen split.
  * Tensor-core waits are bounded (about one second); one that runs out sets CSA2_FLAG_TIMEOUT.
@@ -275,6 +275,9 @@ size_t csa2_sparse_attn_static_scratch_bytes(void);
  * Every layer attends with its own q and window; window rows are bf16, or one E4M3 byte per
  * channel with swa_format = CSA2_SWA_E4M3 (csa2_fp8_quantize).  The first layer must be FULL or
  * REINDEX.
+ * Attention: consecutive layers that attend the same rows run in one launch; with n_split = 0 and
+ * at least two CTAs per SM of (query, layer pair) work (prefill chunks), each CTA takes two layers
+ * and gathers and dequantises their shared rows once.  The results stay within the same tolerance.
  * Execution: the batch is cut into `seq_chunks` groups of whole sequences (0: one group).  With
  * more than one group, the first indexer scan of group c runs on `stream` while the remaining
  * work of group c-1 runs on a library-owned, highest-priority stream of the current device
